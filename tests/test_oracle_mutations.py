@@ -1,0 +1,87 @@
+"""Planted mistakes in the oracle (on the CPU) must trip at least one pin.
+
+Each case swaps a piece of the oracle for a plausible wrong variant and runs the
+pin that is meant to catch it.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import oracle.dcoco as od
+import test_oracle_pins as pins
+
+
+def _unbiased_ln(x, eps=od.LN_EPS):
+    mu = x.mean(axis=-1, keepdims=True)
+    return (x - mu) / np.sqrt(x.var(axis=-1, ddof=1, keepdims=True) + eps)
+
+
+def _eps_outside_ln(x, eps=od.LN_EPS):
+    mu = x.mean(axis=-1, keepdims=True)
+    return (x - mu) / (np.sqrt(((x - mu) ** 2).mean(axis=-1, keepdims=True)) + eps)
+
+
+def _argmax_last(x):
+    y = od.canonical(x)
+    return int(len(y) - 1 - np.argmax(y[::-1]))
+
+
+def _swap(w, a, b):
+    w = dict(w)
+    w[a], w[b] = w[b], w[a]
+    return w
+
+
+ORIG_TS = od.transition_scores
+ORIG_CR = od.candidate_repr
+ORIG_TOPK = od.topk
+
+
+def _ts_swapped_logit_weights(z, s, vals, w):
+    return ORIG_TS(z, s, vals, _swap(w, "u_a", "u_b"))
+
+
+def _ts_swapped_UV(z, s, vals, w):
+    return ORIG_TS(z, s, vals, _swap(w, "U", "V"))
+
+
+def _cr_concat_order(ids, emb, h, w):
+    w = dict(w)
+    r = w["W_f"].shape[0]
+    w["W_f"] = np.hstack([w["W_f"][:, r:], w["W_f"][:, :r]])
+    return ORIG_CR(ids, emb, h, w)
+
+
+def _cr_transposed_gather(ids, emb, h, w):
+    # gathers by candidate position instead of token id
+    pos = np.broadcast_to(np.arange(ids.shape[-1]), ids.shape)
+    return ORIG_CR(pos, emb, h, w)
+
+
+def _topk_ties_high(logits, K):
+    x = od.canonical(np.asarray(logits, dtype=np.float64))
+    order = np.argsort(-x[..., ::-1], axis=-1, kind="stable")[..., :K]
+    order = x.shape[-1] - 1 - order
+    return np.take_along_axis(x, order, axis=-1), order
+
+
+CASES = [
+    ("layer_norm", _unbiased_ln, pins.test_layer_norm_spike_closed_form),
+    ("layer_norm", _eps_outside_ln, pins.test_layer_norm_spike_closed_form),
+    ("_argmax_first", _argmax_last, pins.test_walk_ties_go_to_lower_index),
+    ("transition_scores", _ts_swapped_logit_weights,
+     lambda: pins.test_scores_single_term_closed_form("u_a")),
+    ("transition_scores", _ts_swapped_UV, lambda: pins.test_scores_single_term_closed_form("U")),
+    ("candidate_repr", _cr_concat_order, pins.test_candidate_repr_hidden_path_and_concat_order),
+    ("candidate_repr", _cr_transposed_gather, pins.test_candidate_repr_embedding_path),
+    ("topk", _topk_ties_high, pins.test_topk_all_equal_and_k_equals_v),
+]
+
+
+@pytest.mark.parametrize("name,bad,pin", CASES, ids=[f"{c[0]}:{c[1].__name__}" for c in CASES])
+def test_planted_mistake_is_caught(monkeypatch, name, bad, pin):
+    monkeypatch.setattr(od, name, bad)
+    if hasattr(oracle, name):
+        monkeypatch.setattr(oracle, name, bad)
+    with pytest.raises(AssertionError):
+        pin()
