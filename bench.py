@@ -1,0 +1,344 @@
+"""Benchmark of the DCOCO per-cycle hot path (corrected draft blocks per second).
+
+One step = one whole correction cycle over one batch of synthetic drafter output:
+top-K over the B x V logits of every stream, candidate representations, pair states, all
+(B-1)K^2 transition scores, the prefix-first walk and greedy verification.  Default workload:
+32 concurrent streams, B=16, K=16, V=151936, d=E=4096, r=256, H=512, bf16 inputs.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs its own replica on its own streams (no collective on
+the data path); the time is the max over ranks.  `--impl reference` times the float64 CPU
+oracle on the host cores instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads as wl  # noqa: E402
+
+METRIC = "corrected draft blocks/sec (B=16,K=16,32 streams) + % of HBM/tensor roofline"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p.get("bf16_tflops", 1900.0)), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, 1900.0, "fallback"
+
+
+# ----------------------------------------------------------------------------- CPU oracle arm
+
+ORACLE_SNIPPET = r"""
+import json, os, sys, time
+sys.path.insert(0, {root!r})
+import numpy as np
+import oracle, workloads as wl
+cfg = wl.CONFIGS[{cfg!r}].replace(N=1)
+n_streams, reps = {n_streams}, {reps}
+emb = wl.embedding(cfg)
+w = wl.weights(cfg)
+f = lambda a: wl.to_f64(a, cfg.dtype)
+W = {{k: f(v) for k, v in w.items()}}
+streams = []
+for n in range(n_streams):
+    c = cfg.replace(base_seed=cfg.base_seed + n)
+    streams.append((wl.logits(c), wl.hidden(c)))
+times = []
+for r in range(reps):
+    t0 = time.perf_counter()
+    for lg, h in streams:
+        vals, ids = oracle.topk(f(lg), cfg.K)
+        uniq, inv = np.unique(ids, return_inverse=True)
+        rep = oracle.candidate_repr(inv.reshape(ids.shape), f(emb[uniq]), f(h), W)
+        s = oracle.pair_state(f(h), W)
+        S = oracle.transition_scores(rep["z"], s, vals, W)
+        k, tok = oracle.select(S, vals, ids)
+        t = wl.verifier_tokens(cfg, tok)
+        oracle.verify_greedy(tok, t)
+    times.append(time.perf_counter() - t0)
+print(json.dumps({{"times": times, "streams": n_streams}}))
+"""
+
+
+def run_oracle(cfg_name: str, n_streams: int, reps: int):
+    """Times the oracle in a fresh single-threaded process (no CUDA context, no fork)."""
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+        env[k] = "1"
+    code = ORACLE_SNIPPET.format(root=ROOT, cfg=cfg_name, n_streams=n_streams, reps=reps)
+    res = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env)
+    if res.returncode != 0:
+        raise RuntimeError(f"oracle run failed:\n{res.stderr[-2000:]}")
+    return json.loads(res.stdout.strip().splitlines()[-1])
+
+
+def reference_arm(args, cfg):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    n_streams = 2
+    r = run_oracle(cfg.name, n_streams, args.warmup + args.steps)
+    timed = r["times"][args.warmup:]
+    sec = sum(timed)
+    value = n_streams * len(timed) / sec
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "blocks/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec / len(timed),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_dict(cfg),
+            "cpu_baseline": {"value": value, "unit": "blocks/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{n_streams} of {cfg.N} streams per step (one full block each), "
+                                       f"same shapes and distributions"},
+            "e2e": {"value": value, "unit": "blocks/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+
+def config_dict(cfg):
+    return {"workload": cfg.name, "streams": cfg.N, "B": cfg.B, "K": cfg.K, "V": cfg.V, "d": cfg.d, "E": cfg.E,
+            "r": cfg.r, "H": cfg.H, "verify": "greedy", "parallelism": "replicas (streams sharded, no collective)",
+            "l2": "flushed (256 MB write) before every timed step"}
+
+
+class ClockSampler:
+    """nvidia-smi samples during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except FileNotFoundError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[3:7]):
+                if flag.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_arm(args, cfg):
+    import torch
+    import torch.distributed as dist
+
+    import draft_correction_gb300 as dc
+    from draft_correction_gb300 import build as dcb
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 or world == 1:
+        dcb.build()
+    if world > 1:
+        dist.barrier()
+    dc.lib()
+
+    # Inputs: every rank owns its own N streams (seeds offset by rank); table and weights shared.
+    rcfg = cfg.replace(base_seed=cfg.base_seed + rank * cfg.N) if rank else cfg
+    logits_h = wl.logits(rcfg)
+    hidden_h = wl.hidden(rcfg)
+    emb = dc.to_device(wl.embedding(cfg), cfg.dtype, dev)
+    w = dc.CorrectorWeights.from_numpy(wl.weights(cfg), cfg.dtype, dev)
+    logits = dc.to_device(logits_h, cfg.dtype, dev)
+    hidden = dc.to_device(hidden_h, cfg.dtype, dev)
+    cyc = dc.Cycle(w, cfg.N, cfg.B, cfg.K, cfg.V, device=dev, keep_intermediates=True)
+
+    # Greedy verifier tokens drawn against this stream's own corrected draft.
+    t_zero = torch.zeros((cfg.N, cfg.B + 1), dtype=torch.int32, device=dev)
+    out = cyc.run(logits, emb, hidden, t=t_zero)
+    torch.cuda.synchronize()
+    t_host = wl.verifier_tokens(rcfg, out["tokens"].cpu().numpy())
+    t_dev = dc.to_device(t_host, "i32", dev)
+
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+
+    # One cycle captured as a CUDA graph (11 kernels, no host work between them).
+    for _ in range(2):
+        cyc.run(logits, emb, hidden, t=t_dev)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        cyc.run(logits, emb, hidden, t=t_dev)
+    torch.cuda.synchronize()
+
+    def timed_loop(fn, steps, warmup):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for _ in range(warmup):
+            flush.fill_(1)
+            fn()
+        torch.cuda.synchronize()
+        for s, e in ev:
+            flush.fill_(1)
+            s.record(stream)
+            fn()
+            e.record(stream)
+        torch.cuda.synchronize()
+        return [s.elapsed_time(e) for s, e in ev]
+
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        ms = timed_loop(graph.replay, args.steps, args.warmup)
+    torch.cuda.synchronize()
+    total_ms = sum(ms)
+    if world > 1:
+        tt = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    blocks = world * cfg.N * args.steps
+    value = blocks / (total_ms / 1e3)
+    assert dc.device_status() == 0, "device status word reports a fault"
+
+    # Per-stage device times (same inputs, same launch configuration, L2 flushed).
+    ids, vals = cyc.out["ids"], cyc.out["vals"]
+    uz = torch.empty((cfg.N, cfg.B, cfg.K, cfg.H), dtype=w.act_dtype, device=dev)
+    stage_steps = max(5, min(args.steps, 30))
+    stages = {
+        "topk": lambda: dc.topk(logits, cfg.K, vals=vals, ids=ids),
+        "pair_state": lambda: dc.pair_state(hidden, w),
+        "candidate_repr": lambda: dc.candidate_repr(ids, emb, hidden, w),
+    }
+    uzv = dc.candidate_repr(ids, emb, hidden, w)
+    wsp = dc.pair_state(hidden, w)
+    S = dc.score_transitions(uzv[0], uzv[1], wsp, vals, w)
+    stages["score_transitions"] = lambda: dc.score_transitions(uzv[0], uzv[1], wsp, vals, w)
+    stages["select"] = lambda: dc.select(S, vals, ids)
+    stages["verify"] = lambda: dc.verify(cyc.out["tokens"], t=t_dev)
+    del uz
+    stage_us = {k: 1e3 * statistics.mean(timed_loop(fn, stage_steps, 2)) for k, fn in stages.items()}
+
+    # Roofline of the dominant kernel (top-K, HBM-bound): algorithmic bytes per launch.
+    hbm, _, peak_kind = peaks()
+    topk_bytes = cfg.N * cfg.B * cfg.V * 2 + cfg.N * cfg.B * cfg.K * 8
+    topk_s = stage_us["topk"] * 1e-6
+    achieved = topk_bytes / topk_s / 1e9
+    roofline = {"bound": "hbm", "kernel": "topk_kernel", "achieved": round(achieved, 1), "peak": hbm,
+                "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": None,
+                "peak_source": f"{peak_kind} hbm_gbs (burst)", "algorithmic_bytes_per_launch": topk_bytes}
+
+    # End to end through the public API: pinned host inputs -> device, cycle, results -> host.
+    logits_pin = torch.from_numpy(logits_h.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hidden_pin = torch.from_numpy(hidden_h.view(np.int16)).view(torch.bfloat16).pin_memory()
+    t_pin = torch.from_numpy(t_host).pin_memory()
+    com_pin = torch.empty((cfg.N, cfg.B + 1), dtype=torch.int32).pin_memory()
+    acc_pin = torch.empty((cfg.N,), dtype=torch.int32).pin_memory()
+
+    def e2e_step():
+        logits.copy_(logits_pin, non_blocking=True)
+        hidden.copy_(hidden_pin, non_blocking=True)
+        t_dev.copy_(t_pin, non_blocking=True)
+        o = cyc.run(logits, emb, hidden, t=t_dev)
+        com_pin.copy_(o["committed"], non_blocking=True)
+        acc_pin.copy_(o["accept_len"], non_blocking=True)
+
+    e2e_ms = timed_loop(e2e_step, max(5, min(args.steps, 30)), 2)
+    e2e_val = cfg.N * len(e2e_ms) / (sum(e2e_ms) / 1e3) * world
+    h2d = logits_h.nbytes + hidden_h.nbytes + t_host.nbytes
+    d2h = com_pin.numel() * 4 + acc_pin.numel() * 4
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n_streams = 2
+        r = run_oracle(cfg.name, n_streams, 2)
+        sec = statistics.mean(r["times"])
+        cpu = {"value": n_streams / sec, "unit": "blocks/s", "cores": 1, "kind": "oracle",
+               "sample": f"{n_streams} of {cfg.N} streams, full cycle each, single host thread"}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": round(value, 1), "unit": "blocks/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": config_dict(cfg), "roofline": roofline, "cpu_baseline": cpu,
+                "e2e": {"value": round(e2e_val, 1), "unit": "blocks/s", "h2d_bytes_per_step": h2d,
+                        "d2h_bytes_per_step": d2h},
+                "gpu_launches": 11 * args.steps, "clocks": clk.summary(),
+                "stages_us": {k: round(v, 2) for k, v in stage_us.items()},
+                "step_ms_p10_p50_p90": [round(float(np.percentile(ms, q)), 4) for q in (10, 50, 90)]}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default=wl.HEADLINE.name, choices=sorted(wl.CONFIGS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
+    cfg = wl.CONFIGS[args.config]
+    if args.impl == "reference":
+        return reference_arm(args, cfg)
+    return gpu_arm(args, cfg)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

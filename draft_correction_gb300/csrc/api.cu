@@ -1,0 +1,629 @@
+// C ABI of the library: argument checking, workspace layout, tensor maps and launches.
+// Every entry point validates all of its arguments before it enqueues anything.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "../../include/dcoco.h"
+#include "internal.h"
+
+using namespace dcoco;
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return code;
+}
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(DCOCO_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+void clear_err() { g_err[0] = '\0'; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+int g_topk_split = 0;  // 0 = automatic
+
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Bump allocator over the caller's workspace.
+struct Carve {
+  char* base;
+  size_t used = 0;
+  explicit Carve(void* b) : base(static_cast<char*>(b)) {}
+  template <typename T>
+  T* take(size_t bytes) {
+    T* p = reinterpret_cast<T*>(base ? base + used : nullptr);
+    used += round256(bytes);
+    return p;
+  }
+};
+
+int check_weights(const dcoco_weights* w) {
+  if (w == nullptr) return fail(DCOCO_ERR_INVALID_ARG, "weights is NULL");
+  if (w->dtype != DCOCO_BF16 && w->dtype != DCOCO_F32) return fail(DCOCO_ERR_UNSUPPORTED, "weights dtype %d", w->dtype);
+  if (w->d <= 0 || w->E <= 0 || w->r <= 0 || w->H <= 0)
+    return fail(DCOCO_ERR_INVALID_ARG, "non-positive weight dims d=%d E=%d r=%d H=%d", w->d, w->E, w->r, w->H);
+  const int r = w->r;
+  if (r != 32 && r != 64 && r != 128 && r != 256 && r != 512)
+    return fail(DCOCO_ERR_UNSUPPORTED, "corrector width r=%d (supported: 32, 64, 128, 256, 512)", r);
+  if (w->H % 64 != 0) return fail(DCOCO_ERR_UNSUPPORTED, "MLP width H=%d is not a multiple of 64", w->H);
+  if (w->d % 8 != 0 || w->E % 8 != 0)
+    return fail(DCOCO_ERR_UNSUPPORTED, "d=%d and E=%d must be multiples of 8", w->d, w->E);
+  const void* ptrs[] = {w->W_e, w->W_h, w->W_f, w->W_pair, w->U, w->V, w->W, w->u_a, w->u_b, w->b1, w->w2, w->b2};
+  const char* names[] = {"W_e", "W_h", "W_f", "W_pair", "U", "V", "W", "u_a", "u_b", "b1", "w2", "b2"};
+  for (int i = 0; i < 12; ++i) {
+    if (ptrs[i] == nullptr) return fail(DCOCO_ERR_INVALID_ARG, "weight %s is NULL", names[i]);
+    if (!aligned16(ptrs[i])) return fail(DCOCO_ERR_INVALID_ARG, "weight %s is not 16-byte aligned", names[i]);
+  }
+  return DCOCO_OK;
+}
+
+int check_block(int N, int B, int K) {
+  if (N < 1 || B < 2 || B > 64 || K < 1 || K > 64)
+    return fail(DCOCO_ERR_INVALID_ARG, "shape N=%d B=%d K=%d outside N>=1, 2<=B<=64, 1<=K<=64", N, B, K);
+  if (static_cast<int64_t>(N) * B > 65535 * 8 || static_cast<int64_t>(N) * (B - 1) > (1ll << 31) - 1)
+    return fail(DCOCO_ERR_UNSUPPORTED, "too many streams N=%d", N);
+  return DCOCO_OK;
+}
+
+int check_ptr(const void* p, const char* name) {
+  if (p == nullptr) return fail(DCOCO_ERR_INVALID_ARG, "%s is NULL", name);
+  if (!aligned16(p)) return fail(DCOCO_ERR_INVALID_ARG, "%s is not 16-byte aligned", name);
+  return DCOCO_OK;
+}
+
+#define DCOCO_TRY(x)             \
+  do {                           \
+    const int _rc = (x);         \
+    if (_rc != DCOCO_OK) return _rc; \
+  } while (0)
+
+unsigned int* status_word(int* rc) {
+  static unsigned int* words[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    *rc = fail(DCOCO_ERR_CUDA, "no current CUDA device");
+    return nullptr;
+  }
+  if (words[dev] == nullptr) {
+    cudaError_t e;
+    unsigned int* p = device_status_word(&e);
+    if (e != cudaSuccess) {
+      *rc = cuda_fail(e, "cudaGetSymbolAddress(status word)");
+      return nullptr;
+    }
+    words[dev] = p;
+  }
+  *rc = DCOCO_OK;
+  return words[dev];
+}
+
+// N-tile width for an output group of width n (n a multiple of 64, or r in {32..512}).
+int pick_bn(int n, bool allow512) {
+  if (allow512 && n == 512) return 512;
+  if (n % 256 == 0) return 256;
+  if (n % 128 == 0) return 128;
+  if (n % 64 == 0) return 64;
+  return 32;
+}
+
+// Split-K factor: fill the SMs without giving any split fewer than 2 K blocks.
+int pick_split(int m_tiles, int n_tiles, int nkb, int BN) {
+  if (BN > 256) return 1;
+  int s = 1;
+  while (s < 8 && m_tiles * n_tiles * s * 2 <= 148 && nkb / (s * 2) >= 2) s *= 2;
+  return s;
+}
+
+struct Dims {
+  bool bf16;
+  size_t esz;
+  int N, B, K, d, E, r, H;
+  int M() const { return N * B * K; }
+  int NB() const { return N * B; }
+  int NP() const { return N * (B - 1); }
+};
+
+Dims dims_of(const dcoco_weights* w, int N, int B, int K) {
+  Dims D;
+  D.bf16 = w->dtype == DCOCO_BF16;
+  D.esz = D.bf16 ? 2 : 4;
+  D.N = N;
+  D.B = B;
+  D.K = K;
+  D.d = w->d;
+  D.E = w->E;
+  D.r = w->r;
+  D.H = w->H;
+  return D;
+}
+
+// ---------------------------------------------------------------- workspace layouts
+struct ReprScratch {
+  void* b;     // [M, r] act
+  void* z;     // [M, r] act
+  void* g;     // [NB, r] act
+  float* gw;   // [NB, r]
+};
+size_t repr_scratch(const Dims& D, Carve& c, ReprScratch* s) {
+  const size_t start = c.used;
+  s->b = c.take<void>(static_cast<size_t>(D.M()) * D.r * D.esz);
+  s->z = c.take<void>(static_cast<size_t>(D.M()) * D.r * D.esz);
+  s->g = c.take<void>(static_cast<size_t>(D.NB()) * D.r * D.esz);
+  s->gw = c.take<float>(static_cast<size_t>(D.NB()) * D.r * 4);
+  return c.used - start;
+}
+struct PairScratch {
+  float* hp;  // [NB, 2r]
+  void* s;    // [NP, r] act
+};
+size_t pair_scratch(const Dims& D, Carve& c, PairScratch* s) {
+  const size_t start = c.used;
+  s->hp = c.take<float>(static_cast<size_t>(D.NB()) * 2 * D.r * 4);
+  s->s = c.take<void>(static_cast<size_t>(D.NP()) * D.r * D.esz);
+  return c.used - start;
+}
+
+// ---------------------------------------------------------------- GEMM helpers
+int gemm_group(GemmGroup* g, const void* w_base, const Dims& D, uint64_t rows, uint64_t cols, uint64_t pitch, int BN,
+               void* out, int ldo, int epi) {
+  const char* err = nullptr;
+  if (!make_tmap(&g->b_map, w_base, D.bf16, rows, cols, pitch, static_cast<uint32_t>(std::min(BN, 256)), &err))
+    return fail(DCOCO_ERR_CUDA, "%s", err);
+  g->out = out;
+  g->ldo = ldo;
+  g->epi = epi;
+  g->n_tiles = static_cast<int>(rows / BN);
+  return DCOCO_OK;
+}
+
+int run_gemm(GemmArgs& a, const Dims& D, int BN, cudaStream_t st, const char* what) {
+  int rc;
+  a.status = status_word(&rc);
+  if (rc != DCOCO_OK) return rc;
+  a.ln_eps = 1e-5f;
+  const int m_tiles = (a.M + 127) / 128;
+  const int n_tiles = a.g[0].n_tiles + (a.n_groups > 1 ? a.g[1].n_tiles : 0);
+  const int bk = D.bf16 ? 64 : 32;
+  const int nkb = (a.K + bk - 1) / bk;
+  const int split = pick_split(m_tiles, n_tiles, nkb, BN);
+  const cudaError_t e = launch_gemm(a, D.bf16, BN, split, st);
+  if (e != cudaSuccess) return cuda_fail(e, what);
+  return DCOCO_OK;
+}
+
+int a_map_tiled(GemmArgs& a, const void* base, const Dims& D, uint64_t rows, uint64_t cols, uint64_t pitch) {
+  const char* err = nullptr;
+  if (!make_tmap(&a.a_map, base, D.bf16, rows, cols, pitch, 128, &err)) return fail(DCOCO_ERR_CUDA, "%s", err);
+  a.gather = nullptr;
+  return DCOCO_OK;
+}
+
+// Candidate representation: b, g, gw, z, then uz/vz.
+int enqueue_repr(const Dims& D, const int32_t* ids, const void* emb, int V, const void* h, const dcoco_weights* w,
+                 void* uz, void* vz, const ReprScratch& s, cudaStream_t st) {
+  const int M = D.M(), NB = D.NB(), r = D.r, H = D.H;
+  // b = LN(W_e Emb[ids])   (gathered A operand)
+  {
+    GemmArgs a = {};
+    const char* err = nullptr;
+    if (!make_tmap(&a.a_map, emb, D.bf16, V, D.E, D.E, 1, &err)) return fail(DCOCO_ERR_CUDA, "%s", err);
+    a.gather = ids;
+    a.gather_limit = V;
+    a.M = M;
+    a.K = D.E;
+    a.n_groups = 1;
+    const int BN = pick_bn(r, true);
+    if (BN != r) return fail(DCOCO_ERR_UNSUPPORTED, "r=%d", r);
+    DCOCO_TRY(gemm_group(&a.g[0], w->W_e, D, r, D.E, D.E, BN, s.b, r, EPI_LN));
+    DCOCO_TRY(run_gemm(a, D, BN, st, "gemm b = LN(W_e Emb[c])"));
+  }
+  // g = LN(W_h h)
+  {
+    GemmArgs a = {};
+    DCOCO_TRY(a_map_tiled(a, h, D, NB, D.d, D.d));
+    a.M = NB;
+    a.K = D.d;
+    a.n_groups = 1;
+    const int BN = r;
+    DCOCO_TRY(gemm_group(&a.g[0], w->W_h, D, r, D.d, D.d, BN, s.g, r, EPI_LN));
+    DCOCO_TRY(run_gemm(a, D, BN, st, "gemm g = LN(W_h h)"));
+  }
+  // gw = W_f[:, r:2r] g   (the g half of the fusion, once per slot)
+  {
+    GemmArgs a = {};
+    DCOCO_TRY(a_map_tiled(a, s.g, D, NB, r, r));
+    a.M = NB;
+    a.K = r;
+    a.n_groups = 1;
+    const int BN = pick_bn(r, false);
+    DCOCO_TRY(gemm_group(&a.g[0], static_cast<const char*>(w->W_f) + r * D.esz, D, r, r, 2 * r, BN, s.gw, r, EPI_F32));
+    DCOCO_TRY(run_gemm(a, D, BN, st, "gemm gw = W_f,g g"));
+  }
+  // z = SiLU(W_f[:, 0:r] b + gw[slot])
+  {
+    GemmArgs a = {};
+    DCOCO_TRY(a_map_tiled(a, s.b, D, M, r, r));
+    a.M = M;
+    a.K = r;
+    a.n_groups = 1;
+    a.bias = s.gw;
+    a.bias_div = D.K;
+    a.ld_bias = r;
+    const int BN = pick_bn(r, false);
+    DCOCO_TRY(gemm_group(&a.g[0], w->W_f, D, r, r, 2 * r, BN, s.z, r, EPI_SILU_BIAS));
+    DCOCO_TRY(run_gemm(a, D, BN, st, "gemm z = SiLU(W_f [b; g])"));
+  }
+  // uz = U z, vz = V z
+  {
+    GemmArgs a = {};
+    DCOCO_TRY(a_map_tiled(a, s.z, D, M, r, r));
+    a.M = M;
+    a.K = r;
+    a.n_groups = 2;
+    const int BN = pick_bn(H, false);
+    DCOCO_TRY(gemm_group(&a.g[0], w->U, D, H, r, r, BN, uz, H, EPI_ACT));
+    DCOCO_TRY(gemm_group(&a.g[1], w->V, D, H, r, r, BN, vz, H, EPI_ACT));
+    DCOCO_TRY(run_gemm(a, D, BN, st, "gemm uz, vz"));
+  }
+  return DCOCO_OK;
+}
+
+int enqueue_pair(const Dims& D, const void* h, const dcoco_weights* w, float* wsp, const PairScratch& s,
+                 cudaStream_t st) {
+  const int NB = D.NB(), r = D.r, H = D.H, d = D.d;
+  // hp[:, 0:r] = W_pair[:, 0:d] h,  hp[:, r:2r] = W_pair[:, d:2d] h   (every slot once)
+  {
+    GemmArgs a = {};
+    DCOCO_TRY(a_map_tiled(a, h, D, NB, d, d));
+    a.M = NB;
+    a.K = d;
+    a.n_groups = 2;
+    const int BN = pick_bn(r, false);
+    DCOCO_TRY(gemm_group(&a.g[0], w->W_pair, D, r, d, 2 * d, BN, s.hp, 2 * r, EPI_F32));
+    DCOCO_TRY(gemm_group(&a.g[1], static_cast<const char*>(w->W_pair) + d * D.esz, D, r, d, 2 * d, BN, s.hp + r,
+                         2 * r, EPI_F32));
+    DCOCO_TRY(run_gemm(a, D, BN, st, "gemm W_pair h"));
+  }
+  // s_p = hp[p, 0:r] + hp[p+1, r:2r]
+  {
+    const cudaError_t e = launch_pair_combine(s.hp, s.s, D.bf16, D.N, D.B, r, st);
+    if (e != cudaSuccess) return cuda_fail(e, "pair combine");
+  }
+  // wsp = W s_p
+  {
+    GemmArgs a = {};
+    DCOCO_TRY(a_map_tiled(a, s.s, D, D.NP(), r, r));
+    a.M = D.NP();
+    a.K = r;
+    a.n_groups = 1;
+    const int BN = pick_bn(H, false);
+    DCOCO_TRY(gemm_group(&a.g[0], w->W, D, H, r, r, BN, wsp, H, EPI_F32));
+    DCOCO_TRY(run_gemm(a, D, BN, st, "gemm W s"));
+  }
+  return DCOCO_OK;
+}
+
+int enqueue_scores(const Dims& D, const void* uz, const void* vz, const float* wsp, const float* vals,
+                   const dcoco_weights* w, float* S, cudaStream_t st) {
+  ScoreArgs a;
+  a.uz = uz;
+  a.vz = vz;
+  a.wsp = wsp;
+  a.vals = vals;
+  a.u_a = w->u_a;
+  a.u_b = w->u_b;
+  a.b1 = w->b1;
+  a.w2 = w->w2;
+  a.b2 = w->b2;
+  a.S = S;
+  a.N = D.N;
+  a.B = D.B;
+  a.K = D.K;
+  a.H = D.H;
+  const cudaError_t e = launch_scores(a, D.bf16, st);
+  if (e != cudaSuccess) return cuda_fail(e, "transition scores");
+  return DCOCO_OK;
+}
+
+int topk_split(int rows, int V, bool bf16) {
+  if (g_topk_split > 0) return g_topk_split;
+  const int64_t row_bytes = static_cast<int64_t>(V) * (bf16 ? 2 : 4);
+  int s = 1;
+  while (s < 8 && static_cast<int64_t>(rows) * s < 4 * 152 && row_bytes / (s * 2) >= 16 * 1024) s *= 2;
+  return s;
+}
+
+}  // namespace
+
+extern "C" {
+
+int dcoco_version(void) { return 100; }
+
+const char* dcoco_last_error(void) { return g_err; }
+
+int dcoco_set_topk_split(int ctas_per_row) {
+  const int prev = g_topk_split;
+  g_topk_split = std::max(0, std::min(8, ctas_per_row));
+  return prev;
+}
+
+int dcoco_device_status(void* stream, uint32_t* bits) {
+  clear_err();
+  int rc;
+  unsigned int* w = status_word(&rc);
+  if (rc != DCOCO_OK) return rc;
+  cudaError_t e = cudaStreamSynchronize(as_stream(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  unsigned int v = 0;
+  e = cudaMemcpy(&v, w, sizeof(v), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "read status word");
+  e = cudaMemset(w, 0, sizeof(v));
+  if (e != cudaSuccess) return cuda_fail(e, "clear status word");
+  if (bits) *bits = v;
+  if (v & 7u) return fail(DCOCO_ERR_TIMEOUT, "device status 0x%x: a bounded wait gave up", v);
+  return DCOCO_OK;
+}
+
+int dcoco_topk(const void* logits, int dtype, int N, int B, int V, int K, float* vals, int32_t* ids, void* stream) {
+  clear_err();
+  if (dtype != DCOCO_BF16 && dtype != DCOCO_F32) return fail(DCOCO_ERR_UNSUPPORTED, "logits dtype %d", dtype);
+  if (N < 1 || B < 1 || V < 1 || K < 1 || K > 64 || K > V)
+    return fail(DCOCO_ERR_INVALID_ARG, "shape N=%d B=%d V=%d K=%d (need 1<=K<=min(64,V))", N, B, V, K);
+  if (static_cast<int64_t>(N) * B > 65535) return fail(DCOCO_ERR_UNSUPPORTED, "N*B=%lld rows > 65535", (long long)N * B);
+  DCOCO_TRY(check_ptr(logits, "logits"));
+  DCOCO_TRY(check_ptr(vals, "vals"));
+  DCOCO_TRY(check_ptr(ids, "ids"));
+  const bool bf16 = dtype == DCOCO_BF16;
+  const int rows = N * B;
+  const cudaError_t e = launch_topk(logits, bf16, rows, V, K, topk_split(rows, V, bf16), vals, ids, as_stream(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "top-K launch");
+  return DCOCO_OK;
+}
+
+size_t dcoco_candidate_repr_workspace_size(const dcoco_weights* w, int N, int B, int K) {
+  if (w == nullptr || N < 1 || B < 1 || K < 1) return 0;
+  Carve c(nullptr);
+  ReprScratch s;
+  repr_scratch(dims_of(w, N, B, K), c, &s);
+  return c.used;
+}
+
+int dcoco_candidate_repr(const int32_t* ids, const void* emb, int V, const void* h, const dcoco_weights* w, int N,
+                         int B, int K, void* uz, void* vz, void* workspace, size_t workspace_bytes, void* stream) {
+  clear_err();
+  DCOCO_TRY(check_weights(w));
+  DCOCO_TRY(check_block(N, B, K));
+  if (V < K) return fail(DCOCO_ERR_INVALID_ARG, "V=%d < K=%d", V, K);
+  DCOCO_TRY(check_ptr(ids, "ids"));
+  DCOCO_TRY(check_ptr(emb, "emb"));
+  DCOCO_TRY(check_ptr(h, "h"));
+  DCOCO_TRY(check_ptr(uz, "uz"));
+  DCOCO_TRY(check_ptr(vz, "vz"));
+  const Dims D = dims_of(w, N, B, K);
+  const size_t need = dcoco_candidate_repr_workspace_size(w, N, B, K);
+  if (workspace == nullptr || workspace_bytes < need)
+    return fail(DCOCO_ERR_WORKSPACE, "workspace %zu bytes < %zu required", workspace_bytes, need);
+  if (!aligned16(workspace)) return fail(DCOCO_ERR_INVALID_ARG, "workspace is not 16-byte aligned");
+  Carve c(workspace);
+  ReprScratch s;
+  repr_scratch(D, c, &s);
+  return enqueue_repr(D, ids, emb, V, h, w, uz, vz, s, as_stream(stream));
+}
+
+size_t dcoco_pair_state_workspace_size(const dcoco_weights* w, int N, int B) {
+  if (w == nullptr || N < 1 || B < 2) return 0;
+  Carve c(nullptr);
+  PairScratch s;
+  pair_scratch(dims_of(w, N, B, 1), c, &s);
+  return c.used;
+}
+
+int dcoco_pair_state(const void* h, const dcoco_weights* w, int N, int B, float* ws_pair, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  clear_err();
+  DCOCO_TRY(check_weights(w));
+  DCOCO_TRY(check_block(N, B, 1));
+  DCOCO_TRY(check_ptr(h, "h"));
+  DCOCO_TRY(check_ptr(ws_pair, "ws_pair"));
+  const Dims D = dims_of(w, N, B, 1);
+  const size_t need = dcoco_pair_state_workspace_size(w, N, B);
+  if (workspace == nullptr || workspace_bytes < need)
+    return fail(DCOCO_ERR_WORKSPACE, "workspace %zu bytes < %zu required", workspace_bytes, need);
+  if (!aligned16(workspace)) return fail(DCOCO_ERR_INVALID_ARG, "workspace is not 16-byte aligned");
+  Carve c(workspace);
+  PairScratch s;
+  pair_scratch(D, c, &s);
+  return enqueue_pair(D, h, w, ws_pair, s, as_stream(stream));
+}
+
+int dcoco_score_transitions(const void* uz, const void* vz, const float* ws_pair, const float* vals,
+                            const dcoco_weights* w, int N, int B, int K, float* S, void* stream) {
+  clear_err();
+  DCOCO_TRY(check_weights(w));
+  DCOCO_TRY(check_block(N, B, K));
+  DCOCO_TRY(check_ptr(uz, "uz"));
+  DCOCO_TRY(check_ptr(vz, "vz"));
+  DCOCO_TRY(check_ptr(ws_pair, "ws_pair"));
+  DCOCO_TRY(check_ptr(vals, "vals"));
+  DCOCO_TRY(check_ptr(S, "S"));
+  return enqueue_scores(dims_of(w, N, B, K), uz, vz, ws_pair, vals, w, S, as_stream(stream));
+}
+
+int dcoco_select(const float* S, const float* vals, const int32_t* ids, int N, int B, int K, int32_t* k_sel,
+                 int32_t* tokens, void* stream) {
+  clear_err();
+  DCOCO_TRY(check_block(N, B, K));
+  DCOCO_TRY(check_ptr(S, "S"));
+  DCOCO_TRY(check_ptr(vals, "vals"));
+  DCOCO_TRY(check_ptr(ids, "ids"));
+  DCOCO_TRY(check_ptr(k_sel, "k_sel"));
+  DCOCO_TRY(check_ptr(tokens, "tokens"));
+  SelectVerifyArgs a = {};
+  a.S = S;
+  a.vals = vals;
+  a.ids = ids;
+  a.k_sel = k_sel;
+  a.tokens = tokens;
+  a.mode = -1;
+  a.N = N;
+  a.B = B;
+  a.K = K;
+  a.V = 0;
+  const cudaError_t e = launch_select_verify(a, as_stream(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "select launch");
+  return DCOCO_OK;
+}
+
+static int check_verify(int mode, const int32_t* draft, const int32_t* t, const float* q, const float* u, int N, int B,
+                        int V, int32_t* accept_len, int32_t* committed, int32_t* n_commit, bool need_draft) {
+  if (mode != DCOCO_VERIFY_GREEDY && mode != DCOCO_VERIFY_STOCHASTIC)
+    return fail(DCOCO_ERR_INVALID_ARG, "verify mode %d", mode);
+  if (N < 1 || B < 1 || B > 64) return fail(DCOCO_ERR_INVALID_ARG, "shape N=%d B=%d (need 1<=B<=64)", N, B);
+  if (need_draft) DCOCO_TRY(check_ptr(draft, "draft"));
+  if (mode == DCOCO_VERIFY_GREEDY) {
+    DCOCO_TRY(check_ptr(t, "t"));
+  } else {
+    if (V < 1) return fail(DCOCO_ERR_INVALID_ARG, "V=%d", V);
+    DCOCO_TRY(check_ptr(q, "q"));
+    DCOCO_TRY(check_ptr(u, "u"));
+  }
+  DCOCO_TRY(check_ptr(accept_len, "accept_len"));
+  DCOCO_TRY(check_ptr(committed, "committed"));
+  DCOCO_TRY(check_ptr(n_commit, "n_commit"));
+  return DCOCO_OK;
+}
+
+int dcoco_verify(int mode, const int32_t* draft, const int32_t* t, const float* q, const float* u, int N, int B, int V,
+                 int32_t* accept_len, int32_t* committed, int32_t* n_commit, int32_t* near_tie, void* stream) {
+  clear_err();
+  DCOCO_TRY(check_verify(mode, draft, t, q, u, N, B, V, accept_len, committed, n_commit, true));
+  SelectVerifyArgs a = {};
+  a.mode = mode;
+  a.draft = draft;
+  a.t = t;
+  a.q = q;
+  a.u = u;
+  a.accept_len = accept_len;
+  a.committed = committed;
+  a.n_commit = n_commit;
+  a.near_tie = near_tie;
+  a.N = N;
+  a.B = B;
+  a.K = 1;
+  a.V = V;
+  const cudaError_t e = launch_select_verify(a, as_stream(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "verify launch");
+  return DCOCO_OK;
+}
+
+namespace {
+struct CycleScratch {
+  float* vals;
+  int32_t* ids;
+  float* S;
+  int32_t* k_sel;
+  void* uz;
+  void* vz;
+  float* wsp;
+  ReprScratch repr;
+  PairScratch pair;
+};
+size_t cycle_scratch(const Dims& D, Carve& c, CycleScratch* s) {
+  const size_t start = c.used;
+  const size_t M = static_cast<size_t>(D.M());
+  s->vals = c.take<float>(M * 4);
+  s->ids = c.take<int32_t>(M * 4);
+  s->S = c.take<float>(static_cast<size_t>(D.NP()) * D.K * D.K * 4);
+  s->k_sel = c.take<int32_t>(static_cast<size_t>(D.NB()) * 4);
+  s->uz = c.take<void>(M * D.H * D.esz);
+  s->vz = c.take<void>(M * D.H * D.esz);
+  s->wsp = c.take<float>(static_cast<size_t>(D.NP()) * D.H * 4);
+  repr_scratch(D, c, &s->repr);
+  pair_scratch(D, c, &s->pair);
+  return c.used - start;
+}
+}  // namespace
+
+size_t dcoco_cycle_workspace_size(const dcoco_weights* w, int N, int B, int K) {
+  if (w == nullptr || N < 1 || B < 2 || K < 1) return 0;
+  Carve c(nullptr);
+  CycleScratch s;
+  cycle_scratch(dims_of(w, N, B, K), c, &s);
+  return c.used;
+}
+
+int dcoco_cycle(const void* logits, int V, const void* emb, const void* h, const dcoco_weights* w, int N, int B, int K,
+                int mode, const int32_t* t, const float* q, const float* u, float* vals, int32_t* ids, float* S,
+                int32_t* k_sel, int32_t* tokens, int32_t* accept_len, int32_t* committed, int32_t* n_commit,
+                int32_t* near_tie, void* workspace, size_t workspace_bytes, void* stream) {
+  clear_err();
+  DCOCO_TRY(check_weights(w));
+  DCOCO_TRY(check_block(N, B, K));
+  if (V < K) return fail(DCOCO_ERR_INVALID_ARG, "V=%d < K=%d", V, K);
+  if (static_cast<int64_t>(N) * B > 65535) return fail(DCOCO_ERR_UNSUPPORTED, "N*B > 65535");
+  DCOCO_TRY(check_ptr(logits, "logits"));
+  DCOCO_TRY(check_ptr(emb, "emb"));
+  DCOCO_TRY(check_ptr(h, "h"));
+  DCOCO_TRY(check_ptr(tokens, "tokens"));
+  DCOCO_TRY(check_verify(mode, nullptr, t, q, u, N, B, V, accept_len, committed, n_commit, false));
+  const float* opt[] = {vals, S};
+  for (const float* p : opt)
+    if (p && !aligned16(p)) return fail(DCOCO_ERR_INVALID_ARG, "an optional output is not 16-byte aligned");
+  if ((ids && !aligned16(ids)) || (k_sel && !aligned16(k_sel)))
+    return fail(DCOCO_ERR_INVALID_ARG, "an optional output is not 16-byte aligned");
+  const Dims D = dims_of(w, N, B, K);
+  const size_t need = dcoco_cycle_workspace_size(w, N, B, K);
+  if (workspace == nullptr || workspace_bytes < need)
+    return fail(DCOCO_ERR_WORKSPACE, "workspace %zu bytes < %zu required", workspace_bytes, need);
+  if (!aligned16(workspace)) return fail(DCOCO_ERR_INVALID_ARG, "workspace is not 16-byte aligned");
+  Carve c(workspace);
+  CycleScratch s;
+  cycle_scratch(D, c, &s);
+  float* o_vals = vals ? vals : s.vals;
+  int32_t* o_ids = ids ? ids : s.ids;
+  float* o_S = S ? S : s.S;
+  int32_t* o_k = k_sel ? k_sel : s.k_sel;
+  cudaStream_t st = as_stream(stream);
+
+  const int rows = N * B;
+  cudaError_t e = launch_topk(logits, D.bf16, rows, V, K, topk_split(rows, V, D.bf16), o_vals, o_ids, st);
+  if (e != cudaSuccess) return cuda_fail(e, "top-K launch");
+  DCOCO_TRY(enqueue_pair(D, h, w, s.wsp, s.pair, st));
+  DCOCO_TRY(enqueue_repr(D, o_ids, emb, V, h, w, s.uz, s.vz, s.repr, st));
+  DCOCO_TRY(enqueue_scores(D, s.uz, s.vz, s.wsp, o_vals, w, o_S, st));
+  SelectVerifyArgs a = {};
+  a.S = o_S;
+  a.vals = o_vals;
+  a.ids = o_ids;
+  a.k_sel = o_k;
+  a.tokens = tokens;
+  a.mode = mode;
+  a.t = t;
+  a.q = q;
+  a.u = u;
+  a.accept_len = accept_len;
+  a.committed = committed;
+  a.n_commit = n_commit;
+  a.near_tie = near_tie;
+  a.N = N;
+  a.B = B;
+  a.K = K;
+  a.V = V;
+  e = launch_select_verify(a, st);
+  if (e != cudaSuccess) return cuda_fail(e, "walk/verify launch");
+  return DCOCO_OK;
+}
+
+}  // extern "C"

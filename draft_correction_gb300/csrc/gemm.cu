@@ -1,0 +1,453 @@
+// Dense projections of the corrector on the 5th-generation tensor cores.
+//
+// jaehun.me review of arXiv 2610.12570, §3.2: every projection and MLP parameter of the
+// corrector is shared across slots and transitions, so each projection is one GEMM over
+// all streams' rows: C[m, n] = sum_k A[m, k] B[n, k] with B a weight stored out x in.
+//
+// Kernel shape (one 128-row x BN-column output tile per CTA, 6 warps):
+//   warp 0     TMA producer.  B tiles come from a 2-D tensor map; A tiles either from a
+//              2-D map (activations) or, for the candidate embeddings, as four-row TMA
+//              gathers (tile::gather4) of Emb[c] rows -- the embedding table is read
+//              straight into the swizzled operand layout, never copied to a dense matrix.
+//   warp 1     allocates tensor memory; lane 0 issues tcgen05.mma (bf16 -> kind::f16,
+//              f32 -> kind::tf32) into an fp32 accumulator of 128 lanes x BN columns and
+//              commits each stage back to the producer.
+//   warps 2-5  epilogue: tcgen05.ld of the accumulator, then the fused op of the group
+//              (LayerNorm over the full row, SiLU with a per-slot bias, or a plain store).
+// Split-K: with split_k > 1 the CTAs of one tile form a cluster along z, each reduces a
+// K range, stages its partial tile in its shared memory, and each CTA then sums a slice
+// of rows across the cluster in rank order (distributed shared memory) -- deterministic.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace dcoco {
+namespace {
+
+constexpr int BM = 128;
+constexpr int kThreads = 192;
+constexpr int kMaxStages = 8;
+constexpr int kSmemBudget = 200 * 1024;
+
+__device__ unsigned int g_status_word;
+
+template <bool kBf16>
+struct Elt {
+  static constexpr int BK = kBf16 ? 64 : 32;  // elements per 128-byte row of a stage
+  static constexpr int UK = kBf16 ? 16 : 8;   // K of one MMA instruction (32 bytes)
+  static constexpr uint32_t fmt = kBf16 ? 1u : 2u;
+};
+
+__device__ __forceinline__ float silu(float x) { return x / (1.0f + __expf(-x)); }
+
+template <bool kBf16>
+__device__ __forceinline__ void store_act(void* out, size_t idx, const float* v, int n) {
+  if constexpr (kBf16) {
+    __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out) + idx;
+    for (int i = 0; i < n; i += 8) {
+      uint4 w;
+      __nv_bfloat162 t0 = __floats2bfloat162_rn(v[i + 0], v[i + 1]);
+      __nv_bfloat162 t1 = __floats2bfloat162_rn(v[i + 2], v[i + 3]);
+      __nv_bfloat162 t2 = __floats2bfloat162_rn(v[i + 4], v[i + 5]);
+      __nv_bfloat162 t3 = __floats2bfloat162_rn(v[i + 6], v[i + 7]);
+      w.x = *reinterpret_cast<uint32_t*>(&t0);
+      w.y = *reinterpret_cast<uint32_t*>(&t1);
+      w.z = *reinterpret_cast<uint32_t*>(&t2);
+      w.w = *reinterpret_cast<uint32_t*>(&t3);
+      *reinterpret_cast<uint4*>(o + i) = w;
+    }
+  } else {
+    float* o = static_cast<float*>(out) + idx;
+    for (int i = 0; i < n; i += 4) *reinterpret_cast<float4*>(o + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+  }
+}
+__device__ __forceinline__ void store_f32(void* out, size_t idx, const float* v, int n) {
+  float* o = static_cast<float*>(out) + idx;
+  for (int i = 0; i < n; i += 4) *reinterpret_cast<float4*>(o + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+}
+template <bool kBf16>
+__device__ __forceinline__ void store_act1(void* out, size_t idx, float v) {
+  if constexpr (kBf16) {
+    static_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(v);
+  } else {
+    static_cast<float*>(out)[idx] = v;
+  }
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+
+template <bool kBf16, int BN, bool kSplit>
+__global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ GemmArgs args, int stages,
+                                                          int split_k) {
+  using T = Elt<kBf16>;
+  constexpr int A_BYTES = BM * 128;
+  constexpr int B_BYTES = BN * 128;
+  constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  constexpr int NH = BN > 256 ? 2 : 1;         // MMA instructions per K step (N <= 256 each)
+  constexpr int NMMA = BN / NH;
+  constexpr uint32_t TMEM_COLS = BN < 32 ? 32 : BN;
+  constexpr uint32_t IDESC = mma_idesc(T::fmt, BM, NMMA);
+  constexpr int LDS = BN + 4;                  // staging row pitch (floats), split-K only
+
+  extern __shared__ uint8_t dyn_smem[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
+  __shared__ __align__(8) uint64_t full_bar[kMaxStages];
+  __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
+  __shared__ __align__(8) uint64_t acc_bar;
+  __shared__ uint32_t tmem_base_s;
+  __shared__ int s_rows[BM];
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int m_tile = blockIdx.x;
+  int gi = 0, nt = blockIdx.y;
+  if (nt >= args.g[0].n_tiles) {
+    gi = 1;
+    nt -= args.g[0].n_tiles;
+  }
+  const GemmGroup& grp = args.g[gi];
+  const int ks = blockIdx.z;
+  const int nkb_total = (args.K + T::BK - 1) / T::BK;
+  const int per = (nkb_total + split_k - 1) / split_k;
+  const int kb0 = ks * per;
+  const int nk = std::max(0, std::min(nkb_total, kb0 + per) - kb0);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(smem_u32(&full_bar[s]), 1);
+      mbar_init(smem_u32(&empty_bar[s]), 1);
+    }
+    mbar_init(smem_u32(&acc_bar), 1);
+    fence_mbar_init();
+    prefetch_tmap(&args.a_map);
+    prefetch_tmap(&grp.b_map);
+  }
+  if (warp == 1) tmem_alloc(smem_u32(&tmem_base_s), TMEM_COLS);
+  if (args.gather != nullptr && threadIdx.x < BM) {
+    const int m = m_tile * BM + threadIdx.x;
+    int row = 0;
+    if (m < args.M) {
+      row = args.gather[m];
+      if (row < 0 || row >= args.gather_limit) {
+        atomicOr(args.status, DEV_BAD_INDEX);
+        row = 0;
+      }
+    }
+    s_rows[threadIdx.x] = row;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_s;
+  const uint32_t smem0 = smem_u32(smem);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    for (int i = 0; i < nk; ++i) {
+      const int s = i % stages;
+      const uint32_t ph = (i / stages) & 1;
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&empty_bar[s]), ph ^ 1))) {
+        if (lane == 0) atomicOr(args.status, DEV_TIMEOUT_MMA);
+        break;
+      }
+      const uint32_t fb = smem_u32(&full_bar[s]);
+      const uint32_t a_s = smem0 + s * STAGE_BYTES;
+      const uint32_t b_s = a_s + A_BYTES;
+      const int kx = (kb0 + i) * T::BK;
+      if (lane == 0) mbar_expect_tx(fb, STAGE_BYTES);
+      __syncwarp();
+      if (args.gather != nullptr) {
+        tma_gather4(a_s + lane * 512, &args.a_map, kx, s_rows[4 * lane], s_rows[4 * lane + 1], s_rows[4 * lane + 2],
+                    s_rows[4 * lane + 3], fb);
+      } else if (lane == 0) {
+        tma_load_2d(a_s, &args.a_map, kx, m_tile * BM, fb);
+      }
+      if (lane == 0) {
+#pragma unroll
+        for (int h = 0; h < NH; ++h) tma_load_2d(b_s + h * NMMA * 128, &grp.b_map, kx, nt * BN + h * NMMA, fb);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      for (int i = 0; i < nk; ++i) {
+        const int s = i % stages;
+        const uint32_t ph = (i / stages) & 1;
+        if (!mbar_wait(smem_u32(&full_bar[s]), ph)) {
+          atomicOr(args.status, DEV_TIMEOUT_TMA);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a_s = smem0 + s * STAGE_BYTES;
+        const uint32_t b_s = a_s + A_BYTES;
+#pragma unroll
+        for (int j = 0; j < T::BK / T::UK; ++j) {
+          const uint64_t ad = sw128_desc(a_s + j * 32);
+#pragma unroll
+          for (int h = 0; h < NH; ++h) {
+            const uint64_t bd = sw128_desc(b_s + h * NMMA * 128 + j * 32);
+            tc_mma<!kBf16>(tmem + h * NMMA, ad, bd, IDESC, (i > 0 || j > 0) ? 1u : 0u);
+          }
+        }
+        tc_commit(smem_u32(&empty_bar[s]));
+      }
+      tc_commit(smem_u32(&acc_bar));
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 2..5)
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int row_local = q * 32 + lane;
+    const int m = m_tile * BM + row_local;
+    // tcgen05.ld is warp-collective: every lane of the warp takes the same path below and
+    // only the stores are predicated on the row being inside M.
+    const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&acc_bar), 0));
+    if (!ok && lane == 0) atomicOr(args.status, DEV_TIMEOUT_ACC);
+    const bool live = m < args.M;
+    tc_fence_after();
+    const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    if constexpr (kSplit) {
+      float* stg = reinterpret_cast<float*>(smem);
+      for (int c = 0; c < BN; c += 32) {
+        float v[32];
+        tmem_ld32(trow + c, v);
+#pragma unroll
+        for (int i = 0; i < 32; i += 4)
+          *reinterpret_cast<float4*>(&stg[row_local * LDS + c + i]) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+      }
+    } else if (ok) {
+      const size_t obase = static_cast<size_t>(live ? m : 0) * grp.ldo + static_cast<size_t>(nt) * BN;
+      if (grp.epi == EPI_LN) {
+        float sum = 0.f;
+        for (int c = 0; c < BN; c += 32) {
+          float v[32];
+          tmem_ld32(trow + c, v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) sum += v[i];
+        }
+        const float mean = sum / BN;
+        float ss = 0.f;
+        for (int c = 0; c < BN; c += 32) {
+          float v[32];
+          tmem_ld32(trow + c, v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ss += (v[i] - mean) * (v[i] - mean);
+        }
+        const float rstd = rsqrtf(ss / BN + args.ln_eps);
+        for (int c = 0; c < BN; c += 32) {
+          float v[32];
+          tmem_ld32(trow + c, v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = (v[i] - mean) * rstd;
+          if (live) store_act<kBf16>(grp.out, obase + c, v, 32);
+        }
+      } else {
+        const float* bias = (grp.epi == EPI_SILU_BIAS && live)
+                                ? args.bias + static_cast<size_t>(m / args.bias_div) * args.ld_bias + nt * BN
+                                : nullptr;
+        for (int c = 0; c < BN; c += 32) {
+          float v[32];
+          tmem_ld32(trow + c, v);
+          if (!live) continue;
+          if (grp.epi == EPI_F32) {
+            store_f32(grp.out, obase + c, v, 32);
+          } else {
+            if (bias != nullptr) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = silu(v[i] + bias[c + i]);
+            }
+            store_act<kBf16>(grp.out, obase + c, v, 32);
+          }
+        }
+      }
+    }
+  }
+
+  if constexpr (kSplit) {
+    // Partial tiles are staged; reduce a slice of rows per CTA across the cluster.
+    tc_fence_before();
+    cluster_sync();
+    if (warp >= 2) {
+      const int rank = static_cast<int>(cluster_rank());  // the cluster spans grid.z
+      const int rpc = BM / split_k;
+      for (int rr = warp - 2; rr < rpc; rr += 4) {
+        const int row_local = rank * rpc + rr;
+        const int m = m_tile * BM + row_local;
+        if (m >= args.M) continue;
+        float v[BN / 32];
+#pragma unroll
+        for (int j = 0; j < BN / 32; ++j) v[j] = 0.f;
+        const uint32_t base = smem_u32(smem) + static_cast<uint32_t>(row_local * LDS) * 4u;
+        for (int src = 0; src < split_k; ++src) {
+          const uint32_t rb = map_to_rank(base, src);
+#pragma unroll
+          for (int j = 0; j < BN / 32; ++j) v[j] += ld_cluster_f32(rb + (lane + 32 * j) * 4);
+        }
+        const size_t obase = static_cast<size_t>(m) * grp.ldo + static_cast<size_t>(nt) * BN;
+        if (grp.epi == EPI_LN) {
+          float s = 0.f;
+#pragma unroll
+          for (int j = 0; j < BN / 32; ++j) s += v[j];
+          const float mean = warp_sum(s) / BN;
+          float ss = 0.f;
+#pragma unroll
+          for (int j = 0; j < BN / 32; ++j) ss += (v[j] - mean) * (v[j] - mean);
+          const float rstd = rsqrtf(warp_sum(ss) / BN + args.ln_eps);
+#pragma unroll
+          for (int j = 0; j < BN / 32; ++j) store_act1<kBf16>(grp.out, obase + lane + 32 * j, (v[j] - mean) * rstd);
+        } else if (grp.epi == EPI_F32) {
+#pragma unroll
+          for (int j = 0; j < BN / 32; ++j) static_cast<float*>(grp.out)[obase + lane + 32 * j] = v[j];
+        } else {
+          const float* bias = (grp.epi == EPI_SILU_BIAS)
+                                  ? args.bias + static_cast<size_t>(m / args.bias_div) * args.ld_bias + nt * BN
+                                  : nullptr;
+#pragma unroll
+          for (int j = 0; j < BN / 32; ++j) {
+            float x = v[j];
+            if (bias != nullptr) x = silu(x + bias[lane + 32 * j]);
+            store_act1<kBf16>(grp.out, obase + lane + 32 * j, x);
+          }
+        }
+      }
+    }
+    cluster_sync();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+template <bool kBf16, int BN, bool kSplit>
+cudaError_t launch_gemm_t(const GemmArgs& args, int split_k, cudaStream_t stream) {
+  constexpr int STAGE_BYTES = BM * 128 + BN * 128;
+  int stages = std::min(kMaxStages, kSmemBudget / STAGE_BYTES);
+  if (kSplit) {
+    const int need = BM * (BN + 4) * 4;
+    while (stages * STAGE_BYTES < need && stages < kMaxStages) ++stages;
+  }
+  const int smem = stages * STAGE_BYTES + 1024;
+  auto kern = gemm_kernel<kBf16, BN, kSplit>;
+  // Function attributes are set once per instantiation (and device), so that later calls
+  // enqueue nothing but the launch and can be captured into a CUDA graph.
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((args.M + BM - 1) / BM, args.g[0].n_tiles + (args.n_groups > 1 ? args.g[1].n_tiles : 0), split_k);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = split_k;
+  cfg.attrs = attr;
+  cfg.numAttrs = kSplit ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, args, stages, split_k);
+}
+
+template <bool kBf16>
+cudaError_t dispatch_bn(const GemmArgs& args, int BN, int split_k, cudaStream_t stream) {
+  const bool sp = split_k > 1;
+  switch (BN) {
+    case 32: return sp ? launch_gemm_t<kBf16, 32, true>(args, split_k, stream) : launch_gemm_t<kBf16, 32, false>(args, 1, stream);
+    case 64: return sp ? launch_gemm_t<kBf16, 64, true>(args, split_k, stream) : launch_gemm_t<kBf16, 64, false>(args, 1, stream);
+    case 128: return sp ? launch_gemm_t<kBf16, 128, true>(args, split_k, stream) : launch_gemm_t<kBf16, 128, false>(args, 1, stream);
+    case 256: return sp ? launch_gemm_t<kBf16, 256, true>(args, split_k, stream) : launch_gemm_t<kBf16, 256, false>(args, 1, stream);
+    case 512: return sp ? cudaErrorInvalidValue : launch_gemm_t<kBf16, 512, false>(args, 1, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <bool kBf16>
+__global__ void pair_combine_kernel(const float* __restrict__ hp, void* __restrict__ s, int N, int B, int r) {
+  const int64_t total = static_cast<int64_t>(N) * (B - 1) * r;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int c = static_cast<int>(i % r);
+    const int64_t np = i / r;  // n * (B-1) + p
+    const int64_t n = np / (B - 1), p = np % (B - 1);
+    const int64_t row = n * B + p;
+    const float v = hp[row * 2 * r + c] + hp[(row + 1) * 2 * r + r + c];
+    store_act1<kBf16>(s, i, v);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const GemmArgs& args, bool is_bf16, int BN, int split_k, cudaStream_t stream) {
+  if (split_k < 1 || split_k > 8 || (BM % split_k) != 0) return cudaErrorInvalidValue;
+  return is_bf16 ? dispatch_bn<true>(args, BN, split_k, stream) : dispatch_bn<false>(args, BN, split_k, stream);
+}
+
+cudaError_t launch_pair_combine(const float* hp, void* s, bool is_bf16, int N, int B, int r, cudaStream_t stream) {
+  const int64_t total = static_cast<int64_t>(N) * (B - 1) * r;
+  const int threads = 256;
+  const int blocks = static_cast<int>(std::min<int64_t>((total + threads - 1) / threads, 152 * 8));
+  if (is_bf16)
+    pair_combine_kernel<true><<<blocks, threads, 0, stream>>>(hp, s, N, B, r);
+  else
+    pair_combine_kernel<false><<<blocks, threads, 0, stream>>>(hp, s, N, B, r);
+  return cudaGetLastError();
+}
+
+unsigned int* device_status_word(cudaError_t* err) {
+  void* p = nullptr;
+  *err = cudaGetSymbolAddress(&p, g_status_word);
+  return static_cast<unsigned int*>(p);
+}
+
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+bool make_tmap(CUtensorMap* map, const void* base, bool is_bf16, uint64_t rows, uint64_t cols, uint64_t pitch_elems,
+               uint32_t box_rows, const char** err) {
+  static EncodeTiled encode = nullptr;
+  if (encode == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr) {
+      *err = "cuTensorMapEncodeTiled is not available from the driver";
+      return false;
+    }
+    encode = reinterpret_cast<EncodeTiled>(fn);
+  }
+  const uint32_t esize = is_bf16 ? 2 : 4;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {pitch_elems * esize};
+  cuuint32_t box[2] = {128u / esize, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = encode(map, is_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                            const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    *err = "cuTensorMapEncodeTiled rejected a tensor map (alignment, pitch or box)";
+    return false;
+  }
+  return true;
+}
+
+}  // namespace dcoco

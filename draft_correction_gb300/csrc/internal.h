@@ -1,0 +1,99 @@
+// Host-side launchers shared between the kernel translation units and the C ABI.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace dcoco {
+
+// ------------------------------------------------------------------ top-K
+// Rows of `logits` ([rows, V], bf16 bits if is_bf16 else f32); ctas_per_row in 1..8.
+cudaError_t launch_topk(const void* logits, bool is_bf16, int rows, int V, int K, int ctas_per_row, float* vals,
+                        int32_t* ids, cudaStream_t stream);
+
+// ------------------------------------------------------------------ GEMM
+// C[m, n] = sum_k A[m, k] * B[n, k] on tcgen05 tensor cores (bf16 -> kind::f16, f32 -> kind::tf32),
+// fp32 accumulation in tensor memory, 128 x BN tiles, optional split-K across a thread-block
+// cluster, and one fused epilogue per B group.
+enum Epilogue : int {
+  EPI_F32 = 0,        // out (f32) = acc
+  EPI_ACT = 1,        // out (activation dtype) = acc
+  EPI_LN = 2,         // out (activation dtype) = LayerNorm_noaffine(acc row)   (group covers the full row)
+  EPI_SILU_BIAS = 3,  // out (activation dtype) = SiLU(acc + bias[m / bias_div, n])  (bias f32)
+};
+
+struct GemmGroup {
+  CUtensorMap b_map;  // B operand [Ng, K] (K contiguous), 128-byte swizzle, box {BK, min(BN,256)}
+  void* out;          // output base; row m, column n at out[m * ldo + n]
+  int ldo;
+  int epi;
+  int n_tiles;        // Ng / BN
+};
+
+struct GemmArgs {
+  CUtensorMap a_map;        // A [M, K] tiled (box {BK, 128}), or the gather table [rows, K] (box {BK, 1})
+  const int32_t* gather;    // non-null: A row m is table row gather[m]
+  int gather_limit;         // rows of the gather table (ids outside [0, limit) are replaced by 0)
+  int M, K;
+  int n_groups;             // 1 or 2
+  GemmGroup g[2];
+  const float* bias;        // EPI_SILU_BIAS
+  int bias_div, ld_bias;
+  float ln_eps;
+  unsigned int* status;
+};
+
+// Encodes a 2-D tensor map over a row-major [rows, cols] matrix with the given row pitch (elements).
+// box_rows = 1 gives a gather4 map.
+bool make_tmap(CUtensorMap* map, const void* base, bool is_bf16, uint64_t rows, uint64_t cols, uint64_t pitch_elems,
+               uint32_t box_rows, const char** err);
+
+// BN in {32, 64, 128, 256, 512}; split_k >= 1 (BN <= 256 when split_k > 1).
+cudaError_t launch_gemm(const GemmArgs& args, bool is_bf16, int BN, int split_k, cudaStream_t stream);
+
+// s[n, p, :] = act(hp[n, p, 0:r] + hp[n, p+1, r:2r]), hp [N, B, 2r] f32, s [N, B-1, r] activation dtype.
+cudaError_t launch_pair_combine(const float* hp, void* s, bool is_bf16, int N, int B, int r, cudaStream_t stream);
+
+// ------------------------------------------------------------------ scores
+struct ScoreArgs {
+  const void* uz;       // [N, B, K, H] activation dtype
+  const void* vz;
+  const float* wsp;     // [N, B-1, H]
+  const float* vals;    // [N, B, K]
+  const void* u_a;      // [H] weight dtype
+  const void* u_b;
+  const void* b1;
+  const void* w2;
+  const void* b2;       // [1]
+  float* S;             // [N, B-1, K, K]
+  int N, B, K, H;
+};
+cudaError_t launch_scores(const ScoreArgs& a, bool is_bf16, cudaStream_t stream);
+
+// ------------------------------------------------------------------ walk + verify
+struct SelectVerifyArgs {
+  // walk (skipped when S == nullptr: `draft` is then read as the block to verify)
+  const float* S;
+  const float* vals;
+  const int32_t* ids;
+  int32_t* k_sel;
+  int32_t* tokens;       // written by the walk, read by verification
+  // verification (skipped when mode < 0)
+  int mode;              // 0 greedy, 1 stochastic, -1 none
+  const int32_t* draft;  // block to verify when there is no walk
+  const int32_t* t;
+  const float* q;
+  const float* u;
+  int32_t* accept_len;
+  int32_t* committed;
+  int32_t* n_commit;
+  int32_t* near_tie;
+  int N, B, K, V;
+};
+cudaError_t launch_select_verify(const SelectVerifyArgs& a, cudaStream_t stream);
+
+// ------------------------------------------------------------------ status word
+unsigned int* device_status_word(cudaError_t* err);
+
+}  // namespace dcoco

@@ -1,0 +1,215 @@
+// a5. Prefix-first greedy walk and a6. verification of the corrected block.
+//
+// Walk (Two Delta blog, "Select using the realized token identities"; jaehun.me review of
+// arXiv 2610.12570 §3.3): slot 0 keeps the drafter's top candidate, every later slot takes
+// the best-scoring successor of the candidate actually chosen before it.  It is the only
+// sequential step: one warp per stream, the stream's score grid staged in shared memory,
+// each step a warp argmax over the K successors (ties to the lower candidate index).
+//
+// Verification (review §3.1, App. D):
+//  greedy      accept while the draft equals the verifier's greedy token; commit the
+//              accepted prefix and the verifier's token at the first rejection.
+//  stochastic  the corrected draft is a point-mass proposal, so slot j is accepted with
+//              probability q_j(y_j) (u < q), and the first rejection draws from the residual
+//              q(v) 1[v != y_j] / (1 - q(y_j)) by inverse CDF in vocabulary order.  Running
+//              sums are in float64: each thread sums one contiguous chunk of the row, the
+//              chunk totals are prefixed in chunk order, and only the chunk holding the
+//              crossing is rescanned, with the same additions.
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace dcoco {
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int kMaxB = 64;
+constexpr int kStageFloats = 8 * 1024;  // score grid staged in shared memory up to 32 KB
+constexpr unsigned kFull = 0xFFFFFFFFu;
+
+__device__ __forceinline__ uint64_t warp_max_u64(uint64_t v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const uint64_t w = __shfl_xor_sync(kFull, v, o);
+    v = w > v ? w : v;
+  }
+  return v;
+}
+
+// argmax over row[0..K) (K <= 64): largest value, lowest index on ties, NaN lowest.
+__device__ __forceinline__ int warp_argmax(const float* row, int K, int lane) {
+  uint64_t k0 = lane < K ? make_key(__float_as_uint(row[lane]), lane) : 0ull;
+  uint64_t k1 = lane + 32 < K ? make_key(__float_as_uint(row[lane + 32]), lane + 32) : 0ull;
+  return static_cast<int>(key_index(warp_max_u64(k0 > k1 ? k0 : k1)));
+}
+
+__global__ void __launch_bounds__(kThreads) select_verify_kernel(const SelectVerifyArgs a) {
+  __shared__ float s_S[kStageFloats];
+  __shared__ int32_t s_draft[kMaxB];
+  __shared__ int s_A;
+  __shared__ double s_part[kThreads];
+  __shared__ double s_pre[kThreads];
+  __shared__ int s_pick;
+  __shared__ double s_R, s_target;
+
+  const int n = blockIdx.x;
+  const int B = a.B, K = a.K, V = a.V;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+
+  // ------------------------------------------------------------------ walk
+  if (a.S != nullptr) {
+    const size_t grid_floats = static_cast<size_t>(B - 1) * K * K;
+    const float* Sn = a.S + static_cast<size_t>(n) * grid_floats;
+    const bool staged = grid_floats <= static_cast<size_t>(kStageFloats);
+    if (staged) {
+      for (size_t i = threadIdx.x; i < grid_floats; i += kThreads) s_S[i] = Sn[i];
+    }
+    __syncthreads();
+    if (warp == 0) {
+      const float* src = staged ? s_S : Sn;
+      const int32_t* idn = a.ids + static_cast<size_t>(n) * B * K;
+      int k = warp_argmax(a.vals + static_cast<size_t>(n) * B * K, K, lane);
+      if (lane == 0) {
+        a.k_sel[static_cast<size_t>(n) * B] = k;
+        s_draft[0] = idn[k];
+      }
+      for (int p = 0; p + 1 < B; ++p) {
+        k = warp_argmax(src + (static_cast<size_t>(p) * K + k) * K, K, lane);
+        if (lane == 0) {
+          a.k_sel[static_cast<size_t>(n) * B + p + 1] = k;
+          s_draft[p + 1] = idn[static_cast<size_t>(p + 1) * K + k];
+        }
+      }
+      __syncwarp();
+      for (int j = lane; j < B; j += 32) a.tokens[static_cast<size_t>(n) * B + j] = s_draft[j];
+    }
+  } else if (a.mode >= 0) {
+    for (int j = threadIdx.x; j < B; j += kThreads) s_draft[j] = a.draft[static_cast<size_t>(n) * B + j];
+  }
+  __syncthreads();
+  if (a.mode < 0) return;
+
+  // ------------------------------------------------------------------ accept length
+  if (warp == 0) {
+    uint64_t acc_mask = 0;  // bit j set when slot j is accepted
+    for (int base = 0; base < B; base += 32) {
+      const int j = base + lane;
+      bool ok = false;
+      if (j < B) {
+        const int32_t y = s_draft[j];
+        if (a.mode == 0) {
+          ok = (y == a.t[static_cast<size_t>(n) * (B + 1) + j]);
+        } else {
+          const float uq = a.u[(static_cast<size_t>(n) * (B + 1) + j) * 2];
+          const float qy = (y >= 0 && y < V) ? a.q[(static_cast<size_t>(n) * (B + 1) + j) * V + y] : 0.f;
+          ok = uq < qy;
+        }
+      }
+      acc_mask |= static_cast<uint64_t>(__ballot_sync(kFull, ok)) << base;
+    }
+    if (lane == 0) {
+      const uint64_t rej = ~acc_mask;  // bits >= B are set too
+      s_A = (rej == 0) ? 64 : __ffsll(static_cast<long long>(rej)) - 1;
+      if (s_A > B) s_A = B;
+    }
+  }
+  __syncthreads();
+  const int A = s_A;
+  int32_t* com = a.committed + static_cast<size_t>(n) * (B + 1);
+
+  if (a.mode == 0) {
+    for (int j = threadIdx.x; j <= B; j += kThreads)
+      com[j] = j < A ? s_draft[j] : (j == A ? a.t[static_cast<size_t>(n) * (B + 1) + A] : -1);
+    if (threadIdx.x == 0) {
+      a.accept_len[n] = A;
+      a.n_commit[n] = A + 1;
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------------ stochastic draw
+  // Row A of q: the residual at the first rejected slot (excluding its draft token), or the
+  // bonus position B (nothing excluded) when every slot was accepted.
+  const int excl = A < B ? s_draft[A] : -1;
+  const float* row = a.q + (static_cast<size_t>(n) * (B + 1) + A) * V;
+  const double u1 = static_cast<double>(a.u[(static_cast<size_t>(n) * (B + 1) + A) * 2 + 1]);
+  const int chunk = (V + kThreads - 1) / kThreads;
+  const int c0 = min(V, static_cast<int>(threadIdx.x) * chunk), c1 = min(V, c0 + chunk);
+  double part = 0.0;
+  for (int v = c0; v < c1; ++v)
+    if (v != excl) part += static_cast<double>(row[v]);
+  s_part[threadIdx.x] = part;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double run = 0.0;
+    for (int t = 0; t < kThreads; ++t) {
+      s_pre[t] = run;
+      run += s_part[t];
+    }
+    const double R = run, target = u1 * R;
+    int pick = -1;
+    if (R > 0.0) {
+      for (int t = 0; t < kThreads; ++t) {
+        if (s_part[t] > 0.0 && target - s_pre[t] < s_part[t]) {
+          pick = t;
+          break;
+        }
+      }
+    }
+    s_R = R;
+    s_target = target;
+    s_pick = pick;
+  }
+  __syncthreads();
+  const int pick = s_pick;
+  const double R = s_R, target = s_target;
+  if (pick >= 0 && static_cast<int>(threadIdx.x) == pick) {
+    // Rescan the crossing chunk with the same additions as its partial sum: a crossing exists
+    // because the chunk's full sum exceeds target - prefix.
+    const double d = target - s_pre[pick];
+    double run = 0.0, before = 0.0;
+    int v_pick = c1 - 1;
+    for (int v = c0; v < c1; ++v) {
+      if (v == excl) continue;
+      before = run;
+      run += static_cast<double>(row[v]);
+      if (run > d) {
+        v_pick = v;
+        break;
+      }
+    }
+    const double tol = 1e-9 * R;
+    const bool near = fabs(s_pre[pick] + run - target) <= tol || fabs(s_pre[pick] + before - target) <= tol;
+    com[A] = v_pick;
+    if (a.near_tie) a.near_tie[n] = near ? 1 : 0;
+  } else if (pick < 0 && threadIdx.x == 0) {
+    // R <= 0: no residual mass, the excluded token stays.  Otherwise the crossing was lost to
+    // rounding at the end of the row: the last token with mass.
+    int v = excl;
+    if (R > 0.0) {
+      for (int w = V - 1; w >= 0; --w)
+        if (w != excl && row[w] > 0.f) {
+          v = w;
+          break;
+        }
+    }
+    com[A] = v;
+    if (a.near_tie) a.near_tie[n] = 1;
+  }
+  if (threadIdx.x == 0) {
+    a.accept_len[n] = A;
+    a.n_commit[n] = A + 1;
+  }
+  for (int j = threadIdx.x; j < A; j += kThreads) com[j] = s_draft[j];
+  for (int j = A + 1 + static_cast<int>(threadIdx.x); j <= B; j += kThreads) com[j] = -1;
+}
+
+}  // namespace
+
+cudaError_t launch_select_verify(const SelectVerifyArgs& a, cudaStream_t stream) {
+  select_verify_kernel<<<a.N, kThreads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace dcoco

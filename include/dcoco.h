@@ -1,0 +1,190 @@
+/*
+ * dcoco.h -- C ABI of the DCOCO per-cycle correction hot path on one GB300 GPU.
+ *
+ * DCOCO (DFlash Contextual Corrector) re-selects a parallel drafter's B-slot block
+ * from the drafter's own top-K candidates: it scores every candidate pair of
+ * neighbouring slots with a small shared network and walks the block left to right,
+ * then the verifier accepts the longest matching prefix.  Sources: Two Delta, "Two
+ * Delta makes NVIDIA Nemotron 3.5 Super even faster with DCOCO" ("How DCOCO works");
+ * jaehun.me review of arXiv 2610.12570, "Contextual Correction of Parallel Drafts for
+ * Speculative Decoding", §3.1-§3.3 and App. D.
+ *
+ * Conventions (all entry points):
+ *  - Return value: a dcoco_status.  Nothing aborts; no C++ exception crosses the ABI.
+ *    On failure, dcoco_last_error() (per host thread) describes the first problem found.
+ *  - Tensor pointers are caller-owned DEVICE memory on the current CUDA device, dense
+ *    row-major, 16-byte aligned, and never alias one another.  The library allocates
+ *    nothing: scratch comes from a caller-supplied workspace of at least the size the
+ *    matching *_workspace_size() call returns (16-byte aligned, contents ignored).
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Work is enqueued
+ *    asynchronously; no entry point synchronises.  Argument errors are reported before
+ *    anything is enqueued; launch errors are reported as DCOCO_ERR_CUDA.
+ *  - Kernel-side faults never trap: a bounded wait that gives up, or a token id outside
+ *    [0, V) reaching the gather, sets a bit in the device status word
+ *    (dcoco_device_status).
+ *  - Shape limits: N >= 1, B >= 2, 1 <= K <= 64, K <= V, B <= 64.  Corrector width r in
+ *    {32, 64, 128, 256, 512}; MLP width H a multiple of 64; d and E multiples of 8.
+ *  - Index conventions: stream n in [0,N), slot i in [0,B), candidate k in [0,K),
+ *    transition p in [0,B-1) scoring slot p -> slot p+1.
+ */
+#ifndef DCOCO_H_
+#define DCOCO_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DCOCO_OK = 0,
+  DCOCO_ERR_INVALID_ARG = 1, /* null pointer, bad shape, misaligned pointer */
+  DCOCO_ERR_UNSUPPORTED = 2, /* shape or dtype outside the supported set */
+  DCOCO_ERR_WORKSPACE = 3,   /* workspace missing or smaller than required */
+  DCOCO_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed */
+  DCOCO_ERR_TIMEOUT = 5      /* device status word reports a bounded wait that gave up */
+} dcoco_status;
+
+typedef enum { DCOCO_F32 = 0, DCOCO_BF16 = 1 } dcoco_dtype;
+
+typedef enum { DCOCO_VERIFY_GREEDY = 0, DCOCO_VERIFY_STOCHASTIC = 1 } dcoco_verify_mode;
+
+/*
+ * Corrector parameters, shared across slots and transitions (jaehun.me review of
+ * arXiv 2610.12570, §3.2).  Every pointer has element type `dtype`; matrices are
+ * [rows, cols] row-major ("out x in").
+ *   W_e    [r, E]   projects the candidate's frozen token embedding
+ *   W_h    [r, d]   projects the slot's drafter hidden state
+ *   W_f    [r, 2r]  fuses [b; g]: columns 0..r-1 act on b, r..2r-1 on g
+ *   W_pair [r, 2d]  pair state from [h_p; h_{p+1}]: columns 0..d-1 act on h_p
+ *   U, V, W [H, r]  first MLP layer blocks on z_{p,a}, z_{p+1,b} and s_p
+ *   u_a, u_b, b1, w2 [H]; b2 [1]   logit weights, first-layer bias, output layer
+ */
+typedef struct dcoco_weights {
+  int dtype; /* dcoco_dtype */
+  int d, E, r, H;
+  const void* W_e;
+  const void* W_h;
+  const void* W_f;
+  const void* W_pair;
+  const void* U;
+  const void* V;
+  const void* W;
+  const void* u_a;
+  const void* u_b;
+  const void* b1;
+  const void* w2;
+  const void* b2;
+} dcoco_weights;
+
+/* Library version (major*10000 + minor*100 + patch). */
+int dcoco_version(void);
+
+/* Description of the last failure on this host thread ("" if none). */
+const char* dcoco_last_error(void);
+
+/*
+ * Reads and clears the device status word of the current device (DEV_* bits: 1 TMA
+ * wait gave up, 2 MMA commit wait gave up, 4 accumulator wait gave up, 8 gathered id
+ * out of range).  Synchronises `stream` first.  Returns DCOCO_ERR_TIMEOUT if any
+ * timeout bit was set, DCOCO_OK otherwise; *bits receives the raw word (may be NULL).
+ */
+int dcoco_device_status(void* stream, uint32_t* bits);
+
+/*
+ * Tuning knob: thread blocks per logits row in dcoco_topk (1..8; 0 = automatic).
+ * Process-wide; returns the previous value.
+ */
+int dcoco_set_topk_split(int ctas_per_row);
+
+/*
+ * a1. Top-K candidate retention (Two Delta blog, "Keep the leading candidates";
+ * review §3.2): for every row (n,i) of `logits` [N, B, V] (dtype bf16 or f32), the K
+ * largest values, sorted by value descending with equal values ordered by ascending
+ * token id.  NaN ranks as -inf and is reported as -inf; -0 is reported as +0.
+ *   vals [N, B, K] float32   the kept logits l_i(k) (exact widening of the input)
+ *   ids  [N, B, K] int32     the token ids c_ik
+ * Deterministic: the result does not depend on scheduling.  No workspace.
+ */
+int dcoco_topk(const void* logits, int dtype, int N, int B, int V, int K, float* vals, int32_t* ids, void* stream);
+
+/*
+ * a2. Candidate representation (Two Delta blog, "Score neighboring candidates in
+ * parallel"; review §3.2) with the first MLP layer's per-candidate blocks:
+ *   b_ik = LN(W_e Emb[c_ik]),  g_i = LN(W_h h_i)   (non-affine LayerNorm, eps 1e-5)
+ *   z_ik = SiLU(W_f [b_ik; g_i])
+ *   uz = U z_ik,  vz = V z_ik
+ *   ids [N, B, K] int32; emb [V, E] (w->dtype); h [N, B, d] (w->dtype)
+ *   uz, vz [N, B, K, H], element type w->dtype (bf16 rounding of the fp32 result)
+ */
+size_t dcoco_candidate_repr_workspace_size(const dcoco_weights* w, int N, int B, int K);
+int dcoco_candidate_repr(const int32_t* ids, const void* emb, int V, const void* h, const dcoco_weights* w, int N,
+                         int B, int K, void* uz, void* vz, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * a3. Pair state (Two Delta blog, the pair context s_p; review §3.2):
+ *   s_p = W_pair [h_p; h_{p+1}],  ws_pair[n, p] = W s_p      for p in [0, B-1)
+ *   h [N, B, d] (w->dtype) -> ws_pair [N, B-1, H] float32
+ */
+size_t dcoco_pair_state_workspace_size(const dcoco_weights* w, int N, int B);
+int dcoco_pair_state(const void* h, const dcoco_weights* w, int N, int B, float* ws_pair, void* workspace,
+                     size_t workspace_bytes, void* stream);
+
+/*
+ * a4. Transition scores (Two Delta blog, "Score neighboring candidates in parallel";
+ * review §3.2), all (B-1)K^2 at once, unnormalised:
+ *   S[n,p,a,b] = l_{p+1}(b) + w2 . SiLU(uz[n,p,a] + vz[n,p+1,b] + ws_pair[n,p]
+ *                                      + u_a l_p(a) + u_b l_{p+1}(b) + b1) + b2
+ *   uz, vz [N, B, K, H] (w->dtype); ws_pair [N, B-1, H] f32; vals [N, B, K] f32
+ *   S [N, B-1, K, K] float32, predecessor a major, successor b minor.
+ */
+int dcoco_score_transitions(const void* uz, const void* vz, const float* ws_pair, const float* vals,
+                            const dcoco_weights* w, int N, int B, int K, float* S, void* stream);
+
+/*
+ * a5. Prefix-first greedy walk (Two Delta blog, "Select using the realized token
+ * identities"; review §3.3): k_0 = argmax_k vals[n,0,k]; k_{p+1} = argmax_b S[n,p,k_p,b];
+ * ties go to the lower candidate index, NaN ranks lowest.
+ *   k_sel [N, B] int32, tokens [N, B] int32 (= ids[n, i, k_sel[n,i]])
+ */
+int dcoco_select(const float* S, const float* vals, const int32_t* ids, int N, int B, int K, int32_t* k_sel,
+                 int32_t* tokens, void* stream);
+
+/*
+ * a6. Verification of the corrected draft (review §3.1 and App. D).
+ *  GREEDY: t [N, B+1] int32 verifier greedy tokens; slot j is accepted while
+ *    draft[j] == t[j]; A = accepted prefix length; commits draft[0..A-1] then t[A].
+ *  STOCHASTIC (point-mass proposal): q [N, B+1, V] f32 verifier probabilities,
+ *    u [N, B+1, 2] f32 uniforms in [0,1).  Slot j is accepted iff u[j,0] < q[j, draft[j]];
+ *    at the first rejection j the committed token is the smallest v != draft[j] whose
+ *    running residual mass (float64, vocabulary order) exceeds u[j,1] * R with
+ *    R = sum_{v != draft[j]} q[j, v]; if all B are accepted the bonus token is drawn the
+ *    same way from q[B] (no exclusion) with u[B,1].  R <= 0 commits draft[j].
+ *  Outputs: accept_len [N], committed [N, B+1] (-1 after the last committed token),
+ *    n_commit [N] = accept_len + 1, all int32.  near_tie [N] int32 (may be NULL,
+ *    stochastic only): 1 where u*R lay within 1e-9 R of a step of the running sum.
+ *  Unused inputs of the other mode may be NULL.
+ */
+int dcoco_verify(int mode, const int32_t* draft, const int32_t* t, const float* q, const float* u, int N, int B, int V,
+                 int32_t* accept_len, int32_t* committed, int32_t* n_commit, int32_t* near_tie, void* stream);
+
+/*
+ * One whole correction cycle a1..a6 on one stream: top-K, candidate representation,
+ * pair state, transition scores, walk and verification, with intermediates in the
+ * workspace.  Inputs as above; `t` (greedy) or `q`,`u` (stochastic) per `mode`.
+ * Outputs (any may be NULL except tokens, accept_len, committed, n_commit):
+ *   vals, ids [N,B,K]; S [N,B-1,K,K]; k_sel, tokens [N,B]; accept_len, n_commit [N];
+ *   committed [N,B+1]; near_tie [N].
+ */
+size_t dcoco_cycle_workspace_size(const dcoco_weights* w, int N, int B, int K);
+int dcoco_cycle(const void* logits, int V, const void* emb, const void* h, const dcoco_weights* w, int N, int B, int K,
+                int mode, const int32_t* t, const float* q, const float* u, float* vals, int32_t* ids, float* S,
+                int32_t* k_sel, int32_t* tokens, int32_t* accept_len, int32_t* committed, int32_t* n_commit,
+                int32_t* near_tie, void* workspace, size_t workspace_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DCOCO_H_ */

@@ -1,0 +1,103 @@
+"""The C ABI library loads, exports every declared entry point, and rejects bad arguments
+on the host before touching the GPU (runs without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import draft_correction_gb300 as dc
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "dcoco.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dcoco_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from draft_correction_gb300 import build
+    build.build()
+    return dc.lib()
+
+
+def test_header_declares_the_hot_path():
+    names = declared_functions()
+    for want in ("dcoco_topk", "dcoco_candidate_repr", "dcoco_pair_state", "dcoco_score_transitions",
+                 "dcoco_select", "dcoco_verify", "dcoco_cycle"):
+        assert want in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+    assert set(declared_functions()) == set(dc._SIGNATURES), "binding signatures out of sync with the header"
+
+
+def test_version_and_error_string(L):
+    assert L.dcoco_version() >= 100
+    assert isinstance(L.dcoco_last_error(), bytes)
+
+
+FAKE = ctypes.c_void_p(0x10000)        # never dereferenced: validation fails first
+MISALIGNED = ctypes.c_void_p(0x10008)
+
+
+def _weights(dtype=dc.DCOCO_BF16, d=64, E=64, r=32, H=64, ptr=0x20000):
+    return dc._Weights(dtype, d, E, r, H, *([ptr] * len(dc.WEIGHT_FIELDS)))
+
+
+def test_topk_argument_errors(L):
+    assert L.dcoco_topk(None, 1, 1, 4, 100, 3, FAKE, FAKE, None) == 1
+    assert "logits" in L.dcoco_last_error().decode()
+    assert L.dcoco_topk(FAKE, 7, 1, 4, 100, 3, FAKE, FAKE, None) == 2     # dtype
+    assert L.dcoco_topk(FAKE, 1, 1, 4, 100, 65, FAKE, FAKE, None) == 1    # K > 64
+    assert L.dcoco_topk(FAKE, 1, 1, 4, 10, 11, FAKE, FAKE, None) == 1     # K > V
+    assert L.dcoco_topk(MISALIGNED, 1, 1, 4, 100, 3, FAKE, FAKE, None) == 1
+    assert L.dcoco_topk(FAKE, 1, 300, 300, 100, 3, FAKE, FAKE, None) == 2  # too many rows
+
+
+def test_weight_and_shape_errors(L):
+    w = _weights(r=48)
+    assert L.dcoco_candidate_repr(FAKE, FAKE, 100, FAKE, ctypes.byref(w), 1, 4, 3, FAKE, FAKE, FAKE, 1 << 30,
+                                  None) == 2
+    w = _weights(H=96)
+    assert L.dcoco_pair_state(FAKE, ctypes.byref(w), 1, 4, FAKE, FAKE, 1 << 30, None) == 2
+    w = _weights()
+    w.U = None
+    assert L.dcoco_score_transitions(FAKE, FAKE, FAKE, FAKE, ctypes.byref(w), 1, 4, 3, FAKE, None) == 1
+    w = _weights()
+    assert L.dcoco_score_transitions(FAKE, FAKE, FAKE, FAKE, ctypes.byref(w), 1, 1, 3, FAKE, None) == 1  # B < 2
+    assert L.dcoco_select(FAKE, FAKE, FAKE, 1, 4, 0, FAKE, FAKE, None) == 1                             # K = 0
+
+
+def test_workspace_errors(L):
+    w = _weights()
+    need = L.dcoco_candidate_repr_workspace_size(ctypes.byref(w), 2, 4, 3)
+    assert need > 0
+    assert L.dcoco_candidate_repr(FAKE, FAKE, 100, FAKE, ctypes.byref(w), 2, 4, 3, FAKE, FAKE, FAKE, need - 1,
+                                  None) == 3
+    assert L.dcoco_candidate_repr(FAKE, FAKE, 100, FAKE, ctypes.byref(w), 2, 4, 3, FAKE, FAKE, None, need,
+                                  None) == 3
+    need = L.dcoco_pair_state_workspace_size(ctypes.byref(w), 2, 4)
+    assert L.dcoco_pair_state(FAKE, ctypes.byref(w), 2, 4, FAKE, FAKE, need - 1, None) == 3
+    need = L.dcoco_cycle_workspace_size(ctypes.byref(w), 2, 4, 3)
+    assert need >= L.dcoco_candidate_repr_workspace_size(ctypes.byref(w), 2, 4, 3)
+    args = [FAKE, 100, FAKE, FAKE, ctypes.byref(w), 2, 4, 3, 0, FAKE, None, None] + [None] * 4 + [FAKE] * 4 + [None]
+    assert L.dcoco_cycle(*args, FAKE, need - 1, None) == 3
+
+
+def test_verify_errors(L):
+    assert L.dcoco_verify(3, FAKE, FAKE, None, None, 1, 4, 0, FAKE, FAKE, FAKE, None, None) == 1
+    assert L.dcoco_verify(0, FAKE, None, None, None, 1, 4, 0, FAKE, FAKE, FAKE, None, None) == 1   # greedy, no t
+    assert L.dcoco_verify(1, FAKE, None, FAKE, None, 1, 4, 10, FAKE, FAKE, FAKE, None, None) == 1  # no u
+    assert L.dcoco_verify(0, FAKE, FAKE, None, None, 1, 65, 0, FAKE, FAKE, FAKE, None, None) == 1  # B > 64
+
+
+def test_topk_split_knob(L):
+    prev = L.dcoco_set_topk_split(3)
+    assert L.dcoco_set_topk_split(prev) == 3

@@ -1,0 +1,146 @@
+"""Whole-cycle parity (a1..a6 through dcoco_cycle) against the float64 oracle.
+
+Small configurations are compared in full.  At the full workload sizes (the launch
+configuration the benchmark times) top-K is compared on every row and the rest on a
+sample of streams that the oracle recomputes end to end.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import draft_correction_gb300 as dc
+import oracle
+import workloads as wl
+from conftest import GOLDEN
+from helpers import assert_scores_close, case, compare_walk, f64, w64
+from test_gpu_kernels import SMALL_BF16, SMALL_R256, SMALL_R512
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from draft_correction_gb300 import build
+    build.build()
+    dc.lib()
+    yield
+    assert dc.device_status() == 0, "a kernel reported a timeout or a bad index"
+
+
+def sample_streams(N):
+    return list(range(N)) if N <= 4 else sorted({0, N // 2, N - 1})
+
+
+def run_cycle_and_compare(cfg, variant=None, logits=None, mode=dc.VERIFY_GREEDY):
+    c = case(cfg, variant)
+    logits = c["logits"] if logits is None else logits
+    W = w64(c["w"], cfg)
+    sam = sample_streams(cfg.N)
+    # top-K parity on every row up to 512 rows, on the sampled streams beyond that
+    rows = list(range(cfg.N)) if cfg.N * cfg.B <= 512 else sam
+    vals_r, ids_r = oracle.topk(f64(logits[rows], cfg), cfg.K)
+    pos = [rows.index(n) for n in sam]
+    vals, ids = vals_r[pos], ids_r[pos]
+    h64 = f64(c["h"][sam], cfg)
+    # the oracle sees exactly the embedding rows it gathers (never the whole table in float64)
+    uniq, inv = np.unique(ids, return_inverse=True)
+    rep = oracle.candidate_repr(inv.reshape(ids.shape), f64(c["emb"][uniq], cfg), h64, W)
+    s = oracle.pair_state(h64, W)
+    S_ref = oracle.transition_scores(rep["z"], s, vals, W)
+    k_ref, tok_ref = oracle.select(S_ref, vals, ids)
+    # the drafter's top-1 stands in as the draft of streams the oracle does not walk
+    draft = np.stack([np.argmax(f64(logits[n], cfg), axis=1) for n in range(cfg.N)]).astype(np.int64)
+    draft[sam] = tok_ref
+    if mode == dc.VERIFY_GREEDY:
+        t = wl.verifier_tokens(cfg, draft)
+        ver_ref = oracle.verify_greedy(tok_ref, t[sam])
+        extra = {"t": dc.to_device(t, "i32")}
+    else:
+        q = wl.verifier_probs(cfg)
+        u = wl.uniforms(cfg)
+        ver_ref = oracle.verify_stochastic(tok_ref, q[sam], u[sam])
+        extra = {"q": dc.to_device(q, "f32"), "u": dc.to_device(u, "f32")}
+
+    w = dc.CorrectorWeights.from_numpy(c["w"], cfg.dtype)
+    cyc = dc.Cycle(w, cfg.N, cfg.B, cfg.K, cfg.V)
+    out = cyc.run(dc.to_device(logits, cfg.dtype), dc.to_device(c["emb"], cfg.dtype), dc.to_device(c["h"], cfg.dtype),
+                  mode=mode, **extra)
+    torch.cuda.synchronize()
+    g = {k: v.cpu().numpy() for k, v in out.items()}
+
+    np.testing.assert_array_equal(g["ids"][rows], ids_r)
+    np.testing.assert_array_equal(g["vals"][rows].astype(np.float64), vals_r)
+    assert_scores_close(g["S"][sam], S_ref)
+    near = compare_walk(g["k_sel"][sam], k_ref, S_ref, vals)
+    exact = [i for i, n in enumerate(sam) if np.array_equal(g["k_sel"][n], k_ref[i])]
+    assert len(exact) >= len(sam) - near
+    for i in exact:
+        n = sam[i]
+        np.testing.assert_array_equal(g["tokens"][n], tok_ref[i])
+        if mode == dc.VERIFY_STOCHASTIC and (ver_ref["near_tie"][i] or g["near_tie"][n]):
+            continue
+        assert g["accept_len"][n] == ver_ref["accept_len"][i]
+        assert g["n_commit"][n] == ver_ref["n_commit"][i]
+        np.testing.assert_array_equal(g["committed"][n], ver_ref["committed"][i])
+    return g, {"k": k_ref, "tokens": tok_ref, "S": S_ref}
+
+
+@pytest.mark.parametrize("variant", [None, "delta_zero", "amplified"])
+def test_cycle_tiny(variant):
+    run_cycle_and_compare(wl.TINY, variant)
+
+
+def test_cycle_tiny_zero_correction_is_drafter_argmax():
+    g, _ = run_cycle_and_compare(wl.TINY, "delta_zero")
+    np.testing.assert_array_equal(g["k_sel"], np.zeros_like(g["k_sel"]))  # sorted grid: argmax is candidate 0
+
+
+def _worked_grid():
+    rows = []
+    for line in open(os.path.join(GOLDEN, "worked_example.txt")):
+        p = line.split()
+        if p and p[0] == "slot":
+            rows.append([float(v) for v in p[3::2]])
+    return rows
+
+
+def test_cycle_worked_example_printed_logits():
+    """The pages' B=4, K=3 grid as drafter logits with the output layer zeroed: the walk
+    returns the per-slot argmax (These, keys, are, missing -> ids 0, 4, 7, 9)."""
+    grid = _worked_grid()
+    cfg = wl.TINY
+    g, ref = run_cycle_and_compare(cfg, "delta_zero", logits=wl.grid_logits(grid, V=cfg.V))
+    assert list(g["tokens"][0]) == [0, 4, 7, 9]
+
+
+@pytest.mark.parametrize("cfg", [SMALL_BF16, SMALL_R256, SMALL_R512, SMALL_BF16.replace(K=1)],
+                         ids=lambda c: f"{c.name}_K{c.K}")
+@pytest.mark.parametrize("variant", [None, "amplified"])
+def test_cycle_small(cfg, variant):
+    run_cycle_and_compare(cfg, variant)
+
+
+@pytest.mark.parametrize("cfg", [SMALL_R256.replace(N=5), SMALL_BF16], ids=lambda c: c.name)
+def test_cycle_small_stochastic(cfg):
+    run_cycle_and_compare(cfg, None, mode=dc.VERIFY_STOCHASTIC)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("cfg", [wl.QWEN3_8B, wl.HEADLINE], ids=lambda c: c.name)
+def test_cycle_full_size(cfg):
+    run_cycle_and_compare(cfg)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("n,b,k,mode", [(4, 8, 4, dc.VERIFY_STOCHASTIC), (128, 16, 16, dc.VERIFY_GREEDY),
+                                        (16, 8, 16, dc.VERIFY_STOCHASTIC)])
+def test_cycle_sweep_points(n, b, k, mode):
+    cfg = wl.HEADLINE.replace(name=f"sweep_n{n}_b{b}_k{k}", N=n, B=b, K=k)
+    run_cycle_and_compare(cfg, mode=mode)
+
+
+@pytest.mark.slow
+def test_cycle_large():
+    run_cycle_and_compare(wl.LARGE)

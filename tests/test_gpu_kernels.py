@@ -1,0 +1,193 @@
+"""Per-step parity of the CUDA library against the float64 oracle (needs a GB300).
+
+Every call goes through the C ABI (ctypes binding); inputs come from the seeded
+generators and are handed to both sides bit-identically.
+"""
+import numpy as np
+import pytest
+import torch
+
+import draft_correction_gb300 as dc
+import oracle
+import workloads as wl
+from helpers import (assert_intermediate_close, assert_scores_close, case, compare_walk, f64, w64)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from draft_correction_gb300 import build
+    build.build()
+    dc.lib()
+    yield
+    assert dc.device_status() == 0, "a kernel reported a timeout or a bad index"
+
+
+def _bf16_rows(x32):
+    return wl.f32_to_bf16(np.asarray(x32, dtype=np.float32))
+
+
+def run_topk(x, dtype, K):
+    t = dc.to_device(x, dtype)
+    vals, ids = dc.topk(t, K)
+    torch.cuda.synchronize()
+    return vals.cpu().numpy(), ids.cpu().numpy()
+
+
+def check_topk(x, dtype, K):
+    vals, ids = run_topk(x, dtype, K)
+    rv, ri = oracle.topk(wl.to_f64(x, dtype), K)
+    np.testing.assert_array_equal(ids, ri)
+    np.testing.assert_array_equal(vals.astype(np.float64), rv)
+    assert not np.signbit(vals[vals == 0]).any()
+
+
+# ---------------------------------------------------------------- a1 top-K
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("V,K", [(1024, 3), (1001, 7), (4099, 16), (64, 64), (40, 40), (20000, 1), (151936, 16),
+                                 (9, 1), (300007, 64), (131, 33)])
+def test_topk_random(dtype, V, K):
+    rng = np.random.default_rng(V * 131 + K)
+    x = rng.normal(0, 3, (3, 5, V)).astype(np.float32)
+    check_topk(_bf16_rows(x) if dtype == "bf16" else x, dtype, K)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_topk_adversarial(dtype):
+    V = 5003
+    rows = []
+    rows.append(np.full(V, 1.5, np.float32))                               # all equal: lowest K ids
+    r = np.zeros(V, np.float32); r[1::2] = -0.0; rows.append(r)            # +-0 ties
+    r = np.full(V, -np.inf, np.float32); r[[7, 4000, 5002]] = np.inf; r[[5, 6]] = np.nan; rows.append(r)
+    r = np.full(V, np.nan, np.float32); r[100] = -np.inf; rows.append(r)  # NaN ranks as -inf
+    r = np.arange(V, dtype=np.float32); rows.append(r)                     # ascending: every element inserts
+    r = -np.arange(V, dtype=np.float32); rows.append(r)                    # descending
+    r = np.random.default_rng(0).normal(0, 1, V).astype(np.float32); r[[0, V - 1]] = 50; rows.append(r)
+    r = np.round(np.random.default_rng(1).normal(0, 1, V), 0).astype(np.float32); rows.append(r)  # many ties
+    x = np.stack(rows)[None]
+    if dtype == "bf16":
+        x = _bf16_rows(x)
+        x[x == 0x7FC1] = 0x7FC0
+    for K in (1, 5, 16, 33, 64):
+        check_topk(x, dtype, K)
+
+
+@pytest.mark.parametrize("split", [1, 2, 3, 5, 8])
+def test_topk_independent_of_split(split):
+    rng = np.random.default_rng(9)
+    x = _bf16_rows(np.round(rng.normal(0, 2, (2, 3, 70001)), 1))
+    prev = dc.set_topk_split(split)
+    try:
+        check_topk(x, "bf16", 16)
+    finally:
+        dc.set_topk_split(prev)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("cfg", [wl.QWEN3_8B, wl.HEADLINE], ids=lambda c: c.name)
+def test_topk_full_size(cfg):
+    check_topk(wl.logits(cfg), cfg.dtype, cfg.K)
+
+
+# ---------------------------------------------------------------- a5 walk, a6 verify
+
+
+@pytest.mark.parametrize("N,B,K", [(3, 4, 3), (8, 16, 16), (5, 7, 33), (2, 64, 64), (2, 3, 1), (40, 16, 5)])
+def test_select_matches_oracle(N, B, K):
+    rng = np.random.default_rng(N * 1000 + B * 10 + K)
+    vals = np.round(rng.normal(0, 1, (N, B, K)), 1).astype(np.float32)
+    S = np.round(rng.normal(0, 1, (N, B - 1, K, K)), 1).astype(np.float32)
+    S[0, 0, :, 0] = np.nan
+    ids = rng.integers(0, 10 ** 6, (N, B, K)).astype(np.int32)
+    k, tok = dc.select(dc.to_device(S, "f32"), dc.to_device(vals, "f32"), dc.to_device(ids, "i32"))
+    rk, rt = oracle.select(S.astype(np.float64), vals.astype(np.float64), ids)
+    np.testing.assert_array_equal(k.cpu().numpy(), rk)
+    np.testing.assert_array_equal(tok.cpu().numpy(), rt)
+
+
+@pytest.mark.parametrize("N,B", [(1, 1), (50, 16), (7, 64), (9, 33)])
+def test_verify_greedy_matches_oracle(N, B):
+    rng = np.random.default_rng(B)
+    draft = rng.integers(0, 4, (N, B)).astype(np.int32)
+    t = rng.integers(0, 4, (N, B + 1)).astype(np.int32)
+    t[0, :B] = draft[0]                          # one fully accepted block
+    out = dc.verify(dc.to_device(draft, "i32"), t=dc.to_device(t, "i32"))
+    ref = oracle.verify_greedy(draft, t)
+    for k in ("accept_len", "committed", "n_commit"):
+        np.testing.assert_array_equal(out[k].cpu().numpy(), ref[k])
+
+
+@pytest.mark.parametrize("N,B,V", [(64, 16, 1000), (8, 8, 151936), (16, 4, 5)])
+def test_verify_stochastic_matches_oracle(N, B, V):
+    cfg = wl.HEADLINE.replace(N=N, B=B, V=V)
+    q = wl.verifier_probs(cfg)
+    u = wl.uniforms(cfg)
+    rng = np.random.default_rng(V)
+    draft = rng.integers(0, V, (N, B)).astype(np.int32)
+    # make acceptance likely at some slots: put mass on the draft token
+    for n in range(0, N, 2):
+        q[n, :B][np.arange(B), draft[n]] = 0.9
+    out = dc.verify(dc.to_device(draft, "i32"), q=dc.to_device(q, "f32"), u=dc.to_device(u, "f32"),
+                    mode=dc.VERIFY_STOCHASTIC)
+    ref = oracle.verify_stochastic(draft, q, u)
+    np.testing.assert_array_equal(out["accept_len"].cpu().numpy(), ref["accept_len"])
+    near = out["near_tie"].cpu().numpy().astype(bool) | ref["near_tie"]
+    com = out["committed"].cpu().numpy()
+    np.testing.assert_array_equal(com[~near], ref["committed"][~near])
+    assert near.sum() <= max(1, N // 20)
+
+
+# ---------------------------------------------------------------- a2, a3, a4
+
+SMALL_BF16 = wl.scaled(wl.QWEN3_8B, N=2, B=5, K=5, V=3001, d=256, E=192, r=64, H=128)
+SMALL_R256 = wl.scaled(wl.HEADLINE, N=3, B=6, K=16, V=5000, d=512, E=512, r=256, H=512)
+SMALL_R512 = wl.scaled(wl.LARGE, N=2, B=4, K=8, V=2000, d=1024, E=1024, r=512, H=1024)
+REPR_CASES = [wl.TINY, SMALL_BF16, SMALL_R256, SMALL_R512]
+
+
+def _device_case(cfg, variant=None):
+    c = case(cfg, variant)
+    dev = {"logits": dc.to_device(c["logits"], cfg.dtype), "h": dc.to_device(c["h"], cfg.dtype),
+           "emb": dc.to_device(c["emb"], cfg.dtype)}
+    w = dc.CorrectorWeights.from_numpy(c["w"], cfg.dtype)
+    return c, dev, w
+
+
+@pytest.mark.parametrize("cfg", REPR_CASES, ids=lambda c: c.name)
+def test_candidate_repr_and_pair_state(cfg):
+    c, dev, w = _device_case(cfg)
+    vals, ids = oracle.topk(f64(c["logits"], cfg), cfg.K)
+    W = w64(c["w"], cfg)
+    rep = oracle.candidate_repr(ids, f64(c["emb"], cfg), f64(c["h"], cfg), W)
+    s = oracle.pair_state(f64(c["h"], cfg), W)
+    uz, vz = dc.candidate_repr(dc.to_device(ids.astype(np.int32), "i32"), dev["emb"], dev["h"], w)
+    wsp = dc.pair_state(dev["h"], w)
+    torch.cuda.synchronize()
+    assert_intermediate_close(uz.float().cpu().numpy(), rep["z"] @ W["U"].T, "uz")
+    assert_intermediate_close(vz.float().cpu().numpy(), rep["z"] @ W["V"].T, "vz")
+    assert_intermediate_close(wsp.cpu().numpy(), s @ W["W"].T, "W s")
+
+
+@pytest.mark.parametrize("cfg", REPR_CASES + [wl.TINY.replace(K=64, V=128), SMALL_BF16.replace(K=3)],
+                         ids=lambda c: f"{c.name}_K{c.K}")
+@pytest.mark.parametrize("variant", [None, "delta_zero", "amplified"])
+def test_score_transitions(cfg, variant):
+    c, dev, w = _device_case(cfg, variant)
+    W = w64(c["w"], cfg)
+    vals, ids = oracle.topk(f64(c["logits"], cfg), cfg.K)
+    rep = oracle.candidate_repr(ids, f64(c["emb"], cfg), f64(c["h"], cfg), W)
+    s = oracle.pair_state(f64(c["h"], cfg), W)
+    S_ref = oracle.transition_scores(rep["z"], s, vals, W)
+    act = "bf16" if cfg.dtype == "bf16" else "f32"
+    to_act = (lambda a: dc.to_device(wl.f32_to_bf16(a.astype(np.float32)), "bf16")) if act == "bf16" else \
+        (lambda a: dc.to_device(a.astype(np.float32), "f32"))
+    S = dc.score_transitions(to_act(rep["z"] @ W["U"].T), to_act(rep["z"] @ W["V"].T),
+                             dc.to_device((s @ W["W"].T).astype(np.float32), "f32"),
+                             dc.to_device(vals.astype(np.float32), "f32"), w)
+    S = S.cpu().numpy()
+    assert_scores_close(S, S_ref)
+    if variant == "delta_zero":
+        np.testing.assert_array_equal(S, np.broadcast_to(vals[:, 1:, None, :], S.shape).astype(np.float32))

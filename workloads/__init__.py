@@ -17,7 +17,9 @@ bf16 tensors are carried as ``uint16`` bit patterns (numpy has no bf16 type);
 """
 from __future__ import annotations
 
+import concurrent.futures
 import dataclasses
+import os
 from typing import Dict, Iterator, Optional
 
 import numpy as np
@@ -116,20 +118,33 @@ TAG_LOGITS, TAG_HIDDEN, TAG_EMB, TAG_WEIGHTS, TAG_VERIFIER, TAG_PROBS = 1, 2, 3,
 _CHUNK = 1 << 24
 
 
-def _rng(seed: int, tag: int) -> np.random.Generator:
-    return np.random.Generator(np.random.PCG64(np.random.SeedSequence(entropy=seed, spawn_key=(tag,))))
+def _rng(seed: int, tag: int, *sub: int) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64(np.random.SeedSequence(entropy=seed, spawn_key=(tag,) + sub)))
 
 
-def _normal(rng: np.random.Generator, shape, sigma: float, dtype: str) -> np.ndarray:
-    """sigma * N(0,1) draws, stored in ``dtype`` (bf16 bits or float32), chunked for big tables."""
+def _normal(seed: int, tag: int, sub: int, shape, sigma: float, dtype: str) -> np.ndarray:
+    """sigma * N(0,1) draws stored in ``dtype`` (bf16 bits or float32).
+
+    The flat tensor is cut into fixed blocks of 2^24 values; block b draws from its own
+    generator (seed, tag, sub, b), so the result does not depend on how many threads fill it.
+    """
     n = int(np.prod(shape))
     out = np.empty(n, dtype=np.uint16 if dtype == "bf16" else np.float32)
-    buf = np.empty(min(n, _CHUNK), dtype=np.float32)
-    for s in range(0, n, _CHUNK):
+
+    def fill(b):
+        s = b * _CHUNK
         m = min(_CHUNK, n - s)
-        rng.standard_normal(out=buf[:m], dtype=np.float32)
-        buf[:m] *= np.float32(sigma)
-        out[s:s + m] = f32_to_bf16(buf[:m]) if dtype == "bf16" else buf[:m]
+        buf = _rng(seed, tag, sub, b).standard_normal(m, dtype=np.float32)
+        buf *= np.float32(sigma)
+        out[s:s + m] = f32_to_bf16(buf) if dtype == "bf16" else buf
+
+    blocks = range((n + _CHUNK - 1) // _CHUNK)
+    if n > _CHUNK:
+        with concurrent.futures.ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as ex:
+            list(ex.map(fill, blocks))
+    else:
+        for b in blocks:
+            fill(b)
     return out.reshape(shape)
 
 
@@ -158,13 +173,13 @@ def hidden(cfg: Config) -> np.ndarray:
     """Drafter hidden states h, shape [N, B, d], ~N(0,1)."""
     out = np.empty((cfg.N, cfg.B, cfg.d), dtype=np.uint16 if cfg.dtype == "bf16" else np.float32)
     for n in range(cfg.N):
-        out[n] = _normal(_rng(cfg.base_seed + n, TAG_HIDDEN), (cfg.B, cfg.d), 1.0, cfg.dtype)
+        out[n] = _normal(cfg.base_seed + n, TAG_HIDDEN, 0, (cfg.B, cfg.d), 1.0, cfg.dtype)
     return out
 
 
 def embedding(cfg: Config) -> np.ndarray:
     """Frozen token-embedding table, shape [V, E], ~N(0, emb_sigma^2)."""
-    return _normal(_rng(cfg.base_seed, TAG_EMB), (cfg.V, cfg.E), cfg.emb_sigma, cfg.dtype)
+    return _normal(cfg.base_seed, TAG_EMB, 0, (cfg.V, cfg.E), cfg.emb_sigma, cfg.dtype)
 
 
 WEIGHT_NAMES = ("W_e", "W_h", "W_f", "W_pair", "U", "V", "W", "u_a", "u_b", "b1", "w2", "b2")
@@ -185,8 +200,8 @@ def weights(cfg: Config, variant: Optional[str] = None) -> Dict[str, np.ndarray]
       'delta_zero' -- output layer zeroed (w2 = b2 = 0), so the correction vanishes
       'amplified'  -- w2 and b2 scaled by 100 so corrections move selections
     """
-    rng = _rng(cfg.base_seed, TAG_WEIGHTS)
-    w = {k: _normal(rng, s, cfg.weight_sigma, cfg.dtype) for k, s in weight_shapes(cfg).items()}
+    w = {k: _normal(cfg.base_seed, TAG_WEIGHTS, i, s, cfg.weight_sigma, cfg.dtype)
+         for i, (k, s) in enumerate(weight_shapes(cfg).items())}
     if variant == "delta_zero":
         for k in ("w2", "b2"):
             w[k] = np.zeros_like(w[k])
