@@ -72,7 +72,8 @@ def run_cycle_and_compare(cfg, variant=None, logits=None, mode=dc.VERIFY_GREEDY)
 
     np.testing.assert_array_equal(g["ids"][rows], ids_r)
     np.testing.assert_array_equal(g["vals"][rows].astype(np.float64), vals_r)
-    assert_scores_close(g["S"][sam], S_ref)
+    unary = np.broadcast_to(vals[:, 1:, None, :], S_ref.shape) if variant == "amplified" else None
+    assert_scores_close(g["S"][sam], S_ref, unary=unary)
     near = compare_walk(g["k_sel"][sam], k_ref, S_ref, vals)
     exact = [i for i, n in enumerate(sam) if np.array_equal(g["k_sel"][n], k_ref[i])]
     assert len(exact) >= len(sam) - near
