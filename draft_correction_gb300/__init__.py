@@ -48,6 +48,7 @@ _SIGNATURES = {
     "dcoco_candidate_repr": ([_P, _P, _I, _P, _WP, _I, _I, _I, _P, _P, _P, _Z, _P], _I),
     "dcoco_pair_state_workspace_size": ([_WP, _I, _I], _Z),
     "dcoco_pair_state": ([_P, _WP, _I, _I, _P, _P, _Z, _P], _I),
+    "dcoco_pair_state_noalloc": ([_P, _WP, _I, _I, _P, _P], _I),
     "dcoco_score_transitions": ([_P, _P, _P, _P, _WP, _I, _I, _I, _P, _P], _I),
     "dcoco_select": ([_P, _P, _P, _I, _I, _I, _P, _P, _P], _I),
     "dcoco_verify": ([_I, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P], _I),
@@ -193,6 +194,19 @@ def pair_state(h: torch.Tensor, w: CorrectorWeights):
     nbytes = lib().dcoco_pair_state_workspace_size(w.ref, N, B)
     ws = _empty((nbytes,), torch.uint8, h)
     _check(lib().dcoco_pair_state(_ptr(h), w.ref, N, B, _ptr(out), _ptr(ws), nbytes, _stream()))
+    return out
+
+
+def pair_state_noalloc(h: torch.Tensor, w: CorrectorWeights, out: Optional[torch.Tensor] = None):
+    """a3 without a workspace: the library's built-in 8 MiB scratch array is used instead.
+
+    For callers that cannot allocate device memory (their allocator owns all of it).  All
+    calls share that array: calls that may overlap on the GPU must be ordered.  `out`
+    ([N, B-1, H] f32) may be passed in so that the call itself allocates nothing.
+    """
+    N, B, _ = h.shape
+    out = _empty((N, B - 1, w.H), torch.float32, h) if out is None else out
+    _check(lib().dcoco_pair_state_noalloc(_ptr(h), w.ref, N, B, _ptr(out), _stream()))
     return out
 
 

@@ -7,6 +7,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 
 #include "../../include/dcoco.h"
 #include "internal.h"
@@ -627,3 +628,55 @@ int dcoco_cycle(const void* logits, int V, const void* emb, const void* h, const
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- allocation-free pair state
+// Scratch of dcoco_pair_state_noalloc: one statically sized array per device, shared by
+// every call.  In host code the name below is only a stand-in for the device object; the
+// device address comes from cudaGetSymbolAddress, looked up once per device.
+static __device__ __align__(256) unsigned char g_pair_state_scratch[DCOCO_PAIR_STATE_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+void* pair_state_scratch(int* rc) {
+  static std::mutex mu;
+  static void* addr[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    *rc = fail(DCOCO_ERR_CUDA, "no current CUDA device");
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_pair_state_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+      *rc = cuda_fail(e, "cudaGetSymbolAddress(pair-state scratch)");
+      return nullptr;
+    }
+    addr[dev] = p;
+  }
+  *rc = DCOCO_OK;
+  return addr[dev];
+}
+}  // namespace
+
+extern "C" int dcoco_pair_state_noalloc(const void* h, const dcoco_weights* w, int N, int B, float* ws_pair,
+                                        void* stream) {
+  clear_err();
+  DCOCO_TRY(check_weights(w));
+  DCOCO_TRY(check_block(N, B, 1));
+  DCOCO_TRY(check_ptr(h, "h"));
+  DCOCO_TRY(check_ptr(ws_pair, "ws_pair"));
+  const size_t need = dcoco_pair_state_workspace_size(w, N, B);
+  if (need > DCOCO_PAIR_STATE_NOALLOC_SCRATCH_BYTES)
+    return fail(DCOCO_ERR_WORKSPACE,
+                "pair state of N=%d B=%d r=%d needs %zu bytes of scratch; the built-in array holds %u "
+                "(call dcoco_pair_state with a workspace instead)",
+                N, B, w->r, need, DCOCO_PAIR_STATE_NOALLOC_SCRATCH_BYTES);
+  int rc;
+  void* scratch = pair_state_scratch(&rc);
+  if (rc != DCOCO_OK) return rc;
+  Carve c(scratch);
+  PairScratch s;
+  pair_scratch(dims_of(w, N, B, 1), c, &s);
+  return enqueue_pair(dims_of(w, N, B, 1), h, w, ws_pair, s, as_stream(stream));
+}

@@ -132,6 +132,29 @@ int dcoco_pair_state(const void* h, const dcoco_weights* w, int N, int B, float*
                      size_t workspace_bytes, void* stream);
 
 /*
+ * dcoco_pair_state without a caller-supplied workspace.  The method's papers have no
+ * counterpart: this exists for callers that cannot allocate device memory themselves --
+ * for example a serving engine that hands nearly all HBM to its own pool up front (its
+ * KV cache) and does not expose that pool, or host code that must not call cudaFree
+ * because it can synchronise the whole device.  Same inputs, outputs and results as
+ * dcoco_pair_state.
+ *  - Scratch is a library-owned, statically sized 8 MiB device array
+ *    (DCOCO_PAIR_STATE_NOALLOC_SCRATCH_BYTES).  Every GPU that loads the library holds it
+ *    until the process exits.  A shape whose scratch (dcoco_pair_state_workspace_size)
+ *    exceeds it is rejected with DCOCO_ERR_WORKSPACE before anything is enqueued.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call before any
+ *    stream capture begins.
+ *  - The call allocates nothing (no cudaMalloc, cudaFree or allocating library routine).
+ *  - All calls share the one array and it keeps the last call's contents.  Nothing in it
+ *    needs to start at zero: every call writes each scratch byte before reading it.  Calls
+ *    that can overlap on the GPU (other streams, other host threads) race on the array
+ *    and corrupt each other's results: order them on one stream or with events.
+ */
+#define DCOCO_PAIR_STATE_NOALLOC_SCRATCH_BYTES (8u << 20)
+int dcoco_pair_state_noalloc(const void* h, const dcoco_weights* w, int N, int B, float* ws_pair, void* stream);
+
+/*
  * a4. Transition scores (Two Delta blog, "Score neighboring candidates in parallel";
  * review §3.2), all (B-1)K^2 at once, unnormalised:
  *   S[n,p,a,b] = l_{p+1}(b) + w2 . SiLU(uz[n,p,a] + vz[n,p+1,b] + ws_pair[n,p]
