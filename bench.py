@@ -113,6 +113,21 @@ def reference_arm(args, cfg):
 # ----------------------------------------------------------------------------- GPU arm
 
 
+def captured_traffic(kernel: str):
+    """DRAM bytes per launch (read + write) from the committed ncu capture of `kernel`, or
+    None when the kernel's source has changed since that capture."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f)[kernel]
+        with open(os.path.join(ROOT, "draft_correction_gb300", "csrc", rec["source"]), "rb") as f:
+            digest = hashlib.sha256(f.read()).hexdigest()
+        return rec["dram_bytes_per_launch"] if digest == rec["source_sha256"] else None
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+
 def config_dict(cfg):
     return {"workload": cfg.name, "streams": cfg.N, "B": cfg.B, "K": cfg.K, "V": cfg.V, "d": cfg.d, "E": cfg.E,
             "r": cfg.r, "H": cfg.H, "verify": "greedy", "parallelism": "replicas (streams sharded, no collective)",
@@ -144,7 +159,10 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self):
+        self.marks = getattr(self, "marks", []) + [time.time()]
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -157,7 +175,17 @@ class ClockSampler:
     def summary(self):
         sm, mx, reasons = [], None, set()
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for ln in self.lines:
+        marks = getattr(self, "marks", [])
+        lines = [ln for _, ln in self.lines]
+        window = "whole measurement"
+        if len(marks) >= 2:
+            inside = [ln for t, ln in self.lines if marks[0] <= t <= marks[-1] + 0.2]
+            if len(inside) >= 3:
+                lines, window = inside, "timed loop"
+            else:
+                lines, window = [ln for t, ln in self.lines if t <= marks[-1] + 0.2], \
+                    "timed loop and the 1 s of identical steps before it"
+        for ln in lines:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 7:
                 continue
@@ -171,7 +199,8 @@ class ClockSampler:
                     reasons.add(name)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm),
+                "window": window}
 
 
 def gpu_arm(args, cfg):
@@ -241,7 +270,17 @@ def gpu_arm(args, cfg):
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
+        # nvidia-smi samples every 200 ms: keep identical steps running for ~1 s before the
+        # timed loop (untimed, part of the warm-up) so that the clock record is not empty
+        t_end = time.time() + 1.0
+        while time.time() < t_end:
+            for _ in range(50):
+                flush.fill_(1)
+                graph.replay()
+            torch.cuda.synchronize()
+        clk.mark()
         ms = timed_loop(graph.replay, args.steps, args.warmup)
+        clk.mark()
     torch.cuda.synchronize()
     total_ms = sum(ms)
     if world > 1:
@@ -276,7 +315,7 @@ def gpu_arm(args, cfg):
     topk_s = stage_us["topk"] * 1e-6
     achieved = topk_bytes / topk_s / 1e9
     roofline = {"bound": "hbm", "kernel": "topk_kernel", "achieved": round(achieved, 1), "peak": hbm,
-                "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": None,
+                "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": captured_traffic("topk"),
                 "peak_source": f"{peak_kind} hbm_gbs (burst)", "algorithmic_bytes_per_launch": topk_bytes}
 
     # End to end through the public API: pinned host inputs -> device, cycle, results -> host.

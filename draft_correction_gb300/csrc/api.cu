@@ -119,11 +119,12 @@ int pick_bn(int n, bool allow512) {
   return 32;
 }
 
-// Split-K factor: fill the SMs without giving any split fewer than 2 K blocks.
+// Split-K factor for long reductions only (>= 16 K blocks): double it while the grid stays
+// within the SMs and every split keeps at least 8 K blocks.  Short reductions run whole.
 int pick_split(int m_tiles, int n_tiles, int nkb, int BN) {
-  if (BN > 256) return 1;
+  if (BN > 256 || nkb < 16) return 1;
   int s = 1;
-  while (s < 8 && m_tiles * n_tiles * s * 2 <= 148 && nkb / (s * 2) >= 2) s *= 2;
+  while (s < 8 && m_tiles * n_tiles * s * 2 <= 152 && nkb / (s * 2) >= 8) s *= 2;
   return s;
 }
 

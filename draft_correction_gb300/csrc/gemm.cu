@@ -274,47 +274,81 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     // Partial tiles are staged; reduce a slice of rows per CTA across the cluster.
     tc_fence_before();
     cluster_sync();
-    if (warp >= 2) {
-      const int rank = static_cast<int>(cluster_rank());  // the cluster spans grid.z
-      const int rpc = BM / split_k;
-      for (int rr = warp - 2; rr < rpc; rr += 4) {
-        const int row_local = rank * rpc + rr;
-        const int m = m_tile * BM + row_local;
-        if (m >= args.M) continue;
-        float v[BN / 32];
+    // Phase A: this CTA owns rows [rank*rpc, (rank+1)*rpc) of the tile.  Every thread sums
+    // float4 column chunks of those rows over the cluster's partial tiles (rank order, so
+    // the result is deterministic) into a local buffer behind the staging area.
+    const int rank = static_cast<int>(cluster_rank());  // the cluster spans grid.z
+    const int rpc = BM / split_k;
+    float* red = reinterpret_cast<float*>(smem) + BM * LDS;
+    const uint32_t stg0 = smem_u32(smem);
+    constexpr int C4 = BN / 4;
+    const int items = rpc * C4;
+    for (int it0 = threadIdx.x; it0 < items; it0 += 4 * kThreads) {
+      float4 acc[4];
+      uint32_t off[4];
 #pragma unroll
-        for (int j = 0; j < BN / 32; ++j) v[j] = 0.f;
-        const uint32_t base = smem_u32(smem) + static_cast<uint32_t>(row_local * LDS) * 4u;
-        for (int src = 0; src < split_k; ++src) {
-          const uint32_t rb = map_to_rank(base, src);
+      for (int q = 0; q < 4; ++q) {
+        acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+        const int it = it0 + q * kThreads;
+        const int rr = it / C4, c4 = it % C4;
+        off[q] = static_cast<uint32_t>(((rank * rpc + rr) * LDS + c4 * 4) * 4);
+      }
+      for (int src = 0; src < split_k; ++src) {
+        const uint32_t rb = map_to_rank(stg0, src);
 #pragma unroll
-          for (int j = 0; j < BN / 32; ++j) v[j] += ld_cluster_f32(rb + (lane + 32 * j) * 4);
-        }
-        const size_t obase = static_cast<size_t>(m) * grp.ldo + static_cast<size_t>(nt) * BN;
-        if (grp.epi == EPI_LN) {
-          float s = 0.f;
-#pragma unroll
-          for (int j = 0; j < BN / 32; ++j) s += v[j];
-          const float mean = warp_sum(s) / BN;
-          float ss = 0.f;
-#pragma unroll
-          for (int j = 0; j < BN / 32; ++j) ss += (v[j] - mean) * (v[j] - mean);
-          const float rstd = rsqrtf(warp_sum(ss) / BN + args.ln_eps);
-#pragma unroll
-          for (int j = 0; j < BN / 32; ++j) store_act1<kBf16>(grp.out, obase + lane + 32 * j, (v[j] - mean) * rstd);
-        } else if (grp.epi == EPI_F32) {
-#pragma unroll
-          for (int j = 0; j < BN / 32; ++j) static_cast<float*>(grp.out)[obase + lane + 32 * j] = v[j];
-        } else {
-          const float* bias = (grp.epi == EPI_SILU_BIAS)
-                                  ? args.bias + static_cast<size_t>(m / args.bias_div) * args.ld_bias + nt * BN
-                                  : nullptr;
-#pragma unroll
-          for (int j = 0; j < BN / 32; ++j) {
-            float x = v[j];
-            if (bias != nullptr) x = silu(x + bias[lane + 32 * j]);
-            store_act1<kBf16>(grp.out, obase + lane + 32 * j, x);
+        for (int q = 0; q < 4; ++q) {
+          if (it0 + q * kThreads < items) {
+            const float4 x = ld_cluster_f32x4(rb + off[q]);
+            acc[q].x += x.x;
+            acc[q].y += x.y;
+            acc[q].z += x.z;
+            acc[q].w += x.w;
           }
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int it = it0 + q * kThreads;
+        if (it < items) *reinterpret_cast<float4*>(&red[(it / C4) * LDS + (it % C4) * 4]) = acc[q];
+      }
+    }
+    __syncthreads();
+    // Phase B: one warp per row from local shared memory, all six warps.
+    for (int rr = warp; rr < rpc; rr += kThreads / 32) {
+      const int m = m_tile * BM + rank * rpc + rr;
+      if (m >= args.M) continue;
+      constexpr int NJ = (BN + 31) / 32;
+      float v[NJ];
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) v[j] = (lane + 32 * j < BN) ? red[rr * LDS + lane + 32 * j] : 0.f;
+      const size_t obase = static_cast<size_t>(m) * grp.ldo + static_cast<size_t>(nt) * BN;
+      if (grp.epi == EPI_LN) {
+        float sum = 0.f;
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) sum += v[j];
+        const float mean = warp_sum(sum) / BN;
+        float ss = 0.f;
+#pragma unroll
+        for (int j = 0; j < NJ; ++j)
+          if (lane + 32 * j < BN) ss += (v[j] - mean) * (v[j] - mean);
+        const float rstd = rsqrtf(warp_sum(ss) / BN + args.ln_eps);
+#pragma unroll
+        for (int j = 0; j < NJ; ++j)
+          if (lane + 32 * j < BN) store_act1<kBf16>(grp.out, obase + lane + 32 * j, (v[j] - mean) * rstd);
+      } else if (grp.epi == EPI_F32) {
+#pragma unroll
+        for (int j = 0; j < NJ; ++j)
+          if (lane + 32 * j < BN) static_cast<float*>(grp.out)[obase + lane + 32 * j] = v[j];
+      } else {
+        const float* bias = (grp.epi == EPI_SILU_BIAS)
+                                ? args.bias + static_cast<size_t>(m / args.bias_div) * args.ld_bias + nt * BN
+                                : nullptr;
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) {
+          if (lane + 32 * j >= BN) continue;
+          float x = v[j];
+          if (bias != nullptr) x = silu(x + bias[lane + 32 * j]);
+          store_act1<kBf16>(grp.out, obase + lane + 32 * j, x);
         }
       }
     }
@@ -333,11 +367,9 @@ template <bool kBf16, int BN, bool kSplit>
 cudaError_t launch_gemm_t(const GemmArgs& args, int split_k, cudaStream_t stream) {
   constexpr int STAGE_BYTES = BM * 128 + BN * 128;
   int stages = std::min(kMaxStages, kSmemBudget / STAGE_BYTES);
-  if (kSplit) {
-    const int need = BM * (BN + 4) * 4;
-    while (stages * STAGE_BYTES < need && stages < kMaxStages) ++stages;
-  }
-  const int smem = stages * STAGE_BYTES + 1024;
+  // split-K reuses the pipeline buffers: partial tile (BM x LDS) plus this CTA's reduced rows
+  const int split_bytes = kSplit ? (BM + BM / 2) * (BN + 4) * 4 : 0;
+  const int smem = std::max(stages * STAGE_BYTES, split_bytes) + 1024;
   auto kern = gemm_kernel<kBf16, BN, kSplit>;
   // Function attributes are set once per instantiation (and device), so that later calls
   // enqueue nothing but the launch and can be captured into a CUDA graph.

@@ -27,12 +27,37 @@ constexpr int kAB = 4;    // predecessor rows per block
 constexpr int kHC = 256;  // hidden units per shared-memory chunk
 constexpr int kPad = 4;   // row padding (floats): neighbouring rows start in different banks
 
+// Hidden units per shared-memory chunk: all of H up to 256, else the largest of 256, 128, 64
+// dividing H (H is a multiple of 64), so every chunk is full.
+__host__ __device__ __forceinline__ int score_chunk(int H) {
+  return H <= kHC ? H : (H % 256 == 0 ? 256 : (H % 128 == 0 ? 128 : 64));
+}
+
 template <bool kBf16>
 __device__ __forceinline__ float ldv(const void* p, size_t i) {
   if constexpr (kBf16) {
     return __bfloat162float(static_cast<const __nv_bfloat16*>(p)[i]);
   } else {
     return static_cast<const float*>(p)[i];
+  }
+}
+
+// Eight consecutive activations (16 bytes of bf16 or 32 bytes of f32) widened to float.
+template <bool kBf16>
+__device__ __forceinline__ void ld8(const void* p, size_t i, float (&x)[8]) {
+  if constexpr (kBf16) {
+    const uint4 w = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p) + i);
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      x[2 * j] = __uint_as_float(u[j] << 16);
+      x[2 * j + 1] = __uint_as_float(u[j] & 0xFFFF0000u);
+    }
+  } else {
+    const float4 a = *reinterpret_cast<const float4*>(static_cast<const float*>(p) + i);
+    const float4 b = *reinterpret_cast<const float4*>(static_cast<const float*>(p) + i + 4);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
   }
 }
 
@@ -50,12 +75,15 @@ __global__ void __launch_bounds__(kThreads) score_kernel(const ScoreArgs a) {
   const int n = np / (B - 1), p = np % (B - 1);
   const int a0 = blockIdx.y * kAB;
   const int na = min(kAB, K - a0);
-  const int hc = min(H, kHC);
+  const int hc = score_chunk(H);
   const int ld = hc + kPad;
   float* P = sm;            // [kAB][ld]
   float* Q = P + kAB * ld;  // [K][ld]
-  float* w2c = Q + K * ld;  // [hc]
-  float* red = w2c + hc;    // [HS][nout], HS * nout <= kThreads
+  float* w2c = Q + K * ld;  // [hc]  output weights of the chunk
+  float* uac = w2c + hc;    // [hc]  u_a
+  float* ubc = uac + hc;    // [hc]  u_b
+  float* bwc = ubc + hc;    // [hc]  b1 + W s_p
+  float* red = bwc + hc;    // [HS][nout], HS * nout <= kThreads
 
   // Work split: nout = na*K outputs.  With nout < kThreads, HS threads share one output and
   // split its hidden units; otherwise each thread owns outputs o, o + kThreads (at most 2).
@@ -69,24 +97,46 @@ __global__ void __launch_bounds__(kThreads) score_kernel(const ScoreArgs a) {
   const float* vals_p = a.vals + row_p;
   const float* vals_q = a.vals + row_q;
   const float* wsp = a.wsp + static_cast<size_t>(np) * H;
+  const int nv = hc / 8;  // 8-wide vectors per row and chunk
 
   float acc0 = 0.f, acc1 = 0.f;
   for (int h0 = 0; h0 < H; h0 += hc) {
     __syncthreads();
-    for (int i = threadIdx.x; i < kAB * hc; i += kThreads) {
-      const int r = i / hc, c = i % hc, h = h0 + c;
-      float v = 0.f;
-      if (r < na) {
-        v = ldv<kBf16>(a.uz, (row_p + a0 + r) * H + h) + wsp[h] + ldv<kBf16>(a.u_a, h) * vals_p[a0 + r] +
-            ldv<kBf16>(a.b1, h);
+    for (int i = threadIdx.x; i < hc; i += kThreads) {
+      w2c[i] = ldv<kBf16>(a.w2, h0 + i);
+      uac[i] = ldv<kBf16>(a.u_a, h0 + i);
+      ubc[i] = ldv<kBf16>(a.u_b, h0 + i);
+      bwc[i] = ldv<kBf16>(a.b1, h0 + i) + wsp[h0 + i];
+    }
+    __syncthreads();
+    // P[a][h] = (uz + b1 + W s + u_a l_p(a)) / 2 and Q[b][h] = (vz + u_b l_{p+1}(b)) / 2
+    for (int i = threadIdx.x; i < (kAB + K) * nv; i += kThreads) {
+      const int r = i / nv, c = (i - r * nv) * 8;
+      const bool is_p = r < kAB;
+      float x[8];
+      float* dst;
+      if (is_p) {
+        dst = P + r * ld + c;
+        if (r < na) {
+          ld8<kBf16>(a.uz, (row_p + a0 + r) * H + h0 + c, x);
+          const float l = vals_p[a0 + r];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[e] = 0.5f * (x[e] + bwc[c + e] + uac[c + e] * l);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[e] = 0.f;
+        }
+      } else {
+        const int rb = r - kAB;
+        dst = Q + rb * ld + c;
+        ld8<kBf16>(a.vz, (row_q + rb) * H + h0 + c, x);
+        const float l = vals_q[rb];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = 0.5f * (x[e] + ubc[c + e] * l);
       }
-      P[r * ld + c] = 0.5f * v;
+      *reinterpret_cast<float4*>(dst) = make_float4(x[0], x[1], x[2], x[3]);
+      *reinterpret_cast<float4*>(dst + 4) = make_float4(x[4], x[5], x[6], x[7]);
     }
-    for (int i = threadIdx.x; i < K * hc; i += kThreads) {
-      const int r = i / hc, c = i % hc, h = h0 + c;
-      Q[r * ld + c] = 0.5f * (ldv<kBf16>(a.vz, (row_q + r) * H + h) + ldv<kBf16>(a.u_b, h) * vals_q[r]);
-    }
-    for (int i = threadIdx.x; i < hc; i += kThreads) w2c[i] = ldv<kBf16>(a.w2, h0 + i);
     __syncthreads();
     for (int t = 0; t < n_mine; ++t) {
       const int oo = o + t * kThreads;
@@ -126,10 +176,10 @@ __global__ void __launch_bounds__(kThreads) score_kernel(const ScoreArgs a) {
 }  // namespace
 
 cudaError_t launch_scores(const ScoreArgs& a, bool is_bf16, cudaStream_t stream) {
-  const int hc = a.H < kHC ? a.H : kHC;
+  const int hc = score_chunk(a.H);
   const int ld = hc + kPad;
-  // P, Q, the w2 chunk, and kThreads floats for combining partial sums (HS * nout <= kThreads)
-  const size_t smem = (static_cast<size_t>(kAB + a.K) * ld + hc + kThreads) * sizeof(float);
+  // P, Q, four per-chunk vectors, and kThreads floats for combining partial sums
+  const size_t smem = (static_cast<size_t>(kAB + a.K) * ld + 4 * hc + kThreads) * sizeof(float);
   dim3 grid(a.N * (a.B - 1), (a.K + kAB - 1) / kAB);
   // The dynamic shared memory ceiling is raised once per device to the largest this kernel
   // can need (K = 64), so later calls enqueue only the launch (CUDA-graph friendly).
@@ -139,7 +189,7 @@ cudaError_t launch_scores(const ScoreArgs& a, bool is_bf16, cudaStream_t stream)
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    const int most = static_cast<int>((static_cast<size_t>(kAB + 64) * (kHC + kPad) + kHC + kThreads) * sizeof(float));
+    const int most = static_cast<int>((static_cast<size_t>(kAB + 64) * (kHC + kPad) + 4 * kHC + kThreads) * sizeof(float));
     e = cudaFuncSetAttribute(score_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(score_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
     if (e != cudaSuccess) return e;

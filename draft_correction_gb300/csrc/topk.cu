@@ -58,6 +58,19 @@ __device__ __forceinline__ uint32_t elem_bits(const uint4& v, int e) {
   }
 }
 
+// Element-wise max of two 16-byte vectors (packed bf16 pairs or f32).
+template <bool kBf16>
+__device__ __forceinline__ uint4 vmax(const uint4& a, const uint4& b) {
+  if constexpr (kBf16) {
+    return make_uint4(bmax2(a.x, b.x), bmax2(a.y, b.y), bmax2(a.z, b.z), bmax2(a.w, b.w));
+  } else {
+    return make_uint4(__float_as_uint(fmaxf(__uint_as_float(a.x), __uint_as_float(b.x))),
+                      __float_as_uint(fmaxf(__uint_as_float(a.y), __uint_as_float(b.y))),
+                      __float_as_uint(fmaxf(__uint_as_float(a.z), __uint_as_float(b.z))),
+                      __float_as_uint(fmaxf(__uint_as_float(a.w), __uint_as_float(b.w))));
+  }
+}
+
 // True when every element of the vector is strictly below `tval` (NaN never rejects).
 template <bool kBf16>
 __device__ __forceinline__ bool all_below(const uint4& v, float tval) {
@@ -171,55 +184,64 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const void* __restrict__
 
   auto key_of = [&](const uint4& v, int e, int elem0) { return make_key(elem_bits<kBf16>(v, e), elem0 + e); };
 
+  // Lanes past the end of the segment see a vector of -inf (bf16 and f32 bit patterns).
+  const uint4 neg_inf = kBf16 ? make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u)
+                              : make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u);
   bool first = true;
   for (int base = vbeg + warp * (kUnroll * 32); base < vend; base += kWarps * kUnroll * 32) {
     uint4 v[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const int vi = base + u * 32 + lane;
-      v[u] = (vi < vend) ? ld_stream(vp + vi) : make_uint4(0, 0, 0, 0);
+      v[u] = (vi < vend) ? ld_stream(vp + vi) : neg_inf;
     }
     const uint64_t shared_t = *reinterpret_cast<volatile unsigned long long*>(&s_thresh);
     if (shared_t > filt) filt = shared_t;
+    if (first && KW == 1) {
+      // Seed the threshold: the K-th largest of the 32 lane maxima of the first vector is a
+      // lower bound for the K-th largest key of the warp's data, so anything below it can go.
+      const int vi = base + lane;
+      uint64_t m = 0;
+      if (vi < vend) {
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) {
+          const uint64_t k = key_of(v[0], e, head + vi * EPV);
+          m = k > m ? k : m;
+        }
+      }
+      int above = 0;  // keys are unique, so exactly one lane has K-1 larger maxima
+      for (int o = 0; o < 32; ++o) above += (__shfl_sync(kFull, m, o) > m);
+      const uint32_t is_kth = __ballot_sync(kFull, m != 0 && above == K - 1);
+      if (is_kth) {
+        const uint64_t t0 = __shfl_sync(kFull, m, __ffs(is_kth) - 1);
+        if (t0 - 1 > filt) filt = t0 - 1;
+      }
+      first = false;
+    }
+    // Common case: one packed max over all kUnroll vectors of the lane, one compare, one vote.
+    const float tval = key_value(filt);
+    const bool fast = filt != 0 && tval > -INFINITY;
+    bool maybe = true;
+    if (fast) {
+      uint4 mx = v[0];
+#pragma unroll
+      for (int u = 1; u < kUnroll; ++u) mx = vmax<kBf16>(mx, v[u]);
+      maybe = !all_below<kBf16>(mx, tval);
+    }
+    if (!__any_sync(kFull, maybe)) continue;
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const int vi = base + u * 32 + lane;
-      const bool valid = vi < vend;
-      const int elem0 = head + vi * EPV;
-      if (first && KW == 1) {
-        // Seed the threshold: the K-th largest of the 32 lane maxima is a lower bound for the
-        // K-th largest key of the warp's data, so anything below it can be skipped.
-        uint64_t m = 0;
-        if (valid) {
-#pragma unroll
-          for (int e = 0; e < EPV; ++e) {
-            const uint64_t k = key_of(v[u], e, elem0);
-            m = k > m ? k : m;
-          }
-        }
-        // rank of m among the lane maxima (ties impossible: keys are unique, zeros excluded)
-        int above = 0;
-        for (int o = 0; o < 32; ++o) above += (__shfl_sync(kFull, m, o) > m);
-        const uint32_t is_kth = __ballot_sync(kFull, m != 0 && above == K - 1);
-        if (is_kth) {
-          const uint64_t t0 = __shfl_sync(kFull, m, __ffs(is_kth) - 1);
-          if (t0 - 1 > filt) filt = t0 - 1;
-        }
-        first = false;
-      }
+      const float tv = key_value(filt);
+      const bool fst = filt != 0 && tv > -INFINITY;
+      const bool slow = vi < vend && !(fst && all_below<kBf16>(v[u], tv));
+      if (!__any_sync(kFull, slow)) continue;
       uint32_t pend = 0;
       uint64_t keys[EPV];
-      const float tval = key_value(filt);
-      const bool fast = filt != 0 && tval > -INFINITY;
-      if (valid && !(fast && all_below<kBf16>(v[u], tval))) {
 #pragma unroll
-        for (int e = 0; e < EPV; ++e) {
-          keys[e] = key_of(v[u], e, elem0);
-          if (keys[e] > filt) pend |= 1u << e;
-        }
-      } else {
-#pragma unroll
-        for (int e = 0; e < EPV; ++e) keys[e] = 0;
+      for (int e = 0; e < EPV; ++e) {
+        keys[e] = slow ? key_of(v[u], e, head + vi * EPV) : 0ull;
+        if (keys[e] > filt) pend |= 1u << e;
       }
       offer<KW, EPV>(L, keys, pend, filt, lane, &s_thresh);
     }

@@ -145,7 +145,8 @@ def test_verify_stochastic_matches_oracle(N, B, V):
 SMALL_BF16 = wl.scaled(wl.QWEN3_8B, N=2, B=5, K=5, V=3001, d=256, E=192, r=64, H=128)
 SMALL_R256 = wl.scaled(wl.HEADLINE, N=3, B=6, K=16, V=5000, d=512, E=512, r=256, H=512)
 SMALL_R512 = wl.scaled(wl.LARGE, N=2, B=4, K=8, V=2000, d=1024, E=1024, r=512, H=1024)
-REPR_CASES = [wl.TINY, SMALL_BF16, SMALL_R256, SMALL_R512]
+SMALL_H320 = wl.scaled(wl.QWEN3_8B, N=2, B=4, K=6, V=2000, d=128, E=128, r=64, H=320)
+REPR_CASES = [wl.TINY, SMALL_BF16, SMALL_R256, SMALL_R512, SMALL_H320]
 
 
 def _device_case(cfg, variant=None):
