@@ -223,6 +223,8 @@ int enqueue_repr(const Dims& D, const int32_t* ids, const void* emb, int V, cons
     if (!make_tmap(&a.a_map, emb, D.bf16, V, D.E, D.E, 1, &err)) return fail(DCOCO_ERR_CUDA, "%s", err);
     a.gather = ids;
     a.gather_limit = V;
+    a.gather_base = emb;
+    a.gather_pitch_bytes = static_cast<int>(D.E * D.esz);
     a.M = M;
     a.K = D.E;
     a.n_groups = 1;
@@ -339,13 +341,8 @@ int enqueue_scores(const Dims& D, const void* uz, const void* vz, const float* w
   return DCOCO_OK;
 }
 
-int topk_split(int rows, int V, bool bf16) {
-  if (g_topk_split > 0) return g_topk_split;
-  const int64_t row_bytes = static_cast<int64_t>(V) * (bf16 ? 2 : 4);
-  int s = 1;
-  while (s < 8 && static_cast<int64_t>(rows) * s < 4 * 152 && row_bytes / (s * 2) >= 16 * 1024) s *= 2;
-  return s;
-}
+// 0 lets the top-K launcher choose the split from the device's occupancy.
+int topk_split(int, int, bool) { return g_topk_split; }
 
 }  // namespace
 

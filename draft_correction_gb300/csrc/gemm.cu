@@ -31,6 +31,7 @@ constexpr int BM = 128;
 constexpr int kThreads = 192;
 constexpr int kMaxStages = 8;
 constexpr int kSmemBudget = 200 * 1024;
+constexpr int kBiasStageBytes = 20 * 1024;  // per-slot bias rows of one tile (SiLU epilogue)
 
 __device__ unsigned int g_status_word;
 
@@ -85,7 +86,7 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 template <bool kBf16, int BN, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ GemmArgs args, int stages,
-                                                          int split_k) {
+                                                          int split_k, int bias_stage_offset) {
   using T = Elt<kBf16>;
   constexpr int A_BYTES = BM * 128;
   constexpr int B_BYTES = BN * 128;
@@ -141,6 +142,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       }
     }
     s_rows[threadIdx.x] = row;
+    if (m < args.M && nk > 0) {
+      // Pull this row's K range into L2 as one contiguous request; the four-row TMA gathers
+      // below then read it from L2 in 128-byte pieces.
+      const int esz = kBf16 ? 2 : 4;
+      const int k0 = kb0 * T::BK, k1 = min(args.K, (kb0 + nk) * T::BK);
+      prefetch_l2_bulk(static_cast<const char*>(args.gather_base) + static_cast<size_t>(row) * args.gather_pitch_bytes +
+                           static_cast<size_t>(k0) * esz,
+                       static_cast<uint32_t>((k1 - k0) * esz));
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -208,6 +218,24 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     const int m = m_tile * BM + row_local;
     // tcgen05.ld is warp-collective: every lane of the warp takes the same path below and
     // only the stores are predicated on the row being inside M.
+    // While the main loop runs, stage this tile's per-slot bias rows in shared memory.
+    const float* sbias = nullptr;
+    int first_slot = 0;
+    if (grp.epi == EPI_SILU_BIAS) {
+      first_slot = (m_tile * BM) / args.bias_div;
+      const int last_slot = (min(args.M, m_tile * BM + BM) - 1) / args.bias_div;
+      const int nslots = last_slot - first_slot + 1;
+      if (nslots * BN * 4 <= kBiasStageBytes) {
+        float* dst = reinterpret_cast<float*>(smem + bias_stage_offset);
+        for (int i = threadIdx.x - 64; i < nslots * (BN / 4); i += 128) {
+          const int sl = i / (BN / 4), c4 = i % (BN / 4);
+          *reinterpret_cast<float4*>(dst + sl * BN + c4 * 4) = *reinterpret_cast<const float4*>(
+              args.bias + static_cast<size_t>(first_slot + sl) * args.ld_bias + nt * BN + c4 * 4);
+        }
+        sbias = dst;
+      }
+      named_barrier_sync(1, 128);
+    }
     const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&acc_bar), 0));
     if (!ok && lane == 0) atomicOr(args.status, DEV_TIMEOUT_ACC);
     const bool live = m < args.M;
@@ -249,9 +277,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           if (live) store_act<kBf16>(grp.out, obase + c, v, 32);
         }
       } else {
-        const float* bias = (grp.epi == EPI_SILU_BIAS && live)
-                                ? args.bias + static_cast<size_t>(m / args.bias_div) * args.ld_bias + nt * BN
-                                : nullptr;
+        const float* bias = nullptr;
+        if (grp.epi == EPI_SILU_BIAS && live) {
+          bias = sbias != nullptr ? sbias + (m / args.bias_div - first_slot) * BN
+                                  : args.bias + static_cast<size_t>(m / args.bias_div) * args.ld_bias + nt * BN;
+        }
         for (int c = 0; c < BN; c += 32) {
           float v[32];
           tmem_ld32(trow + c, v);
@@ -261,7 +291,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           } else {
             if (bias != nullptr) {
 #pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] = silu(v[i] + bias[c + i]);
+              for (int i = 0; i < 32; i += 4) {
+                const float4 bb = *reinterpret_cast<const float4*>(bias + c + i);
+                v[i] = silu(v[i] + bb.x);
+                v[i + 1] = silu(v[i + 1] + bb.y);
+                v[i + 2] = silu(v[i + 2] + bb.z);
+                v[i + 3] = silu(v[i + 3] + bb.w);
+              }
             }
             store_act<kBf16>(grp.out, obase + c, v, 32);
           }
@@ -369,19 +405,22 @@ cudaError_t launch_gemm_t(const GemmArgs& args, int split_k, cudaStream_t stream
   int stages = std::min(kMaxStages, kSmemBudget / STAGE_BYTES);
   // split-K reuses the pipeline buffers: partial tile (BM x LDS) plus this CTA's reduced rows
   const int split_bytes = kSplit ? (BM + BM / 2) * (BN + 4) * 4 : 0;
-  const int smem = std::max(stages * STAGE_BYTES, split_bytes) + 1024;
+  const bool has_bias = args.g[0].epi == EPI_SILU_BIAS || (args.n_groups > 1 && args.g[1].epi == EPI_SILU_BIAS);
+  if (has_bias) stages = std::min(stages, 4);
+  const int bias_off = std::max(stages * STAGE_BYTES, split_bytes);
+  const int smem = bias_off + (has_bias ? kBiasStageBytes : 0) + 1024;
   auto kern = gemm_kernel<kBf16, BN, kSplit>;
   // Function attributes are set once per instantiation (and device), so that later calls
   // enqueue nothing but the launch and can be captured into a CUDA graph.
-  static bool configured[64] = {};
+  static int configured[64] = {};  // largest dynamic shared memory size set so far, per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!configured[dev]) {
+  if (smem > configured[dev]) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    configured[dev] = true;
+    configured[dev] = smem;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((args.M + BM - 1) / BM, args.g[0].n_tiles + (args.n_groups > 1 ? args.g[1].n_tiles : 0), split_k);
@@ -395,7 +434,7 @@ cudaError_t launch_gemm_t(const GemmArgs& args, int split_k, cudaStream_t stream
   attr[0].val.clusterDim.z = split_k;
   cfg.attrs = attr;
   cfg.numAttrs = kSplit ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kern, args, stages, split_k);
+  return cudaLaunchKernelEx(&cfg, kern, args, stages, split_k, bias_off);
 }
 
 template <bool kBf16>

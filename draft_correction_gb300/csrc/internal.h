@@ -35,6 +35,8 @@ struct GemmArgs {
   CUtensorMap a_map;        // A [M, K] tiled (box {BK, 128}), or the gather table [rows, K] (box {BK, 1})
   const int32_t* gather;    // non-null: A row m is table row gather[m]
   int gather_limit;         // rows of the gather table (ids outside [0, limit) are replaced by 0)
+  const void* gather_base;  // the gather table (for L2 prefetch of each gathered row's K range)
+  int gather_pitch_bytes;
   int M, K;
   int n_groups;             // 1 or 2
   GemmGroup g[2];

@@ -8,12 +8,14 @@
 // once upstream; this kernel forms the K x K broadcast sum on chip and never writes the
 // [K, K, H] hidden layer to memory.
 //
-// One thread block handles one transition (n, p) and AB predecessor rows a.  Per chunk of
+// One thread block handles one transition (n, p) and AB = 8 predecessor rows a.  Per chunk of
 // HC hidden units it stages, in shared memory,
 //   P[a][h] = (uz[n,p,a,h] + ws[n,p,h] + u_a[h] l_p(a) + b1[h]) / 2
 //   Q[b][h] = (vz[n,p+1,b,h] + u_b[h] l_{p+1}(b)) / 2
 // so that with x = 2(P + Q):  SiLU(x) = x sigmoid(x) = y + y tanh(y), y = P + Q.
-// The tanh uses the SFU's tanh.approx.f32 (one instruction per hidden unit and pair).
+// Each thread owns a 2 x 4 tile of (a, b) outputs over a strided subset of the hidden units
+// (7 shared-memory vector loads per 32 SiLUs); the partial sums are then added in a fixed
+// order.  The tanh uses the SFU's tanh.approx.f32.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -22,9 +24,11 @@
 namespace dcoco {
 namespace {
 
-constexpr int kThreads = 128;
-constexpr int kAB = 4;    // predecessor rows per block
-constexpr int kHC = 256;  // hidden units per shared-memory chunk
+constexpr int kThreads = 256;
+constexpr int kAB = 8;    // predecessor rows per block
+constexpr int kTA = 2;    // predecessor rows per thread tile
+constexpr int kTB = 4;    // successor rows per thread tile
+constexpr int kHC = 256;  // hidden units per shared-memory chunk (at most)
 constexpr int kPad = 4;   // row padding (floats): neighbouring rows start in different banks
 
 // Hidden units per shared-memory chunk: all of H up to 256, else the largest of 256, 128, 64
@@ -75,22 +79,24 @@ __global__ void __launch_bounds__(kThreads) score_kernel(const ScoreArgs a) {
   const int n = np / (B - 1), p = np % (B - 1);
   const int a0 = blockIdx.y * kAB;
   const int na = min(kAB, K - a0);
+  const int Kp = (K + kTB - 1) / kTB * kTB;  // successor rows padded to the thread tile
   const int hc = score_chunk(H);
   const int ld = hc + kPad;
-  float* P = sm;            // [kAB][ld]
-  float* Q = P + kAB * ld;  // [K][ld]
-  float* w2c = Q + K * ld;  // [hc]  output weights of the chunk
-  float* uac = w2c + hc;    // [hc]  u_a
-  float* ubc = uac + hc;    // [hc]  u_b
-  float* bwc = ubc + hc;    // [hc]  b1 + W s_p
-  float* red = bwc + hc;    // [HS][nout], HS * nout <= kThreads
+  float* P = sm;             // [kAB][ld]
+  float* Q = P + kAB * ld;   // [Kp][ld]
+  float* w2c = Q + Kp * ld;  // [hc]  output weights of the chunk
+  float* uac = w2c + hc;     // [hc]  u_a
+  float* ubc = uac + hc;     // [hc]  u_b
+  float* bwc = ubc + hc;     // [hc]  b1 + W s_p
+  float* red = bwc + hc;     // [kThreads][kTA * kTB] partial sums
 
-  // Work split: nout = na*K outputs.  With nout < kThreads, HS threads share one output and
-  // split its hidden units; otherwise each thread owns outputs o, o + kThreads (at most 2).
-  const int nout = na * K;
-  const int HS = nout >= kThreads ? 1 : kThreads / nout;
-  const int o = threadIdx.x % nout, hs = threadIdx.x / nout;
-  const int n_mine = (hs < HS) ? (HS == 1 ? (nout - o + kThreads - 1) / kThreads : 1) : 0;
+  // Thread tiles: OT = (kAB/kTA) x (Kp/kTB); HS threads share a tile and split the hidden units.
+  const int tiles_b = Kp / kTB;
+  const int OT = (kAB / kTA) * tiles_b;
+  const int HS = kThreads / OT;  // OT <= 64 (K <= 64), so HS >= 4
+  const int ot = threadIdx.x % OT, hs = threadIdx.x / OT;
+  const bool active = hs < HS;
+  const int ta = ot / tiles_b, tb = ot % tiles_b;
 
   const size_t row_p = (static_cast<size_t>(n) * B + p) * K;      // candidate rows of slot p
   const size_t row_q = (static_cast<size_t>(n) * B + p + 1) * K;  // candidate rows of slot p+1
@@ -99,7 +105,12 @@ __global__ void __launch_bounds__(kThreads) score_kernel(const ScoreArgs a) {
   const float* wsp = a.wsp + static_cast<size_t>(np) * H;
   const int nv = hc / 8;  // 8-wide vectors per row and chunk
 
-  float acc0 = 0.f, acc1 = 0.f;
+  float acc[kTA][kTB];
+#pragma unroll
+  for (int i = 0; i < kTA; ++i)
+#pragma unroll
+    for (int j = 0; j < kTB; ++j) acc[i][j] = 0.f;
+
   for (int h0 = 0; h0 < H; h0 += hc) {
     __syncthreads();
     for (int i = threadIdx.x; i < hc; i += kThreads) {
@@ -109,13 +120,13 @@ __global__ void __launch_bounds__(kThreads) score_kernel(const ScoreArgs a) {
       bwc[i] = ldv<kBf16>(a.b1, h0 + i) + wsp[h0 + i];
     }
     __syncthreads();
-    // P[a][h] = (uz + b1 + W s + u_a l_p(a)) / 2 and Q[b][h] = (vz + u_b l_{p+1}(b)) / 2
-    for (int i = threadIdx.x; i < (kAB + K) * nv; i += kThreads) {
+    // P[a][h] = (uz + b1 + W s + u_a l_p(a)) / 2 and Q[b][h] = (vz + u_b l_{p+1}(b)) / 2; rows
+    // past na (P) or K (Q) are zero.
+    for (int i = threadIdx.x; i < (kAB + Kp) * nv; i += kThreads) {
       const int r = i / nv, c = (i - r * nv) * 8;
-      const bool is_p = r < kAB;
       float x[8];
       float* dst;
-      if (is_p) {
+      if (r < kAB) {
         dst = P + r * ld + c;
         if (r < na) {
           ld8<kBf16>(a.uz, (row_p + a0 + r) * H + h0 + c, x);
@@ -129,47 +140,64 @@ __global__ void __launch_bounds__(kThreads) score_kernel(const ScoreArgs a) {
       } else {
         const int rb = r - kAB;
         dst = Q + rb * ld + c;
-        ld8<kBf16>(a.vz, (row_q + rb) * H + h0 + c, x);
-        const float l = vals_q[rb];
+        if (rb < K) {
+          ld8<kBf16>(a.vz, (row_q + rb) * H + h0 + c, x);
+          const float l = vals_q[rb];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] = 0.5f * (x[e] + ubc[c + e] * l);
+          for (int e = 0; e < 8; ++e) x[e] = 0.5f * (x[e] + ubc[c + e] * l);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[e] = 0.f;
+        }
       }
       *reinterpret_cast<float4*>(dst) = make_float4(x[0], x[1], x[2], x[3]);
       *reinterpret_cast<float4*>(dst + 4) = make_float4(x[4], x[5], x[6], x[7]);
     }
     __syncthreads();
-    for (int t = 0; t < n_mine; ++t) {
-      const int oo = o + t * kThreads;
-      const float4* p4 = reinterpret_cast<const float4*>(P + (oo / K) * ld);
-      const float4* q4 = reinterpret_cast<const float4*>(Q + (oo % K) * ld);
+    if (active) {
       const float4* w4 = reinterpret_cast<const float4*>(w2c);
-      float s = 0.f;
+      const float4* p4 = reinterpret_cast<const float4*>(P + ta * kTA * ld);
+      const float4* q4 = reinterpret_cast<const float4*>(Q + tb * kTB * ld);
+      const int ld4 = ld / 4;
       for (int c = hs; c < hc / 4; c += HS) {
-        const float4 pp = p4[c], qq = q4[c], ww = w4[c];
-        float y;
-        y = pp.x + qq.x; s = fmaf(ww.x, fmaf(y, tanh_fast(y), y), s);
-        y = pp.y + qq.y; s = fmaf(ww.y, fmaf(y, tanh_fast(y), y), s);
-        y = pp.z + qq.z; s = fmaf(ww.z, fmaf(y, tanh_fast(y), y), s);
-        y = pp.w + qq.w; s = fmaf(ww.w, fmaf(y, tanh_fast(y), y), s);
+        const float4 w = w4[c];
+        float4 pv[kTA], qv[kTB];
+#pragma unroll
+        for (int i = 0; i < kTA; ++i) pv[i] = p4[i * ld4 + c];
+#pragma unroll
+        for (int j = 0; j < kTB; ++j) qv[j] = q4[j * ld4 + c];
+#pragma unroll
+        for (int i = 0; i < kTA; ++i) {
+#pragma unroll
+          for (int j = 0; j < kTB; ++j) {
+            float y, s = acc[i][j];
+            y = pv[i].x + qv[j].x; s = fmaf(w.x, fmaf(y, tanh_fast(y), y), s);
+            y = pv[i].y + qv[j].y; s = fmaf(w.y, fmaf(y, tanh_fast(y), y), s);
+            y = pv[i].z + qv[j].z; s = fmaf(w.z, fmaf(y, tanh_fast(y), y), s);
+            y = pv[i].w + qv[j].w; s = fmaf(w.w, fmaf(y, tanh_fast(y), y), s);
+            acc[i][j] = s;
+          }
+        }
       }
-      if (t == 0) acc0 += s; else acc1 += s;
     }
   }
 
+  // Add the HS partial sums of every output in a fixed order.
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < kTA; ++i)
+#pragma unroll
+    for (int j = 0; j < kTB; ++j) red[threadIdx.x * (kTA * kTB) + i * kTB + j] = active ? acc[i][j] : 0.f;
+  __syncthreads();
   const float b2 = ldv<kBf16>(a.b2, 0);
   float* Sp = a.S + (static_cast<size_t>(np) * K + a0) * K;  // rows a0.. of this transition
-  if (HS > 1) {
-    // Combine the HS partial sums of each output in a fixed order.
-    if (hs < HS) red[hs * nout + o] = acc0;
-    __syncthreads();
-    if (threadIdx.x < nout) {
-      float s = 0.f;
-      for (int j = 0; j < HS; ++j) s += red[j * nout + threadIdx.x];
-      Sp[threadIdx.x] = vals_q[threadIdx.x % K] + s + b2;
-    }
-  } else {
-    if (n_mine > 0) Sp[o] = vals_q[o % K] + acc0 + b2;
-    if (n_mine > 1) Sp[o + kThreads] = vals_q[(o + kThreads) % K] + acc1 + b2;
+  for (int o = threadIdx.x; o < na * K; o += kThreads) {
+    const int ar = o / K, bc = o % K;
+    const int t = (ar / kTA) * tiles_b + bc / kTB;
+    const int idx = (ar % kTA) * kTB + bc % kTB;
+    float s = 0.f;
+    for (int h = 0; h < HS; ++h) s += red[(h * OT + t) * (kTA * kTB) + idx];
+    Sp[o] = vals_q[bc] + s + b2;
   }
 }
 
@@ -178,8 +206,9 @@ __global__ void __launch_bounds__(kThreads) score_kernel(const ScoreArgs a) {
 cudaError_t launch_scores(const ScoreArgs& a, bool is_bf16, cudaStream_t stream) {
   const int hc = score_chunk(a.H);
   const int ld = hc + kPad;
-  // P, Q, four per-chunk vectors, and kThreads floats for combining partial sums
-  const size_t smem = (static_cast<size_t>(kAB + a.K) * ld + 4 * hc + kThreads) * sizeof(float);
+  const int Kp = (a.K + kTB - 1) / kTB * kTB;
+  // P, Q, four per-chunk vectors, and the partial sums of every thread
+  const size_t smem = (static_cast<size_t>(kAB + Kp) * ld + 4 * hc + kThreads * kTA * kTB) * sizeof(float);
   dim3 grid(a.N * (a.B - 1), (a.K + kAB - 1) / kAB);
   // The dynamic shared memory ceiling is raised once per device to the largest this kernel
   // can need (K = 64), so later calls enqueue only the launch (CUDA-graph friendly).
@@ -189,7 +218,8 @@ cudaError_t launch_scores(const ScoreArgs& a, bool is_bf16, cudaStream_t stream)
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    const int most = static_cast<int>((static_cast<size_t>(kAB + 64) * (kHC + kPad) + 4 * kHC + kThreads) * sizeof(float));
+    const int most =
+        static_cast<int>((static_cast<size_t>(kAB + 64) * (kHC + kPad) + 4 * kHC + kThreads * kTA * kTB) * sizeof(float));
     e = cudaFuncSetAttribute(score_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(score_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
     if (e != cudaSuccess) return e;

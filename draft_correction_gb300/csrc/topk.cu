@@ -8,18 +8,24 @@
 // Design (HBM-bound; one pass over the logits):
 //  * Every candidate is a 64-bit key: the order-preserving code of its float value in the
 //    high word and (0xFFFFFFFF - id) in the low word, so "larger key" means "larger value,
-//    then smaller id".  Keys are unique within a row, which makes every merge exact and
+//    then smaller id".  Keys are unique within a row, which makes every selection exact and
 //    independent of scheduling.
-//  * A row is split over a cluster of `S` thread blocks (grid.x = S).  Each warp streams
-//    its share with 128-bit loads (8 bf16 per lane) and keeps a sorted top-K list in
-//    registers (one or two entries per lane).  A vector is rejected with three packed
-//    bf16 max instructions when all 8 values fall below the current threshold; only
-//    survivors are keyed and inserted.
-//  * The threshold is the largest K-th entry any warp of the block has seen (shared
-//    memory atomicMax), seeded per warp from the K-th largest of its first 32 lane maxima.
-//  * Warp lists are merged in shared memory by rank counting, then the S block results are
-//    pushed into block 0's shared memory over the cluster (DSMEM) and merged the same way.
+//  * A row is split over a cluster of S thread blocks (grid.x = S, S <= 8, chosen so the
+//    grid fills whole waves of the GPU).  A block streams its segment with 128-bit loads
+//    (8 bf16 per lane), the next iteration's loads in flight while the current one is
+//    filtered.
+//  * Filtering is against one block-wide key threshold: a lane rejects its 16 values with
+//    packed bf16 max instructions when all fall below it.  Survivors are appended to a
+//    block-wide candidate buffer in shared memory.  At the end of an iteration, if the
+//    buffer holds more than 128 keys, the block keeps its K largest (rank counting) and
+//    the K-th becomes the new threshold.  The first iteration is seeded per warp with the
+//    K-th largest of its 32 lane maxima, a valid lower bound on the K-th value.
+//  * The buffer can take one full iteration of appends on top of 128 entries, so it never
+//    overflows.  At the end each block selects its K largest keys, pushes them into block
+//    0 of the cluster (distributed shared memory), and block 0 merges S*K keys.
 #include <cuda_bf16.h>
+
+#include <cmath>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -29,9 +35,16 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kUnroll = 4;
+constexpr int kU = 2;          // 16-byte vectors per lane per iteration
 constexpr int kMaxSplit = 8;
+constexpr int kMaxK = 64;
+constexpr int kCapLow = 128;   // compaction trigger
 constexpr unsigned kFull = 0xFFFFFFFFu;
+
+template <bool kBf16>
+constexpr int kEpv = kBf16 ? 8 : 4;  // elements per 16-byte vector
+template <bool kBf16>
+constexpr int kCap = kCapLow + kThreads * kU * kEpv<kBf16> + 32;  // + one warp of head/tail
 
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
   uint4 v;
@@ -58,7 +71,7 @@ __device__ __forceinline__ uint32_t elem_bits(const uint4& v, int e) {
   }
 }
 
-// Element-wise max of two 16-byte vectors (packed bf16 pairs or f32).
+// Element-wise max of two 16-byte vectors (packed bf16 pairs or f32); a NaN operand is dropped.
 template <bool kBf16>
 __device__ __forceinline__ uint4 vmax(const uint4& a, const uint4& b) {
   if constexpr (kBf16) {
@@ -71,103 +84,58 @@ __device__ __forceinline__ uint4 vmax(const uint4& a, const uint4& b) {
   }
 }
 
+// Largest element of a vector as float bits (NaN only if every element is NaN).
+template <bool kBf16>
+__device__ __forceinline__ uint32_t vec_max_bits(const uint4& v) {
+  if constexpr (kBf16) {
+    const uint32_t m = bmax2(bmax2(v.x, v.y), bmax2(v.z, v.w));
+    const float hi = __uint_as_float(m & 0xFFFF0000u), lo = __uint_as_float(m << 16);
+    return __float_as_uint(fmaxf(hi, lo));
+  } else {
+    return __float_as_uint(fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)),
+                                 fmaxf(__uint_as_float(v.z), __uint_as_float(v.w))));
+  }
+}
+
 // True when every element of the vector is strictly below `tval` (NaN never rejects).
 template <bool kBf16>
 __device__ __forceinline__ bool all_below(const uint4& v, float tval) {
-  if constexpr (kBf16) {
-    const uint32_t m = bmax2(bmax2(v.x, v.y), bmax2(v.z, v.w));
-    return (__uint_as_float(m & 0xFFFF0000u) < tval) && (__uint_as_float(m << 16) < tval);
-  } else {
-    const float m = fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)),
-                          fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
-    return m < tval;  // fmaxf drops a NaN operand; a vector of all NaN fails the test
-  }
+  return __uint_as_float(vec_max_bits<kBf16>(v)) < tval;
 }
 
-// A descending top-K list spread over a warp: entry j*32 + lane lives in e[j] of `lane`.
-template <int KW>
-struct WarpTopK {
-  uint64_t e[KW];
-  int K;
-  uint64_t kth;  // entry K-1 (0 while the list is not full)
-
-  __device__ __forceinline__ void init(int k) {
-#pragma unroll
-    for (int j = 0; j < KW; ++j) e[j] = 0;
-    K = k;
-    kth = 0;
+// Keep the K largest keys of s_buf[0, cnt) in s_keep[0, K) (descending; 0 where cnt < K).
+// Called by every thread of the block.
+__device__ __forceinline__ void select_top(const uint64_t* s_buf, int cnt, int K, uint64_t* s_keep) {
+  if (threadIdx.x < K) s_keep[threadIdx.x] = 0;
+  __syncthreads();
+  for (int c = threadIdx.x; c < cnt; c += kThreads) {
+    const uint64_t x = s_buf[c];
+    int above = 0;
+    for (int o = 0; o < cnt; ++o) above += (s_buf[o] > x);
+    if (above < K) s_keep[above] = x;
   }
-  // Insert key x (warp-uniform call).
-  __device__ __forceinline__ void insert(uint64_t x, int lane) {
-    int pos = 0;
-#pragma unroll
-    for (int j = 0; j < KW; ++j) pos += __popc(__ballot_sync(kFull, e[j] > x));
-    uint64_t prev[KW];
-#pragma unroll
-    for (int j = 0; j < KW; ++j) {
-      const uint64_t up = __shfl_up_sync(kFull, e[j], 1);
-      const uint64_t wrap = (j > 0) ? __shfl_sync(kFull, e[j > 0 ? j - 1 : 0], 31) : 0ull;
-      prev[j] = (lane == 0) ? wrap : up;
-    }
-#pragma unroll
-    for (int j = 0; j < KW; ++j) {
-      const int idx = j * 32 + lane;
-      e[j] = (idx < pos) ? e[j] : (idx == pos ? x : prev[j]);
-    }
-    const int last = K - 1;
-    uint64_t t = 0;
-#pragma unroll
-    for (int j = 0; j < KW; ++j) {
-      const uint64_t v = __shfl_sync(kFull, e[j], last & 31);
-      if ((last >> 5) == j) t = v;
-    }
-    kth = t;
-  }
-};
-
-// Offer this lane's candidate keys (bit e of `pend` marks keys[e]) to the warp list.
-template <int KW, int EPV>
-__device__ __forceinline__ void offer(WarpTopK<KW>& L, const uint64_t (&keys)[EPV], uint32_t pend, uint64_t& filt,
-                                      int lane, unsigned long long* s_thresh) {
-  for (;;) {
-    const uint32_t any = __ballot_sync(kFull, pend != 0);
-    if (!any) break;
-    const int src = __ffs(any) - 1;
-    uint64_t mine = 0;
-    if (pend) {
-      const int e = __ffs(pend) - 1;
-#pragma unroll
-      for (int t = 0; t < EPV; ++t)
-        if (t == e) mine = keys[t];
-    }
-    const uint64_t x = __shfl_sync(kFull, mine, src);
-    if (lane == src) pend &= pend - 1;
-    if (x > filt) {
-      L.insert(x, lane);
-      if (L.kth > filt) {
-        filt = L.kth;
-        if (lane == 0) atomicMax(s_thresh, static_cast<unsigned long long>(filt));
-      }
-    }
-  }
+  __syncthreads();
 }
 
-template <bool kBf16, int KW>
+template <bool kBf16>
 __global__ void __launch_bounds__(kThreads) topk_kernel(const void* __restrict__ logits, int V, int K, int S,
                                                         float* __restrict__ vals, int32_t* __restrict__ ids) {
-  constexpr int EPV = kBf16 ? 8 : 4;  // elements per 16-byte vector
-  __shared__ uint64_t s_warp[kWarps * 32 * KW];
-  __shared__ uint64_t s_block[32 * KW];
-  __shared__ uint64_t s_cluster[kMaxSplit * 32 * KW];
-  __shared__ unsigned long long s_thresh;
+  constexpr int EPV = kEpv<kBf16>;
+  constexpr int CAP = kCap<kBf16>;
+  __shared__ uint64_t s_buf[CAP];
+  __shared__ uint64_t s_keep[kMaxK];
+  __shared__ uint64_t s_cluster[kMaxSplit * kMaxK];
+  __shared__ uint64_t s_thr;
+  __shared__ int s_cnt;
 
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int rank = blockIdx.x;  // == rank in the cluster (the cluster spans grid.x)
   const int64_t row = blockIdx.y;
-
-  if (threadIdx.x == 0) s_thresh = 0;
-  __syncthreads();
+  if (threadIdx.x == 0) {
+    s_cnt = 0;
+    s_thr = 0;
+  }
 
   const int64_t e0 = row * static_cast<int64_t>(V);
   int head = static_cast<int>((EPV - (e0 % EPV)) % EPV);
@@ -177,154 +145,149 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const void* __restrict__
   const uint4* vp = reinterpret_cast<const uint4*>(static_cast<const char*>(logits) + (e0 + head) * (kBf16 ? 2 : 4));
   const int vbeg = static_cast<int>(static_cast<int64_t>(rank) * nvec / S);
   const int vend = static_cast<int>(static_cast<int64_t>(rank + 1) * nvec / S);
+  constexpr int CH = kWarps * kU * 32;  // vectors per block iteration
+  const int iters = (vend - vbeg + CH - 1) / CH;
 
-  WarpTopK<KW> L;
-  L.init(K);
-  uint64_t filt = 0;  // keys <= filt cannot be in the row's top K
-
-  auto key_of = [&](const uint4& v, int e, int elem0) { return make_key(elem_bits<kBf16>(v, e), elem0 + e); };
-
-  // Lanes past the end of the segment see a vector of -inf (bf16 and f32 bit patterns).
   const uint4 neg_inf = kBf16 ? make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u)
                               : make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u);
-  bool first = true;
-  for (int base = vbeg + warp * (kUnroll * 32); base < vend; base += kWarps * kUnroll * 32) {
-    uint4 v[kUnroll];
+  auto vidx = [&](int it, int u) { return vbeg + it * CH + (warp * kU + u) * 32 + lane; };
+  uint4 cur[kU], nxt[kU];
+  if (iters > 0) {
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int vi = base + u * 32 + lane;
-      v[u] = (vi < vend) ? ld_stream(vp + vi) : neg_inf;
-    }
-    const uint64_t shared_t = *reinterpret_cast<volatile unsigned long long*>(&s_thresh);
-    if (shared_t > filt) filt = shared_t;
-    if (first && KW == 1) {
-      // Seed the threshold: the K-th largest of the 32 lane maxima of the first vector is a
-      // lower bound for the K-th largest key of the warp's data, so anything below it can go.
-      const int vi = base + lane;
-      uint64_t m = 0;
-      if (vi < vend) {
-#pragma unroll
-        for (int e = 0; e < EPV; ++e) {
-          const uint64_t k = key_of(v[0], e, head + vi * EPV);
-          m = k > m ? k : m;
-        }
-      }
-      int above = 0;  // keys are unique, so exactly one lane has K-1 larger maxima
-      for (int o = 0; o < 32; ++o) above += (__shfl_sync(kFull, m, o) > m);
-      const uint32_t is_kth = __ballot_sync(kFull, m != 0 && above == K - 1);
-      if (is_kth) {
-        const uint64_t t0 = __shfl_sync(kFull, m, __ffs(is_kth) - 1);
-        if (t0 - 1 > filt) filt = t0 - 1;
-      }
-      first = false;
-    }
-    // Common case: one packed max over all kUnroll vectors of the lane, one compare, one vote.
-    const float tval = key_value(filt);
-    const bool fast = filt != 0 && tval > -INFINITY;
-    bool maybe = true;
-    if (fast) {
-      uint4 mx = v[0];
-#pragma unroll
-      for (int u = 1; u < kUnroll; ++u) mx = vmax<kBf16>(mx, v[u]);
-      maybe = !all_below<kBf16>(mx, tval);
-    }
-    if (!__any_sync(kFull, maybe)) continue;
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int vi = base + u * 32 + lane;
-      const float tv = key_value(filt);
-      const bool fst = filt != 0 && tv > -INFINITY;
-      const bool slow = vi < vend && !(fst && all_below<kBf16>(v[u], tv));
-      if (!__any_sync(kFull, slow)) continue;
-      uint32_t pend = 0;
-      uint64_t keys[EPV];
-#pragma unroll
-      for (int e = 0; e < EPV; ++e) {
-        keys[e] = slow ? key_of(v[u], e, head + vi * EPV) : 0ull;
-        if (keys[e] > filt) pend |= 1u << e;
-      }
-      offer<KW, EPV>(L, keys, pend, filt, lane, &s_thresh);
+    for (int u = 0; u < kU; ++u) {
+      const int vi = vidx(0, u);
+      cur[u] = vi < vend ? ld_stream(vp + vi) : neg_inf;
     }
   }
+  __syncthreads();
 
-  // Unaligned head (rank 0) and tail (last rank) elements, one per lane.
-  if (warp == 0) {
-    uint64_t keys[EPV];
+  uint64_t warp_thr = 0;
+  for (int it = 0; it < iters; ++it) {
+    if (it + 1 < iters) {
 #pragma unroll
-    for (int e = 0; e < EPV; ++e) keys[e] = 0;
-    uint32_t pend = 0;
+      for (int u = 0; u < kU; ++u) {
+        const int vi = vidx(it + 1, u);
+        nxt[u] = vi < vend ? ld_stream(vp + vi) : neg_inf;
+      }
+    }
+    uint64_t thr = s_thr;
+    if (it == 0 && K <= 32) {
+      // Seed: the K-th largest of the warp's 32 lane maxima.  At least K elements reach that
+      // value, so a key threshold with that value and index part 0 drops only elements that
+      // cannot be in the top K.
+      uint32_t mb = vec_max_bits<kBf16>(cur[0]);
+#pragma unroll
+      for (int u = 1; u < kU; ++u) mb = __float_as_uint(fmaxf(__uint_as_float(mb), __uint_as_float(vec_max_bits<kBf16>(cur[u]))));
+      const uint64_t m = (static_cast<uint64_t>(ord32(mb)) << 32) | static_cast<uint64_t>(31 - lane);
+      int above = 0;
+      for (int o = 0; o < 32; ++o) above += (__shfl_sync(kFull, m, o) > m);
+      const uint32_t is_kth = __ballot_sync(kFull, above == K - 1);
+      const uint64_t kth = __shfl_sync(kFull, m, __ffs(is_kth) - 1);
+      warp_thr = kth & 0xFFFFFFFF00000000ull;
+    }
+    if (it == 0 && warp_thr > thr) thr = warp_thr;
+    const float tval = key_value(thr);
+    const bool fast = thr != 0 && tval > -INFINITY;
+    bool maybe = true;
+    if (fast) {
+      uint4 mx = cur[0];
+#pragma unroll
+      for (int u = 1; u < kU; ++u) mx = vmax<kBf16>(mx, cur[u]);
+      maybe = !all_below<kBf16>(mx, tval);
+    }
+    if (__any_sync(kFull, maybe)) {
+      uint32_t mask = 0;  // bit u*EPV + e: element e of vector u is a candidate
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int vi = vidx(it, u);
+        if (maybe && vi < vend) {
+#pragma unroll
+          for (int e = 0; e < EPV; ++e)
+            if (make_key(elem_bits<kBf16>(cur[u], e), head + vi * EPV + e) > thr) mask |= 1u << (u * EPV + e);
+        }
+      }
+      const int n = __popc(mask);
+      int incl = n;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += t;
+      }
+      const int total = __shfl_sync(kFull, incl, 31);
+      int start = 0;
+      if (lane == 31 && total > 0) start = atomicAdd(&s_cnt, total);
+      int pos = __shfl_sync(kFull, start, 31) + incl - n;
+      while (mask) {
+        const int b = __ffs(mask) - 1;
+        mask &= mask - 1;
+        const int u = b / EPV, e = b % EPV;
+        uint4 vv = cur[0];
+#pragma unroll
+        for (int q = 1; q < kU; ++q)
+          if (q == u) vv = cur[q];
+        s_buf[pos++] = make_key(elem_bits<kBf16>(vv, e), head + vidx(it, u) * EPV + e);
+      }
+    }
+    __syncthreads();
+    const int cnt = s_cnt;
+    __syncthreads();  // every thread has read the count before the next appends
+    if (cnt > kCapLow) {
+      select_top(s_buf, cnt, K, s_keep);
+      if (threadIdx.x < K) s_buf[threadIdx.x] = s_keep[threadIdx.x];
+      if (threadIdx.x == 0) {
+        s_cnt = K;
+        s_thr = s_keep[K - 1];
+      }
+      __syncthreads();
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) cur[u] = nxt[u];
+  }
+
+  // Unaligned head (rank 0) and tail (last rank) elements, one per lane of warp 0.
+  if (warp == 0) {
     const char* rowp = static_cast<const char*>(logits) + e0 * (kBf16 ? 2 : 4);
-    auto scalar_key = [&](int idx) {
+    int idx = -1;
+    if (rank == 0 && lane < head) idx = lane;
+    if (rank == S - 1 && lane >= 16 && lane - 16 < tail) idx = head + nvec * EPV + (lane - 16);
+    const bool has = idx >= 0;
+    const uint32_t bal = __ballot_sync(kFull, has);
+    int start = 0;
+    if (lane == 0 && bal) start = atomicAdd(&s_cnt, __popc(bal));
+    start = __shfl_sync(kFull, start, 0);
+    if (has) {
       uint32_t bits;
       if constexpr (kBf16) {
         bits = static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(rowp)[idx]) << 16;
       } else {
         bits = reinterpret_cast<const uint32_t*>(rowp)[idx];
       }
-      return make_key(bits, idx);
-    };
-    if (rank == 0 && lane < head) {
-      keys[0] = scalar_key(lane);
-      pend = keys[0] > filt ? 1u : 0u;
+      s_buf[start + __popc(bal & ((1u << lane) - 1))] = make_key(bits, idx);
     }
-    offer<KW, EPV>(L, keys, pend, filt, lane, &s_thresh);
-    pend = 0;
-    keys[0] = 0;
-    if (rank == S - 1 && lane < tail) {
-      keys[0] = scalar_key(head + nvec * EPV + lane);
-      pend = keys[0] > filt ? 1u : 0u;
-    }
-    offer<KW, EPV>(L, keys, pend, filt, lane, &s_thresh);
-  }
-
-  // Block merge: rank every warp entry among all of them.
-#pragma unroll
-  for (int j = 0; j < KW; ++j) {
-    const int idx = j * 32 + lane;
-    if (idx < K) s_warp[warp * K + idx] = L.e[j];
-  }
-  if (threadIdx.x < K) s_block[threadIdx.x] = 0;
-  __syncthreads();
-  const int total = kWarps * K;
-  for (int c = threadIdx.x; c < total; c += kThreads) {
-    const uint64_t x = s_warp[c];
-    if (x == 0) continue;
-    int above = 0;
-    for (int o = 0; o < total; ++o) above += (s_warp[o] > x);
-    if (above < K) s_block[above] = x;
   }
   __syncthreads();
+  select_top(s_buf, s_cnt, K, s_keep);
 
-  const uint64_t* final_keys = s_block;
   if (S > 1) {
     // Push this block's K keys into block 0 of the cluster, then block 0 merges S*K keys.
     if (threadIdx.x < K) {
       const uint32_t dst = map_to_rank(smem_u32(&s_cluster[rank * K + threadIdx.x]), 0);
-      st_cluster_u64(dst, s_block[threadIdx.x]);
+      st_cluster_u64(dst, s_keep[threadIdx.x]);
     }
     cluster_sync();
     if (rank != 0) return;
-    if (threadIdx.x < K) s_block[threadIdx.x] = 0;
-    __syncthreads();
-    const int tot = S * K;
-    for (int c = threadIdx.x; c < tot; c += kThreads) {
-      const uint64_t x = s_cluster[c];
-      if (x == 0) continue;
-      int above = 0;
-      for (int o = 0; o < tot; ++o) above += (s_cluster[o] > x);
-      if (above < K) s_block[above] = x;
-    }
-    __syncthreads();
-    final_keys = s_block;
+    int tot = S * K;
+    // drop empty slots (blocks whose segment held fewer than K elements) before ranking
+    select_top(s_cluster, tot, K, s_keep);
   }
   if (threadIdx.x < K) {
-    const uint64_t x = final_keys[threadIdx.x];
+    const uint64_t x = s_keep[threadIdx.x];
     vals[row * K + threadIdx.x] = key_value(x);
     ids[row * K + threadIdx.x] = static_cast<int32_t>(key_index(x));
   }
 }
 
-template <bool kBf16, int KW>
+template <bool kBf16>
 cudaError_t launch_topk_t(const void* logits, int rows, int V, int K, int S, float* vals, int32_t* ids,
                           cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
@@ -339,21 +302,47 @@ cudaError_t launch_topk_t(const void* logits, int rows, int V, int K, int S, flo
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = S > 1 ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, topk_kernel<kBf16, KW>, logits, V, K, S, vals, ids);
+  return cudaLaunchKernelEx(&cfg, topk_kernel<kBf16>, logits, V, K, S, vals, ids);
+}
+
+// Blocks per row: the split (<= 8) whose grid fills the most of its last wave, preferring
+// fewer blocks on ties and keeping every segment at 16 KB or more.
+int auto_split(int rows, int V, bool bf16) {
+  static int slots = 0;
+  if (slots == 0) {
+    int dev = 0, sms = 152, per_sm = 1;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (bf16)
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, topk_kernel<true>, kThreads, 0);
+    else
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, topk_kernel<false>, kThreads, 0);
+    slots = sms * (per_sm > 0 ? per_sm : 1);
+  }
+  const int64_t row_bytes = static_cast<int64_t>(V) * (bf16 ? 2 : 4);
+  int best = 1;
+  double best_eff = -1.0;
+  for (int s = 1; s <= kMaxSplit; ++s) {
+    if (s > 1 && row_bytes / s < 16 * 1024) break;
+    const double waves = static_cast<double>(rows) * s / slots;
+    const double eff = waves / std::ceil(waves);
+    if (eff > best_eff + 1e-3) {
+      best_eff = eff;
+      best = s;
+    }
+  }
+  return best;
 }
 
 }  // namespace
 
 cudaError_t launch_topk(const void* logits, bool is_bf16, int rows, int V, int K, int ctas_per_row, float* vals,
                         int32_t* ids, cudaStream_t stream) {
-  const int S = ctas_per_row < 1 ? 1 : (ctas_per_row > kMaxSplit ? kMaxSplit : ctas_per_row);
-  if (rows > 65535) return cudaErrorInvalidConfiguration;
-  if (is_bf16) {
-    return K <= 32 ? launch_topk_t<true, 1>(logits, rows, V, K, S, vals, ids, stream)
-                   : launch_topk_t<true, 2>(logits, rows, V, K, S, vals, ids, stream);
-  }
-  return K <= 32 ? launch_topk_t<false, 1>(logits, rows, V, K, S, vals, ids, stream)
-                 : launch_topk_t<false, 2>(logits, rows, V, K, S, vals, ids, stream);
+  if (rows > 65535 || K > kMaxK) return cudaErrorInvalidConfiguration;
+  int S = ctas_per_row > 0 ? ctas_per_row : auto_split(rows, V, is_bf16);
+  S = S < 1 ? 1 : (S > kMaxSplit ? kMaxSplit : S);
+  return is_bf16 ? launch_topk_t<true>(logits, rows, V, K, S, vals, ids, stream)
+                 : launch_topk_t<false>(logits, rows, V, K, S, vals, ids, stream);
 }
 
 }  // namespace dcoco
