@@ -13,16 +13,17 @@
 //  * A row is split over a cluster of S thread blocks (grid.x = S, S <= 8, chosen so the
 //    grid fills whole waves of the GPU).  A block streams its segment with 128-bit loads
 //    (8 bf16 per lane), the next iteration's loads in flight while the current one is
-//    filtered.
-//  * Filtering is against one block-wide key threshold: a lane rejects its 16 values with
-//    packed bf16 max instructions when all fall below it.  Survivors are appended to a
-//    block-wide candidate buffer in shared memory.  At the end of an iteration, if the
-//    buffer holds more than 128 keys, the block keeps its K largest (rank counting) and
-//    the K-th becomes the new threshold.  The first iteration is seeded per warp with the
-//    K-th largest of its 32 lane maxima, a valid lower bound on the K-th value.
-//  * The buffer can take one full iteration of appends on top of 128 entries, so it never
-//    overflows.  At the end each block selects its K largest keys, pushes them into block
-//    0 of the cluster (distributed shared memory), and block 0 merges S*K keys.
+//    filtered.  The streaming loop has no barrier.
+//  * Threshold: from the block's first 256 x 16 values, the K-th largest of the 256 lane
+//    maxima (each warp sorts its 32 maxima with shuffles; ranks come from binary searches
+//    in the 8 sorted lists).  K values reach it, so anything smaller is not in the top K.
+//    Lanes reject their values with packed bf16 max instructions; only vectors that may hold
+//    a candidate are looked at element by element, and only survivors become keys.
+//  * Survivors go to a block-wide shared-memory buffer.  At the end the block selects its K
+//    largest keys by rank counting, pushes them into block 0 of the cluster (distributed
+//    shared memory), and block 0 ranks the S sorted lists by binary search.
+//  * Rows that defeat the threshold (all values equal, sorted rows, NaN rows) overflow the
+//    buffer; the block then recomputes its segment exactly with per-warp register lists.
 #include <cuda_bf16.h>
 
 #include <cmath>
@@ -38,13 +39,11 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kU = 2;          // 16-byte vectors per lane per iteration
 constexpr int kMaxSplit = 8;
 constexpr int kMaxK = 64;
-constexpr int kCapLow = 128;   // compaction trigger
+constexpr int kCap = 1024;     // candidate buffer (keys)
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
 template <bool kBf16>
 constexpr int kEpv = kBf16 ? 8 : 4;  // elements per 16-byte vector
-template <bool kBf16>
-constexpr int kCap = kCapLow + kThreads * kU * kEpv<kBf16> + 32;  // + one warp of head/tail
 
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
   uint4 v;
@@ -89,18 +88,38 @@ template <bool kBf16>
 __device__ __forceinline__ uint32_t vec_max_bits(const uint4& v) {
   if constexpr (kBf16) {
     const uint32_t m = bmax2(bmax2(v.x, v.y), bmax2(v.z, v.w));
-    const float hi = __uint_as_float(m & 0xFFFF0000u), lo = __uint_as_float(m << 16);
-    return __float_as_uint(fmaxf(hi, lo));
+    return __float_as_uint(fmaxf(__uint_as_float(m & 0xFFFF0000u), __uint_as_float(m << 16)));
   } else {
     return __float_as_uint(fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)),
                                  fmaxf(__uint_as_float(v.z), __uint_as_float(v.w))));
   }
 }
 
-// True when every element of the vector is strictly below `tval` (NaN never rejects).
-template <bool kBf16>
-__device__ __forceinline__ bool all_below(const uint4& v, float tval) {
-  return __uint_as_float(vec_max_bits<kBf16>(v)) < tval;
+// Descending bitonic sort of one key per lane across the warp.
+__device__ __forceinline__ uint64_t warp_sort_desc(uint64_t x, int lane) {
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const uint64_t y = __shfl_xor_sync(kFull, x, j);
+      const bool keep_max = ((lane & j) == 0) == ((lane & k) == 0);
+      x = keep_max ? (x > y ? x : y) : (x < y ? x : y);
+    }
+  }
+  return x;
+}
+
+// Number of entries greater than x in a descending list of n keys.
+__device__ __forceinline__ int count_greater(const uint64_t* list, int n, uint64_t x) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (list[mid] > x)
+      lo = mid + 1;
+    else
+      hi = mid;
+  }
+  return lo;
 }
 
 // Keep the K largest keys of s_buf[0, cnt) in s_keep[0, K) (descending; 0 where cnt < K).
@@ -117,16 +136,108 @@ __device__ __forceinline__ void select_top(const uint64_t* s_buf, int cnt, int K
   __syncthreads();
 }
 
-template <bool kBf16>
+// Exact fallback for rows the threshold cannot thin out: a descending top-K list per warp in
+// registers (entry j*32 + lane in e[j] of `lane`), one insertion per surviving key.
+template <int KW>
+struct WarpTopK {
+  uint64_t e[KW];
+  int K;
+  uint64_t kth;  // entry K-1 (0 while the list is not full)
+
+  __device__ __forceinline__ void init(int k) {
+#pragma unroll
+    for (int j = 0; j < KW; ++j) e[j] = 0;
+    K = k;
+    kth = 0;
+  }
+  __device__ __forceinline__ void insert(uint64_t x, int lane) {
+    int pos = 0;
+#pragma unroll
+    for (int j = 0; j < KW; ++j) pos += __popc(__ballot_sync(kFull, e[j] > x));
+    uint64_t prev[KW];
+#pragma unroll
+    for (int j = 0; j < KW; ++j) {
+      const uint64_t up = __shfl_up_sync(kFull, e[j], 1);
+      const uint64_t wrap = (j > 0) ? __shfl_sync(kFull, e[j > 0 ? j - 1 : 0], 31) : 0ull;
+      prev[j] = (lane == 0) ? wrap : up;
+    }
+#pragma unroll
+    for (int j = 0; j < KW; ++j) {
+      const int idx = j * 32 + lane;
+      e[j] = (idx < pos) ? e[j] : (idx == pos ? x : prev[j]);
+    }
+    const int last = K - 1;
+    uint64_t t = 0;
+#pragma unroll
+    for (int j = 0; j < KW; ++j) {
+      const uint64_t v = __shfl_sync(kFull, e[j], last & 31);
+      if ((last >> 5) == j) t = v;
+    }
+    kth = t;
+  }
+  // Offer one key per lane (0 = none), lowest lane first.
+  __device__ __forceinline__ void offer(uint64_t mine, int lane) {
+    uint32_t pend = __ballot_sync(kFull, mine > kth);
+    while (pend) {
+      const int src = __ffs(pend) - 1;
+      pend &= pend - 1;
+      const uint64_t x = __shfl_sync(kFull, mine, src);
+      if (x > kth) insert(x, lane);
+    }
+  }
+};
+
+struct Segment {
+  const char* rowp;  // first element of the row
+  const uint4* vp;   // first 16-byte aligned vector of the row
+  int head, nvec, tail, vbeg, vend;
+};
+
+template <bool kBf16, int KW>
+__device__ __noinline__ void exact_segment_topk(const Segment& g, int K, int rank, int S, uint64_t* s_wl,
+                                                uint64_t* s_keep) {
+  constexpr int EPV = kEpv<kBf16>;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  WarpTopK<KW> L;
+  L.init(K);
+  for (int vi = g.vbeg + static_cast<int>(threadIdx.x); vi - lane < g.vend; vi += kThreads) {  // warp-uniform trip count
+    const bool valid = vi < g.vend;
+    const uint4 v = valid ? ld_stream(g.vp + vi) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) L.offer(valid ? make_key(elem_bits<kBf16>(v, e), g.head + vi * EPV + e) : 0ull, lane);
+  }
+  if (warp == 0) {
+    int idx = -1;
+    if (rank == 0 && lane < g.head) idx = lane;
+    if (rank == S - 1 && lane >= 16 && lane - 16 < g.tail) idx = g.head + g.nvec * EPV + (lane - 16);
+    uint64_t k = 0;
+    if (idx >= 0) {
+      const uint32_t bits = kBf16 ? static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(g.rowp)[idx]) << 16
+                                  : reinterpret_cast<const uint32_t*>(g.rowp)[idx];
+      k = make_key(bits, idx);
+    }
+    L.offer(k, lane);
+  }
+#pragma unroll
+  for (int j = 0; j < KW; ++j) {
+    const int idx = j * 32 + lane;
+    if (idx < K) s_wl[warp * K + idx] = L.e[j];
+  }
+  __syncthreads();
+  select_top(s_wl, kWarps * K, K, s_keep);
+}
+
+template <bool kBf16, int KW>
 __global__ void __launch_bounds__(kThreads) topk_kernel(const void* __restrict__ logits, int V, int K, int S,
                                                         float* __restrict__ vals, int32_t* __restrict__ ids) {
   constexpr int EPV = kEpv<kBf16>;
-  constexpr int CAP = kCap<kBf16>;
-  __shared__ uint64_t s_buf[CAP];
+  __shared__ uint64_t s_buf[kCap];
+  __shared__ uint64_t s_sorted[kThreads];  // each warp's lane maxima, sorted
+  __shared__ uint64_t s_wl[kWarps * kMaxK];
   __shared__ uint64_t s_keep[kMaxK];
   __shared__ uint64_t s_cluster[kMaxSplit * kMaxK];
   __shared__ uint64_t s_thr;
-  __shared__ int s_cnt;
+  __shared__ int s_cnt, s_overflow;
 
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
@@ -134,76 +245,88 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const void* __restrict__
   const int64_t row = blockIdx.y;
   if (threadIdx.x == 0) {
     s_cnt = 0;
+    s_overflow = 0;
     s_thr = 0;
   }
 
+  Segment g;
   const int64_t e0 = row * static_cast<int64_t>(V);
-  int head = static_cast<int>((EPV - (e0 % EPV)) % EPV);
-  if (head > V) head = V;
-  const int nvec = (V - head) / EPV;
-  const int tail = V - head - nvec * EPV;
-  const uint4* vp = reinterpret_cast<const uint4*>(static_cast<const char*>(logits) + (e0 + head) * (kBf16 ? 2 : 4));
-  const int vbeg = static_cast<int>(static_cast<int64_t>(rank) * nvec / S);
-  const int vend = static_cast<int>(static_cast<int64_t>(rank + 1) * nvec / S);
+  g.rowp = static_cast<const char*>(logits) + e0 * (kBf16 ? 2 : 4);
+  g.head = static_cast<int>((EPV - (e0 % EPV)) % EPV);
+  if (g.head > V) g.head = V;
+  g.nvec = (V - g.head) / EPV;
+  g.tail = V - g.head - g.nvec * EPV;
+  g.vp = reinterpret_cast<const uint4*>(g.rowp + static_cast<int64_t>(g.head) * (kBf16 ? 2 : 4));
+  g.vbeg = static_cast<int>(static_cast<int64_t>(rank) * g.nvec / S);
+  g.vend = static_cast<int>(static_cast<int64_t>(rank + 1) * g.nvec / S);
   constexpr int CH = kWarps * kU * 32;  // vectors per block iteration
-  const int iters = (vend - vbeg + CH - 1) / CH;
+  const int iters = (g.vend - g.vbeg + CH - 1) / CH;
+  auto vidx = [&](int it, int u) { return g.vbeg + it * CH + (warp * kU + u) * 32 + lane; };
 
+  // Lanes past the end of the segment see -inf.
   const uint4 neg_inf = kBf16 ? make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u)
                               : make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u);
-  auto vidx = [&](int it, int u) { return vbeg + it * CH + (warp * kU + u) * 32 + lane; };
   uint4 cur[kU], nxt[kU];
-  if (iters > 0) {
+#pragma unroll
+  for (int u = 0; u < kU; ++u) {
+    const int vi = vidx(0, u);
+    cur[u] = (iters > 0 && vi < g.vend) ? ld_stream(g.vp + vi) : neg_inf;
+  }
+
+  // Seed threshold: the K-th largest of the block's 256 lane maxima (first iteration).
+  {
+    uint64_t mk = 0;
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
-      const int vi = vidx(0, u);
-      cur[u] = vi < vend ? ld_stream(vp + vi) : neg_inf;
+      if (iters > 0 && vidx(0, u) < g.vend) {
+        const uint64_t k = (static_cast<uint64_t>(ord32(vec_max_bits<kBf16>(cur[u]))) << 32) |
+                           static_cast<uint64_t>(0xFFFFFFFFu - threadIdx.x);
+        mk = k > mk ? k : mk;
+      }
     }
+    s_sorted[threadIdx.x] = warp_sort_desc(mk, lane);
+    __syncthreads();
+    const uint64_t x = s_sorted[threadIdx.x];
+    if (x != 0 && K <= kThreads) {
+      int above = 0;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) above += count_greater(s_sorted + w * 32, 32, x);
+      if (above == K - 1) s_thr = x & 0xFFFFFFFF00000000ull;  // value part only: keeps ties
+    }
+    __syncthreads();
   }
-  __syncthreads();
+  const uint64_t thr = s_thr;
+  const float tval = key_value(thr);
+  const bool fast = thr != 0 && tval > -INFINITY;
 
-  uint64_t warp_thr = 0;
   for (int it = 0; it < iters; ++it) {
     if (it + 1 < iters) {
 #pragma unroll
       for (int u = 0; u < kU; ++u) {
         const int vi = vidx(it + 1, u);
-        nxt[u] = vi < vend ? ld_stream(vp + vi) : neg_inf;
+        nxt[u] = vi < g.vend ? ld_stream(g.vp + vi) : neg_inf;
       }
     }
-    uint64_t thr = s_thr;
-    if (it == 0 && K <= 32) {
-      // Seed: the K-th largest of the warp's 32 lane maxima.  At least K elements reach that
-      // value, so a key threshold with that value and index part 0 drops only elements that
-      // cannot be in the top K.
-      uint32_t mb = vec_max_bits<kBf16>(cur[0]);
-#pragma unroll
-      for (int u = 1; u < kU; ++u) mb = __float_as_uint(fmaxf(__uint_as_float(mb), __uint_as_float(vec_max_bits<kBf16>(cur[u]))));
-      const uint64_t m = (static_cast<uint64_t>(ord32(mb)) << 32) | static_cast<uint64_t>(31 - lane);
-      int above = 0;
-      for (int o = 0; o < 32; ++o) above += (__shfl_sync(kFull, m, o) > m);
-      const uint32_t is_kth = __ballot_sync(kFull, above == K - 1);
-      const uint64_t kth = __shfl_sync(kFull, m, __ffs(is_kth) - 1);
-      warp_thr = kth & 0xFFFFFFFF00000000ull;
-    }
-    if (it == 0 && warp_thr > thr) thr = warp_thr;
-    const float tval = key_value(thr);
-    const bool fast = thr != 0 && tval > -INFINITY;
     bool maybe = true;
     if (fast) {
       uint4 mx = cur[0];
 #pragma unroll
       for (int u = 1; u < kU; ++u) mx = vmax<kBf16>(mx, cur[u]);
-      maybe = !all_below<kBf16>(mx, tval);
+      maybe = !(__uint_as_float(vec_max_bits<kBf16>(mx)) < tval);
     }
     if (__any_sync(kFull, maybe)) {
       uint32_t mask = 0;  // bit u*EPV + e: element e of vector u is a candidate
 #pragma unroll
       for (int u = 0; u < kU; ++u) {
         const int vi = vidx(it, u);
-        if (maybe && vi < vend) {
+        if (maybe && vi < g.vend && !(fast && __uint_as_float(vec_max_bits<kBf16>(cur[u])) < tval)) {
 #pragma unroll
-          for (int e = 0; e < EPV; ++e)
-            if (make_key(elem_bits<kBf16>(cur[u], e), head + vi * EPV + e) > thr) mask |= 1u << (u * EPV + e);
+          for (int e = 0; e < EPV; ++e) {
+            const uint32_t bits = elem_bits<kBf16>(cur[u], e);
+            if (!fast || __uint_as_float(bits) >= tval) {
+              if (make_key(bits, g.head + vi * EPV + e) > thr) mask |= 1u << (u * EPV + e);
+            }
+          }
         }
       }
       const int n = __popc(mask);
@@ -214,31 +337,25 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const void* __restrict__
         if (lane >= o) incl += t;
       }
       const int total = __shfl_sync(kFull, incl, 31);
-      int start = 0;
-      if (lane == 31 && total > 0) start = atomicAdd(&s_cnt, total);
-      int pos = __shfl_sync(kFull, start, 31) + incl - n;
-      while (mask) {
-        const int b = __ffs(mask) - 1;
-        mask &= mask - 1;
-        const int u = b / EPV, e = b % EPV;
-        uint4 vv = cur[0];
+      if (total > 0) {
+        int start = 0;
+        if (lane == 31) start = atomicAdd(&s_cnt, total);
+        int pos = __shfl_sync(kFull, start, 31) + incl - n;
+        while (mask) {
+          const int b = __ffs(mask) - 1;
+          mask &= mask - 1;
+          const int u = b / EPV, e = b % EPV;
+          uint4 vv = cur[0];
 #pragma unroll
-        for (int q = 1; q < kU; ++q)
-          if (q == u) vv = cur[q];
-        s_buf[pos++] = make_key(elem_bits<kBf16>(vv, e), head + vidx(it, u) * EPV + e);
+          for (int q = 1; q < kU; ++q)
+            if (q == u) vv = cur[q];
+          if (pos < kCap)
+            s_buf[pos] = make_key(elem_bits<kBf16>(vv, e), g.head + vidx(it, u) * EPV + e);
+          else
+            s_overflow = 1;
+          ++pos;
+        }
       }
-    }
-    __syncthreads();
-    const int cnt = s_cnt;
-    __syncthreads();  // every thread has read the count before the next appends
-    if (cnt > kCapLow) {
-      select_top(s_buf, cnt, K, s_keep);
-      if (threadIdx.x < K) s_buf[threadIdx.x] = s_keep[threadIdx.x];
-      if (threadIdx.x == 0) {
-        s_cnt = K;
-        s_thr = s_keep[K - 1];
-      }
-      __syncthreads();
     }
 #pragma unroll
     for (int u = 0; u < kU; ++u) cur[u] = nxt[u];
@@ -246,39 +363,50 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const void* __restrict__
 
   // Unaligned head (rank 0) and tail (last rank) elements, one per lane of warp 0.
   if (warp == 0) {
-    const char* rowp = static_cast<const char*>(logits) + e0 * (kBf16 ? 2 : 4);
     int idx = -1;
-    if (rank == 0 && lane < head) idx = lane;
-    if (rank == S - 1 && lane >= 16 && lane - 16 < tail) idx = head + nvec * EPV + (lane - 16);
+    if (rank == 0 && lane < g.head) idx = lane;
+    if (rank == S - 1 && lane >= 16 && lane - 16 < g.tail) idx = g.head + g.nvec * EPV + (lane - 16);
     const bool has = idx >= 0;
     const uint32_t bal = __ballot_sync(kFull, has);
     int start = 0;
     if (lane == 0 && bal) start = atomicAdd(&s_cnt, __popc(bal));
     start = __shfl_sync(kFull, start, 0);
     if (has) {
-      uint32_t bits;
-      if constexpr (kBf16) {
-        bits = static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(rowp)[idx]) << 16;
-      } else {
-        bits = reinterpret_cast<const uint32_t*>(rowp)[idx];
-      }
-      s_buf[start + __popc(bal & ((1u << lane) - 1))] = make_key(bits, idx);
+      const uint32_t bits = kBf16 ? static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(g.rowp)[idx]) << 16
+                                  : reinterpret_cast<const uint32_t*>(g.rowp)[idx];
+      const int pos = start + __popc(bal & ((1u << lane) - 1));
+      if (pos < kCap)
+        s_buf[pos] = make_key(bits, idx);
+      else
+        s_overflow = 1;
     }
   }
   __syncthreads();
-  select_top(s_buf, s_cnt, K, s_keep);
+  if (s_overflow)
+    exact_segment_topk<kBf16, KW>(g, K, rank, S, s_wl, s_keep);
+  else
+    select_top(s_buf, s_cnt, K, s_keep);
 
   if (S > 1) {
-    // Push this block's K keys into block 0 of the cluster, then block 0 merges S*K keys.
+    // Push this block's K keys into block 0 of the cluster; block 0 ranks every key among the
+    // S sorted lists with binary searches.
     if (threadIdx.x < K) {
       const uint32_t dst = map_to_rank(smem_u32(&s_cluster[rank * K + threadIdx.x]), 0);
       st_cluster_u64(dst, s_keep[threadIdx.x]);
     }
     cluster_sync();
     if (rank != 0) return;
-    int tot = S * K;
-    // drop empty slots (blocks whose segment held fewer than K elements) before ranking
-    select_top(s_cluster, tot, K, s_keep);
+    for (int c = threadIdx.x; c < S * K; c += kThreads) {
+      const uint64_t x = s_cluster[c];
+      if (x == 0) continue;
+      int above = 0;
+      for (int w = 0; w < S; ++w) above += count_greater(s_cluster + w * K, K, x);
+      if (above < K) {
+        vals[row * K + above] = key_value(x);
+        ids[row * K + above] = static_cast<int32_t>(key_index(x));
+      }
+    }
+    return;
   }
   if (threadIdx.x < K) {
     const uint64_t x = s_keep[threadIdx.x];
@@ -287,7 +415,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const void* __restrict__
   }
 }
 
-template <bool kBf16>
+template <bool kBf16, int KW>
 cudaError_t launch_topk_t(const void* logits, int rows, int V, int K, int S, float* vals, int32_t* ids,
                           cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
@@ -302,7 +430,7 @@ cudaError_t launch_topk_t(const void* logits, int rows, int V, int K, int S, flo
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = S > 1 ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, topk_kernel<kBf16>, logits, V, K, S, vals, ids);
+  return cudaLaunchKernelEx(&cfg, topk_kernel<kBf16, KW>, logits, V, K, S, vals, ids);
 }
 
 // Blocks per row: the split (<= 8) whose grid fills the most of its last wave, preferring
@@ -314,9 +442,9 @@ int auto_split(int rows, int V, bool bf16) {
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (bf16)
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, topk_kernel<true>, kThreads, 0);
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, topk_kernel<true, 1>, kThreads, 0);
     else
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, topk_kernel<false>, kThreads, 0);
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, topk_kernel<false, 1>, kThreads, 0);
     slots = sms * (per_sm > 0 ? per_sm : 1);
   }
   const int64_t row_bytes = static_cast<int64_t>(V) * (bf16 ? 2 : 4);
@@ -341,8 +469,11 @@ cudaError_t launch_topk(const void* logits, bool is_bf16, int rows, int V, int K
   if (rows > 65535 || K > kMaxK) return cudaErrorInvalidConfiguration;
   int S = ctas_per_row > 0 ? ctas_per_row : auto_split(rows, V, is_bf16);
   S = S < 1 ? 1 : (S > kMaxSplit ? kMaxSplit : S);
-  return is_bf16 ? launch_topk_t<true>(logits, rows, V, K, S, vals, ids, stream)
-                 : launch_topk_t<false>(logits, rows, V, K, S, vals, ids, stream);
+  if (is_bf16)
+    return K <= 32 ? launch_topk_t<true, 1>(logits, rows, V, K, S, vals, ids, stream)
+                   : launch_topk_t<true, 2>(logits, rows, V, K, S, vals, ids, stream);
+  return K <= 32 ? launch_topk_t<false, 1>(logits, rows, V, K, S, vals, ids, stream)
+                 : launch_topk_t<false, 2>(logits, rows, V, K, S, vals, ids, stream);
 }
 
 }  // namespace dcoco
