@@ -178,10 +178,14 @@ size_t pair_scratch(const Dims& D, Carve& c, PairScratch* s) {
 }
 
 // ---------------------------------------------------------------- GEMM helpers
+// One output group: weight block [rows, cols] (pitch in elements) -> out [M, rows] (pitch ldo).
 int gemm_group(GemmGroup* g, const void* w_base, const Dims& D, uint64_t rows, uint64_t cols, uint64_t pitch, int BN,
-               void* out, int ldo, int epi) {
+               void* out, int ldo, int epi, int M) {
   const char* err = nullptr;
   if (!make_tmap(&g->b_map, w_base, D.bf16, rows, cols, pitch, static_cast<uint32_t>(std::min(BN, 256)), &err))
+    return fail(DCOCO_ERR_CUDA, "%s", err);
+  const bool out_bf16 = D.bf16 && epi != EPI_F32;
+  if (!make_tmap(&g->out_map, out, out_bf16, static_cast<uint64_t>(M), rows, static_cast<uint64_t>(ldo), 32, &err))
     return fail(DCOCO_ERR_CUDA, "%s", err);
   g->out = out;
   g->ldo = ldo;
@@ -230,7 +234,7 @@ int enqueue_repr(const Dims& D, const int32_t* ids, const void* emb, int V, cons
     a.n_groups = 1;
     const int BN = pick_bn(r, true);
     if (BN != r) return fail(DCOCO_ERR_UNSUPPORTED, "r=%d", r);
-    DCOCO_TRY(gemm_group(&a.g[0], w->W_e, D, r, D.E, D.E, BN, s.b, r, EPI_LN));
+    DCOCO_TRY(gemm_group(&a.g[0], w->W_e, D, r, D.E, D.E, BN, s.b, r, EPI_LN, a.M));
     DCOCO_TRY(run_gemm(a, D, BN, st, "gemm b = LN(W_e Emb[c])"));
   }
   // g = LN(W_h h)
@@ -241,7 +245,7 @@ int enqueue_repr(const Dims& D, const int32_t* ids, const void* emb, int V, cons
     a.K = D.d;
     a.n_groups = 1;
     const int BN = r;
-    DCOCO_TRY(gemm_group(&a.g[0], w->W_h, D, r, D.d, D.d, BN, s.g, r, EPI_LN));
+    DCOCO_TRY(gemm_group(&a.g[0], w->W_h, D, r, D.d, D.d, BN, s.g, r, EPI_LN, a.M));
     DCOCO_TRY(run_gemm(a, D, BN, st, "gemm g = LN(W_h h)"));
   }
   // gw = W_f[:, r:2r] g   (the g half of the fusion, once per slot)
@@ -252,7 +256,7 @@ int enqueue_repr(const Dims& D, const int32_t* ids, const void* emb, int V, cons
     a.K = r;
     a.n_groups = 1;
     const int BN = pick_bn(r, false);
-    DCOCO_TRY(gemm_group(&a.g[0], static_cast<const char*>(w->W_f) + r * D.esz, D, r, r, 2 * r, BN, s.gw, r, EPI_F32));
+    DCOCO_TRY(gemm_group(&a.g[0], static_cast<const char*>(w->W_f) + r * D.esz, D, r, r, 2 * r, BN, s.gw, r, EPI_F32, a.M));
     DCOCO_TRY(run_gemm(a, D, BN, st, "gemm gw = W_f,g g"));
   }
   // z = SiLU(W_f[:, 0:r] b + gw[slot])
@@ -266,7 +270,7 @@ int enqueue_repr(const Dims& D, const int32_t* ids, const void* emb, int V, cons
     a.bias_div = D.K;
     a.ld_bias = r;
     const int BN = pick_bn(r, false);
-    DCOCO_TRY(gemm_group(&a.g[0], w->W_f, D, r, r, 2 * r, BN, s.z, r, EPI_SILU_BIAS));
+    DCOCO_TRY(gemm_group(&a.g[0], w->W_f, D, r, r, 2 * r, BN, s.z, r, EPI_SILU_BIAS, a.M));
     DCOCO_TRY(run_gemm(a, D, BN, st, "gemm z = SiLU(W_f [b; g])"));
   }
   // uz = U z, vz = V z
@@ -277,8 +281,8 @@ int enqueue_repr(const Dims& D, const int32_t* ids, const void* emb, int V, cons
     a.K = r;
     a.n_groups = 2;
     const int BN = pick_bn(H, false);
-    DCOCO_TRY(gemm_group(&a.g[0], w->U, D, H, r, r, BN, uz, H, EPI_ACT));
-    DCOCO_TRY(gemm_group(&a.g[1], w->V, D, H, r, r, BN, vz, H, EPI_ACT));
+    DCOCO_TRY(gemm_group(&a.g[0], w->U, D, H, r, r, BN, uz, H, EPI_ACT, a.M));
+    DCOCO_TRY(gemm_group(&a.g[1], w->V, D, H, r, r, BN, vz, H, EPI_ACT, a.M));
     DCOCO_TRY(run_gemm(a, D, BN, st, "gemm uz, vz"));
   }
   return DCOCO_OK;
@@ -295,9 +299,9 @@ int enqueue_pair(const Dims& D, const void* h, const dcoco_weights* w, float* ws
     a.K = d;
     a.n_groups = 2;
     const int BN = pick_bn(r, false);
-    DCOCO_TRY(gemm_group(&a.g[0], w->W_pair, D, r, d, 2 * d, BN, s.hp, 2 * r, EPI_F32));
+    DCOCO_TRY(gemm_group(&a.g[0], w->W_pair, D, r, d, 2 * d, BN, s.hp, 2 * r, EPI_F32, a.M));
     DCOCO_TRY(gemm_group(&a.g[1], static_cast<const char*>(w->W_pair) + d * D.esz, D, r, d, 2 * d, BN, s.hp + r,
-                         2 * r, EPI_F32));
+                         2 * r, EPI_F32, a.M));
     DCOCO_TRY(run_gemm(a, D, BN, st, "gemm W_pair h"));
   }
   // s_p = hp[p, 0:r] + hp[p+1, r:2r]
@@ -313,7 +317,7 @@ int enqueue_pair(const Dims& D, const void* h, const dcoco_weights* w, float* ws
     a.K = r;
     a.n_groups = 1;
     const int BN = pick_bn(H, false);
-    DCOCO_TRY(gemm_group(&a.g[0], w->W, D, H, r, r, BN, wsp, H, EPI_F32));
+    DCOCO_TRY(gemm_group(&a.g[0], w->W, D, H, r, r, BN, wsp, H, EPI_F32, a.M));
     DCOCO_TRY(run_gemm(a, D, BN, st, "gemm W s"));
   }
   return DCOCO_OK;
@@ -599,6 +603,10 @@ int dcoco_cycle(const void* logits, int V, const void* emb, const void* h, const
   const int rows = N * B;
   cudaError_t e = launch_topk(logits, D.bf16, rows, V, K, topk_split(rows, V, D.bf16), o_vals, o_ids, st);
   if (e != cudaSuccess) return cuda_fail(e, "top-K launch");
+  // Start fetching the chosen embedding rows into L2 now, whole rows at a time; the pair-state
+  // projections run meanwhile and the gather below then mostly reads L2.
+  e = launch_prefetch_rows(o_ids, D.M(), emb, V, static_cast<int>(D.E * D.esz), st);
+  if (e != cudaSuccess) return cuda_fail(e, "embedding prefetch launch");
   DCOCO_TRY(enqueue_pair(D, h, w, s.wsp, s.pair, st));
   DCOCO_TRY(enqueue_repr(D, o_ids, emb, V, h, w, s.uz, s.vz, s.repr, st));
   DCOCO_TRY(enqueue_scores(D, s.uz, s.vz, s.wsp, o_vals, w, o_S, st));

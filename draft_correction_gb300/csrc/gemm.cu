@@ -42,7 +42,35 @@ struct Elt {
   static constexpr uint32_t fmt = kBf16 ? 1u : 2u;
 };
 
-__device__ __forceinline__ float silu(float x) { return x / (1.0f + __expf(-x)); }
+// SiLU(x) = x sigmoid(x) = h + h tanh(h), h = x/2 (one SFU instruction).
+__device__ __forceinline__ float silu(float x) {
+  const float h = 0.5f * x;
+  return fmaf(h, tanh_approx(h), h);
+}
+
+// One thread's row of a 128-byte-wide output sub-tile into the 128-byte swizzled staging
+// layout a tensor-map store expects (16-byte chunk c of row r at r*128 + (c ^ (r & 7))*16).
+template <bool kOutBf16>
+__device__ __forceinline__ void stage_row(uint8_t* buf, int r, const float* v) {
+  constexpr int NV = kOutBf16 ? 64 : 32;  // values in 128 bytes
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    uint4 w;
+    if constexpr (kOutBf16) {
+      __nv_bfloat162 t0 = __floats2bfloat162_rn(v[8 * c + 0], v[8 * c + 1]);
+      __nv_bfloat162 t1 = __floats2bfloat162_rn(v[8 * c + 2], v[8 * c + 3]);
+      __nv_bfloat162 t2 = __floats2bfloat162_rn(v[8 * c + 4], v[8 * c + 5]);
+      __nv_bfloat162 t3 = __floats2bfloat162_rn(v[8 * c + 6], v[8 * c + 7]);
+      w = make_uint4(*reinterpret_cast<uint32_t*>(&t0), *reinterpret_cast<uint32_t*>(&t1),
+                     *reinterpret_cast<uint32_t*>(&t2), *reinterpret_cast<uint32_t*>(&t3));
+    } else {
+      w = make_uint4(__float_as_uint(v[4 * c]), __float_as_uint(v[4 * c + 1]), __float_as_uint(v[4 * c + 2]),
+                     __float_as_uint(v[4 * c + 3]));
+    }
+    *reinterpret_cast<uint4*>(buf + r * 128 + ((c ^ (r & 7)) << 4)) = w;
+  }
+  (void)NV;
+}
 
 template <bool kBf16>
 __device__ __forceinline__ void store_act(void* out, size_t idx, const float* v, int n) {
@@ -64,10 +92,6 @@ __device__ __forceinline__ void store_act(void* out, size_t idx, const float* v,
     float* o = static_cast<float*>(out) + idx;
     for (int i = 0; i < n; i += 4) *reinterpret_cast<float4*>(o + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
   }
-}
-__device__ __forceinline__ void store_f32(void* out, size_t idx, const float* v, int n) {
-  float* o = static_cast<float*>(out) + idx;
-  for (int i = 0; i < n; i += 4) *reinterpret_cast<float4*>(o + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
 }
 template <bool kBf16>
 __device__ __forceinline__ void store_act1(void* out, size_t idx, float v) {
@@ -251,7 +275,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           *reinterpret_cast<float4*>(&stg[row_local * LDS + c + i]) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
       }
     } else if (ok) {
-      const size_t obase = static_cast<size_t>(live ? m : 0) * grp.ldo + static_cast<size_t>(nt) * BN;
+      // Row-per-thread values go through a swizzled staging buffer per warp (two 32 x 128-byte
+      // halves, reusing the drained pipeline buffers) and leave with tensor-map stores, which
+      // write whole rows coalesced and clip rows past M.
+      const bool out_bf16 = kBf16 && grp.epi != EPI_F32;
+      const int cps = out_bf16 ? 64 : 32;  // output columns per 128-byte sub-tile
+      uint8_t* stg = smem + q * 8192;
+      const int y0 = m_tile * BM + q * 32;
+      const bool any_rows = y0 < args.M;
+      float mean = 0.f, rstd = 1.f;
       if (grp.epi == EPI_LN) {
         float sum = 0.f;
         for (int c = 0; c < BN; c += 32) {
@@ -260,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 #pragma unroll
           for (int i = 0; i < 32; ++i) sum += v[i];
         }
-        const float mean = sum / BN;
+        mean = sum / BN;
         float ss = 0.f;
         for (int c = 0; c < BN; c += 32) {
           float v[32];
@@ -268,41 +300,56 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 #pragma unroll
           for (int i = 0; i < 32; ++i) ss += (v[i] - mean) * (v[i] - mean);
         }
-        const float rstd = rsqrtf(ss / BN + args.ln_eps);
-        for (int c = 0; c < BN; c += 32) {
-          float v[32];
-          tmem_ld32(trow + c, v);
+        rstd = rsqrtf(ss / BN + args.ln_eps);
+      }
+      const float* bias = nullptr;
+      if (grp.epi == EPI_SILU_BIAS && live) {
+        bias = sbias != nullptr ? sbias + (m / args.bias_div - first_slot) * BN
+                                : args.bias + static_cast<size_t>(m / args.bias_div) * args.ld_bias + nt * BN;
+      }
+      // The fused op on 32 consecutive columns starting at `col` (compile-time trip counts).
+      auto apply32 = [&](float(&x)[32], int col) {
+        if (grp.epi == EPI_LN) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = (v[i] - mean) * rstd;
-          if (live) store_act<kBf16>(grp.out, obase + c, v, 32);
-        }
-      } else {
-        const float* bias = nullptr;
-        if (grp.epi == EPI_SILU_BIAS && live) {
-          bias = sbias != nullptr ? sbias + (m / args.bias_div - first_slot) * BN
-                                  : args.bias + static_cast<size_t>(m / args.bias_div) * args.ld_bias + nt * BN;
-        }
-        for (int c = 0; c < BN; c += 32) {
-          float v[32];
-          tmem_ld32(trow + c, v);
-          if (!live) continue;
-          if (grp.epi == EPI_F32) {
-            store_f32(grp.out, obase + c, v, 32);
-          } else {
-            if (bias != nullptr) {
+          for (int i = 0; i < 32; ++i) x[i] = (x[i] - mean) * rstd;
+        } else if (bias != nullptr) {
 #pragma unroll
-              for (int i = 0; i < 32; i += 4) {
-                const float4 bb = *reinterpret_cast<const float4*>(bias + c + i);
-                v[i] = silu(v[i] + bb.x);
-                v[i + 1] = silu(v[i + 1] + bb.y);
-                v[i + 2] = silu(v[i + 2] + bb.z);
-                v[i + 3] = silu(v[i + 3] + bb.w);
-              }
-            }
-            store_act<kBf16>(grp.out, obase + c, v, 32);
+          for (int i = 0; i < 32; i += 4) {
+            const float4 bb = *reinterpret_cast<const float4*>(bias + col + i);
+            x[i] = silu(x[i] + bb.x);
+            x[i + 1] = silu(x[i + 1] + bb.y);
+            x[i + 2] = silu(x[i + 2] + bb.z);
+            x[i + 3] = silu(x[i + 3] + bb.w);
           }
         }
+      };
+      for (int j = 0; j < BN / cps; ++j) {
+        float v[64];
+        float(&lo)[32] = *reinterpret_cast<float(*)[32]>(v);
+        float(&hi)[32] = *reinterpret_cast<float(*)[32]>(v + 32);
+        tmem_ld32(trow + j * cps, lo);
+        apply32(lo, j * cps);
+        if (out_bf16) {
+          tmem_ld32(trow + j * cps + 32, hi);
+          apply32(hi, j * cps + 32);
+        }
+        uint8_t* buf = stg + (j & 1) * 4096;
+        if (j >= 2) {
+          if (lane == 0) bulk_wait_read<1>();  // the store that used this half has read it
+          __syncwarp();
+        }
+        if (out_bf16)
+          stage_row<true>(buf, lane, v);
+        else
+          stage_row<false>(buf, lane, v);
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0 && any_rows) {
+          tma_store_2d(&grp.out_map, nt * BN + j * cps, y0, smem_u32(buf));
+          bulk_commit();
+        }
       }
+      if (lane == 0) bulk_wait<0>();
     }
   }
 
@@ -464,7 +511,22 @@ __global__ void pair_combine_kernel(const float* __restrict__ hp, void* __restri
   }
 }
 
+__global__ void prefetch_rows_kernel(const int32_t* __restrict__ ids, int n, const char* __restrict__ table,
+                                     int table_rows, int row_bytes) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const int r = ids[i];
+  if (r >= 0 && r < table_rows) prefetch_l2_bulk(table + static_cast<size_t>(r) * row_bytes, row_bytes);
+}
+
 }  // namespace
+
+cudaError_t launch_prefetch_rows(const int32_t* ids, int n, const void* table, int table_rows, int row_bytes,
+                                 cudaStream_t stream) {
+  prefetch_rows_kernel<<<(n + 255) / 256, 256, 0, stream>>>(ids, n, static_cast<const char*>(table), table_rows,
+                                                            row_bytes);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_gemm(const GemmArgs& args, bool is_bf16, int BN, int split_k, cudaStream_t stream) {
   if (split_k < 1 || split_k > 8 || (BM % split_k) != 0) return cudaErrorInvalidValue;

@@ -24,8 +24,9 @@ enum Epilogue : int {
 };
 
 struct GemmGroup {
-  CUtensorMap b_map;  // B operand [Ng, K] (K contiguous), 128-byte swizzle, box {BK, min(BN,256)}
-  void* out;          // output base; row m, column n at out[m * ldo + n]
+  CUtensorMap b_map;    // B operand [Ng, K] (K contiguous), 128-byte swizzle, box {BK, min(BN,256)}
+  CUtensorMap out_map;  // output [M, Ng] (pitch ldo), 128-byte swizzle, box {128 bytes, 32 rows}
+  void* out;            // output base; row m, column n at out[m * ldo + n]
   int ldo;
   int epi;
   int n_tiles;        // Ng / BN
@@ -50,6 +51,10 @@ struct GemmArgs {
 // box_rows = 1 gives a gather4 map.
 bool make_tmap(CUtensorMap* map, const void* base, bool is_bf16, uint64_t rows, uint64_t cols, uint64_t pitch_elems,
                uint32_t box_rows, const char** err);
+
+// Asynchronous L2 prefetch of whole table rows table[ids[i]] (row_bytes each), i < n.
+cudaError_t launch_prefetch_rows(const int32_t* ids, int n, const void* table, int table_rows, int row_bytes,
+                                 cudaStream_t stream);
 
 // BN in {32, 64, 128, 256, 512}; split_k >= 1 (BN <= 256 when split_k > 1).
 cudaError_t launch_gemm(const GemmArgs& args, bool is_bf16, int BN, int split_k, cudaStream_t stream);

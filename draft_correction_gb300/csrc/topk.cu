@@ -295,9 +295,9 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const void* __restrict__
     }
     __syncthreads();
   }
-  const uint64_t thr = s_thr;
-  const float tval = key_value(thr);
-  const bool fast = thr != 0 && tval > -INFINITY;
+  uint64_t thr = s_thr;
+  float tval = key_value(thr);
+  bool fast = thr != 0 && tval > -INFINITY;
 
   for (int it = 0; it < iters; ++it) {
     if (it + 1 < iters) {
@@ -359,6 +359,24 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const void* __restrict__
     }
 #pragma unroll
     for (int u = 0; u < kU; ++u) cur[u] = nxt[u];
+    if (((it + 2) & (it + 1)) == 0 && it + 1 < iters) {
+      // Checkpoint after iterations 1, 3, 7, 15, ...: the K-th largest key seen so far becomes
+      // the threshold and the buffer keeps only the K largest (every block thread takes part).
+      __syncthreads();
+      const int cnt = s_cnt;
+      if (cnt > K && !s_overflow) {
+        select_top(s_buf, cnt, K, s_keep);
+        if (threadIdx.x < K) s_buf[threadIdx.x] = s_keep[threadIdx.x];
+        if (threadIdx.x == 0) {
+          s_cnt = K;
+          if (s_keep[K - 1] > s_thr) s_thr = s_keep[K - 1];
+        }
+      }
+      __syncthreads();
+      thr = s_thr;
+      tval = key_value(thr);
+      fast = thr != 0 && tval > -INFINITY;
+    }
   }
 
   // Unaligned head (rank 0) and tail (last rank) elements, one per lane of warp 0.
@@ -433,31 +451,27 @@ cudaError_t launch_topk_t(const void* logits, int rows, int V, int K, int S, flo
   return cudaLaunchKernelEx(&cfg, topk_kernel<kBf16, KW>, logits, V, K, S, vals, ids);
 }
 
-// Blocks per row: the split (<= 8) whose grid fills the most of its last wave, preferring
-// fewer blocks on ties and keeping every segment at 16 KB or more.
+// Blocks per row: the smallest split (<= 8) that spreads the blocks over the SMs to within 6%
+// of an even load (blocks per SM, rounded up), keeping every segment at 16 KB or more.
 int auto_split(int rows, int V, bool bf16) {
-  static int slots = 0;
-  if (slots == 0) {
-    int dev = 0, sms = 152, per_sm = 1;
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0;
     cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (bf16)
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, topk_kernel<true, 1>, kThreads, 0);
-    else
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, topk_kernel<false, 1>, kThreads, 0);
-    slots = sms * (per_sm > 0 ? per_sm : 1);
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 152;
   }
   const int64_t row_bytes = static_cast<int64_t>(V) * (bf16 ? 2 : 4);
   int best = 1;
   double best_eff = -1.0;
   for (int s = 1; s <= kMaxSplit; ++s) {
     if (s > 1 && row_bytes / s < 16 * 1024) break;
-    const double waves = static_cast<double>(rows) * s / slots;
-    const double eff = waves / std::ceil(waves);
-    if (eff > best_eff + 1e-3) {
+    const double per_sm = static_cast<double>(rows) * s / sms;
+    const double eff = per_sm < 1.0 ? per_sm : per_sm / std::ceil(per_sm);
+    if (eff > best_eff + 1e-6) {
       best_eff = eff;
       best = s;
     }
+    if (eff >= 0.94) break;
   }
   return best;
 }
