@@ -603,10 +603,6 @@ int dcoco_cycle(const void* logits, int V, const void* emb, const void* h, const
   const int rows = N * B;
   cudaError_t e = launch_topk(logits, D.bf16, rows, V, K, topk_split(rows, V, D.bf16), o_vals, o_ids, st);
   if (e != cudaSuccess) return cuda_fail(e, "top-K launch");
-  // Start fetching the chosen embedding rows into L2 now, whole rows at a time; the pair-state
-  // projections run meanwhile and the gather below then mostly reads L2.
-  e = launch_prefetch_rows(o_ids, D.M(), emb, V, static_cast<int>(D.E * D.esz), st);
-  if (e != cudaSuccess) return cuda_fail(e, "embedding prefetch launch");
   DCOCO_TRY(enqueue_pair(D, h, w, s.wsp, s.pair, st));
   DCOCO_TRY(enqueue_repr(D, o_ids, emb, V, h, w, s.uz, s.vz, s.repr, st));
   DCOCO_TRY(enqueue_scores(D, s.uz, s.vz, s.wsp, o_vals, w, o_S, st));

@@ -31,6 +31,7 @@ constexpr int BM = 128;
 constexpr int kThreads = 192;
 constexpr int kMaxStages = 8;
 constexpr int kSmemBudget = 200 * 1024;
+constexpr int kGatherThreads = 128;  // epilogue warps that gather the A operand
 constexpr int kBiasStageBytes = 20 * 1024;  // per-slot bias rows of one tile (SiLU epilogue)
 
 __device__ unsigned int g_status_word;
@@ -144,9 +145,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   const int kb0 = ks * per;
   const int nk = std::max(0, std::min(nkb_total, kb0 + per) - kb0);
 
+  const bool gather = args.gather != nullptr;
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
-      mbar_init(smem_u32(&full_bar[s]), 1);
+      // gathered A: the B tile's transaction count plus one arrival per gathering thread
+      mbar_init(smem_u32(&full_bar[s]), gather ? 1 + kGatherThreads : 1);
       mbar_init(smem_u32(&empty_bar[s]), 1);
     }
     mbar_init(smem_u32(&acc_bar), 1);
@@ -166,15 +169,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       }
     }
     s_rows[threadIdx.x] = row;
-    if (m < args.M && nk > 0) {
-      // Pull this row's K range into L2 as one contiguous request; the four-row TMA gathers
-      // below then read it from L2 in 128-byte pieces.
-      const int esz = kBf16 ? 2 : 4;
-      const int k0 = kb0 * T::BK, k1 = min(args.K, (kb0 + nk) * T::BK);
-      prefetch_l2_bulk(static_cast<const char*>(args.gather_base) + static_cast<size_t>(row) * args.gather_pitch_bytes +
-                           static_cast<size_t>(k0) * esz,
-                       static_cast<uint32_t>((k1 - k0) * esz));
-    }
   }
   tc_fence_before();
   __syncthreads();
@@ -195,14 +189,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       const uint32_t a_s = smem0 + s * STAGE_BYTES;
       const uint32_t b_s = a_s + A_BYTES;
       const int kx = (kb0 + i) * T::BK;
-      if (lane == 0) mbar_expect_tx(fb, STAGE_BYTES);
+      if (lane == 0) mbar_expect_tx(fb, gather ? B_BYTES : STAGE_BYTES);
       __syncwarp();
-      if (args.gather != nullptr) {
-        tma_gather4(a_s + lane * 512, &args.a_map, kx, s_rows[4 * lane], s_rows[4 * lane + 1], s_rows[4 * lane + 2],
-                    s_rows[4 * lane + 3], fb);
-      } else if (lane == 0) {
-        tma_load_2d(a_s, &args.a_map, kx, m_tile * BM, fb);
-      }
+      if (!gather && lane == 0) tma_load_2d(a_s, &args.a_map, kx, m_tile * BM, fb);
       if (lane == 0) {
 #pragma unroll
         for (int h = 0; h < NH; ++h) tma_load_2d(b_s + h * NMMA * 128, &grp.b_map, kx, nt * BN + h * NMMA, fb);
@@ -210,6 +199,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    if (gather && lane > 0 && nk > 0) {
+      // Meanwhile the other lanes pull each gathered row's K range into L2 as one contiguous
+      // request, so that the 128-byte pieces the gather reads come from L2.
+      const int esz = kBf16 ? 2 : 4;
+      const int k0 = kb0 * T::BK, k1 = min(args.K, (kb0 + nk) * T::BK);
+      for (int r = lane - 1; r < BM; r += 31)
+        if (m_tile * BM + r < args.M)
+          prefetch_l2_bulk(static_cast<const char*>(args.gather_base) +
+                               static_cast<size_t>(s_rows[r]) * args.gather_pitch_bytes + static_cast<size_t>(k0) * esz,
+                           static_cast<uint32_t>((k1 - k0) * esz));
+    }
     if (lane == 0) {
       for (int i = 0; i < nk; ++i) {
         const int s = i % stages;
@@ -237,6 +237,50 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue (warps 2..5)
+    if (gather) {
+      // Gathered A operand: while the main loop runs these 128 threads copy Emb[c] rows into
+      // the stages with 16-byte asynchronous copies straight into the 128-byte swizzled layout
+      // (eight threads per 128-byte row piece, so global reads stay coalesced), then hand each
+      // stage to the tensor core with a generic-to-async proxy fence and one arrival.
+      const int t = threadIdx.x - 64;
+      const int c = t & 7;                     // 16-byte chunk of the 128-byte row piece
+      const int cs = c ^ ((t >> 3) & 7);       // its swizzled position (row & 7 == (t >> 3) & 7)
+      const int esz = kBf16 ? 2 : 4;
+      const char* rowb[8];  // start of the table row behind each of this thread's 8 tile rows
+#pragma unroll
+      for (int it = 0; it < 8; ++it)
+        rowb[it] = static_cast<const char*>(args.gather_base) +
+                   static_cast<size_t>(s_rows[it * 16 + (t >> 3)]) * args.gather_pitch_bytes;
+      const int lag = stages - 1;
+      bool alive = true;
+      for (int i = 0; i < nk && alive; ++i) {
+        const int s = i % stages;
+        const uint32_t ph = (i / stages) & 1;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&empty_bar[s]), ph ^ 1))) {
+          if (lane == 0) atomicOr(args.status, DEV_TIMEOUT_MMA);
+          alive = false;
+          break;
+        }
+        const uint32_t a_s = smem0 + s * STAGE_BYTES;
+        const int kcol = (kb0 + i) * T::BK + c * (16 / esz);  // first element of this chunk
+        const uint32_t nbytes = kcol < args.K ? 16u : 0u;      // K is a multiple of 16 bytes
+        const size_t koff = static_cast<size_t>(kcol) * esz;
+#pragma unroll
+        for (int it = 0; it < 8; ++it)
+          cp_async16(a_s + (it * 16 + (t >> 3)) * 128 + cs * 16, rowb[it] + (nbytes ? koff : 0), nbytes);
+        cp_async_commit();
+        if (i >= lag) {
+          cp_async_wait(lag);
+          fence_proxy_async();
+          mbar_arrive(smem_u32(&full_bar[(i - lag) % stages]));
+        }
+      }
+      cp_async_wait(0);
+      fence_proxy_async();
+      if (alive) {
+        for (int i = nk > lag ? nk - lag : 0; i < nk; ++i) mbar_arrive(smem_u32(&full_bar[i % stages]));
+      }
+    }
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row_local = q * 32 + lane;
     const int m = m_tile * BM + row_local;
@@ -511,22 +555,7 @@ __global__ void pair_combine_kernel(const float* __restrict__ hp, void* __restri
   }
 }
 
-__global__ void prefetch_rows_kernel(const int32_t* __restrict__ ids, int n, const char* __restrict__ table,
-                                     int table_rows, int row_bytes) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= n) return;
-  const int r = ids[i];
-  if (r >= 0 && r < table_rows) prefetch_l2_bulk(table + static_cast<size_t>(r) * row_bytes, row_bytes);
-}
-
 }  // namespace
-
-cudaError_t launch_prefetch_rows(const int32_t* ids, int n, const void* table, int table_rows, int row_bytes,
-                                 cudaStream_t stream) {
-  prefetch_rows_kernel<<<(n + 255) / 256, 256, 0, stream>>>(ids, n, static_cast<const char*>(table), table_rows,
-                                                            row_bytes);
-  return cudaGetLastError();
-}
 
 cudaError_t launch_gemm(const GemmArgs& args, bool is_bf16, int BN, int split_k, cudaStream_t stream) {
   if (split_k < 1 || split_k > 8 || (BM % split_k) != 0) return cudaErrorInvalidValue;

@@ -52,9 +52,6 @@ struct GemmArgs {
 bool make_tmap(CUtensorMap* map, const void* base, bool is_bf16, uint64_t rows, uint64_t cols, uint64_t pitch_elems,
                uint32_t box_rows, const char** err);
 
-// Asynchronous L2 prefetch of whole table rows table[ids[i]] (row_bytes each), i < n.
-cudaError_t launch_prefetch_rows(const int32_t* ids, int n, const void* table, int table_rows, int row_bytes,
-                                 cudaStream_t stream);
 
 // BN in {32, 64, 128, 256, 512}; split_k >= 1 (BN <= 256 when split_k > 1).
 cudaError_t launch_gemm(const GemmArgs& args, bool is_bf16, int BN, int split_k, cudaStream_t stream);
