@@ -216,27 +216,9 @@ int a_map_tiled(GemmArgs& a, const void* base, const Dims& D, uint64_t rows, uin
   return DCOCO_OK;
 }
 
-// Candidate representation: b, g, gw, z, then uz/vz.
-int enqueue_repr(const Dims& D, const int32_t* ids, const void* emb, int V, const void* h, const dcoco_weights* w,
-                 void* uz, void* vz, const ReprScratch& s, cudaStream_t st) {
-  const int M = D.M(), NB = D.NB(), r = D.r, H = D.H;
-  // b = LN(W_e Emb[ids])   (gathered A operand)
-  {
-    GemmArgs a = {};
-    const char* err = nullptr;
-    if (!make_tmap(&a.a_map, emb, D.bf16, V, D.E, D.E, 1, &err)) return fail(DCOCO_ERR_CUDA, "%s", err);
-    a.gather = ids;
-    a.gather_limit = V;
-    a.gather_base = emb;
-    a.gather_pitch_bytes = static_cast<int>(D.E * D.esz);
-    a.M = M;
-    a.K = D.E;
-    a.n_groups = 1;
-    const int BN = pick_bn(r, true);
-    if (BN != r) return fail(DCOCO_ERR_UNSUPPORTED, "r=%d", r);
-    DCOCO_TRY(gemm_group(&a.g[0], w->W_e, D, r, D.E, D.E, BN, s.b, r, EPI_LN, a.M));
-    DCOCO_TRY(run_gemm(a, D, BN, st, "gemm b = LN(W_e Emb[c])"));
-  }
+// Candidate representation, slot part (needs only h): g = LN(W_h h), gw = W_f[:, r:2r] g.
+int enqueue_repr_slot(const Dims& D, const void* h, const dcoco_weights* w, const ReprScratch& s, cudaStream_t st) {
+  const int NB = D.NB(), r = D.r;
   // g = LN(W_h h)
   {
     GemmArgs a = {};
@@ -259,6 +241,37 @@ int enqueue_repr(const Dims& D, const int32_t* ids, const void* emb, int V, cons
     DCOCO_TRY(gemm_group(&a.g[0], static_cast<const char*>(w->W_f) + r * D.esz, D, r, r, 2 * r, BN, s.gw, r, EPI_F32, a.M));
     DCOCO_TRY(run_gemm(a, D, BN, st, "gemm gw = W_f,g g"));
   }
+  return DCOCO_OK;
+}
+
+// Candidate representation, gather part: b = LN(W_e Emb[c]) (needs the ids).
+int enqueue_repr_gather(const Dims& D, const int32_t* ids, const void* emb, int V, const dcoco_weights* w,
+                        const ReprScratch& s, cudaStream_t st) {
+  const int M = D.M(), r = D.r;
+  // b = LN(W_e Emb[ids])   (gathered A operand)
+  {
+    GemmArgs a = {};
+    const char* err = nullptr;
+    if (!make_tmap(&a.a_map, emb, D.bf16, V, D.E, D.E, 1, &err)) return fail(DCOCO_ERR_CUDA, "%s", err);
+    a.gather = ids;
+    a.gather_limit = V;
+    a.gather_base = emb;
+    a.gather_pitch_bytes = static_cast<int>(D.E * D.esz);
+    a.M = M;
+    a.K = D.E;
+    a.n_groups = 1;
+    const int BN = pick_bn(r, true);
+    if (BN != r) return fail(DCOCO_ERR_UNSUPPORTED, "r=%d", r);
+    DCOCO_TRY(gemm_group(&a.g[0], w->W_e, D, r, D.E, D.E, BN, s.b, r, EPI_LN, a.M));
+    DCOCO_TRY(run_gemm(a, D, BN, st, "gemm b = LN(W_e Emb[c])"));
+  }
+  return DCOCO_OK;
+}
+
+// Candidate representation, fusion part: z = SiLU(W_f[:, 0:r] b + gw[slot]), uz = U z, vz = V z.
+int enqueue_repr_fuse(const Dims& D, const dcoco_weights* w, void* uz, void* vz, const ReprScratch& s,
+                      cudaStream_t st) {
+  const int M = D.M(), r = D.r, H = D.H;
   // z = SiLU(W_f[:, 0:r] b + gw[slot])
   {
     GemmArgs a = {};
@@ -285,6 +298,37 @@ int enqueue_repr(const Dims& D, const int32_t* ids, const void* emb, int V, cons
     DCOCO_TRY(gemm_group(&a.g[1], w->V, D, H, r, r, BN, vz, H, EPI_ACT, a.M));
     DCOCO_TRY(run_gemm(a, D, BN, st, "gemm uz, vz"));
   }
+  return DCOCO_OK;
+}
+
+int enqueue_repr(const Dims& D, const int32_t* ids, const void* emb, int V, const void* h, const dcoco_weights* w,
+                 void* uz, void* vz, const ReprScratch& s, cudaStream_t st) {
+  DCOCO_TRY(enqueue_repr_gather(D, ids, emb, V, w, s, st));
+  DCOCO_TRY(enqueue_repr_slot(D, h, w, s, st));
+  return enqueue_repr_fuse(D, w, uz, vz, s, st);
+}
+
+// Per-device helper stream (highest priority) and fork/join events for dcoco_cycle; the
+// mutex keeps one enqueue sequence at a time per process.
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+std::mutex g_side_mu;
+int side_stream(SideStream** out) {
+  static SideStream per_dev[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return fail(DCOCO_ERR_CUDA, "no current CUDA device");
+  SideStream& s = per_dev[dev];
+  if (s.stream == nullptr) {
+    int lo = 0, hi = 0;
+    cudaError_t e = cudaDeviceGetStreamPriorityRange(&lo, &hi);
+    if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&s.stream, cudaStreamNonBlocking, hi);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming);
+    if (e != cudaSuccess) return cuda_fail(e, "helper stream set-up");
+  }
+  *out = &s;
   return DCOCO_OK;
 }
 
@@ -601,10 +645,25 @@ int dcoco_cycle(const void* logits, int V, const void* emb, const void* h, const
   cudaStream_t st = as_stream(stream);
 
   const int rows = N * B;
-  cudaError_t e = launch_topk(logits, D.bf16, rows, V, K, topk_split(rows, V, D.bf16), o_vals, o_ids, st);
+  // Everything that needs only h (pair states, W s, g, the g half of the fusion) runs on the
+  // helper stream while top-K streams the logits and the embedding rows are gathered.
+  std::lock_guard<std::mutex> lock(g_side_mu);
+  SideStream* side = nullptr;
+  DCOCO_TRY(side_stream(&side));
+  cudaError_t e = cudaEventRecord(side->fork, st);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(side->stream, side->fork, 0);
+  if (e != cudaSuccess) return cuda_fail(e, "fork to helper stream");
+  DCOCO_TRY(enqueue_pair(D, h, w, s.wsp, s.pair, side->stream));
+  DCOCO_TRY(enqueue_repr_slot(D, h, w, s.repr, side->stream));
+  e = cudaEventRecord(side->join, side->stream);
+  if (e != cudaSuccess) return cuda_fail(e, "join from helper stream");
+
+  e = launch_topk(logits, D.bf16, rows, V, K, topk_split(rows, V, D.bf16), o_vals, o_ids, st);
   if (e != cudaSuccess) return cuda_fail(e, "top-K launch");
-  DCOCO_TRY(enqueue_pair(D, h, w, s.wsp, s.pair, st));
-  DCOCO_TRY(enqueue_repr(D, o_ids, emb, V, h, w, s.uz, s.vz, s.repr, st));
+  DCOCO_TRY(enqueue_repr_gather(D, o_ids, emb, V, w, s.repr, st));
+  e = cudaStreamWaitEvent(st, side->join, 0);
+  if (e != cudaSuccess) return cuda_fail(e, "join from helper stream");
+  DCOCO_TRY(enqueue_repr_fuse(D, w, s.uz, s.vz, s.repr, st));
   DCOCO_TRY(enqueue_scores(D, s.uz, s.vz, s.wsp, o_vals, w, o_S, st));
   SelectVerifyArgs a = {};
   a.S = o_S;

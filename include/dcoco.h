@@ -193,9 +193,14 @@ int dcoco_verify(int mode, const int32_t* draft, const int32_t* t, const float* 
                  int32_t* accept_len, int32_t* committed, int32_t* n_commit, int32_t* near_tie, void* stream);
 
 /*
- * One whole correction cycle a1..a6 on one stream: top-K, candidate representation,
- * pair state, transition scores, walk and verification, with intermediates in the
- * workspace.  Inputs as above; `t` (greedy) or `q`,`u` (stochastic) per `mode`.
+ * One whole correction cycle a1..a6: top-K, candidate representation, pair state,
+ * transition scores, walk and verification, with intermediates in the workspace.  Inputs as
+ * above; `t` (greedy) or `q`,`u` (stochastic) per `mode`.
+ * The projections that need only h (pair states, W s, g and its fusion half) run on a
+ * library-owned helper stream of the current device (created on the first call, highest
+ * priority) that forks from and joins back into `stream` through events, so they overlap
+ * top-K; the call can be captured into a CUDA graph after that first call.  Enqueueing is
+ * serialised per process by a mutex.
  * Outputs (any may be NULL except tokens, accept_len, committed, n_commit):
  *   vals, ids [N,B,K]; S [N,B-1,K,K]; k_sel, tokens [N,B]; accept_len, n_commit [N];
  *   committed [N,B+1]; near_tie [N].
