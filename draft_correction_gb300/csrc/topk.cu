@@ -40,6 +40,7 @@ constexpr int kU = 2;          // 16-byte vectors per lane per iteration
 constexpr int kMaxSplit = 8;
 constexpr int kMaxK = 64;
 constexpr int kCap = 1024;     // candidate buffer (keys)
+constexpr int kSusCap = 2048;  // suspect lanes between checkpoints
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
 template <bool kBf16>
@@ -228,7 +229,7 @@ __device__ __noinline__ void exact_segment_topk(const Segment& g, int K, int ran
 }
 
 template <bool kBf16, int KW>
-__global__ void __launch_bounds__(kThreads) topk_kernel(const void* __restrict__ logits, int V, int K, int S,
+__global__ void __launch_bounds__(kThreads, 8) topk_kernel(const void* __restrict__ logits, int V, int K, int S,
                                                         float* __restrict__ vals, int32_t* __restrict__ ids) {
   constexpr int EPV = kEpv<kBf16>;
   __shared__ uint64_t s_buf[kCap];
@@ -236,8 +237,9 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const void* __restrict__
   __shared__ uint64_t s_wl[kWarps * kMaxK];
   __shared__ uint64_t s_keep[kMaxK];
   __shared__ uint64_t s_cluster[kMaxSplit * kMaxK];
+  __shared__ int s_sus[kSusCap];  // first vector index of lanes that may hold a candidate
   __shared__ uint64_t s_thr;
-  __shared__ int s_cnt, s_overflow;
+  __shared__ int s_cnt, s_overflow, s_nsus;
 
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
@@ -246,6 +248,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const void* __restrict__
   if (threadIdx.x == 0) {
     s_cnt = 0;
     s_overflow = 0;
+    s_nsus = 0;
     s_thr = 0;
   }
 
@@ -266,12 +269,17 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const void* __restrict__
   // Lanes past the end of the segment see -inf.
   const uint4 neg_inf = kBf16 ? make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u)
                               : make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u);
-  uint4 cur[kU], nxt[kU];
+  // Three iterations of vectors in registers: the current one and two in flight.
+  uint4 c0[kU], c1[kU], c2[kU];
+  auto load = [&](int it, uint4(&v)[kU]) {
 #pragma unroll
-  for (int u = 0; u < kU; ++u) {
-    const int vi = vidx(0, u);
-    cur[u] = (iters > 0 && vi < g.vend) ? ld_stream(g.vp + vi) : neg_inf;
-  }
+    for (int u = 0; u < kU; ++u) {
+      const int vi = vidx(it, u);
+      v[u] = (it < iters && vi < g.vend) ? ld_stream(g.vp + vi) : neg_inf;
+    }
+  };
+  load(0, c0);
+  load(1, c1);
 
   // Seed threshold: the K-th largest of the block's 256 lane maxima (first iteration).
   {
@@ -279,7 +287,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const void* __restrict__
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
       if (iters > 0 && vidx(0, u) < g.vend) {
-        const uint64_t k = (static_cast<uint64_t>(ord32(vec_max_bits<kBf16>(cur[u]))) << 32) |
+        const uint64_t k = (static_cast<uint64_t>(ord32(vec_max_bits<kBf16>(c0[u]))) << 32) |
                            static_cast<uint64_t>(0xFFFFFFFFu - threadIdx.x);
         mk = k > mk ? k : mk;
       }
@@ -299,71 +307,68 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const void* __restrict__
   float tval = key_value(thr);
   bool fast = thr != 0 && tval > -INFINITY;
 
-  for (int it = 0; it < iters; ++it) {
-    if (it + 1 < iters) {
+  // Key every element of the suspect lanes' vectors and keep the keys above the threshold.
+  auto process_suspects = [&]() {
+    const int ns = min(s_nsus, kSusCap);
+    for (int j = threadIdx.x; j < ns; j += kThreads) {
+      const int vi0 = s_sus[j];
 #pragma unroll
       for (int u = 0; u < kU; ++u) {
-        const int vi = vidx(it + 1, u);
-        nxt[u] = vi < g.vend ? ld_stream(g.vp + vi) : neg_inf;
-      }
-    }
-    bool maybe = true;
-    if (fast) {
-      uint4 mx = cur[0];
+        const int vi = vi0 + u * 32;
+        if (vi >= g.vend) continue;
+        const uint4 v = ld_stream(g.vp + vi);
 #pragma unroll
-      for (int u = 1; u < kU; ++u) mx = vmax<kBf16>(mx, cur[u]);
-      maybe = !(__uint_as_float(vec_max_bits<kBf16>(mx)) < tval);
-    }
-    if (__any_sync(kFull, maybe)) {
-      uint32_t mask = 0;  // bit u*EPV + e: element e of vector u is a candidate
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int vi = vidx(it, u);
-        if (maybe && vi < g.vend && !(fast && __uint_as_float(vec_max_bits<kBf16>(cur[u])) < tval)) {
-#pragma unroll
-          for (int e = 0; e < EPV; ++e) {
-            const uint32_t bits = elem_bits<kBf16>(cur[u], e);
-            if (!fast || __uint_as_float(bits) >= tval) {
-              if (make_key(bits, g.head + vi * EPV + e) > thr) mask |= 1u << (u * EPV + e);
-            }
+        for (int e = 0; e < EPV; ++e) {
+          const uint64_t key = make_key(elem_bits<kBf16>(v, e), g.head + vi * EPV + e);
+          if (key > thr) {
+            const int pos = atomicAdd(&s_cnt, 1);
+            if (pos < kCap)
+              s_buf[pos] = key;
+            else
+              s_overflow = 1;
           }
         }
       }
-      const int n = __popc(mask);
-      int incl = n;
+    }
+  };
+
+  for (int it = 0; it < iters; ++it) {
+    load(it + 2, c2);
+    // Hot loop: one packed max over the lane's vectors and one compare.  A lane that may hold a
+    // key above the threshold only records where its vectors are.
+    bool maybe = vidx(it, 0) < g.vend;
+    if (fast) {
+      uint4 mx = c0[0];
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_up_sync(kFull, incl, o);
-        if (lane >= o) incl += t;
-      }
-      const int total = __shfl_sync(kFull, incl, 31);
-      if (total > 0) {
-        int start = 0;
-        if (lane == 31) start = atomicAdd(&s_cnt, total);
-        int pos = __shfl_sync(kFull, start, 31) + incl - n;
-        while (mask) {
-          const int b = __ffs(mask) - 1;
-          mask &= mask - 1;
-          const int u = b / EPV, e = b % EPV;
-          uint4 vv = cur[0];
-#pragma unroll
-          for (int q = 1; q < kU; ++q)
-            if (q == u) vv = cur[q];
-          if (pos < kCap)
-            s_buf[pos] = make_key(elem_bits<kBf16>(vv, e), g.head + vidx(it, u) * EPV + e);
-          else
-            s_overflow = 1;
-          ++pos;
-        }
+      for (int u = 1; u < kU; ++u) mx = vmax<kBf16>(mx, c0[u]);
+      maybe = !(__uint_as_float(vec_max_bits<kBf16>(mx)) < tval);
+    }
+    const uint32_t bal = __ballot_sync(kFull, maybe);
+    if (bal) {
+      int base = 0;
+      if (lane == 0) base = atomicAdd(&s_nsus, __popc(bal));
+      base = __shfl_sync(kFull, base, 0);
+      if (maybe) {
+        const int pos = base + __popc(bal & ((1u << lane) - 1));
+        if (pos < kSusCap)
+          s_sus[pos] = vidx(it, 0);
+        else
+          s_overflow = 1;
       }
     }
 #pragma unroll
-    for (int u = 0; u < kU; ++u) cur[u] = nxt[u];
+    for (int u = 0; u < kU; ++u) {
+      c0[u] = c1[u];
+      c1[u] = c2[u];
+    }
     if (((it + 2) & (it + 1)) == 0 && it + 1 < iters) {
-      // Checkpoint after iterations 1, 3, 7, 15, ...: the K-th largest key seen so far becomes
-      // the threshold and the buffer keeps only the K largest (every block thread takes part).
+      // Checkpoint after iterations 1, 3, 7, 15, ...: key the suspects, then the K-th largest
+      // key seen so far becomes the threshold and the buffer keeps only the K largest.
+      __syncthreads();
+      process_suspects();
       __syncthreads();
       const int cnt = s_cnt;
+      if (threadIdx.x == 0) s_nsus = 0;
       if (cnt > K && !s_overflow) {
         select_top(s_buf, cnt, K, s_keep);
         if (threadIdx.x < K) s_buf[threadIdx.x] = s_keep[threadIdx.x];
@@ -378,6 +383,8 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const void* __restrict__
       fast = thr != 0 && tval > -INFINITY;
     }
   }
+  __syncthreads();
+  process_suspects();
 
   // Unaligned head (rank 0) and tail (last rank) elements, one per lane of warp 0.
   if (warp == 0) {
@@ -451,22 +458,35 @@ cudaError_t launch_topk_t(const void* logits, int rows, int V, int K, int S, flo
   return cudaLaunchKernelEx(&cfg, topk_kernel<kBf16, KW>, logits, V, K, S, vals, ids);
 }
 
-// Blocks per row: the smallest split (<= 8) that spreads the blocks over the SMs to within 6%
-// of an even load (blocks per SM, rounded up), keeping every segment at 16 KB or more.
+// Blocks per row: the smallest split (<= 8) whose grid loads the GPU to within 6% of even --
+// blocks per SM rounded up while they all fit at once, whole waves beyond that -- keeping
+// every segment at 16 KB or more.
 int auto_split(int rows, int V, bool bf16) {
-  static int sms = 0;
+  static int sms = 0, occ = 0;
   if (sms == 0) {
     int dev = 0;
     cudaGetDevice(&dev);
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 152;
+    if (bf16)
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, topk_kernel<true, 1>, kThreads, 0);
+    else
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, topk_kernel<false, 1>, kThreads, 0);
+    if (occ <= 0) occ = 1;
   }
   const int64_t row_bytes = static_cast<int64_t>(V) * (bf16 ? 2 : 4);
   int best = 1;
   double best_eff = -1.0;
   for (int s = 1; s <= kMaxSplit; ++s) {
     if (s > 1 && row_bytes / s < 16 * 1024) break;
-    const double per_sm = static_cast<double>(rows) * s / sms;
-    const double eff = per_sm < 1.0 ? per_sm : per_sm / std::ceil(per_sm);
+    const double n = static_cast<double>(rows) * s;
+    const double per_sm = n / sms;
+    double eff;
+    if (per_sm <= occ) {
+      eff = per_sm < 1.0 ? per_sm : per_sm / std::ceil(per_sm);
+    } else {
+      const double waves = n / (static_cast<double>(sms) * occ);
+      eff = waves / std::ceil(waves);
+    }
     if (eff > best_eff + 1e-6) {
       best_eff = eff;
       best = s;
