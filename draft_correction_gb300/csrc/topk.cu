@@ -14,14 +14,14 @@
 //    grid fills whole waves of the GPU).  A block streams its segment with 128-bit loads
 //    (8 bf16 per lane), the next iteration's loads in flight while the current one is
 //    filtered.  The streaming loop has no barrier.
-//  * Threshold: from the block's first 256 x 16 values, the K-th largest of the 256 lane
-//    maxima (each warp sorts its 32 maxima with shuffles; ranks come from binary searches
-//    in the 8 sorted lists).  K values reach it, so anything smaller is not in the top K.
-//    Lanes reject their values with packed bf16 max instructions; only vectors that may hold
-//    a candidate are looked at element by element, and only survivors become keys.
-//  * Survivors go to a block-wide shared-memory buffer.  At the end the block selects its K
-//    largest keys by rank counting, pushes them into block 0 of the cluster (distributed
-//    shared memory), and block 0 ranks the S sorted lists by binary search.
+//  * Threshold: the K-th largest of the block's 256 lane maxima over its first 4 iterations
+//    (each warp sorts its 32 maxima with shuffles; ranks come from binary searches in the 8
+//    sorted lists).  K values reach it, so anything smaller is not in the top K.
+//  * Streaming loop, no barrier: a lane tests the packed max of its vectors against the
+//    threshold and, if it may hold a candidate, records the vectors' position (a "suspect").
+//    After the loop the block keys the suspect vectors element by element, keeps the keys above
+//    the threshold, selects its K largest by rank counting, pushes them into block 0 of the
+//    cluster (distributed shared memory), and block 0 ranks the S sorted lists by binary search.
 //  * Rows that defeat the threshold (all values equal, sorted rows, NaN rows) overflow the
 //    buffer; the block then recomputes its segment exactly with per-warp register lists.
 #include <cuda_bf16.h>
@@ -40,7 +40,8 @@ constexpr int kU = 2;          // 16-byte vectors per lane per iteration
 constexpr int kMaxSplit = 8;
 constexpr int kMaxK = 64;
 constexpr int kCap = 1024;     // candidate buffer (keys)
-constexpr int kSusCap = 2048;  // suspect lanes between checkpoints
+constexpr int kSusCap = 2048;  // lanes that may hold a candidate (per block)
+constexpr int kSeedIters = 4;  // iterations whose lane maxima seed the threshold
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
 template <bool kBf16>
@@ -229,7 +230,7 @@ __device__ __noinline__ void exact_segment_topk(const Segment& g, int K, int ran
 }
 
 template <bool kBf16, int KW>
-__global__ void __launch_bounds__(kThreads, 8) topk_kernel(const void* __restrict__ logits, int V, int K, int S,
+__global__ void __launch_bounds__(kThreads, 6) topk_kernel(const void* __restrict__ logits, int V, int K, int S,
                                                         float* __restrict__ vals, int32_t* __restrict__ ids) {
   constexpr int EPV = kEpv<kBf16>;
   __shared__ uint64_t s_buf[kCap];
@@ -278,20 +279,33 @@ __global__ void __launch_bounds__(kThreads, 8) topk_kernel(const void* __restric
       v[u] = (it < iters && vi < g.vend) ? ld_stream(g.vp + vi) : neg_inf;
     }
   };
-  load(0, c0);
-  load(1, c1);
 
-  // Seed threshold: the K-th largest of the block's 256 lane maxima (first iteration).
+  // Seed threshold: the K-th largest of the block's 256 lane maxima over the first kSeedIters
+  // iterations.  K elements reach that value, so nothing below it is in the top K.  Those
+  // iterations are read again (from L2) by the main loop.
   {
-    uint64_t mk = 0;
+    uint32_t mb = 0xFF800000u;  // -inf
+    bool any = false;
+    load(0, c0);
+    load(1, c1);
 #pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      if (iters > 0 && vidx(0, u) < g.vend) {
-        const uint64_t k = (static_cast<uint64_t>(ord32(vec_max_bits<kBf16>(c0[u]))) << 32) |
-                           static_cast<uint64_t>(0xFFFFFFFFu - threadIdx.x);
-        mk = k > mk ? k : mk;
+    for (int it = 0; it < kSeedIters; ++it) {
+      load(it + 2, c2);
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        if (it < iters && vidx(it, u) < g.vend) {
+          mb = __float_as_uint(fmaxf(__uint_as_float(mb), __uint_as_float(vec_max_bits<kBf16>(c0[u]))));
+          any = true;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        c0[u] = c1[u];
+        c1[u] = c2[u];
       }
     }
+    const uint64_t mk = any ? (static_cast<uint64_t>(ord32(mb)) << 32) | static_cast<uint64_t>(0xFFFFFFFFu - threadIdx.x)
+                            : 0ull;
     s_sorted[threadIdx.x] = warp_sort_desc(mk, lane);
     __syncthreads();
     const uint64_t x = s_sorted[threadIdx.x];
@@ -303,39 +317,16 @@ __global__ void __launch_bounds__(kThreads, 8) topk_kernel(const void* __restric
     }
     __syncthreads();
   }
-  uint64_t thr = s_thr;
-  float tval = key_value(thr);
-  bool fast = thr != 0 && tval > -INFINITY;
+  const uint64_t thr = s_thr;
+  const float tval = key_value(thr);
+  const bool fast = thr != 0 && tval > -INFINITY;
 
-  // Key every element of the suspect lanes' vectors and keep the keys above the threshold.
-  auto process_suspects = [&]() {
-    const int ns = min(s_nsus, kSusCap);
-    for (int j = threadIdx.x; j < ns; j += kThreads) {
-      const int vi0 = s_sus[j];
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int vi = vi0 + u * 32;
-        if (vi >= g.vend) continue;
-        const uint4 v = ld_stream(g.vp + vi);
-#pragma unroll
-        for (int e = 0; e < EPV; ++e) {
-          const uint64_t key = make_key(elem_bits<kBf16>(v, e), g.head + vi * EPV + e);
-          if (key > thr) {
-            const int pos = atomicAdd(&s_cnt, 1);
-            if (pos < kCap)
-              s_buf[pos] = key;
-            else
-              s_overflow = 1;
-          }
-        }
-      }
-    }
-  };
-
+  // Hot loop: one packed max over the lane's vectors and one compare per iteration.  A lane
+  // that may hold a key above the threshold only records where its vectors are.
+  load(0, c0);
+  load(1, c1);
   for (int it = 0; it < iters; ++it) {
     load(it + 2, c2);
-    // Hot loop: one packed max over the lane's vectors and one compare.  A lane that may hold a
-    // key above the threshold only records where its vectors are.
     bool maybe = vidx(it, 0) < g.vend;
     if (fast) {
       uint4 mx = c0[0];
@@ -361,30 +352,32 @@ __global__ void __launch_bounds__(kThreads, 8) topk_kernel(const void* __restric
       c0[u] = c1[u];
       c1[u] = c2[u];
     }
-    if (((it + 2) & (it + 1)) == 0 && it + 1 < iters) {
-      // Checkpoint after iterations 1, 3, 7, 15, ...: key the suspects, then the K-th largest
-      // key seen so far becomes the threshold and the buffer keeps only the K largest.
-      __syncthreads();
-      process_suspects();
-      __syncthreads();
-      const int cnt = s_cnt;
-      if (threadIdx.x == 0) s_nsus = 0;
-      if (cnt > K && !s_overflow) {
-        select_top(s_buf, cnt, K, s_keep);
-        if (threadIdx.x < K) s_buf[threadIdx.x] = s_keep[threadIdx.x];
-        if (threadIdx.x == 0) {
-          s_cnt = K;
-          if (s_keep[K - 1] > s_thr) s_thr = s_keep[K - 1];
-        }
-      }
-      __syncthreads();
-      thr = s_thr;
-      tval = key_value(thr);
-      fast = thr != 0 && tval > -INFINITY;
-    }
   }
   __syncthreads();
-  process_suspects();
+  // Key every element of the suspect lanes' vectors; keep the keys above the threshold.
+  if (!s_overflow) {
+    const int ns = min(s_nsus, kSusCap);
+    for (int j = threadIdx.x; j < ns; j += kThreads) {
+      const int vi0 = s_sus[j];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int vi = vi0 + u * 32;
+        if (vi >= g.vend) continue;
+        const uint4 v = ld_stream(g.vp + vi);
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) {
+          const uint64_t key = make_key(elem_bits<kBf16>(v, e), g.head + vi * EPV + e);
+          if (key > thr) {
+            const int pos = atomicAdd(&s_cnt, 1);
+            if (pos < kCap)
+              s_buf[pos] = key;
+            else
+              s_overflow = 1;
+          }
+        }
+      }
+    }
+  }
 
   // Unaligned head (rank 0) and tail (last rank) elements, one per lane of warp 0.
   if (warp == 0) {
