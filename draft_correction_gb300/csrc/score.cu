@@ -15,8 +15,10 @@
 // so that with x = 2(P + Q):  SiLU(x) = x sigmoid(x) = y + y tanh(y), y = P + Q.
 // Each thread owns a 2 x 4 tile of (a, b) outputs over a strided subset of the hidden units
 // (7 shared-memory vector loads per 32 SiLUs); the partial sums are then added in a fixed
-// order.  The tanh uses the SFU's tanh.approx.f32.
+// order.  For bf16 inputs the tanh runs as packed half-precision SFU instructions (two values
+// each; pre-activations and sums stay fp32); for f32 inputs as tanh.approx.f32.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -69,6 +71,23 @@ __device__ __forceinline__ float tanh_fast(float x) {
   float y;
   asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// tanh of four floats with two packed half-precision SFU instructions.  Inputs beyond the half
+// range round to +-inf, whose tanh is the exact limit +-1, so no input is out of range.
+__device__ __forceinline__ void tanh4_f16(float a, float b, float c, float d, float& ta, float& tb, float& tc,
+                                          float& td) {
+  uint32_t p0, p1, r0, r1;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(p0) : "f"(b), "f"(a));
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(p1) : "f"(d), "f"(c));
+  asm("tanh.approx.f16x2 %0, %1;" : "=r"(r0) : "r"(p0));
+  asm("tanh.approx.f16x2 %0, %1;" : "=r"(r1) : "r"(p1));
+  const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&r0));
+  const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&r1));
+  ta = f0.x;
+  tb = f0.y;
+  tc = f1.x;
+  td = f1.y;
 }
 
 template <bool kBf16>
@@ -170,11 +189,22 @@ __global__ void __launch_bounds__(kThreads) score_kernel(const ScoreArgs a) {
         for (int i = 0; i < kTA; ++i) {
 #pragma unroll
           for (int j = 0; j < kTB; ++j) {
-            float y, s = acc[i][j];
-            y = pv[i].x + qv[j].x; s = fmaf(w.x, fmaf(y, tanh_fast(y), y), s);
-            y = pv[i].y + qv[j].y; s = fmaf(w.y, fmaf(y, tanh_fast(y), y), s);
-            y = pv[i].z + qv[j].z; s = fmaf(w.z, fmaf(y, tanh_fast(y), y), s);
-            y = pv[i].w + qv[j].w; s = fmaf(w.w, fmaf(y, tanh_fast(y), y), s);
+            const float y0 = pv[i].x + qv[j].x, y1 = pv[i].y + qv[j].y;
+            const float y2 = pv[i].z + qv[j].z, y3 = pv[i].w + qv[j].w;
+            float t0, t1, t2, t3;
+            if constexpr (kBf16) {
+              tanh4_f16(y0, y1, y2, y3, t0, t1, t2, t3);
+            } else {
+              t0 = tanh_fast(y0);
+              t1 = tanh_fast(y1);
+              t2 = tanh_fast(y2);
+              t3 = tanh_fast(y3);
+            }
+            float s = acc[i][j];
+            s = fmaf(w.x, fmaf(y0, t0, y0), s);
+            s = fmaf(w.y, fmaf(y1, t1, y1), s);
+            s = fmaf(w.z, fmaf(y2, t2, y2), s);
+            s = fmaf(w.w, fmaf(y3, t3, y3), s);
             acc[i][j] = s;
           }
         }

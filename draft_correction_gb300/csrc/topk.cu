@@ -451,35 +451,23 @@ cudaError_t launch_topk_t(const void* logits, int rows, int V, int K, int S, flo
   return cudaLaunchKernelEx(&cfg, topk_kernel<kBf16, KW>, logits, V, K, S, vals, ids);
 }
 
-// Blocks per row: the smallest split (<= 8) whose grid loads the GPU to within 6% of even --
-// blocks per SM rounded up while they all fit at once, whole waves beyond that -- keeping
-// every segment at 16 KB or more.
+// Blocks per row: the smallest split (<= 8) that spreads the blocks over the SMs to within 6%
+// of an even load (blocks per SM, rounded up), keeping every segment at 16 KB or more.
 int auto_split(int rows, int V, bool bf16) {
-  static int sms = 0, occ = 0;
+  static int sms = 0;
   if (sms == 0) {
     int dev = 0;
     cudaGetDevice(&dev);
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 152;
-    if (bf16)
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, topk_kernel<true, 1>, kThreads, 0);
-    else
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, topk_kernel<false, 1>, kThreads, 0);
-    if (occ <= 0) occ = 1;
   }
   const int64_t row_bytes = static_cast<int64_t>(V) * (bf16 ? 2 : 4);
   int best = 1;
   double best_eff = -1.0;
   for (int s = 1; s <= kMaxSplit; ++s) {
     if (s > 1 && row_bytes / s < 16 * 1024) break;
-    const double n = static_cast<double>(rows) * s;
-    const double per_sm = n / sms;
-    double eff;
-    if (per_sm <= occ) {
-      eff = per_sm < 1.0 ? per_sm : per_sm / std::ceil(per_sm);
-    } else {
-      const double waves = n / (static_cast<double>(sms) * occ);
-      eff = waves / std::ceil(waves);
-    }
+    // blocks are scheduled as earlier ones finish, so what matters is blocks per SM
+    const double per_sm = static_cast<double>(rows) * s / sms;
+    const double eff = per_sm < 1.0 ? per_sm : per_sm / std::ceil(per_sm);
     if (eff > best_eff + 1e-6) {
       best_eff = eff;
       best = s;
