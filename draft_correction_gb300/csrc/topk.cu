@@ -14,7 +14,7 @@
 //    grid fills whole waves of the GPU).  A block streams its segment with 128-bit loads
 //    (8 bf16 per lane), the next iteration's loads in flight while the current one is
 //    filtered.  The streaming loop has no barrier.
-//  * Threshold: the K-th largest of the block's 256 lane maxima over its first 4 iterations
+//  * Threshold: the K-th largest of the block's 256 lane maxima over its first 2 iterations
 //    (each warp sorts its 32 maxima with shuffles; ranks come from binary searches in the 8
 //    sorted lists).  K values reach it, so anything smaller is not in the top K.
 //  * Streaming loop, no barrier: a lane tests the packed max of its vectors against the
@@ -36,12 +36,12 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kU = 2;          // 16-byte vectors per lane per iteration
+constexpr int kU = 4;          // 16-byte vectors per lane per iteration
 constexpr int kMaxSplit = 8;
 constexpr int kMaxK = 64;
 constexpr int kCap = 1024;     // candidate buffer (keys)
 constexpr int kSusCap = 2048;  // lanes that may hold a candidate (per block)
-constexpr int kSeedIters = 4;  // iterations whose lane maxima seed the threshold
+constexpr int kSeedIters = 2;  // iterations whose lane maxima seed the threshold
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
 template <bool kBf16>
@@ -230,7 +230,7 @@ __device__ __noinline__ void exact_segment_topk(const Segment& g, int K, int ran
 }
 
 template <bool kBf16, int KW>
-__global__ void __launch_bounds__(kThreads, 6) topk_kernel(const void* __restrict__ logits, int V, int K, int S,
+__global__ void __launch_bounds__(kThreads, 4) topk_kernel(const void* __restrict__ logits, int V, int K, int S,
                                                         float* __restrict__ vals, int32_t* __restrict__ ids) {
   constexpr int EPV = kEpv<kBf16>;
   __shared__ uint64_t s_buf[kCap];
@@ -451,8 +451,9 @@ cudaError_t launch_topk_t(const void* logits, int rows, int V, int K, int S, flo
   return cudaLaunchKernelEx(&cfg, topk_kernel<kBf16, KW>, logits, V, K, S, vals, ids);
 }
 
-// Blocks per row: the smallest split (<= 8) that spreads the blocks over the SMs to within 6%
-// of an even load (blocks per SM, rounded up), keeping every segment at 16 KB or more.
+// Blocks per row: one block per row once there are at least two rows per SM (more blocks per
+// row only add per-block overhead); fewer rows are split until the grid covers the SMs, at
+// most 8 ways and keeping every segment at 16 KB or more.
 int auto_split(int rows, int V, bool bf16) {
   static int sms = 0;
   if (sms == 0) {
@@ -460,21 +461,12 @@ int auto_split(int rows, int V, bool bf16) {
     cudaGetDevice(&dev);
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 152;
   }
+  if (rows >= 2 * sms) return 1;
   const int64_t row_bytes = static_cast<int64_t>(V) * (bf16 ? 2 : 4);
-  int best = 1;
-  double best_eff = -1.0;
-  for (int s = 1; s <= kMaxSplit; ++s) {
-    if (s > 1 && row_bytes / s < 16 * 1024) break;
-    // blocks are scheduled as earlier ones finish, so what matters is blocks per SM
-    const double per_sm = static_cast<double>(rows) * s / sms;
-    const double eff = per_sm < 1.0 ? per_sm : per_sm / std::ceil(per_sm);
-    if (eff > best_eff + 1e-6) {
-      best_eff = eff;
-      best = s;
-    }
-    if (eff >= 0.94) break;
-  }
-  return best;
+  int s = (2 * sms + rows - 1) / rows;
+  if (s > kMaxSplit) s = kMaxSplit;
+  while (s > 1 && row_bytes / s < 16 * 1024) --s;
+  return s;
 }
 
 }  // namespace
