@@ -28,24 +28,22 @@ constexpr int kMaxB = 64;
 constexpr int kStageFloats = 8 * 1024;  // score grid staged in shared memory up to 32 KB
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
-__device__ __forceinline__ uint64_t warp_max_u64(uint64_t v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const uint64_t w = __shfl_xor_sync(kFull, v, o);
-    v = w > v ? w : v;
-  }
-  return v;
+// argmax over the order codes row[0..K) (K <= 64; 0 marks no entry): the largest code, the
+// lowest index among equal ones.  One warp reduction and a ballot.
+__device__ __forceinline__ int warp_argmax_ord(uint32_t a, uint32_t b, int lane) {
+  const uint32_t m = __reduce_max_sync(kFull, a > b ? a : b);
+  const uint32_t ba = __ballot_sync(kFull, a == m);
+  if (ba) return __ffs(ba) - 1;
+  return 32 + __ffs(__ballot_sync(kFull, b == m)) - 1;
 }
-
-// argmax over row[0..K) (K <= 64): largest value, lowest index on ties, NaN lowest.
 __device__ __forceinline__ int warp_argmax(const float* row, int K, int lane) {
-  uint64_t k0 = lane < K ? make_key(__float_as_uint(row[lane]), lane) : 0ull;
-  uint64_t k1 = lane + 32 < K ? make_key(__float_as_uint(row[lane + 32]), lane + 32) : 0ull;
-  return static_cast<int>(key_index(warp_max_u64(k0 > k1 ? k0 : k1)));
+  const uint32_t a = lane < K ? ord32(__float_as_uint(row[lane])) : 0u;
+  const uint32_t b = lane + 32 < K ? ord32(__float_as_uint(row[lane + 32])) : 0u;
+  return warp_argmax_ord(a, b, lane);
 }
 
 __global__ void __launch_bounds__(kThreads) select_verify_kernel(const SelectVerifyArgs a) {
-  __shared__ float s_S[kStageFloats];
+  __shared__ uint32_t s_S[kStageFloats];  // order codes of the stream's scores
   __shared__ int32_t s_draft[kMaxB];
   __shared__ int s_A;
   __shared__ double s_part[kThreads];
@@ -63,11 +61,10 @@ __global__ void __launch_bounds__(kThreads) select_verify_kernel(const SelectVer
     const float* Sn = a.S + static_cast<size_t>(n) * grid_floats;
     const bool staged = grid_floats <= static_cast<size_t>(kStageFloats);
     if (staged) {
-      for (size_t i = threadIdx.x; i < grid_floats; i += kThreads) s_S[i] = Sn[i];
+      for (size_t i = threadIdx.x; i < grid_floats; i += kThreads) s_S[i] = ord32(__float_as_uint(Sn[i]));
     }
     __syncthreads();
     if (warp == 0) {
-      const float* src = staged ? s_S : Sn;
       const int32_t* idn = a.ids + static_cast<size_t>(n) * B * K;
       int k = warp_argmax(a.vals + static_cast<size_t>(n) * B * K, K, lane);
       if (lane == 0) {
@@ -75,7 +72,14 @@ __global__ void __launch_bounds__(kThreads) select_verify_kernel(const SelectVer
         s_draft[0] = idn[k];
       }
       for (int p = 0; p + 1 < B; ++p) {
-        k = warp_argmax(src + (static_cast<size_t>(p) * K + k) * K, K, lane);
+        const size_t row = (static_cast<size_t>(p) * K + k) * K;
+        if (staged) {
+          const uint32_t x = lane < K ? s_S[row + lane] : 0u;
+          const uint32_t y = lane + 32 < K ? s_S[row + lane + 32] : 0u;
+          k = warp_argmax_ord(x, y, lane);
+        } else {
+          k = warp_argmax(Sn + row, K, lane);
+        }
         if (lane == 0) {
           a.k_sel[static_cast<size_t>(n) * B + p + 1] = k;
           s_draft[p + 1] = idn[static_cast<size_t>(p + 1) * K + k];

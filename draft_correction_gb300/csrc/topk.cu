@@ -14,8 +14,8 @@
 //    grid fills whole waves of the GPU).  A block streams its segment with 128-bit loads
 //    (8 bf16 per lane), the next iteration's loads in flight while the current one is
 //    filtered.  The streaming loop has no barrier.
-//  * Threshold: the K-th largest of the block's 256 lane maxima over its first 2 iterations
-//    (each warp sorts its 32 maxima with shuffles; ranks come from binary searches in the 8
+//  * Threshold: the K-th largest of the block's 128 lane maxima over its first 2 iterations
+//    (each warp sorts its 32 maxima with shuffles; ranks come from binary searches in the 4
 //    sorted lists).  K values reach it, so anything smaller is not in the top K.
 //  * Streaming loop, no barrier: a lane tests the packed max of its vectors against the
 //    threshold and, if it may hold a candidate, records the vectors' position (a "suspect").
@@ -34,14 +34,13 @@
 namespace dcoco {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 128;
 constexpr int kWarps = kThreads / 32;
 constexpr int kU = 4;          // 16-byte vectors per lane per iteration
 constexpr int kMaxSplit = 8;
 constexpr int kMaxK = 64;
 constexpr int kCap = 1024;     // candidate buffer (keys)
 constexpr int kSusCap = 2048;  // lanes that may hold a candidate (per block)
-constexpr int kSeedIters = 2;  // iterations whose lane maxima seed the threshold
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
 template <bool kBf16>
@@ -230,7 +229,7 @@ __device__ __noinline__ void exact_segment_topk(const Segment& g, int K, int ran
 }
 
 template <bool kBf16, int KW>
-__global__ void __launch_bounds__(kThreads, 4) topk_kernel(const void* __restrict__ logits, int V, int K, int S,
+__global__ void __launch_bounds__(kThreads, 8) topk_kernel(const void* __restrict__ logits, int V, int K, int S,
                                                         float* __restrict__ vals, int32_t* __restrict__ ids) {
   constexpr int EPV = kEpv<kBf16>;
   __shared__ uint64_t s_buf[kCap];
@@ -280,28 +279,22 @@ __global__ void __launch_bounds__(kThreads, 4) topk_kernel(const void* __restric
     }
   };
 
-  // Seed threshold: the K-th largest of the block's 256 lane maxima over the first kSeedIters
-  // iterations.  K elements reach that value, so nothing below it is in the top K.  Those
-  // iterations are read again (from L2) by the main loop.
+  // Seed threshold: the K-th largest of the block's lane maxima over the first two iterations
+  // (already in registers).  K elements reach that value, so nothing below it is in the top K.
+  load(0, c0);
+  load(1, c1);
   {
     uint32_t mb = 0xFF800000u;  // -inf
     bool any = false;
-    load(0, c0);
-    load(1, c1);
 #pragma unroll
-    for (int it = 0; it < kSeedIters; ++it) {
-      load(it + 2, c2);
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        if (it < iters && vidx(it, u) < g.vend) {
-          mb = __float_as_uint(fmaxf(__uint_as_float(mb), __uint_as_float(vec_max_bits<kBf16>(c0[u]))));
-          any = true;
-        }
+    for (int u = 0; u < kU; ++u) {
+      if (iters > 0 && vidx(0, u) < g.vend) {
+        mb = __float_as_uint(fmaxf(__uint_as_float(mb), __uint_as_float(vec_max_bits<kBf16>(c0[u]))));
+        any = true;
       }
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        c0[u] = c1[u];
-        c1[u] = c2[u];
+      if (iters > 1 && vidx(1, u) < g.vend) {
+        mb = __float_as_uint(fmaxf(__uint_as_float(mb), __uint_as_float(vec_max_bits<kBf16>(c1[u]))));
+        any = true;
       }
     }
     const uint64_t mk = any ? (static_cast<uint64_t>(ord32(mb)) << 32) | static_cast<uint64_t>(0xFFFFFFFFu - threadIdx.x)
@@ -323,8 +316,6 @@ __global__ void __launch_bounds__(kThreads, 4) topk_kernel(const void* __restric
 
   // Hot loop: one packed max over the lane's vectors and one compare per iteration.  A lane
   // that may hold a key above the threshold only records where its vectors are.
-  load(0, c0);
-  load(1, c1);
   for (int it = 0; it < iters; ++it) {
     load(it + 2, c2);
     bool maybe = vidx(it, 0) < g.vend;
@@ -451,9 +442,9 @@ cudaError_t launch_topk_t(const void* logits, int rows, int V, int K, int S, flo
   return cudaLaunchKernelEx(&cfg, topk_kernel<kBf16, KW>, logits, V, K, S, vals, ids);
 }
 
-// Blocks per row: one block per row once there are at least two rows per SM (more blocks per
-// row only add per-block overhead); fewer rows are split until the grid covers the SMs, at
-// most 8 ways and keeping every segment at 16 KB or more.
+// Blocks per row: enough for at least four blocks per SM (one block per row once there are that
+// many rows; more blocks per row only add per-block overhead), at most 8, keeping every segment
+// at 16 KB or more.
 int auto_split(int rows, int V, bool bf16) {
   static int sms = 0;
   if (sms == 0) {
@@ -461,9 +452,8 @@ int auto_split(int rows, int V, bool bf16) {
     cudaGetDevice(&dev);
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 152;
   }
-  if (rows >= 2 * sms) return 1;
   const int64_t row_bytes = static_cast<int64_t>(V) * (bf16 ? 2 : 4);
-  int s = (2 * sms + rows - 1) / rows;
+  int s = (4 * sms + rows - 1) / rows;
   if (s > kMaxSplit) s = kMaxSplit;
   while (s > 1 && row_bytes / s < 16 * 1024) --s;
   return s;
