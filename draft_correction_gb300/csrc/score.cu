@@ -8,7 +8,7 @@
 // once upstream; this kernel forms the K x K broadcast sum on chip and never writes the
 // [K, K, H] hidden layer to memory.
 //
-// One thread block handles one transition (n, p) and AB = 8 predecessor rows a.  Per chunk of
+// One thread block handles one transition (n, p) and AB = 4 predecessor rows a.  Per chunk of
 // HC hidden units it stages, in shared memory,
 //   P[a][h] = (uz[n,p,a,h] + ws[n,p,h] + u_a[h] l_p(a) + b1[h]) / 2
 //   Q[b][h] = (vz[n,p+1,b,h] + u_b[h] l_{p+1}(b)) / 2
@@ -26,8 +26,8 @@
 namespace dcoco {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kAB = 8;    // predecessor rows per block
+constexpr int kThreads = 128;
+constexpr int kAB = 4;    // predecessor rows per block
 constexpr int kTA = 2;    // predecessor rows per thread tile
 constexpr int kTB = 4;    // successor rows per thread tile
 constexpr int kHC = 256;  // hidden units per shared-memory chunk (at most)
@@ -112,7 +112,7 @@ __global__ void __launch_bounds__(kThreads) score_kernel(const ScoreArgs a) {
   // Thread tiles: OT = (kAB/kTA) x (Kp/kTB); HS threads share a tile and split the hidden units.
   const int tiles_b = Kp / kTB;
   const int OT = (kAB / kTA) * tiles_b;
-  const int HS = kThreads / OT;  // OT <= 64 (K <= 64), so HS >= 4
+  const int HS = kThreads / OT;  // OT <= 32 (K <= 64), so HS >= 4
   const int ot = threadIdx.x % OT, hs = threadIdx.x / OT;
   const bool active = hs < HS;
   const int ta = ot / tiles_b, tb = ot % tiles_b;

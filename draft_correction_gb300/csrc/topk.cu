@@ -14,8 +14,8 @@
 //    grid fills whole waves of the GPU).  A block streams its segment with 128-bit loads
 //    (8 bf16 per lane), the next iteration's loads in flight while the current one is
 //    filtered.  The streaming loop has no barrier.
-//  * Threshold: the K-th largest of the block's 128 lane maxima over its first 2 iterations
-//    (each warp sorts its 32 maxima with shuffles; ranks come from binary searches in the 4
+//  * Threshold: the K-th largest of the block's 256 lane maxima over its first 2 iterations
+//    (each warp sorts its 32 maxima with shuffles; ranks come from binary searches in the 8
 //    sorted lists).  K values reach it, so anything smaller is not in the top K.
 //  * Streaming loop, no barrier: a lane tests the packed max of its vectors against the
 //    threshold and, if it may hold a candidate, records the vectors' position (a "suspect").
@@ -34,7 +34,7 @@
 namespace dcoco {
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kU = 4;          // 16-byte vectors per lane per iteration
 constexpr int kMaxSplit = 8;
@@ -124,16 +124,42 @@ __device__ __forceinline__ int count_greater(const uint64_t* list, int n, uint64
 }
 
 // Keep the K largest keys of s_buf[0, cnt) in s_keep[0, K) (descending; 0 where cnt < K).
-// Called by every thread of the block.
-__device__ __forceinline__ void select_top(const uint64_t* s_buf, int cnt, int K, uint64_t* s_keep) {
+// Called by every thread of the block.  Small buffers rank every key against all others;
+// larger ones (up to kCap) are sorted in place with a bitonic network, padded with zeros.
+__device__ __forceinline__ void select_top(uint64_t* s_buf, int cnt, int K, uint64_t* s_keep) {
   if (threadIdx.x < K) s_keep[threadIdx.x] = 0;
   __syncthreads();
-  for (int c = threadIdx.x; c < cnt; c += kThreads) {
-    const uint64_t x = s_buf[c];
-    int above = 0;
-    for (int o = 0; o < cnt; ++o) above += (s_buf[o] > x);
-    if (above < K) s_keep[above] = x;
+  if (cnt <= 128) {
+    for (int c = threadIdx.x; c < cnt; c += kThreads) {
+      const uint64_t x = s_buf[c];
+      int above = 0;
+      for (int o = 0; o < cnt; ++o) above += (s_buf[o] > x);
+      if (above < K) s_keep[above] = x;
+    }
+    __syncthreads();
+    return;
   }
+  int n = 256;
+  while (n < cnt) n <<= 1;
+  for (int i = cnt + threadIdx.x; i < n; i += kThreads) s_buf[i] = 0;
+  __syncthreads();
+  for (int k = 2; k <= n; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < n; i += kThreads) {
+        const int l = i ^ j;
+        if (l > i) {
+          const uint64_t a = s_buf[i], b = s_buf[l];
+          const bool desc = (i & k) == 0;  // descending blocks end up first: overall descending
+          if (desc ? (a < b) : (a > b)) {
+            s_buf[i] = b;
+            s_buf[l] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  if (threadIdx.x < K) s_keep[threadIdx.x] = s_buf[threadIdx.x];
   __syncthreads();
 }
 
@@ -229,7 +255,7 @@ __device__ __noinline__ void exact_segment_topk(const Segment& g, int K, int ran
 }
 
 template <bool kBf16, int KW>
-__global__ void __launch_bounds__(kThreads, 8) topk_kernel(const void* __restrict__ logits, int V, int K, int S,
+__global__ void __launch_bounds__(kThreads, 4) topk_kernel(const void* __restrict__ logits, int V, int K, int S,
                                                         float* __restrict__ vals, int32_t* __restrict__ ids) {
   constexpr int EPV = kEpv<kBf16>;
   __shared__ uint64_t s_buf[kCap];
@@ -442,9 +468,9 @@ cudaError_t launch_topk_t(const void* logits, int rows, int V, int K, int S, flo
   return cudaLaunchKernelEx(&cfg, topk_kernel<kBf16, KW>, logits, V, K, S, vals, ids);
 }
 
-// Blocks per row: enough for at least four blocks per SM (one block per row once there are that
-// many rows; more blocks per row only add per-block overhead), at most 8, keeping every segment
-// at 16 KB or more.
+// Blocks per row: one block per row once there are at least two rows per SM (more blocks per
+// row only add per-block overhead); fewer rows are split until there are about four blocks per
+// SM, at most 8 ways, keeping every segment at 16 KB or more.
 int auto_split(int rows, int V, bool bf16) {
   static int sms = 0;
   if (sms == 0) {
@@ -452,6 +478,7 @@ int auto_split(int rows, int V, bool bf16) {
     cudaGetDevice(&dev);
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 152;
   }
+  if (rows >= 2 * sms) return 1;
   const int64_t row_bytes = static_cast<int64_t>(V) * (bf16 ? 2 : 4);
   int s = (4 * sms + rows - 1) / rows;
   if (s > kMaxSplit) s = kMaxSplit;
