@@ -8,7 +8,7 @@
 // once upstream; this kernel forms the K x K broadcast sum on chip and never writes the
 // [K, K, H] hidden layer to memory.
 //
-// One thread block handles one transition (n, p) and AB = 4 predecessor rows a.  Per chunk of
+// One thread block handles one transition (n, p) and AB = 8 predecessor rows a.  Per chunk of
 // HC hidden units it stages, in shared memory,
 //   P[a][h] = (uz[n,p,a,h] + ws[n,p,h] + u_a[h] l_p(a) + b1[h]) / 2
 //   Q[b][h] = (vz[n,p+1,b,h] + u_b[h] l_{p+1}(b)) / 2
@@ -20,23 +20,25 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "internal.h"
 #include "ptx.cuh"
 
 namespace dcoco {
 namespace {
 
-constexpr int kThreads = 128;
-constexpr int kAB = 4;    // predecessor rows per block
+constexpr int kThreads = 256;
+constexpr int kAB = 8;    // predecessor rows per block
 constexpr int kTA = 2;    // predecessor rows per thread tile
 constexpr int kTB = 4;    // successor rows per thread tile
-constexpr int kHC = 256;  // hidden units per shared-memory chunk (at most)
+constexpr int kHC = 128;  // hidden units per shared-memory chunk (at most)
 constexpr int kPad = 4;   // row padding (floats): neighbouring rows start in different banks
 
-// Hidden units per shared-memory chunk: all of H up to 256, else the largest of 256, 128, 64
-// dividing H (H is a multiple of 64), so every chunk is full.
+// Hidden units per shared-memory chunk: all of H up to 128, else 128 or 64, whichever divides H
+// (H is a multiple of 64), so every chunk is full.
 __host__ __device__ __forceinline__ int score_chunk(int H) {
-  return H <= kHC ? H : (H % 256 == 0 ? 256 : (H % 128 == 0 ? 128 : 64));
+  return H <= kHC ? H : (H % 128 == 0 ? 128 : 64);
 }
 
 template <bool kBf16>
@@ -67,6 +69,25 @@ __device__ __forceinline__ void ld8(const void* p, size_t i, float (&x)[8]) {
   }
 }
 
+// Eight consecutive activations of a shared-memory row widened to float.
+template <bool kBf16, typename Act>
+__device__ __forceinline__ void ld8_smem(const Act* p, float (&x)[8]) {
+  if constexpr (kBf16) {
+    const uint4 w = *reinterpret_cast<const uint4*>(p);
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      x[2 * j] = __uint_as_float(u[j] << 16);
+      x[2 * j + 1] = __uint_as_float(u[j] & 0xFFFF0000u);
+    }
+  } else {
+    const float4 a = *reinterpret_cast<const float4*>(p);
+    const float4 b = *reinterpret_cast<const float4*>(p + 4);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+  }
+}
+
 __device__ __forceinline__ float tanh_fast(float x) {
   float y;
   asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -92,27 +113,31 @@ __device__ __forceinline__ void tanh4_f16(float a, float b, float c, float d, fl
 
 template <bool kBf16>
 __global__ void __launch_bounds__(kThreads) score_kernel(const ScoreArgs a) {
-  extern __shared__ float sm[];
+  using Act = typename std::conditional<kBf16, __nv_bfloat16, float>::type;
+  extern __shared__ __align__(16) float sm[];
   const int K = a.K, H = a.H, B = a.B;
   const int np = blockIdx.x;  // n * (B-1) + p
   const int n = np / (B - 1), p = np % (B - 1);
   const int a0 = blockIdx.y * kAB;
   const int na = min(kAB, K - a0);
   const int Kp = (K + kTB - 1) / kTB * kTB;  // successor rows padded to the thread tile
-  const int hc = score_chunk(H);
+  const int hc = score_chunk(H);  // 64 or 128
+  const int hc_shift = hc == 128 ? 7 : 6;
   const int ld = hc + kPad;
-  float* P = sm;             // [kAB][ld]
-  float* Q = P + kAB * ld;   // [Kp][ld]
-  float* w2c = Q + Kp * ld;  // [hc]  output weights of the chunk
-  float* uac = w2c + hc;     // [hc]  u_a
-  float* ubc = uac + hc;     // [hc]  u_b
-  float* bwc = ubc + hc;     // [hc]  b1 + W s_p
-  float* red = bwc + hc;     // [kThreads][kTA * kTB] partial sums
+  const int rows = kAB + Kp;
+  float* w2v = sm;            // [H]  output weights
+  float* uav = w2v + H;       // [H]  u_a
+  float* ubv = uav + H;       // [H]  u_b
+  float* bwv = ubv + H;       // [H]  b1 + W s_p
+  float* P = bwv + H;         // [kAB][ld]   current chunk
+  float* Q = P + kAB * ld;    // [Kp][ld]
+  float* red = Q + Kp * ld;   // [kThreads][kTA * kTB] partial sums
+  Act* raw = reinterpret_cast<Act*>(red + kThreads * kTA * kTB);  // [rows][hc] next chunk, as stored
 
   // Thread tiles: OT = (kAB/kTA) x (Kp/kTB); HS threads share a tile and split the hidden units.
   const int tiles_b = Kp / kTB;
   const int OT = (kAB / kTA) * tiles_b;
-  const int HS = kThreads / OT;  // OT <= 32 (K <= 64), so HS >= 4
+  const int HS = kThreads / OT;  // OT <= 64 (K <= 64), so HS >= 4
   const int ot = threadIdx.x % OT, hs = threadIdx.x / OT;
   const bool active = hs < HS;
   const int ta = ot / tiles_b, tb = ot % tiles_b;
@@ -122,7 +147,30 @@ __global__ void __launch_bounds__(kThreads) score_kernel(const ScoreArgs a) {
   const float* vals_p = a.vals + row_p;
   const float* vals_q = a.vals + row_q;
   const float* wsp = a.wsp + static_cast<size_t>(np) * H;
-  const int nv = hc / 8;  // 8-wide vectors per row and chunk
+  const int cpr = hc * static_cast<int>(sizeof(Act)) / 16;  // 16-byte pieces per row and chunk
+
+  // Raw rows of one chunk (predecessor rows from uz, successor rows from vz) by cp.async.
+  auto fetch = [&](int h0) {
+    const uint32_t base = smem_u32(raw);
+    for (int i = threadIdx.x; i < rows * cpr; i += kThreads) {
+      const int r = i / cpr, c = i - r * cpr;
+      const Act* src = nullptr;
+      if (r < kAB) {
+        if (r < na) src = static_cast<const Act*>(a.uz) + (row_p + a0 + r) * H + h0;
+      } else if (r - kAB < K) {
+        src = static_cast<const Act*>(a.vz) + (row_q + r - kAB) * H + h0;
+      }
+      if (src != nullptr) cp_async16(base + (r * hc) * sizeof(Act) + c * 16, reinterpret_cast<const char*>(src) + c * 16, 16);
+    }
+    cp_async_commit();
+  };
+  fetch(0);
+  for (int i = threadIdx.x; i < H; i += kThreads) {
+    w2v[i] = ldv<kBf16>(a.w2, i);
+    uav[i] = ldv<kBf16>(a.u_a, i);
+    ubv[i] = ldv<kBf16>(a.u_b, i);
+    bwv[i] = ldv<kBf16>(a.b1, i) + wsp[i];
+  }
 
   float acc[kTA][kTB];
 #pragma unroll
@@ -131,27 +179,21 @@ __global__ void __launch_bounds__(kThreads) score_kernel(const ScoreArgs a) {
     for (int j = 0; j < kTB; ++j) acc[i][j] = 0.f;
 
   for (int h0 = 0; h0 < H; h0 += hc) {
-    __syncthreads();
-    for (int i = threadIdx.x; i < hc; i += kThreads) {
-      w2c[i] = ldv<kBf16>(a.w2, h0 + i);
-      uac[i] = ldv<kBf16>(a.u_a, h0 + i);
-      ubc[i] = ldv<kBf16>(a.u_b, h0 + i);
-      bwc[i] = ldv<kBf16>(a.b1, h0 + i) + wsp[h0 + i];
-    }
-    __syncthreads();
+    cp_async_wait(0);
+    __syncthreads();  // this chunk's raw rows and the vectors are visible; P/Q are free
     // P[a][h] = (uz + b1 + W s + u_a l_p(a)) / 2 and Q[b][h] = (vz + u_b l_{p+1}(b)) / 2; rows
     // past na (P) or K (Q) are zero.
-    for (int i = threadIdx.x; i < (kAB + Kp) * nv; i += kThreads) {
-      const int r = i / nv, c = (i - r * nv) * 8;
+    for (int i = threadIdx.x; i < (rows << hc_shift) / 8; i += kThreads) {
+      const int r = (i * 8) >> hc_shift, c = (i * 8) & (hc - 1), h = h0 + c;
       float x[8];
       float* dst;
       if (r < kAB) {
         dst = P + r * ld + c;
         if (r < na) {
-          ld8<kBf16>(a.uz, (row_p + a0 + r) * H + h0 + c, x);
+          ld8_smem<kBf16>(raw + r * hc + c, x);
           const float l = vals_p[a0 + r];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) x[e] = 0.5f * (x[e] + bwc[c + e] + uac[c + e] * l);
+          for (int e = 0; e < 8; ++e) x[e] = 0.5f * (x[e] + bwv[h + e] + uav[h + e] * l);
         } else {
 #pragma unroll
           for (int e = 0; e < 8; ++e) x[e] = 0.f;
@@ -160,10 +202,10 @@ __global__ void __launch_bounds__(kThreads) score_kernel(const ScoreArgs a) {
         const int rb = r - kAB;
         dst = Q + rb * ld + c;
         if (rb < K) {
-          ld8<kBf16>(a.vz, (row_q + rb) * H + h0 + c, x);
+          ld8_smem<kBf16>(raw + r * hc + c, x);
           const float l = vals_q[rb];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) x[e] = 0.5f * (x[e] + ubc[c + e] * l);
+          for (int e = 0; e < 8; ++e) x[e] = 0.5f * (x[e] + ubv[h + e] * l);
         } else {
 #pragma unroll
           for (int e = 0; e < 8; ++e) x[e] = 0.f;
@@ -172,9 +214,10 @@ __global__ void __launch_bounds__(kThreads) score_kernel(const ScoreArgs a) {
       *reinterpret_cast<float4*>(dst) = make_float4(x[0], x[1], x[2], x[3]);
       *reinterpret_cast<float4*>(dst + 4) = make_float4(x[4], x[5], x[6], x[7]);
     }
-    __syncthreads();
+    __syncthreads();  // P/Q ready; the raw buffer is free for the next chunk
+    if (h0 + hc < H) fetch(h0 + hc);
     if (active) {
-      const float4* w4 = reinterpret_cast<const float4*>(w2c);
+      const float4* w4 = reinterpret_cast<const float4*>(w2v + h0);
       const float4* p4 = reinterpret_cast<const float4*>(P + ta * kTA * ld);
       const float4* q4 = reinterpret_cast<const float4*>(Q + tb * kTB * ld);
       const int ld4 = ld / 4;
@@ -213,7 +256,6 @@ __global__ void __launch_bounds__(kThreads) score_kernel(const ScoreArgs a) {
   }
 
   // Add the HS partial sums of every output in a fixed order.
-  __syncthreads();
 #pragma unroll
   for (int i = 0; i < kTA; ++i)
 #pragma unroll
@@ -233,12 +275,17 @@ __global__ void __launch_bounds__(kThreads) score_kernel(const ScoreArgs a) {
 
 }  // namespace
 
-cudaError_t launch_scores(const ScoreArgs& a, bool is_bf16, cudaStream_t stream) {
-  const int hc = score_chunk(a.H);
+size_t score_smem_bytes(int H, int K, bool is_bf16) {
+  const int hc = score_chunk(H);
   const int ld = hc + kPad;
-  const int Kp = (a.K + kTB - 1) / kTB * kTB;
-  // P, Q, four per-chunk vectors, and the partial sums of every thread
-  const size_t smem = (static_cast<size_t>(kAB + Kp) * ld + 4 * hc + kThreads * kTA * kTB) * sizeof(float);
+  const int Kp = (K + kTB - 1) / kTB * kTB;
+  // vectors, P and Q, partial sums, and one chunk of raw rows
+  return (4 * static_cast<size_t>(H) + static_cast<size_t>(kAB + Kp) * ld + kThreads * kTA * kTB) * sizeof(float) +
+         static_cast<size_t>(kAB + Kp) * hc * (is_bf16 ? 2 : 4);
+}
+
+cudaError_t launch_scores(const ScoreArgs& a, bool is_bf16, cudaStream_t stream) {
+  const size_t smem = score_smem_bytes(a.H, a.K, is_bf16);
   dim3 grid(a.N * (a.B - 1), (a.K + kAB - 1) / kAB);
   // The dynamic shared memory ceiling is raised once per device to the largest this kernel
   // can need (K = 64), so later calls enqueue only the launch (CUDA-graph friendly).
@@ -248,8 +295,7 @@ cudaError_t launch_scores(const ScoreArgs& a, bool is_bf16, cudaStream_t stream)
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    const int most =
-        static_cast<int>((static_cast<size_t>(kAB + 64) * (kHC + kPad) + 4 * kHC + kThreads * kTA * kTB) * sizeof(float));
+    const int most = 227 * 1024;
     e = cudaFuncSetAttribute(score_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(score_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
     if (e != cudaSuccess) return e;
