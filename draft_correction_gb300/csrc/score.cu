@@ -88,6 +88,22 @@ __device__ __forceinline__ void ld8_smem(const Act* p, float (&x)[8]) {
   }
 }
 
+// sum over 8 hidden units of w * SiLU(2y) / 2 ... written as w * (y + y tanh(y)) with y = p + q,
+// in packed half precision; returns the two interleaved partial sums.
+__device__ __forceinline__ __half2 silu_dot8(const uint4& p, const uint4& q, const uint4& w) {
+  const uint32_t pp[4] = {p.x, p.y, p.z, p.w}, qq[4] = {q.x, q.y, q.z, q.w}, ww[4] = {w.x, w.y, w.z, w.w};
+  __half2 acc = __float2half2_rn(0.f);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const __half2 y = __hadd2(*reinterpret_cast<const __half2*>(&pp[k]), *reinterpret_cast<const __half2*>(&qq[k]));
+    uint32_t t;
+    asm("tanh.approx.f16x2 %0, %1;" : "=r"(t) : "r"(*reinterpret_cast<const uint32_t*>(&y)));
+    const __half2 sv = __hfma2(y, *reinterpret_cast<const __half2*>(&t), y);
+    acc = __hfma2(*reinterpret_cast<const __half2*>(&ww[k]), sv, acc);
+  }
+  return acc;
+}
+
 __device__ __forceinline__ float tanh_fast(float x) {
   float y;
   asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -123,18 +139,22 @@ __global__ void __launch_bounds__(kThreads) score_kernel(const ScoreArgs a) {
   const int Kp = (K + kTB - 1) / kTB * kTB;  // successor rows padded to the thread tile
   const int hc = score_chunk(H);  // 64 or 128
   const int hc_shift = hc == 128 ? 7 : 6;
-  const int ld = hc + kPad;
+  const int ld = hc + kPad;   // row pitch of P and Q in floats (f32 path)
+  const int ldh = hc + 8;     // row pitch in halves (bf16 path): rows start on 16-byte boundaries
   const int rows = kAB + Kp;
   float* w2v = sm;            // [H]  output weights
   float* uav = w2v + H;       // [H]  u_a
   float* ubv = uav + H;       // [H]  u_b
   float* bwv = ubv + H;       // [H]  b1 + W s_p
-  float* P = bwv + H;         // [kAB][ld]   current chunk
+  __half* w2h = reinterpret_cast<__half*>(bwv + H);  // [H] output weights in half precision
+  float* P = bwv + H + H / 2;  // [kAB][ld]   current chunk (halves on the bf16 path)
   float* Q = P + kAB * ld;    // [Kp][ld]
   float* red = Q + Kp * ld;   // [kThreads][kTA * kTB] partial sums
   Act* raw = reinterpret_cast<Act*>(red + kThreads * kTA * kTB);  // [rows][hc] next chunk, as stored
 
   // Thread tiles: OT = (kAB/kTA) x (Kp/kTB); HS threads share a tile and split the hidden units.
+  // Tile (ta, tb) holds predecessor rows ta*kTA + i and successor rows tb + j*tiles_b (strided, so
+  // that neighbouring threads read rows in different shared-memory banks).
   const int tiles_b = Kp / kTB;
   const int OT = (kAB / kTA) * tiles_b;
   const int HS = kThreads / OT;  // OT <= 64 (K <= 64), so HS >= 4
@@ -170,6 +190,7 @@ __global__ void __launch_bounds__(kThreads) score_kernel(const ScoreArgs a) {
     uav[i] = ldv<kBf16>(a.u_a, i);
     ubv[i] = ldv<kBf16>(a.u_b, i);
     bwv[i] = ldv<kBf16>(a.b1, i) + wsp[i];
+    w2h[i] = __float2half_rn(w2v[i]);
   }
 
   float acc[kTA][kTB];
@@ -188,7 +209,7 @@ __global__ void __launch_bounds__(kThreads) score_kernel(const ScoreArgs a) {
       float x[8];
       float* dst;
       if (r < kAB) {
-        dst = P + r * ld + c;
+        dst = kBf16 ? reinterpret_cast<float*>(reinterpret_cast<__half*>(P) + r * ldh + c) : P + r * ld + c;
         if (r < na) {
           ld8_smem<kBf16>(raw + r * hc + c, x);
           const float l = vals_p[a0 + r];
@@ -200,7 +221,7 @@ __global__ void __launch_bounds__(kThreads) score_kernel(const ScoreArgs a) {
         }
       } else {
         const int rb = r - kAB;
-        dst = Q + rb * ld + c;
+        dst = kBf16 ? reinterpret_cast<float*>(reinterpret_cast<__half*>(Q) + rb * ldh + c) : Q + rb * ld + c;
         if (rb < K) {
           ld8_smem<kBf16>(raw + r * hc + c, x);
           const float l = vals_q[rb];
@@ -211,44 +232,77 @@ __global__ void __launch_bounds__(kThreads) score_kernel(const ScoreArgs a) {
           for (int e = 0; e < 8; ++e) x[e] = 0.f;
         }
       }
-      *reinterpret_cast<float4*>(dst) = make_float4(x[0], x[1], x[2], x[3]);
-      *reinterpret_cast<float4*>(dst + 4) = make_float4(x[4], x[5], x[6], x[7]);
+      if constexpr (kBf16) {
+        // half precision, clamped to +-30000 so that a sum of two never overflows
+        __half2* d16 = reinterpret_cast<__half2*>(dst);  // rows of ld halves
+        uint4 w;
+        __half2 hh[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          hh[e] = __floats2half2_rn(fminf(fmaxf(x[2 * e], -30000.f), 30000.f),
+                                    fminf(fmaxf(x[2 * e + 1], -30000.f), 30000.f));
+        w.x = *reinterpret_cast<uint32_t*>(&hh[0]);
+        w.y = *reinterpret_cast<uint32_t*>(&hh[1]);
+        w.z = *reinterpret_cast<uint32_t*>(&hh[2]);
+        w.w = *reinterpret_cast<uint32_t*>(&hh[3]);
+        *reinterpret_cast<uint4*>(d16) = w;
+      } else {
+        *reinterpret_cast<float4*>(dst) = make_float4(x[0], x[1], x[2], x[3]);
+        *reinterpret_cast<float4*>(dst + 4) = make_float4(x[4], x[5], x[6], x[7]);
+      }
     }
     __syncthreads();  // P/Q ready; the raw buffer is free for the next chunk
     if (h0 + hc < H) fetch(h0 + hc);
     if (active) {
-      const float4* w4 = reinterpret_cast<const float4*>(w2v + h0);
-      const float4* p4 = reinterpret_cast<const float4*>(P + ta * kTA * ld);
-      const float4* q4 = reinterpret_cast<const float4*>(Q + tb * kTB * ld);
-      const int ld4 = ld / 4;
-      for (int c = hs; c < hc / 4; c += HS) {
-        const float4 w = w4[c];
-        float4 pv[kTA], qv[kTB];
+      if constexpr (kBf16) {
+        // Packed half precision: 8 hidden units per step, two per instruction.  Each output keeps
+        // an f16 pair of partial sums for the step and adds it to its fp32 total.
+        const uint4* p8 = reinterpret_cast<const uint4*>(reinterpret_cast<const __half*>(P) + ta * kTA * ldh);
+        const uint4* q8 = reinterpret_cast<const uint4*>(reinterpret_cast<const __half*>(Q) + tb * ldh);
+        const uint4* w8 = reinterpret_cast<const uint4*>(w2h + h0);
+        const int ld8 = ldh / 8;
+        for (int c = hs; c < hc / 8; c += HS) {
+          const uint4 w = w8[c];
+          uint4 pv[kTA], qv[kTB];
 #pragma unroll
-        for (int i = 0; i < kTA; ++i) pv[i] = p4[i * ld4 + c];
+          for (int i = 0; i < kTA; ++i) pv[i] = p8[i * ld8 + c];
 #pragma unroll
-        for (int j = 0; j < kTB; ++j) qv[j] = q4[j * ld4 + c];
+          for (int j = 0; j < kTB; ++j) qv[j] = q8[j * tiles_b * ld8 + c];
 #pragma unroll
-        for (int i = 0; i < kTA; ++i) {
+          for (int i = 0; i < kTA; ++i) {
 #pragma unroll
-          for (int j = 0; j < kTB; ++j) {
-            const float y0 = pv[i].x + qv[j].x, y1 = pv[i].y + qv[j].y;
-            const float y2 = pv[i].z + qv[j].z, y3 = pv[i].w + qv[j].w;
-            float t0, t1, t2, t3;
-            if constexpr (kBf16) {
-              tanh4_f16(y0, y1, y2, y3, t0, t1, t2, t3);
-            } else {
-              t0 = tanh_fast(y0);
-              t1 = tanh_fast(y1);
-              t2 = tanh_fast(y2);
-              t3 = tanh_fast(y3);
+            for (int j = 0; j < kTB; ++j) {
+              __half2 sacc = silu_dot8(pv[i], qv[j], w);
+              const float2 f = __half22float2(sacc);
+              acc[i][j] += f.x + f.y;
             }
-            float s = acc[i][j];
-            s = fmaf(w.x, fmaf(y0, t0, y0), s);
-            s = fmaf(w.y, fmaf(y1, t1, y1), s);
-            s = fmaf(w.z, fmaf(y2, t2, y2), s);
-            s = fmaf(w.w, fmaf(y3, t3, y3), s);
-            acc[i][j] = s;
+          }
+        }
+      } else {
+        const float4* w4 = reinterpret_cast<const float4*>(w2v + h0);
+        const float4* p4 = reinterpret_cast<const float4*>(P + ta * kTA * ld);
+        const float4* q4 = reinterpret_cast<const float4*>(Q + tb * ld);
+        const int ld4 = ld / 4;
+        for (int c = hs; c < hc / 4; c += HS) {
+          const float4 w = w4[c];
+          float4 pv[kTA], qv[kTB];
+#pragma unroll
+          for (int i = 0; i < kTA; ++i) pv[i] = p4[i * ld4 + c];
+#pragma unroll
+          for (int j = 0; j < kTB; ++j) qv[j] = q4[j * tiles_b * ld4 + c];
+#pragma unroll
+          for (int i = 0; i < kTA; ++i) {
+#pragma unroll
+            for (int j = 0; j < kTB; ++j) {
+              const float y0 = pv[i].x + qv[j].x, y1 = pv[i].y + qv[j].y;
+              const float y2 = pv[i].z + qv[j].z, y3 = pv[i].w + qv[j].w;
+              float s = acc[i][j];
+              s = fmaf(w.x, fmaf(y0, tanh_fast(y0), y0), s);
+              s = fmaf(w.y, fmaf(y1, tanh_fast(y1), y1), s);
+              s = fmaf(w.z, fmaf(y2, tanh_fast(y2), y2), s);
+              s = fmaf(w.w, fmaf(y3, tanh_fast(y3), y3), s);
+              acc[i][j] = s;
+            }
           }
         }
       }
@@ -265,8 +319,8 @@ __global__ void __launch_bounds__(kThreads) score_kernel(const ScoreArgs a) {
   float* Sp = a.S + (static_cast<size_t>(np) * K + a0) * K;  // rows a0.. of this transition
   for (int o = threadIdx.x; o < na * K; o += kThreads) {
     const int ar = o / K, bc = o % K;
-    const int t = (ar / kTA) * tiles_b + bc / kTB;
-    const int idx = (ar % kTA) * kTB + bc % kTB;
+    const int t = (ar / kTA) * tiles_b + bc % tiles_b;
+    const int idx = (ar % kTA) * kTB + bc / tiles_b;
     float s = 0.f;
     for (int h = 0; h < HS; ++h) s += red[(h * OT + t) * (kTA * kTB) + idx];
     Sp[o] = vals_q[bc] + s + b2;
@@ -280,7 +334,7 @@ size_t score_smem_bytes(int H, int K, bool is_bf16) {
   const int ld = hc + kPad;
   const int Kp = (K + kTB - 1) / kTB * kTB;
   // vectors, P and Q, partial sums, and one chunk of raw rows
-  return (4 * static_cast<size_t>(H) + static_cast<size_t>(kAB + Kp) * ld + kThreads * kTA * kTB) * sizeof(float) +
+  return (4 * static_cast<size_t>(H) + H / 2 + static_cast<size_t>(kAB + Kp) * ld + kThreads * kTA * kTB) * sizeof(float) +
          static_cast<size_t>(kAB + Kp) * hc * (is_bf16 ? 2 : 4);
 }
 
