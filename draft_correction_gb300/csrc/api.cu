@@ -203,7 +203,8 @@ int run_gemm(GemmArgs& a, const Dims& D, int BN, cudaStream_t st, const char* wh
   const int n_tiles = a.g[0].n_tiles + (a.n_groups > 1 ? a.g[1].n_tiles : 0);
   const int bk = D.bf16 ? 64 : 32;
   const int nkb = (a.K + bk - 1) / bk;
-  const int split = pick_split(m_tiles, n_tiles, nkb, BN);
+  const bool prep = a.g[0].epi == EPI_PREP || (a.n_groups > 1 && a.g[1].epi == EPI_PREP);
+  const int split = prep ? 1 : pick_split(m_tiles, n_tiles, nkb, BN);
   const cudaError_t e = launch_gemm(a, D.bf16, BN, split, st);
   if (e != cudaSuccess) return cuda_fail(e, what);
   return DCOCO_OK;
@@ -269,8 +270,10 @@ int enqueue_repr_gather(const Dims& D, const int32_t* ids, const void* emb, int 
 }
 
 // Candidate representation, fusion part: z = SiLU(W_f[:, 0:r] b + gw[slot]), uz = U z, vz = V z.
+// With prep_vals set, the U z / V z epilogue writes the scorer's operands instead:
+// uz <- (U z + b1 + W s + u_a l)/2 and vz <- (V z + u_b l)/2 (W s from prep_wsp).
 int enqueue_repr_fuse(const Dims& D, const dcoco_weights* w, void* uz, void* vz, const ReprScratch& s,
-                      cudaStream_t st) {
+                      cudaStream_t st, const float* prep_vals = nullptr, const float* prep_wsp = nullptr) {
   const int M = D.M(), r = D.r, H = D.H;
   // z = SiLU(W_f[:, 0:r] b + gw[slot])
   {
@@ -294,8 +297,19 @@ int enqueue_repr_fuse(const Dims& D, const dcoco_weights* w, void* uz, void* vz,
     a.K = r;
     a.n_groups = 2;
     const int BN = pick_bn(H, false);
-    DCOCO_TRY(gemm_group(&a.g[0], w->U, D, H, r, r, BN, uz, H, EPI_ACT, a.M));
-    DCOCO_TRY(gemm_group(&a.g[1], w->V, D, H, r, r, BN, vz, H, EPI_ACT, a.M));
+    const int epi = prep_vals != nullptr ? EPI_PREP : EPI_ACT;
+    DCOCO_TRY(gemm_group(&a.g[0], w->U, D, H, r, r, BN, uz, H, epi, a.M));
+    DCOCO_TRY(gemm_group(&a.g[1], w->V, D, H, r, r, BN, vz, H, epi, a.M));
+    if (prep_vals != nullptr) {
+      a.row_l = prep_vals;
+      a.bias_div = D.K;
+      a.slots = D.B;
+      a.ld_bias = H;
+      a.g[0].col_u = w->u_a;
+      a.g[0].col_b = w->b1;
+      a.g[0].row_bias = prep_wsp;
+      a.g[1].col_u = w->u_b;
+    }
     DCOCO_TRY(run_gemm(a, D, BN, st, "gemm uz, vz"));
   }
   return DCOCO_OK;
@@ -385,6 +399,24 @@ int enqueue_scores(const Dims& D, const void* uz, const void* vz, const float* w
   a.K = D.K;
   a.H = D.H;
   const cudaError_t e = launch_scores(a, D.bf16, st);
+  if (e != cudaSuccess) return cuda_fail(e, "transition scores");
+  return DCOCO_OK;
+}
+
+int enqueue_scores_prepped(const Dims& D, const void* P, const void* Q, const float* vals, const dcoco_weights* w,
+                           float* S, cudaStream_t st) {
+  ScoreArgs a = {};
+  a.uz = P;
+  a.vz = Q;
+  a.vals = vals;
+  a.w2 = w->w2;
+  a.b2 = w->b2;
+  a.S = S;
+  a.N = D.N;
+  a.B = D.B;
+  a.K = D.K;
+  a.H = D.H;
+  const cudaError_t e = launch_scores_prepped(a, D.bf16, st);
   if (e != cudaSuccess) return cuda_fail(e, "transition scores");
   return DCOCO_OK;
 }
@@ -663,8 +695,9 @@ int dcoco_cycle(const void* logits, int V, const void* emb, const void* h, const
   DCOCO_TRY(enqueue_repr_gather(D, o_ids, emb, V, w, s.repr, st));
   e = cudaStreamWaitEvent(st, side->join, 0);
   if (e != cudaSuccess) return cuda_fail(e, "join from helper stream");
-  DCOCO_TRY(enqueue_repr_fuse(D, w, s.uz, s.vz, s.repr, st));
-  DCOCO_TRY(enqueue_scores(D, s.uz, s.vz, s.wsp, o_vals, w, o_S, st));
+  // uz/vz scratch holds the scorer's prepared operands P and Q here.
+  DCOCO_TRY(enqueue_repr_fuse(D, w, s.uz, s.vz, s.repr, st, o_vals, s.wsp));
+  DCOCO_TRY(enqueue_scores_prepped(D, s.uz, s.vz, o_vals, w, o_S, st));
   SelectVerifyArgs a = {};
   a.S = o_S;
   a.vals = o_vals;

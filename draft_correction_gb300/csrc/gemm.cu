@@ -18,6 +18,7 @@
 // K range, stages its partial tile in its shared memory, and each CTA then sums a slice
 // of rows across the cluster in rank order (distributed shared memory) -- deterministic.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include <algorithm>
 
@@ -51,17 +52,26 @@ __device__ __forceinline__ float silu(float x) {
 
 // One thread's row of a 128-byte-wide output sub-tile into the 128-byte swizzled staging
 // layout a tensor-map store expects (16-byte chunk c of row r at r*128 + (c ^ (r & 7))*16).
-template <bool kOutBf16>
+// kOut: 0 f32, 1 bf16, 2 f16.
+template <int kOut>
 __device__ __forceinline__ void stage_row(uint8_t* buf, int r, const float* v) {
-  constexpr int NV = kOutBf16 ? 64 : 32;  // values in 128 bytes
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
     uint4 w;
-    if constexpr (kOutBf16) {
+    if constexpr (kOut == 1) {
       __nv_bfloat162 t0 = __floats2bfloat162_rn(v[8 * c + 0], v[8 * c + 1]);
       __nv_bfloat162 t1 = __floats2bfloat162_rn(v[8 * c + 2], v[8 * c + 3]);
       __nv_bfloat162 t2 = __floats2bfloat162_rn(v[8 * c + 4], v[8 * c + 5]);
       __nv_bfloat162 t3 = __floats2bfloat162_rn(v[8 * c + 6], v[8 * c + 7]);
+      w = make_uint4(*reinterpret_cast<uint32_t*>(&t0), *reinterpret_cast<uint32_t*>(&t1),
+                     *reinterpret_cast<uint32_t*>(&t2), *reinterpret_cast<uint32_t*>(&t3));
+    } else if constexpr (kOut == 2) {
+      // half precision clamped to +-30000 (so that a sum of two stays finite)
+      const __half2 lim = __float2half2_rn(30000.f), nlim = __float2half2_rn(-30000.f);
+      __half2 t0 = __hmax2(__hmin2(__floats2half2_rn(v[8 * c + 0], v[8 * c + 1]), lim), nlim);
+      __half2 t1 = __hmax2(__hmin2(__floats2half2_rn(v[8 * c + 2], v[8 * c + 3]), lim), nlim);
+      __half2 t2 = __hmax2(__hmin2(__floats2half2_rn(v[8 * c + 4], v[8 * c + 5]), lim), nlim);
+      __half2 t3 = __hmax2(__hmin2(__floats2half2_rn(v[8 * c + 6], v[8 * c + 7]), lim), nlim);
       w = make_uint4(*reinterpret_cast<uint32_t*>(&t0), *reinterpret_cast<uint32_t*>(&t1),
                      *reinterpret_cast<uint32_t*>(&t2), *reinterpret_cast<uint32_t*>(&t3));
     } else {
@@ -70,30 +80,20 @@ __device__ __forceinline__ void stage_row(uint8_t* buf, int r, const float* v) {
     }
     *reinterpret_cast<uint4*>(buf + r * 128 + ((c ^ (r & 7)) << 4)) = w;
   }
-  (void)NV;
 }
 
+// Four consecutive entries of a weight-dtype vector as float.
 template <bool kBf16>
-__device__ __forceinline__ void store_act(void* out, size_t idx, const float* v, int n) {
+__device__ __forceinline__ float4 ldw4(const void* p, int i) {
   if constexpr (kBf16) {
-    __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out) + idx;
-    for (int i = 0; i < n; i += 8) {
-      uint4 w;
-      __nv_bfloat162 t0 = __floats2bfloat162_rn(v[i + 0], v[i + 1]);
-      __nv_bfloat162 t1 = __floats2bfloat162_rn(v[i + 2], v[i + 3]);
-      __nv_bfloat162 t2 = __floats2bfloat162_rn(v[i + 4], v[i + 5]);
-      __nv_bfloat162 t3 = __floats2bfloat162_rn(v[i + 6], v[i + 7]);
-      w.x = *reinterpret_cast<uint32_t*>(&t0);
-      w.y = *reinterpret_cast<uint32_t*>(&t1);
-      w.z = *reinterpret_cast<uint32_t*>(&t2);
-      w.w = *reinterpret_cast<uint32_t*>(&t3);
-      *reinterpret_cast<uint4*>(o + i) = w;
-    }
+    const uint2 w = *reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(p) + i);
+    return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u), __uint_as_float(w.y << 16),
+                       __uint_as_float(w.y & 0xFFFF0000u));
   } else {
-    float* o = static_cast<float*>(out) + idx;
-    for (int i = 0; i < n; i += 4) *reinterpret_cast<float4*>(o + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+    return *reinterpret_cast<const float4*>(static_cast<const float*>(p) + i);
   }
 }
+
 template <bool kBf16>
 __device__ __forceinline__ void store_act1(void* out, size_t idx, float v) {
   if constexpr (kBf16) {
@@ -288,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     // only the stores are predicated on the row being inside M.
     // While the main loop runs, stage this tile's per-slot bias rows in shared memory.
     const float* sbias = nullptr;
-    int first_slot = 0;
+    int first_slot = 0, prep_nslots = 0;
     if (grp.epi == EPI_SILU_BIAS) {
       first_slot = (m_tile * BM) / args.bias_div;
       const int last_slot = (min(args.M, m_tile * BM + BM) - 1) / args.bias_div;
@@ -301,6 +301,37 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
               args.bias + static_cast<size_t>(first_slot + sl) * args.ld_bias + nt * BN + c4 * 4);
         }
         sbias = dst;
+      }
+      named_barrier_sync(1, 128);
+    } else if (grp.epi == EPI_PREP) {
+      // Rows 0..nslots-1: (col_b + the slot's pair-bias row) / 2; row nslots: col_u / 2.
+      first_slot = (m_tile * BM) / args.bias_div;
+      const int last_slot = (min(args.M, m_tile * BM + BM) - 1) / args.bias_div;
+      const int nslots = last_slot - first_slot + 1;
+      if ((nslots + 1) * BN * 4 <= kBiasStageBytes) {
+        float* dst = reinterpret_cast<float*>(smem + bias_stage_offset);
+        for (int i = threadIdx.x - 64; i < (nslots + 1) * (BN / 4); i += 128) {
+          const int sl = i / (BN / 4), c4 = i % (BN / 4);
+          const int col = nt * BN + c4 * 4;
+          float4 v;
+          if (sl == nslots) {
+            v = ldw4<kBf16>(grp.col_u, col);
+          } else {
+            v = grp.col_b != nullptr ? ldw4<kBf16>(grp.col_b, col) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const int qs = first_slot + sl, stream_i = qs / args.slots;
+            if (grp.row_bias != nullptr && qs - stream_i * args.slots < args.slots - 1) {
+              const float4 rb = *reinterpret_cast<const float4*>(
+                  grp.row_bias + static_cast<size_t>(qs - stream_i) * args.ld_bias + col);
+              v.x += rb.x;
+              v.y += rb.y;
+              v.z += rb.z;
+              v.w += rb.w;
+            }
+          }
+          *reinterpret_cast<float4*>(dst + sl * BN + c4 * 4) = make_float4(0.5f * v.x, 0.5f * v.y, 0.5f * v.z, 0.5f * v.w);
+        }
+        sbias = dst;
+        prep_nslots = nslots;
       }
       named_barrier_sync(1, 128);
     }
@@ -351,6 +382,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         bias = sbias != nullptr ? sbias + (m / args.bias_div - first_slot) * BN
                                 : args.bias + static_cast<size_t>(m / args.bias_div) * args.ld_bias + nt * BN;
       }
+      // EPI_PREP: this row's scale and pair-bias row
+      float row_l = 0.f;
+      const float* rbias = nullptr;
+      if (grp.epi == EPI_PREP && live) {
+        row_l = args.row_l[m];
+        const int q_slot = m / args.bias_div;  // stream * slots + slot
+        const int stream_i = q_slot / args.slots, slot = q_slot - stream_i * args.slots;
+        if (grp.row_bias != nullptr && slot < args.slots - 1)
+          rbias = grp.row_bias + static_cast<size_t>(q_slot - stream_i) * args.ld_bias + nt * BN;
+      }
       // The fused op on 32 consecutive columns starting at `col` (compile-time trip counts).
       auto apply32 = [&](float(&x)[32], int col) {
         if (grp.epi == EPI_LN) {
@@ -364,6 +405,36 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             x[i + 1] = silu(x[i + 1] + bb.y);
             x[i + 2] = silu(x[i + 2] + bb.z);
             x[i + 3] = silu(x[i + 3] + bb.w);
+          }
+        } else if (grp.epi == EPI_PREP && sbias != nullptr) {
+          const float* add = sbias + (m / args.bias_div - first_slot) * BN + col;
+          const float* uu = sbias + prep_nslots * BN + col;
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            const float4 a4 = live ? *reinterpret_cast<const float4*>(add + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 u4 = *reinterpret_cast<const float4*>(uu + i);
+            x[i] = fmaf(0.5f, x[i], fmaf(u4.x, row_l, a4.x));
+            x[i + 1] = fmaf(0.5f, x[i + 1], fmaf(u4.y, row_l, a4.y));
+            x[i + 2] = fmaf(0.5f, x[i + 2], fmaf(u4.z, row_l, a4.z));
+            x[i + 3] = fmaf(0.5f, x[i + 3], fmaf(u4.w, row_l, a4.w));
+          }
+        } else if (grp.epi == EPI_PREP) {
+          const int c0 = nt * BN + col;
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            const float4 uu = ldw4<kBf16>(grp.col_u, c0 + i);
+            float4 add = grp.col_b != nullptr ? ldw4<kBf16>(grp.col_b, c0 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            if (rbias != nullptr) {
+              const float4 rb = *reinterpret_cast<const float4*>(rbias + col + i);
+              add.x += rb.x;
+              add.y += rb.y;
+              add.z += rb.z;
+              add.w += rb.w;
+            }
+            x[i] = 0.5f * (x[i] + add.x + uu.x * row_l);
+            x[i + 1] = 0.5f * (x[i + 1] + add.y + uu.y * row_l);
+            x[i + 2] = 0.5f * (x[i + 2] + add.z + uu.z * row_l);
+            x[i + 3] = 0.5f * (x[i + 3] + add.w + uu.w * row_l);
           }
         }
       };
@@ -382,10 +453,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           if (lane == 0) bulk_wait_read<1>();  // the store that used this half has read it
           __syncwarp();
         }
-        if (out_bf16)
-          stage_row<true>(buf, lane, v);
+        if (grp.epi == EPI_PREP && kBf16)
+          stage_row<2>(buf, lane, v);
+        else if (out_bf16)
+          stage_row<1>(buf, lane, v);
         else
-          stage_row<false>(buf, lane, v);
+          stage_row<0>(buf, lane, v);
         fence_proxy_async();
         __syncwarp();
         if (lane == 0 && any_rows) {
@@ -492,11 +565,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 
 template <bool kBf16, int BN, bool kSplit>
 cudaError_t launch_gemm_t(const GemmArgs& args, int split_k, cudaStream_t stream) {
+  // The split-K reduction has no scorer-operand epilogue.
+  if (kSplit && (args.g[0].epi == EPI_PREP || (args.n_groups > 1 && args.g[1].epi == EPI_PREP)))
+    return cudaErrorInvalidValue;
   constexpr int STAGE_BYTES = BM * 128 + BN * 128;
   int stages = std::min(kMaxStages, kSmemBudget / STAGE_BYTES);
   // split-K reuses the pipeline buffers: partial tile (BM x LDS) plus this CTA's reduced rows
   const int split_bytes = kSplit ? (BM + BM / 2) * (BN + 4) * 4 : 0;
-  const bool has_bias = args.g[0].epi == EPI_SILU_BIAS || (args.n_groups > 1 && args.g[1].epi == EPI_SILU_BIAS);
+  auto staged = [](int epi) { return epi == EPI_SILU_BIAS || epi == EPI_PREP; };
+  const bool has_bias = staged(args.g[0].epi) || (args.n_groups > 1 && staged(args.g[1].epi));
   if (has_bias) stages = std::min(stages, 4);
   const int bias_off = std::max(stages * STAGE_BYTES, split_bytes);
   const int smem = bias_off + (has_bias ? kBiasStageBytes : 0) + 1024;

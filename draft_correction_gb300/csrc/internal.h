@@ -21,6 +21,12 @@ enum Epilogue : int {
   EPI_ACT = 1,        // out (activation dtype) = acc
   EPI_LN = 2,         // out (activation dtype) = LayerNorm_noaffine(acc row)   (group covers the full row)
   EPI_SILU_BIAS = 3,  // out (activation dtype) = SiLU(acc + bias[m / bias_div, n])  (bias f32)
+  // Scorer operand (no split-K): out = (acc + col_b[n] + col_u[n] * row_l[m] + row_bias[pair(m), n]) / 2,
+  // written in half precision (clamped to +-30000) for bf16 inputs, f32 otherwise.  Row m is
+  // candidate (stream, slot, k) with m / bias_div = stream * slots + slot; the pair row is
+  // stream * (slots - 1) + slot and the last slot of a stream takes no row bias.  col_b and
+  // row_bias may be null.
+  EPI_PREP = 4,
 };
 
 struct GemmGroup {
@@ -30,6 +36,9 @@ struct GemmGroup {
   int ldo;
   int epi;
   int n_tiles;        // Ng / BN
+  const void* col_u;      // EPI_PREP: [Ng] weight dtype
+  const void* col_b;      // EPI_PREP: [Ng] weight dtype, or null
+  const float* row_bias;  // EPI_PREP: [pairs, Ng] f32 (pitch ld_bias), or null
 };
 
 struct GemmArgs {
@@ -43,6 +52,8 @@ struct GemmArgs {
   GemmGroup g[2];
   const float* bias;        // EPI_SILU_BIAS
   int bias_div, ld_bias;
+  const float* row_l;       // EPI_PREP: [M] per-row scale
+  int slots;                // EPI_PREP: slots per stream
   float ln_eps;
   unsigned int* status;
 };
@@ -74,6 +85,10 @@ struct ScoreArgs {
   int N, B, K, H;
 };
 cudaError_t launch_scores(const ScoreArgs& a, bool is_bf16, cudaStream_t stream);
+// Scores from operands already prepared by the EPI_PREP epilogue: uz holds the P rows
+// (uz + b1 + W s + u_a l)/2 and vz the Q rows (vz + u_b l)/2, in half precision for bf16
+// weights and f32 otherwise; wsp, u_a, u_b and b1 are not read.
+cudaError_t launch_scores_prepped(const ScoreArgs& a, bool is_bf16, cudaStream_t stream);
 
 // ------------------------------------------------------------------ walk + verify
 struct SelectVerifyArgs {

@@ -20,6 +20,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <algorithm>
 #include <type_traits>
 
 #include "internal.h"
@@ -47,25 +48,6 @@ __device__ __forceinline__ float ldv(const void* p, size_t i) {
     return __bfloat162float(static_cast<const __nv_bfloat16*>(p)[i]);
   } else {
     return static_cast<const float*>(p)[i];
-  }
-}
-
-// Eight consecutive activations (16 bytes of bf16 or 32 bytes of f32) widened to float.
-template <bool kBf16>
-__device__ __forceinline__ void ld8(const void* p, size_t i, float (&x)[8]) {
-  if constexpr (kBf16) {
-    const uint4 w = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p) + i);
-    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      x[2 * j] = __uint_as_float(u[j] << 16);
-      x[2 * j + 1] = __uint_as_float(u[j] & 0xFFFF0000u);
-    }
-  } else {
-    const float4 a = *reinterpret_cast<const float4*>(static_cast<const float*>(p) + i);
-    const float4 b = *reinterpret_cast<const float4*>(static_cast<const float*>(p) + i + 4);
-    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
   }
 }
 
@@ -110,23 +92,112 @@ __device__ __forceinline__ float tanh_fast(float x) {
   return y;
 }
 
-// tanh of four floats with two packed half-precision SFU instructions.  Inputs beyond the half
-// range round to +-inf, whose tanh is the exact limit +-1, so no input is out of range.
-__device__ __forceinline__ void tanh4_f16(float a, float b, float c, float d, float& ta, float& tb, float& tc,
-                                          float& td) {
-  uint32_t p0, p1, r0, r1;
-  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(p0) : "f"(b), "f"(a));
-  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(p1) : "f"(d), "f"(c));
-  asm("tanh.approx.f16x2 %0, %1;" : "=r"(r0) : "r"(p0));
-  asm("tanh.approx.f16x2 %0, %1;" : "=r"(r1) : "r"(p1));
-  const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&r0));
-  const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&r1));
-  ta = f0.x;
-  tb = f0.y;
-  tc = f1.x;
-  td = f1.y;
+// Thread tiles: OT = (kAB/kTA) x (Kp/kTB); HS threads share a tile and split the hidden units.
+// Tile (ta, tb) holds predecessor rows ta*kTA + i and successor rows tb + j*tiles_b (strided, so
+// that neighbouring threads read rows in different shared-memory banks).
+struct Tile {
+  int tiles_b, OT, HS, hs, ta, tb;
+  bool active;
+};
+template <int NT>
+__device__ __forceinline__ Tile make_tile(int Kp) {
+  Tile t;
+  t.tiles_b = Kp / kTB;
+  t.OT = (kAB / kTA) * t.tiles_b;
+  t.HS = NT / t.OT;  // OT <= 64 (K <= 64), so HS >= NT / 64
+  const int ot = threadIdx.x % t.OT;
+  t.hs = threadIdx.x / t.OT;
+  t.active = t.hs < t.HS;
+  t.ta = ot / t.tiles_b;
+  t.tb = ot % t.tiles_b;
+  return t;
 }
 
+// Adds hc hidden units of w . (y + y tanh y), y = P[a] + Q[b], to the thread's kTA x kTB outputs.
+// bf16 path: P, Q and w in half precision (rows of ld halves), 8 units per step, two per
+// instruction, with an f16 pair of partial sums per step added to the fp32 total.  f32 path:
+// fp32 throughout (rows of ld floats).
+template <bool kBf16>
+__device__ __forceinline__ void accumulate(float (&acc)[kTA][kTB], const void* P, const void* Q, int ld, const void* w,
+                                           int hc, const Tile& t) {
+  if (!t.active) return;
+  if constexpr (kBf16) {
+    const uint4* p8 = reinterpret_cast<const uint4*>(static_cast<const __half*>(P) + t.ta * kTA * ld);
+    const uint4* q8 = reinterpret_cast<const uint4*>(static_cast<const __half*>(Q) + t.tb * ld);
+    const uint4* w8 = static_cast<const uint4*>(w);
+    const int ld8 = ld / 8, qs = t.tiles_b * ld8;
+    for (int c = t.hs; c < hc / 8; c += t.HS) {
+      const uint4 wv = w8[c];
+      uint4 pv[kTA], qv[kTB];
+#pragma unroll
+      for (int i = 0; i < kTA; ++i) pv[i] = p8[i * ld8 + c];
+#pragma unroll
+      for (int j = 0; j < kTB; ++j) qv[j] = q8[j * qs + c];
+#pragma unroll
+      for (int i = 0; i < kTA; ++i) {
+#pragma unroll
+        for (int j = 0; j < kTB; ++j) {
+          const float2 f = __half22float2(silu_dot8(pv[i], qv[j], wv));
+          acc[i][j] += f.x + f.y;
+        }
+      }
+    }
+  } else {
+    const float4* p4 = reinterpret_cast<const float4*>(static_cast<const float*>(P) + t.ta * kTA * ld);
+    const float4* q4 = reinterpret_cast<const float4*>(static_cast<const float*>(Q) + t.tb * ld);
+    const float4* w4 = static_cast<const float4*>(w);
+    const int ld4 = ld / 4, qs = t.tiles_b * ld4;
+    for (int c = t.hs; c < hc / 4; c += t.HS) {
+      const float4 wv = w4[c];
+      float4 pv[kTA], qv[kTB];
+#pragma unroll
+      for (int i = 0; i < kTA; ++i) pv[i] = p4[i * ld4 + c];
+#pragma unroll
+      for (int j = 0; j < kTB; ++j) qv[j] = q4[j * qs + c];
+#pragma unroll
+      for (int i = 0; i < kTA; ++i) {
+#pragma unroll
+        for (int j = 0; j < kTB; ++j) {
+          const float y0 = pv[i].x + qv[j].x, y1 = pv[i].y + qv[j].y;
+          const float y2 = pv[i].z + qv[j].z, y3 = pv[i].w + qv[j].w;
+          float s = acc[i][j];
+          s = fmaf(wv.x, fmaf(y0, tanh_fast(y0), y0), s);
+          s = fmaf(wv.y, fmaf(y1, tanh_fast(y1), y1), s);
+          s = fmaf(wv.z, fmaf(y2, tanh_fast(y2), y2), s);
+          s = fmaf(wv.w, fmaf(y3, tanh_fast(y3), y3), s);
+          acc[i][j] = s;
+        }
+      }
+    }
+  }
+}
+
+// Adds the HS partial sums of every output in a fixed order and writes
+// S[n,p,a0+ar,bc] = l_{p+1}(bc) + sum + b2 for the block's na predecessor rows.
+template <int NT>
+__device__ __forceinline__ void finish(const float (&acc)[kTA][kTB], float* red, const Tile& t, float* Sp,
+                                       const float* vals_q, float b2, int na, int K) {
+#pragma unroll
+  for (int i = 0; i < kTA; ++i)
+#pragma unroll
+    for (int j = 0; j < kTB; ++j) red[threadIdx.x * (kTA * kTB) + i * kTB + j] = t.active ? acc[i][j] : 0.f;
+  __syncthreads();
+  for (int o = threadIdx.x; o < na * K; o += NT) {
+    const int ar = o / K, bc = o % K;
+    const int ti = (ar / kTA) * t.tiles_b + bc % t.tiles_b;
+    const int idx = (ar % kTA) * kTB + bc / t.tiles_b;
+    float s = 0.f;
+    for (int h = 0; h < t.HS; ++h) s += red[(h * t.OT + ti) * (kTA * kTB) + idx];
+    Sp[o] = vals_q[bc] + s + b2;
+  }
+}
+
+// ------------------------------------------------------------------ from uz, vz and W s
+// One thread block handles one transition (n, p) and kAB predecessor rows.  Per chunk of HC
+// hidden units it stages, in shared memory,
+//   P[a][h] = (uz[n,p,a,h] + ws[n,p,h] + u_a[h] l_p(a) + b1[h]) / 2
+//   Q[b][h] = (vz[n,p+1,b,h] + u_b[h] l_{p+1}(b)) / 2
+// (the raw rows of the next chunk arrive by cp.async while the current chunk computes).
 template <bool kBf16>
 __global__ void __launch_bounds__(kThreads) score_kernel(const ScoreArgs a) {
   using Act = typename std::conditional<kBf16, __nv_bfloat16, float>::type;
@@ -139,8 +210,7 @@ __global__ void __launch_bounds__(kThreads) score_kernel(const ScoreArgs a) {
   const int Kp = (K + kTB - 1) / kTB * kTB;  // successor rows padded to the thread tile
   const int hc = score_chunk(H);  // 64 or 128
   const int hc_shift = hc == 128 ? 7 : 6;
-  const int ld = hc + kPad;   // row pitch of P and Q in floats (f32 path)
-  const int ldh = hc + 8;     // row pitch in halves (bf16 path): rows start on 16-byte boundaries
+  const int ld = kBf16 ? hc + 8 : hc + kPad;  // P/Q row pitch (halves or floats): 16-byte aligned rows
   const int rows = kAB + Kp;
   float* w2v = sm;            // [H]  output weights
   float* uav = w2v + H;       // [H]  u_a
@@ -148,19 +218,10 @@ __global__ void __launch_bounds__(kThreads) score_kernel(const ScoreArgs a) {
   float* bwv = ubv + H;       // [H]  b1 + W s_p
   __half* w2h = reinterpret_cast<__half*>(bwv + H);  // [H] output weights in half precision
   float* P = bwv + H + H / 2;  // [kAB][ld]   current chunk (halves on the bf16 path)
-  float* Q = P + kAB * ld;    // [Kp][ld]
-  float* red = Q + Kp * ld;   // [kThreads][kTA * kTB] partial sums
+  float* Q = P + kAB * (hc + kPad);  // [Kp][ld]
+  float* red = Q + Kp * (hc + kPad);  // [kThreads][kTA * kTB] partial sums
   Act* raw = reinterpret_cast<Act*>(red + kThreads * kTA * kTB);  // [rows][hc] next chunk, as stored
-
-  // Thread tiles: OT = (kAB/kTA) x (Kp/kTB); HS threads share a tile and split the hidden units.
-  // Tile (ta, tb) holds predecessor rows ta*kTA + i and successor rows tb + j*tiles_b (strided, so
-  // that neighbouring threads read rows in different shared-memory banks).
-  const int tiles_b = Kp / kTB;
-  const int OT = (kAB / kTA) * tiles_b;
-  const int HS = kThreads / OT;  // OT <= 64 (K <= 64), so HS >= 4
-  const int ot = threadIdx.x % OT, hs = threadIdx.x / OT;
-  const bool active = hs < HS;
-  const int ta = ot / tiles_b, tb = ot % tiles_b;
+  const Tile t = make_tile<kThreads>(Kp);
 
   const size_t row_p = (static_cast<size_t>(n) * B + p) * K;      // candidate rows of slot p
   const size_t row_q = (static_cast<size_t>(n) * B + p + 1) * K;  // candidate rows of slot p+1
@@ -202,129 +263,133 @@ __global__ void __launch_bounds__(kThreads) score_kernel(const ScoreArgs a) {
   for (int h0 = 0; h0 < H; h0 += hc) {
     cp_async_wait(0);
     __syncthreads();  // this chunk's raw rows and the vectors are visible; P/Q are free
-    // P[a][h] = (uz + b1 + W s + u_a l_p(a)) / 2 and Q[b][h] = (vz + u_b l_{p+1}(b)) / 2; rows
-    // past na (P) or K (Q) are zero.
+    // Rows past na (P) or K (Q) are zero.
     for (int i = threadIdx.x; i < (rows << hc_shift) / 8; i += kThreads) {
       const int r = (i * 8) >> hc_shift, c = (i * 8) & (hc - 1), h = h0 + c;
       float x[8];
-      float* dst;
-      if (r < kAB) {
-        dst = kBf16 ? reinterpret_cast<float*>(reinterpret_cast<__half*>(P) + r * ldh + c) : P + r * ld + c;
-        if (r < na) {
-          ld8_smem<kBf16>(raw + r * hc + c, x);
+      const bool is_p = r < kAB;
+      const int rr = is_p ? r : r - kAB;
+      if (is_p ? r < na : rr < K) {
+        ld8_smem<kBf16>(raw + r * hc + c, x);
+        if (is_p) {
           const float l = vals_p[a0 + r];
 #pragma unroll
           for (int e = 0; e < 8; ++e) x[e] = 0.5f * (x[e] + bwv[h + e] + uav[h + e] * l);
         } else {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) x[e] = 0.f;
-        }
-      } else {
-        const int rb = r - kAB;
-        dst = kBf16 ? reinterpret_cast<float*>(reinterpret_cast<__half*>(Q) + rb * ldh + c) : Q + rb * ld + c;
-        if (rb < K) {
-          ld8_smem<kBf16>(raw + r * hc + c, x);
-          const float l = vals_q[rb];
+          const float l = vals_q[rr];
 #pragma unroll
           for (int e = 0; e < 8; ++e) x[e] = 0.5f * (x[e] + ubv[h + e] * l);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) x[e] = 0.f;
         }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = 0.f;
       }
       if constexpr (kBf16) {
         // half precision, clamped to +-30000 so that a sum of two never overflows
-        __half2* d16 = reinterpret_cast<__half2*>(dst);  // rows of ld halves
-        uint4 w;
-        __half2 hh[4];
+        __half* dst = reinterpret_cast<__half*>(is_p ? P : Q) + rr * ld + c;
+        uint32_t hw[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          hh[e] = __floats2half2_rn(fminf(fmaxf(x[2 * e], -30000.f), 30000.f),
-                                    fminf(fmaxf(x[2 * e + 1], -30000.f), 30000.f));
-        w.x = *reinterpret_cast<uint32_t*>(&hh[0]);
-        w.y = *reinterpret_cast<uint32_t*>(&hh[1]);
-        w.z = *reinterpret_cast<uint32_t*>(&hh[2]);
-        w.w = *reinterpret_cast<uint32_t*>(&hh[3]);
-        *reinterpret_cast<uint4*>(d16) = w;
+        for (int e = 0; e < 4; ++e) {
+          const __half2 hh = __floats2half2_rn(fminf(fmaxf(x[2 * e], -30000.f), 30000.f),
+                                               fminf(fmaxf(x[2 * e + 1], -30000.f), 30000.f));
+          hw[e] = *reinterpret_cast<const uint32_t*>(&hh);
+        }
+        *reinterpret_cast<uint4*>(dst) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
       } else {
+        float* dst = (is_p ? P : Q) + rr * ld + c;
         *reinterpret_cast<float4*>(dst) = make_float4(x[0], x[1], x[2], x[3]);
         *reinterpret_cast<float4*>(dst + 4) = make_float4(x[4], x[5], x[6], x[7]);
       }
     }
     __syncthreads();  // P/Q ready; the raw buffer is free for the next chunk
     if (h0 + hc < H) fetch(h0 + hc);
-    if (active) {
-      if constexpr (kBf16) {
-        // Packed half precision: 8 hidden units per step, two per instruction.  Each output keeps
-        // an f16 pair of partial sums for the step and adds it to its fp32 total.
-        const uint4* p8 = reinterpret_cast<const uint4*>(reinterpret_cast<const __half*>(P) + ta * kTA * ldh);
-        const uint4* q8 = reinterpret_cast<const uint4*>(reinterpret_cast<const __half*>(Q) + tb * ldh);
-        const uint4* w8 = reinterpret_cast<const uint4*>(w2h + h0);
-        const int ld8 = ldh / 8;
-        for (int c = hs; c < hc / 8; c += HS) {
-          const uint4 w = w8[c];
-          uint4 pv[kTA], qv[kTB];
-#pragma unroll
-          for (int i = 0; i < kTA; ++i) pv[i] = p8[i * ld8 + c];
-#pragma unroll
-          for (int j = 0; j < kTB; ++j) qv[j] = q8[j * tiles_b * ld8 + c];
-#pragma unroll
-          for (int i = 0; i < kTA; ++i) {
-#pragma unroll
-            for (int j = 0; j < kTB; ++j) {
-              __half2 sacc = silu_dot8(pv[i], qv[j], w);
-              const float2 f = __half22float2(sacc);
-              acc[i][j] += f.x + f.y;
-            }
-          }
-        }
-      } else {
-        const float4* w4 = reinterpret_cast<const float4*>(w2v + h0);
-        const float4* p4 = reinterpret_cast<const float4*>(P + ta * kTA * ld);
-        const float4* q4 = reinterpret_cast<const float4*>(Q + tb * ld);
-        const int ld4 = ld / 4;
-        for (int c = hs; c < hc / 4; c += HS) {
-          const float4 w = w4[c];
-          float4 pv[kTA], qv[kTB];
-#pragma unroll
-          for (int i = 0; i < kTA; ++i) pv[i] = p4[i * ld4 + c];
-#pragma unroll
-          for (int j = 0; j < kTB; ++j) qv[j] = q4[j * tiles_b * ld4 + c];
-#pragma unroll
-          for (int i = 0; i < kTA; ++i) {
-#pragma unroll
-            for (int j = 0; j < kTB; ++j) {
-              const float y0 = pv[i].x + qv[j].x, y1 = pv[i].y + qv[j].y;
-              const float y2 = pv[i].z + qv[j].z, y3 = pv[i].w + qv[j].w;
-              float s = acc[i][j];
-              s = fmaf(w.x, fmaf(y0, tanh_fast(y0), y0), s);
-              s = fmaf(w.y, fmaf(y1, tanh_fast(y1), y1), s);
-              s = fmaf(w.z, fmaf(y2, tanh_fast(y2), y2), s);
-              s = fmaf(w.w, fmaf(y3, tanh_fast(y3), y3), s);
-              acc[i][j] = s;
-            }
-          }
-        }
-      }
+    accumulate<kBf16>(acc, P, Q, ld, kBf16 ? static_cast<const void*>(w2h + h0) : static_cast<const void*>(w2v + h0),
+                      hc, t);
+  }
+  finish<kThreads>(acc, red, t, a.S + (static_cast<size_t>(np) * K + a0) * K, vals_q, ldv<kBf16>(a.b2, 0), na, K);
+}
+
+// ------------------------------------------------------------------ from prepared operands
+// P and Q rows come ready-made from the epilogue of the U z / V z projection (f16 for bf16
+// weights, f32 otherwise; P rows are indexed like uz, Q rows like vz), so a block only copies
+// them into shared memory: all H hidden units at once when they fit in kPrepBudget bytes, else
+// chunks of 64 or 128.  Blocks of 128 threads keep ~7 blocks resident per SM, so the whole grid
+// of a typical batch runs in one wave; the partial sums reuse the operand buffers at the end.
+constexpr int kPrepThreads = 128;
+constexpr int kPrepBudget = 96 * 1024;
+
+template <bool kBf16>
+__host__ __device__ __forceinline__ int prep_chunk(int H, int K) {
+  const int esz = kBf16 ? 2 : 4;
+  const int Kp = (K + kTB - 1) / kTB * kTB;
+  return (kAB + Kp) * (H * esz + 16) <= kPrepBudget ? H : score_chunk(H);
+}
+
+template <bool kBf16>
+__global__ void __launch_bounds__(kPrepThreads, 8) score_prepped_kernel(const ScoreArgs a) {
+  using Op = typename std::conditional<kBf16, __half, float>::type;
+  constexpr int esz = sizeof(Op);
+  extern __shared__ __align__(16) float sm[];
+  const int K = a.K, H = a.H, B = a.B;
+  const int np = blockIdx.x;  // n * (B-1) + p
+  const int n = np / (B - 1), p = np % (B - 1);
+  const int a0 = blockIdx.y * kAB;
+  const int na = min(kAB, K - a0);
+  const int Kp = (K + kTB - 1) / kTB * kTB;
+  const int hc = prep_chunk<kBf16>(H, K);
+  const int ld = hc + 16 / esz;  // row pitch (elements): rows start on 16-byte boundaries
+  const int rows = kAB + Kp;
+  Op* wv = reinterpret_cast<Op*>(sm);  // [H] output weights
+  Op* P = wv + H;                      // [kAB][ld]
+  Op* Q = P + kAB * ld;                // [Kp][ld]
+  // partial sums [kPrepThreads][kTA * kTB], over P/Q once every thread is done with them
+  float* red = reinterpret_cast<float*>(P);
+  const Tile t = make_tile<kPrepThreads>(Kp);
+
+  const size_t row_p = (static_cast<size_t>(n) * B + p) * K + a0;  // first predecessor row
+  const size_t row_q = (static_cast<size_t>(n) * B + p + 1) * K;   // first successor row
+  const int ppr = hc * esz / 16;  // 16-byte pieces per row and chunk
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  // Rows past na (P) or K (Q) are zero-filled.
+  auto fetch = [&](int h0) {
+    for (int r = warp; r < rows; r += kPrepThreads / 32) {
+      const bool is_p = r < kAB;
+      const int rr = is_p ? r : r - kAB;
+      const bool live = is_p ? rr < na : rr < K;
+      const Op* src = static_cast<const Op*>(is_p ? a.uz : a.vz) +
+                      (live ? (is_p ? row_p : row_q) + rr : 0) * static_cast<size_t>(H) + h0;
+      const uint32_t dst = smem_u32((is_p ? P : Q) + rr * ld);
+      for (int c = lane; c < ppr; c += 32)
+        cp_async16(dst + c * 16, reinterpret_cast<const char*>(src) + c * 16, live ? 16u : 0u);
     }
+    cp_async_commit();
+  };
+  fetch(0);
+  for (int i = threadIdx.x; i < H; i += kPrepThreads) {
+    if constexpr (kBf16)
+      wv[i] = __float2half_rn(ldv<true>(a.w2, i));
+    else
+      wv[i] = ldv<false>(a.w2, i);
   }
 
-  // Add the HS partial sums of every output in a fixed order.
+  float acc[kTA][kTB];
 #pragma unroll
   for (int i = 0; i < kTA; ++i)
 #pragma unroll
-    for (int j = 0; j < kTB; ++j) red[threadIdx.x * (kTA * kTB) + i * kTB + j] = active ? acc[i][j] : 0.f;
-  __syncthreads();
-  const float b2 = ldv<kBf16>(a.b2, 0);
-  float* Sp = a.S + (static_cast<size_t>(np) * K + a0) * K;  // rows a0.. of this transition
-  for (int o = threadIdx.x; o < na * K; o += kThreads) {
-    const int ar = o / K, bc = o % K;
-    const int t = (ar / kTA) * tiles_b + bc % tiles_b;
-    const int idx = (ar % kTA) * kTB + bc / tiles_b;
-    float s = 0.f;
-    for (int h = 0; h < HS; ++h) s += red[(h * OT + t) * (kTA * kTB) + idx];
-    Sp[o] = vals_q[bc] + s + b2;
+    for (int j = 0; j < kTB; ++j) acc[i][j] = 0.f;
+
+  for (int h0 = 0; h0 < H; h0 += hc) {
+    if (h0 > 0) {
+      __syncthreads();  // every thread is done with the previous chunk
+      fetch(h0);
+    }
+    cp_async_wait(0);
+    __syncthreads();
+    accumulate<kBf16>(acc, P, Q, ld, wv + h0, hc, t);
   }
+  __syncthreads();  // P/Q are free for the partial sums
+  finish<kPrepThreads>(acc, red, t, a.S + (static_cast<size_t>(np) * K + a0) * K, a.vals + row_q,
+                       ldv<kBf16>(a.b2, 0), na, K);
 }
 
 }  // namespace
@@ -333,32 +398,67 @@ size_t score_smem_bytes(int H, int K, bool is_bf16) {
   const int hc = score_chunk(H);
   const int ld = hc + kPad;
   const int Kp = (K + kTB - 1) / kTB * kTB;
-  // vectors, P and Q, partial sums, and one chunk of raw rows
+  // vectors (four f32, one f16), P and Q, partial sums, and one chunk of raw rows
   return (4 * static_cast<size_t>(H) + H / 2 + static_cast<size_t>(kAB + Kp) * ld + kThreads * kTA * kTB) * sizeof(float) +
          static_cast<size_t>(kAB + Kp) * hc * (is_bf16 ? 2 : 4);
 }
 
-cudaError_t launch_scores(const ScoreArgs& a, bool is_bf16, cudaStream_t stream) {
-  const size_t smem = score_smem_bytes(a.H, a.K, is_bf16);
-  dim3 grid(a.N * (a.B - 1), (a.K + kAB - 1) / kAB);
-  // The dynamic shared memory ceiling is raised once per device to the largest this kernel
-  // can need (K = 64), so later calls enqueue only the launch (CUDA-graph friendly).
+size_t score_prepped_smem_bytes(int H, int K, bool is_bf16) {
+  const size_t esz = is_bf16 ? 2 : 4;
+  const int hc = is_bf16 ? prep_chunk<true>(H, K) : prep_chunk<false>(H, K);
+  const int Kp = (K + kTB - 1) / kTB * kTB;
+  // the partial sums reuse the P/Q buffers; the chunk of a small H may leave them shorter
+  return static_cast<size_t>(H) * esz +
+         std::max(static_cast<size_t>(kAB + Kp) * (hc * esz + 16),
+                  static_cast<size_t>(kPrepThreads) * kTA * kTB * sizeof(float));
+}
+
+namespace {
+// The dynamic shared memory ceiling of both kernels is raised once per device to the most they
+// can need, so later calls enqueue only the launch (CUDA-graph friendly).
+cudaError_t configure_once() {
   static bool configured[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!configured[dev]) {
-    const int most = 227 * 1024;
-    e = cudaFuncSetAttribute(score_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(score_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+  if (configured[dev]) return cudaSuccess;
+  const int most = 227 * 1024;
+  const void* fns[] = {reinterpret_cast<const void*>(score_kernel<true>), reinterpret_cast<const void*>(score_kernel<false>),
+                       reinterpret_cast<const void*>(score_prepped_kernel<true>),
+                       reinterpret_cast<const void*>(score_prepped_kernel<false>)};
+  for (const void* f : fns) {
+    e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
     if (e != cudaSuccess) return e;
-    configured[dev] = true;
   }
+  configured[dev] = true;
+  return cudaSuccess;
+}
+}  // namespace
+
+cudaError_t launch_scores(const ScoreArgs& a, bool is_bf16, cudaStream_t stream) {
+  const size_t smem = score_smem_bytes(a.H, a.K, is_bf16);
+  if (smem > 227 * 1024) return cudaErrorInvalidValue;
+  const dim3 grid(a.N * (a.B - 1), (a.K + kAB - 1) / kAB);
+  cudaError_t e = configure_once();
+  if (e != cudaSuccess) return e;
   if (is_bf16)
     score_kernel<true><<<grid, kThreads, smem, stream>>>(a);
   else
     score_kernel<false><<<grid, kThreads, smem, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scores_prepped(const ScoreArgs& a, bool is_bf16, cudaStream_t stream) {
+  const size_t smem = score_prepped_smem_bytes(a.H, a.K, is_bf16);
+  if (smem > 227 * 1024) return cudaErrorInvalidValue;
+  const dim3 grid(a.N * (a.B - 1), (a.K + kAB - 1) / kAB);
+  cudaError_t e = configure_once();
+  if (e != cudaSuccess) return e;
+  if (is_bf16)
+    score_prepped_kernel<true><<<grid, kPrepThreads, smem, stream>>>(a);
+  else
+    score_prepped_kernel<false><<<grid, kPrepThreads, smem, stream>>>(a);
   return cudaGetLastError();
 }
 

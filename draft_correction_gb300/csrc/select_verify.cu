@@ -45,6 +45,8 @@ __device__ __forceinline__ int warp_argmax(const float* row, int K, int lane) {
 __global__ void __launch_bounds__(kThreads) select_verify_kernel(const SelectVerifyArgs a) {
   __shared__ uint32_t s_S[kStageFloats];  // order codes of the stream's scores
   __shared__ int32_t s_draft[kMaxB];
+  __shared__ int32_t s_k[kMaxB];       // walk: chosen candidate per slot
+  __shared__ int32_t s_t[kMaxB + 1];   // greedy verification: the verifier's tokens
   __shared__ int s_A;
   __shared__ double s_part[kThreads];
   __shared__ double s_pre[kThreads];
@@ -65,12 +67,10 @@ __global__ void __launch_bounds__(kThreads) select_verify_kernel(const SelectVer
     }
     __syncthreads();
     if (warp == 0) {
-      const int32_t* idn = a.ids + static_cast<size_t>(n) * B * K;
+      // The chain of argmaxes touches only shared memory (and registers); the token ids of
+      // the chosen candidates are looked up together afterwards.
       int k = warp_argmax(a.vals + static_cast<size_t>(n) * B * K, K, lane);
-      if (lane == 0) {
-        a.k_sel[static_cast<size_t>(n) * B] = k;
-        s_draft[0] = idn[k];
-      }
+      if (lane == 0) s_k[0] = k;
       for (int p = 0; p + 1 < B; ++p) {
         const size_t row = (static_cast<size_t>(p) * K + k) * K;
         if (staged) {
@@ -80,16 +80,25 @@ __global__ void __launch_bounds__(kThreads) select_verify_kernel(const SelectVer
         } else {
           k = warp_argmax(Sn + row, K, lane);
         }
-        if (lane == 0) {
-          a.k_sel[static_cast<size_t>(n) * B + p + 1] = k;
-          s_draft[p + 1] = idn[static_cast<size_t>(p + 1) * K + k];
-        }
+        if (lane == 0) s_k[p + 1] = k;
       }
       __syncwarp();
-      for (int j = lane; j < B; j += 32) a.tokens[static_cast<size_t>(n) * B + j] = s_draft[j];
+      const int32_t* idn = a.ids + static_cast<size_t>(n) * B * K;
+      for (int j = lane; j < B; j += 32) {
+        const int kj = s_k[j];
+        const int32_t tok = idn[static_cast<size_t>(j) * K + kj];
+        s_draft[j] = tok;
+        a.k_sel[static_cast<size_t>(n) * B + j] = kj;
+        a.tokens[static_cast<size_t>(n) * B + j] = tok;
+      }
+    } else if (warp == 1 && a.mode == 0) {
+      // the verifier's greedy tokens, fetched while the walk runs
+      for (int j = lane; j <= B; j += 32) s_t[j] = a.t[static_cast<size_t>(n) * (B + 1) + j];
     }
   } else if (a.mode >= 0) {
     for (int j = threadIdx.x; j < B; j += kThreads) s_draft[j] = a.draft[static_cast<size_t>(n) * B + j];
+    if (a.mode == 0)
+      for (int j = threadIdx.x; j <= B; j += kThreads) s_t[j] = a.t[static_cast<size_t>(n) * (B + 1) + j];
   }
   __syncthreads();
   if (a.mode < 0) return;
@@ -103,7 +112,7 @@ __global__ void __launch_bounds__(kThreads) select_verify_kernel(const SelectVer
       if (j < B) {
         const int32_t y = s_draft[j];
         if (a.mode == 0) {
-          ok = (y == a.t[static_cast<size_t>(n) * (B + 1) + j]);
+          ok = (y == s_t[j]);
         } else {
           const float uq = a.u[(static_cast<size_t>(n) * (B + 1) + j) * 2];
           const float qy = (y >= 0 && y < V) ? a.q[(static_cast<size_t>(n) * (B + 1) + j) * V + y] : 0.f;
@@ -124,7 +133,7 @@ __global__ void __launch_bounds__(kThreads) select_verify_kernel(const SelectVer
 
   if (a.mode == 0) {
     for (int j = threadIdx.x; j <= B; j += kThreads)
-      com[j] = j < A ? s_draft[j] : (j == A ? a.t[static_cast<size_t>(n) * (B + 1) + A] : -1);
+      com[j] = j < A ? s_draft[j] : (j == A ? s_t[A] : -1);
     if (threadIdx.x == 0) {
       a.accept_len[n] = A;
       a.n_commit[n] = A + 1;
