@@ -65,6 +65,54 @@ def _topk_ties_high(logits, K):
     return np.take_along_axis(x, order, axis=-1), order
 
 
+def _ts_dropped_b1(z, s, vals, w):
+    w = dict(w)
+    w["b1"] = np.zeros_like(w["b1"])
+    return ORIG_TS(z, s, vals, w)
+
+
+def _ts_flipped_correction(z, s, vals, w):
+    # S = l - Delta instead of l + Delta
+    base = np.broadcast_to(vals[:, 1:, None, :], (z.shape[0], z.shape[1] - 1, z.shape[2], z.shape[2]))
+    return 2 * base - ORIG_TS(z, s, vals, w)
+
+
+def _select_transposed(S, vals, ids):
+    # walks the column S_p(., k_p) instead of the row S_p(k_p, .)
+    return ORIG_SELECT(np.swapaxes(S, -1, -2), vals, ids)
+
+
+def _select_first_slot_assumed_zero(S, vals, ids):
+    # takes candidate 0 for slot 0 instead of the argmax of the drafter's logits
+    v = np.array(vals, dtype=np.float64, copy=True)
+    v[:, 0, :] = 0.0
+    v[:, 0, 0] = 1.0
+    return ORIG_SELECT(S, v, ids)
+
+
+def _verify_greedy_commits_draft(draft, t):
+    out = ORIG_VG(draft, t)
+    com = out["committed"].copy()
+    for n, A in enumerate(out["accept_len"]):
+        if A < draft.shape[1]:
+            com[n, A] = draft[n, A]
+    return {**out, "committed": com}
+
+
+def _verify_stochastic_non_strict(draft, q, u):
+    # accepts when u == q(y)
+    return ORIG_VS(draft, q, np.nextafter(u, -np.inf))
+
+
+def _residual_keeps_draft(q, u, exclude):
+    return ORIG_RD(q, u, -1)
+
+
+ORIG_SELECT = od.select
+ORIG_VG = od.verify_greedy
+ORIG_VS = od.verify_stochastic
+ORIG_RD = od.residual_draw
+
 CASES = [
     ("layer_norm", _unbiased_ln, pins.test_layer_norm_spike_closed_form),
     ("layer_norm", _eps_outside_ln, pins.test_layer_norm_spike_closed_form),
@@ -75,6 +123,13 @@ CASES = [
     ("candidate_repr", _cr_concat_order, pins.test_candidate_repr_hidden_path_and_concat_order),
     ("candidate_repr", _cr_transposed_gather, pins.test_candidate_repr_embedding_path),
     ("topk", _topk_ties_high, pins.test_topk_all_equal_and_k_equals_v),
+    ("transition_scores", _ts_dropped_b1, pins.test_scores_bias_only_closed_form),
+    ("transition_scores", _ts_flipped_correction, pins.test_scores_bias_only_closed_form),
+    ("select", _select_transposed, lambda: [pins.test_walk_matches_brute_force(i) for i in range(8)]),
+    ("select", _select_first_slot_assumed_zero, lambda: [pins.test_walk_matches_brute_force(i) for i in range(8)]),
+    ("verify_greedy", _verify_greedy_commits_draft, pins.test_greedy_verify_closed_form),
+    ("verify_stochastic", _verify_stochastic_non_strict, pins.test_stochastic_verify_hand_cases),
+    ("residual_draw", _residual_keeps_draft, pins.test_stochastic_verify_hand_cases),
 ]
 
 
