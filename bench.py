@@ -51,7 +51,7 @@ sys.path.insert(0, {root!r})
 import numpy as np
 import oracle, workloads as wl
 cfg = wl.CONFIGS[{cfg!r}].replace(N=1)
-n_streams, reps = {n_streams}, {reps}
+n_streams, reps, budget = {n_streams}, {reps}, {budget}
 emb = wl.embedding(cfg)
 w = wl.weights(cfg)
 f = lambda a: wl.to_f64(a, cfg.dtype)
@@ -61,7 +61,7 @@ for n in range(n_streams):
     c = cfg.replace(base_seed=cfg.base_seed + n)
     streams.append((wl.logits(c), wl.hidden(c)))
 times = []
-for r in range(reps):
+while len(times) < reps and (budget <= 0 or sum(times) < budget):
     t0 = time.perf_counter()
     for lg, h in streams:
         vals, ids = oracle.topk(f(lg), cfg.K)
@@ -77,12 +77,13 @@ print(json.dumps({{"times": times, "streams": n_streams}}))
 """
 
 
-def run_oracle(cfg_name: str, n_streams: int, reps: int):
-    """Times the oracle in a fresh single-threaded process (no CUDA context, no fork)."""
+def run_oracle(cfg_name: str, n_streams: int, reps: int, budget_s: float = 0.0):
+    """Times the oracle in a fresh single-threaded process (no CUDA context, no fork):
+    `reps` repetitions, or fewer once `budget_s` seconds of timed work are done."""
     env = dict(os.environ)
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
         env[k] = "1"
-    code = ORACLE_SNIPPET.format(root=ROOT, cfg=cfg_name, n_streams=n_streams, reps=reps)
+    code = ORACLE_SNIPPET.format(root=ROOT, cfg=cfg_name, n_streams=n_streams, reps=reps, budget=budget_s)
     res = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env)
     if res.returncode != 0:
         raise RuntimeError(f"oracle run failed:\n{res.stderr[-2000:]}")
@@ -319,8 +320,13 @@ def gpu_arm(args, cfg):
                 "peak_source": f"{peak_kind} hbm_gbs (burst)", "algorithmic_bytes_per_launch": topk_bytes}
 
     # End to end through the public API: pinned host inputs -> device, cycle, results -> host.
-    logits_pin = torch.from_numpy(logits_h.view(np.int16)).view(torch.bfloat16).pin_memory()
-    hidden_pin = torch.from_numpy(hidden_h.view(np.int16)).view(torch.bfloat16).pin_memory()
+    def pinned(a):
+        if cfg.dtype == "bf16":
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory()
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).pin_memory()
+
+    logits_pin = pinned(logits_h)
+    hidden_pin = pinned(hidden_h)
     t_pin = torch.from_numpy(t_host).pin_memory()
     com_pin = torch.empty((cfg.N, cfg.B + 1), dtype=torch.int32).pin_memory()
     acc_pin = torch.empty((cfg.N,), dtype=torch.int32).pin_memory()
@@ -340,16 +346,19 @@ def gpu_arm(args, cfg):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        n_streams = 2
-        r = run_oracle(cfg.name, n_streams, 2)
+        # a bounded sample of about 10 s of host work: a few streams, repeated
+        n_streams = min(2, cfg.N)
+        r = run_oracle(cfg.name, n_streams, 200, budget_s=10.0)
+        reps = len(r["times"])
         sec = statistics.mean(r["times"])
         cpu = {"value": n_streams / sec, "unit": "blocks/s", "cores": 1, "kind": "oracle",
-               "sample": f"{n_streams} of {cfg.N} streams, full cycle each, single host thread"}
+               "sample": f"{n_streams} of {cfg.N} streams, full cycle each, {reps} repetitions, "
+                         f"single host thread"}
 
     if rank == 0:
         line = {"metric": METRIC, "value": round(value, 1), "unit": "blocks/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic",
                 "config": config_dict(cfg), "roofline": roofline, "cpu_baseline": cpu,
                 "e2e": {"value": round(e2e_val, 1), "unit": "blocks/s", "h2d_bytes_per_step": h2d,
                         "d2h_bytes_per_step": d2h},
