@@ -312,7 +312,7 @@ def gpu_arm(args, cfg):
 
     # Roofline of the dominant kernel (top-K, HBM-bound): algorithmic bytes per launch.
     hbm, _, peak_kind = peaks()
-    topk_bytes = cfg.N * cfg.B * cfg.V * 2 + cfg.N * cfg.B * cfg.K * 8
+    topk_bytes = cfg.N * cfg.B * cfg.V * (2 if cfg.dtype == "bf16" else 4) + cfg.N * cfg.B * cfg.K * 8
     topk_s = stage_us["topk"] * 1e-6
     achieved = topk_bytes / topk_s / 1e9
     roofline = {"bound": "hbm", "kernel": "topk_kernel", "achieved": round(achieved, 1), "peak": hbm,
