@@ -12,8 +12,10 @@
 //   warp 1     allocates tensor memory; lane 0 issues tcgen05.mma (bf16 -> kind::f16,
 //              f32 -> kind::tf32) into an fp32 accumulator of 128 lanes x BN columns and
 //              commits each stage back to the producer.
-//   warps 2-5  epilogue: tcgen05.ld of the accumulator, then the fused op of the group
-//              (LayerNorm over the full row, SiLU with a per-slot bias, or a plain store).
+//   warps 2-9  epilogue: tcgen05.ld of the accumulator, then the fused op of the group
+//              (LayerNorm over the full row, SiLU with a per-slot bias, the scorer operands,
+//              or a plain store).  Two warps share each 32-lane quarter of the accumulator
+//              and split its columns; LayerNorm exchanges row partial sums in shared memory.
 // Split-K: with split_k > 1 the CTAs of one tile form a cluster along z, each reduces a
 // K range, stages its partial tile in its shared memory, and each CTA then sums a slice
 // of rows across the cluster in rank order (distributed shared memory) -- deterministic.
@@ -29,10 +31,12 @@ namespace dcoco {
 namespace {
 
 constexpr int BM = 128;
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;  // two per TMEM lane quarter, each with half of the tile's columns
+constexpr int kEpiThreads = kEpiWarps * 32;
+constexpr int kThreads = 64 + kEpiThreads;
 constexpr int kMaxStages = 8;
 constexpr int kSmemBudget = 200 * 1024;
-constexpr int kGatherThreads = 128;  // epilogue warps that gather the A operand
+constexpr int kGatherThreads = kEpiThreads;  // epilogue warps that gather the A operand
 constexpr int kBiasStageBytes = 20 * 1024;  // per-slot bias rows of one tile (SiLU epilogue)
 
 __device__ unsigned int g_status_word;
@@ -129,6 +133,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   __shared__ __align__(8) uint64_t acc_bar;
   __shared__ uint32_t tmem_base_s;
   __shared__ int s_rows[BM];
+  __shared__ float s_ln[2][BM];  // LayerNorm partial row sums of the two column halves
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -242,15 +247,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       // the stages with 16-byte asynchronous copies straight into the 128-byte swizzled layout
       // (eight threads per 128-byte row piece, so global reads stay coalesced), then hand each
       // stage to the tensor core with a generic-to-async proxy fence and one arrival.
+      constexpr int RPT = BM * 8 / kGatherThreads;  // tile rows per thread (4)
+      constexpr int RSTEP = kGatherThreads / 8;     // rows covered by one pass of the threads
       const int t = threadIdx.x - 64;
       const int c = t & 7;                     // 16-byte chunk of the 128-byte row piece
       const int cs = c ^ ((t >> 3) & 7);       // its swizzled position (row & 7 == (t >> 3) & 7)
       const int esz = kBf16 ? 2 : 4;
-      const char* rowb[8];  // start of the table row behind each of this thread's 8 tile rows
+      const char* rowb[RPT];  // start of the table row behind each of this thread's tile rows
 #pragma unroll
-      for (int it = 0; it < 8; ++it)
+      for (int it = 0; it < RPT; ++it)
         rowb[it] = static_cast<const char*>(args.gather_base) +
-                   static_cast<size_t>(s_rows[it * 16 + (t >> 3)]) * args.gather_pitch_bytes;
+                   static_cast<size_t>(s_rows[it * RSTEP + (t >> 3)]) * args.gather_pitch_bytes;
       const int lag = stages - 1;
       bool alive = true;
       for (int i = 0; i < nk && alive; ++i) {
@@ -266,8 +273,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         const uint32_t nbytes = kcol < args.K ? 16u : 0u;      // K is a multiple of 16 bytes
         const size_t koff = static_cast<size_t>(kcol) * esz;
 #pragma unroll
-        for (int it = 0; it < 8; ++it)
-          cp_async16(a_s + (it * 16 + (t >> 3)) * 128 + cs * 16, rowb[it] + (nbytes ? koff : 0), nbytes);
+        for (int it = 0; it < RPT; ++it)
+          cp_async16(a_s + (it * RSTEP + (t >> 3)) * 128 + cs * 16, rowb[it] + (nbytes ? koff : 0), nbytes);
         cp_async_commit();
         if (i >= lag) {
           cp_async_wait(lag);
@@ -282,6 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       }
     }
     const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int half = (warp - 2) >> 2;  // which half of the tile's columns (when split)
     const int row_local = q * 32 + lane;
     const int m = m_tile * BM + row_local;
     // tcgen05.ld is warp-collective: every lane of the warp takes the same path below and
@@ -295,14 +303,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       const int nslots = last_slot - first_slot + 1;
       if (nslots * BN * 4 <= kBiasStageBytes) {
         float* dst = reinterpret_cast<float*>(smem + bias_stage_offset);
-        for (int i = threadIdx.x - 64; i < nslots * (BN / 4); i += 128) {
+        for (int i = threadIdx.x - 64; i < nslots * (BN / 4); i += kEpiThreads) {
           const int sl = i / (BN / 4), c4 = i % (BN / 4);
           *reinterpret_cast<float4*>(dst + sl * BN + c4 * 4) = *reinterpret_cast<const float4*>(
               args.bias + static_cast<size_t>(first_slot + sl) * args.ld_bias + nt * BN + c4 * 4);
         }
         sbias = dst;
       }
-      named_barrier_sync(1, 128);
+      named_barrier_sync(1, kEpiThreads);
     } else if (grp.epi == EPI_PREP) {
       // Rows 0..nslots-1: (col_b + the slot's pair-bias row) / 2; row nslots: col_u / 2.
       first_slot = (m_tile * BM) / args.bias_div;
@@ -310,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       const int nslots = last_slot - first_slot + 1;
       if ((nslots + 1) * BN * 4 <= kBiasStageBytes) {
         float* dst = reinterpret_cast<float*>(smem + bias_stage_offset);
-        for (int i = threadIdx.x - 64; i < (nslots + 1) * (BN / 4); i += 128) {
+        for (int i = threadIdx.x - 64; i < (nslots + 1) * (BN / 4); i += kEpiThreads) {
           const int sl = i / (BN / 4), c4 = i % (BN / 4);
           const int col = nt * BN + c4 * 4;
           float4 v;
@@ -333,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         sbias = dst;
         prep_nslots = nslots;
       }
-      named_barrier_sync(1, 128);
+      named_barrier_sync(1, kEpiThreads);
     }
     const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&acc_bar), 0));
     if (!ok && lane == 0) atomicOr(args.status, DEV_TIMEOUT_ACC);
@@ -342,38 +350,58 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16);
     if constexpr (kSplit) {
       float* stg = reinterpret_cast<float*>(smem);
-      for (int c = 0; c < BN; c += 32) {
+      constexpr int SH = BN >= 64 ? 2 : 1;  // warps per quarter sharing the columns
+      for (int c = half * BN / SH; half < SH && c < (half + 1) * BN / SH; c += 32) {
         float v[32];
         tmem_ld32(trow + c, v);
 #pragma unroll
         for (int i = 0; i < 32; i += 4)
           *reinterpret_cast<float4*>(&stg[row_local * LDS + c + i]) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
       }
-    } else if (ok) {
+    } else {
       // Row-per-thread values go through a swizzled staging buffer per warp (two 32 x 128-byte
       // halves, reusing the drained pipeline buffers) and leave with tensor-map stores, which
-      // write whole rows coalesced and clip rows past M.
+      // write whole rows coalesced and clip rows past M.  Every epilogue warp runs this block,
+      // even after a timed-out wait (then nothing is stored), so the named barriers always
+      // see all of them.
       const bool out_bf16 = kBf16 && grp.epi != EPI_F32;
       const int cps = out_bf16 ? 64 : 32;  // output columns per 128-byte sub-tile
-      uint8_t* stg = smem + q * 8192;
+      const int nsub = BN / cps;           // 128-byte sub-tiles in the tile's columns
+      const int halves = nsub >= 2 ? 2 : 1;
+      const int j0 = half * nsub / halves, j1 = (half + 1) * nsub / halves;  // this warp's sub-tiles
+      uint8_t* stg = smem + (warp - 2) * 8192;
       const int y0 = m_tile * BM + q * 32;
       const bool any_rows = y0 < args.M;
       float mean = 0.f, rstd = 1.f;
       if (grp.epi == EPI_LN) {
+        // Two-pass row statistics over the full row: each warp sums its columns, the two
+        // warps of a quarter exchange their partial sums.
+        const int c0 = half < halves ? j0 * cps : 0, c1 = half < halves ? j1 * cps : 0;
         float sum = 0.f;
-        for (int c = 0; c < BN; c += 32) {
+        for (int c = c0; c < c1; c += 32) {
           float v[32];
           tmem_ld32(trow + c, v);
 #pragma unroll
           for (int i = 0; i < 32; ++i) sum += v[i];
         }
+        if (halves == 2) {
+          s_ln[half][row_local] = sum;
+          named_barrier_sync(2, kEpiThreads);
+          sum = s_ln[0][row_local] + s_ln[1][row_local];
+        }
         mean = sum / BN;
         float ss = 0.f;
-        for (int c = 0; c < BN; c += 32) {
+        for (int c = c0; c < c1; c += 32) {
           float v[32];
           tmem_ld32(trow + c, v);
 #pragma unroll
           for (int i = 0; i < 32; ++i) ss += (v[i] - mean) * (v[i] - mean);
+        }
+        if (halves == 2) {
+          named_barrier_sync(2, kEpiThreads);  // everyone has read the first exchange
+          s_ln[half][row_local] = ss;
+          named_barrier_sync(2, kEpiThreads);
+          ss = s_ln[0][row_local] + s_ln[1][row_local];
         }
         rstd = rsqrtf(ss / BN + args.ln_eps);
       }
@@ -438,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           }
         }
       };
-      for (int j = 0; j < BN / cps; ++j) {
+      for (int j = j0; half < halves && j < j1; ++j) {
         float v[64];
         float(&lo)[32] = *reinterpret_cast<float(*)[32]>(v);
         float(&hi)[32] = *reinterpret_cast<float(*)[32]>(v + 32);
@@ -448,8 +476,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           tmem_ld32(trow + j * cps + 32, hi);
           apply32(hi, j * cps + 32);
         }
-        uint8_t* buf = stg + (j & 1) * 4096;
-        if (j >= 2) {
+        uint8_t* buf = stg + ((j - j0) & 1) * 4096;
+        if (j - j0 >= 2) {
           if (lane == 0) bulk_wait_read<1>();  // the store that used this half has read it
           __syncwarp();
         }
@@ -461,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           stage_row<0>(buf, lane, v);
         fence_proxy_async();
         __syncwarp();
-        if (lane == 0 && any_rows) {
+        if (lane == 0 && any_rows && ok) {
           tma_store_2d(&grp.out_map, nt * BN + j * cps, y0, smem_u32(buf));
           bulk_commit();
         }
