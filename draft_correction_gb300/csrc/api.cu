@@ -12,6 +12,10 @@
 #include "../../include/dcoco.h"
 #include "internal.h"
 
+namespace dcoco {
+thread_local bool g_pdl = false;
+}  // namespace dcoco
+
 using namespace dcoco;
 
 namespace {
@@ -695,6 +699,9 @@ int dcoco_cycle(const void* logits, int V, const void* emb, const void* h, const
   DCOCO_TRY(enqueue_repr_gather(D, o_ids, emb, V, w, s.repr, st));
   e = cudaStreamWaitEvent(st, side->join, 0);
   if (e != cudaSuccess) return cuda_fail(e, "join from helper stream");
+  // From here on each kernel may launch while its predecessor finishes (programmatic
+  // dependent launch); each waits for it before touching its data.
+  PdlScope pdl;
   // uz/vz scratch holds the scorer's prepared operands P and Q here.
   DCOCO_TRY(enqueue_repr_fuse(D, w, s.uz, s.vz, s.repr, st, o_vals, s.wsp));
   DCOCO_TRY(enqueue_scores_prepped(D, s.uz, s.vz, o_vals, w, o_S, st));

@@ -163,6 +163,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     prefetch_tmap(&grp.b_map);
   }
   if (warp == 1) tmem_alloc(smem_u32(&tmem_base_s), TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();  // barriers initialised, accumulator allocated
+  tc_fence_after();
+  // The weight (B) tiles of the first stages do not depend on the preceding kernel: request them
+  // before waiting for it.
+  const int pre = std::min(nk, stages);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < pre; ++i) {
+      const uint32_t fb = smem_u32(&full_bar[i]);
+      const uint32_t b_s = smem_u32(smem) + i * STAGE_BYTES + A_BYTES;
+      const int kx = (kb0 + i) * T::BK;
+      mbar_expect_tx(fb, gather ? B_BYTES : STAGE_BYTES);
+#pragma unroll
+      for (int h = 0; h < NH; ++h) tma_load_2d(b_s + h * NMMA * 128, &grp.b_map, kx, nt * BN + h * NMMA, fb);
+    }
+  }
+  grid_dep_wait();
   if (args.gather != nullptr && threadIdx.x < BM) {
     const int m = m_tile * BM + threadIdx.x;
     int row = 0;
@@ -186,21 +203,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     for (int i = 0; i < nk; ++i) {
       const int s = i % stages;
       const uint32_t ph = (i / stages) & 1;
-      if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&empty_bar[s]), ph ^ 1))) {
-        if (lane == 0) atomicOr(args.status, DEV_TIMEOUT_MMA);
-        break;
-      }
       const uint32_t fb = smem_u32(&full_bar[s]);
       const uint32_t a_s = smem0 + s * STAGE_BYTES;
       const uint32_t b_s = a_s + A_BYTES;
       const int kx = (kb0 + i) * T::BK;
-      if (lane == 0) mbar_expect_tx(fb, gather ? B_BYTES : STAGE_BYTES);
-      __syncwarp();
-      if (!gather && lane == 0) tma_load_2d(a_s, &args.a_map, kx, m_tile * BM, fb);
-      if (lane == 0) {
+      if (i >= pre) {  // the first `pre` stages are fresh and already expect their bytes
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&empty_bar[s]), ph ^ 1))) {
+          if (lane == 0) atomicOr(args.status, DEV_TIMEOUT_MMA);
+          break;
+        }
+        if (lane == 0) {
+          mbar_expect_tx(fb, gather ? B_BYTES : STAGE_BYTES);
 #pragma unroll
-        for (int h = 0; h < NH; ++h) tma_load_2d(b_s + h * NMMA * 128, &grp.b_map, kx, nt * BN + h * NMMA, fb);
+          for (int h = 0; h < NH; ++h) tma_load_2d(b_s + h * NMMA * 128, &grp.b_map, kx, nt * BN + h * NMMA, fb);
+        }
       }
+      if (!gather && lane == 0) tma_load_2d(a_s, &args.a_map, kx, m_tile * BM, fb);
+      __syncwarp();
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -345,6 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     }
     const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&acc_bar), 0));
     if (!ok && lane == 0) atomicOr(args.status, DEV_TIMEOUT_ACC);
+    grid_dep_launch();  // main loop done: the next kernel may start its prologue
     const bool live = m < args.M;
     tc_fence_after();
     const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16);
@@ -623,13 +643,14 @@ cudaError_t launch_gemm_t(const GemmArgs& args, int split_k, cudaStream_t stream
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 1;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = split_k;
   cfg.attrs = attr;
   cfg.numAttrs = kSplit ? 1 : 0;
+  cfg.numAttrs += pdl_attr(&attr[cfg.numAttrs]);
   return cudaLaunchKernelEx(&cfg, kern, args, stages, split_k, bias_off);
 }
 
@@ -648,6 +669,8 @@ cudaError_t dispatch_bn(const GemmArgs& args, int BN, int split_k, cudaStream_t 
 
 template <bool kBf16>
 __global__ void pair_combine_kernel(const float* __restrict__ hp, void* __restrict__ s, int N, int B, int r) {
+  grid_dep_wait();  // hp comes from the preceding kernel
+  grid_dep_launch();
   const int64_t total = static_cast<int64_t>(N) * (B - 1) * r;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -671,11 +694,15 @@ cudaError_t launch_pair_combine(const float* hp, void* s, bool is_bf16, int N, i
   const int64_t total = static_cast<int64_t>(N) * (B - 1) * r;
   const int threads = 256;
   const int blocks = static_cast<int>(std::min<int64_t>((total + threads - 1) / threads, 152 * 8));
-  if (is_bf16)
-    pair_combine_kernel<true><<<blocks, threads, 0, stream>>>(hp, s, N, B, r);
-  else
-    pair_combine_kernel<false><<<blocks, threads, 0, stream>>>(hp, s, N, B, r);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks, 1, 1);
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_attr(&attr[0]);
+  return is_bf16 ? cudaLaunchKernelEx(&cfg, pair_combine_kernel<true>, hp, s, N, B, r)
+                 : cudaLaunchKernelEx(&cfg, pair_combine_kernel<false>, hp, s, N, B, r);
 }
 
 unsigned int* device_status_word(cudaError_t* err) {

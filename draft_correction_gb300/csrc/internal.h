@@ -7,6 +7,23 @@
 
 namespace dcoco {
 
+// Kernels enqueued by this thread while set carry the programmatic-stream-serialization launch
+// attribute, so that each may start (prologue, weight loads) while its predecessor finishes.
+// Only the cycle sets it: there every predecessor is one of this library's kernels, none of
+// which writes the weights, and every kernel waits (grid_dep_wait) before touching its data.
+extern thread_local bool g_pdl;
+struct PdlScope {
+  PdlScope() { g_pdl = true; }
+  ~PdlScope() { g_pdl = false; }
+};
+// Fills attr with the programmatic-serialization attribute when g_pdl is set; returns the count (0 or 1).
+inline unsigned pdl_attr(cudaLaunchAttribute* attr) {
+  if (!g_pdl) return 0;
+  attr->id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr->val.programmaticStreamSerializationAllowed = 1;
+  return 1;
+}
+
 // ------------------------------------------------------------------ top-K
 // Rows of `logits` ([rows, V], bf16 bits if is_bf16 else f32); ctas_per_row in 1..8.
 cudaError_t launch_topk(const void* logits, bool is_bf16, int rows, int V, int K, int ctas_per_row, float* vals,

@@ -238,4 +238,12 @@ __device__ __forceinline__ uint32_t key_index(uint64_t key) { return 0xFFFFFFFFu
 // ---------------------------------------------------------------- misc
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
+// Programmatic dependent launch.  grid_dep_wait() returns once the preceding kernel of the
+// stream has completed and its writes are visible (immediately when the kernel was launched
+// without the programmatic-serialization attribute); nothing before it may read that kernel's
+// outputs or write anything it reads.  grid_dep_launch() lets the next kernel start launching;
+// that kernel's own grid_dep_wait() still waits for all of this grid.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 }  // namespace dcoco

@@ -229,6 +229,8 @@ __global__ void __launch_bounds__(kThreads) score_kernel(const ScoreArgs a) {
   const float* vals_q = a.vals + row_q;
   const float* wsp = a.wsp + static_cast<size_t>(np) * H;
   const int cpr = hc * static_cast<int>(sizeof(Act)) / 16;  // 16-byte pieces per row and chunk
+  grid_dep_wait();  // uz, vz, W s and the logits come from preceding kernels
+  grid_dep_launch();
 
   // Raw rows of one chunk (predecessor rows from uz, successor rows from vz) by cp.async.
   auto fetch = [&](int h0) {
@@ -364,13 +366,14 @@ __global__ void __launch_bounds__(kPrepThreads, 8) score_prepped_kernel(const Sc
     }
     cp_async_commit();
   };
-  fetch(0);
   for (int i = threadIdx.x; i < H; i += kPrepThreads) {
     if constexpr (kBf16)
       wv[i] = __float2half_rn(ldv<true>(a.w2, i));
     else
       wv[i] = ldv<false>(a.w2, i);
   }
+  grid_dep_wait();  // P and Q come from the preceding kernel
+  fetch(0);
 
   float acc[kTA][kTB];
 #pragma unroll
@@ -387,6 +390,7 @@ __global__ void __launch_bounds__(kPrepThreads, 8) score_prepped_kernel(const Sc
     __syncthreads();
     accumulate<kBf16>(acc, P, Q, ld, wv + h0, hc, t);
   }
+  grid_dep_launch();
   __syncthreads();  // P/Q are free for the partial sums
   finish<kPrepThreads>(acc, red, t, a.S + (static_cast<size_t>(np) * K + a0) * K, a.vals + row_q,
                        ldv<kBf16>(a.b2, 0), na, K);
@@ -442,11 +446,15 @@ cudaError_t launch_scores(const ScoreArgs& a, bool is_bf16, cudaStream_t stream)
   const dim3 grid(a.N * (a.B - 1), (a.K + kAB - 1) / kAB);
   cudaError_t e = configure_once();
   if (e != cudaSuccess) return e;
-  if (is_bf16)
-    score_kernel<true><<<grid, kThreads, smem, stream>>>(a);
-  else
-    score_kernel<false><<<grid, kThreads, smem, stream>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_attr(&attr[0]);
+  return is_bf16 ? cudaLaunchKernelEx(&cfg, score_kernel<true>, a) : cudaLaunchKernelEx(&cfg, score_kernel<false>, a);
 }
 
 cudaError_t launch_scores_prepped(const ScoreArgs& a, bool is_bf16, cudaStream_t stream) {
@@ -455,11 +463,16 @@ cudaError_t launch_scores_prepped(const ScoreArgs& a, bool is_bf16, cudaStream_t
   const dim3 grid(a.N * (a.B - 1), (a.K + kAB - 1) / kAB);
   cudaError_t e = configure_once();
   if (e != cudaSuccess) return e;
-  if (is_bf16)
-    score_prepped_kernel<true><<<grid, kPrepThreads, smem, stream>>>(a);
-  else
-    score_prepped_kernel<false><<<grid, kPrepThreads, smem, stream>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kPrepThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_attr(&attr[0]);
+  return is_bf16 ? cudaLaunchKernelEx(&cfg, score_prepped_kernel<true>, a)
+                 : cudaLaunchKernelEx(&cfg, score_prepped_kernel<false>, a);
 }
 
 }  // namespace dcoco

@@ -56,6 +56,8 @@ __global__ void __launch_bounds__(kThreads) select_verify_kernel(const SelectVer
   const int n = blockIdx.x;
   const int B = a.B, K = a.K, V = a.V;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  grid_dep_wait();  // scores, logits and ids come from preceding kernels
+  grid_dep_launch();
 
   // ------------------------------------------------------------------ walk
   if (a.S != nullptr) {
@@ -221,8 +223,14 @@ __global__ void __launch_bounds__(kThreads) select_verify_kernel(const SelectVer
 }  // namespace
 
 cudaError_t launch_select_verify(const SelectVerifyArgs& a, cudaStream_t stream) {
-  select_verify_kernel<<<a.N, kThreads, 0, stream>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.N, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_attr(&attr[0]);
+  return cudaLaunchKernelEx(&cfg, select_verify_kernel, a);
 }
 
 }  // namespace dcoco

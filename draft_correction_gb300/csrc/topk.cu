@@ -305,6 +305,8 @@ __global__ void __launch_bounds__(kThreads, 4) topk_kernel(const void* __restric
     }
   };
 
+  grid_dep_wait();  // the logits may come from the preceding kernel
+  grid_dep_launch();
   // Seed threshold: the K-th largest of the block's lane maxima over the first two iterations
   // (already in registers).  K elements reach that value, so nothing below it is in the top K.
   load(0, c0);
@@ -458,13 +460,14 @@ cudaError_t launch_topk_t(const void* logits, int rows, int V, int K, int S, flo
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = S;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = S > 1 ? 1 : 0;
+  cfg.numAttrs += pdl_attr(&attr[cfg.numAttrs]);
   return cudaLaunchKernelEx(&cfg, topk_kernel<kBf16, KW>, logits, V, K, S, vals, ids);
 }
 
