@@ -123,12 +123,23 @@ int pick_bn(int n, bool allow512) {
   return 32;
 }
 
+int sm_count() {
+  static int sms[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+  if (sms[dev] == 0 && (cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+                        sms[dev] <= 0))
+    sms[dev] = 152;
+  return sms[dev];
+}
+
 // Split-K factor for long reductions only (>= 16 K blocks): double it while the grid stays
-// within the SMs and every split keeps at least 8 K blocks.  Short reductions run whole.
-int pick_split(int m_tiles, int n_tiles, int nkb, int BN) {
+// within max_ctas (the SM count by default) and every split keeps at least 8 K blocks.  Short
+// reductions run whole.
+int pick_split(int m_tiles, int n_tiles, int nkb, int BN, int max_ctas) {
   if (BN > 256 || nkb < 16) return 1;
   int s = 1;
-  while (s < 8 && m_tiles * n_tiles * s * 2 <= 152 && nkb / (s * 2) >= 8) s *= 2;
+  while (s < 8 && m_tiles * n_tiles * s * 2 <= max_ctas && nkb / (s * 2) >= 8) s *= 2;
   return s;
 }
 
@@ -198,7 +209,8 @@ int gemm_group(GemmGroup* g, const void* w_base, const Dims& D, uint64_t rows, u
   return DCOCO_OK;
 }
 
-int run_gemm(GemmArgs& a, const Dims& D, int BN, cudaStream_t st, const char* what) {
+// max_ctas bounds the split-K grid (0: the SM count), for GEMMs that share the GPU with another.
+int run_gemm(GemmArgs& a, const Dims& D, int BN, cudaStream_t st, const char* what, int max_ctas = 0) {
   int rc;
   a.status = status_word(&rc);
   if (rc != DCOCO_OK) return rc;
@@ -208,7 +220,7 @@ int run_gemm(GemmArgs& a, const Dims& D, int BN, cudaStream_t st, const char* wh
   const int bk = D.bf16 ? 64 : 32;
   const int nkb = (a.K + bk - 1) / bk;
   const bool prep = a.g[0].epi == EPI_PREP || (a.n_groups > 1 && a.g[1].epi == EPI_PREP);
-  const int split = prep ? 1 : pick_split(m_tiles, n_tiles, nkb, BN);
+  const int split = prep ? 1 : pick_split(m_tiles, n_tiles, nkb, BN, max_ctas > 0 ? max_ctas : sm_count());
   const cudaError_t e = launch_gemm(a, D.bf16, BN, split, st);
   if (e != cudaSuccess) return cuda_fail(e, what);
   return DCOCO_OK;
@@ -222,7 +234,8 @@ int a_map_tiled(GemmArgs& a, const void* base, const Dims& D, uint64_t rows, uin
 }
 
 // Candidate representation, slot part (needs only h): g = LN(W_h h), gw = W_f[:, r:2r] g.
-int enqueue_repr_slot(const Dims& D, const void* h, const dcoco_weights* w, const ReprScratch& s, cudaStream_t st) {
+int enqueue_repr_slot(const Dims& D, const void* h, const dcoco_weights* w, const ReprScratch& s, cudaStream_t st,
+                      int max_ctas = 0) {
   const int NB = D.NB(), r = D.r;
   // g = LN(W_h h)
   {
@@ -233,7 +246,7 @@ int enqueue_repr_slot(const Dims& D, const void* h, const dcoco_weights* w, cons
     a.n_groups = 1;
     const int BN = r;
     DCOCO_TRY(gemm_group(&a.g[0], w->W_h, D, r, D.d, D.d, BN, s.g, r, EPI_LN, a.M));
-    DCOCO_TRY(run_gemm(a, D, BN, st, "gemm g = LN(W_h h)"));
+    DCOCO_TRY(run_gemm(a, D, BN, st, "gemm g = LN(W_h h)", max_ctas));
   }
   // gw = W_f[:, r:2r] g   (the g half of the fusion, once per slot)
   {
@@ -276,8 +289,10 @@ int enqueue_repr_gather(const Dims& D, const int32_t* ids, const void* emb, int 
 // Candidate representation, fusion part: z = SiLU(W_f[:, 0:r] b + gw[slot]), uz = U z, vz = V z.
 // With prep_vals set, the U z / V z epilogue writes the scorer's operands instead:
 // uz <- (U z + b1 + W s + u_a l)/2 and vz <- (V z + u_b l)/2 (W s from prep_wsp).
+// before_uv, when set, is an event the U z / V z GEMM waits for (the producer of prep_wsp).
 int enqueue_repr_fuse(const Dims& D, const dcoco_weights* w, void* uz, void* vz, const ReprScratch& s,
-                      cudaStream_t st, const float* prep_vals = nullptr, const float* prep_wsp = nullptr) {
+                      cudaStream_t st, const float* prep_vals = nullptr, const float* prep_wsp = nullptr,
+                      cudaEvent_t before_uv = nullptr) {
   const int M = D.M(), r = D.r, H = D.H;
   // z = SiLU(W_f[:, 0:r] b + gw[slot])
   {
@@ -292,6 +307,10 @@ int enqueue_repr_fuse(const Dims& D, const dcoco_weights* w, void* uz, void* vz,
     const int BN = pick_bn(r, false);
     DCOCO_TRY(gemm_group(&a.g[0], w->W_f, D, r, r, 2 * r, BN, s.z, r, EPI_SILU_BIAS, a.M));
     DCOCO_TRY(run_gemm(a, D, BN, st, "gemm z = SiLU(W_f [b; g])"));
+  }
+  if (before_uv != nullptr) {
+    const cudaError_t e = cudaStreamWaitEvent(st, before_uv, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "wait for W s");
   }
   // uz = U z, vz = V z
   {
@@ -326,11 +345,19 @@ int enqueue_repr(const Dims& D, const int32_t* ids, const void* emb, int V, cons
   return enqueue_repr_fuse(D, w, uz, vz, s, st);
 }
 
-// Per-device helper stream (highest priority) and fork/join events for dcoco_cycle; the
+// CTAs of the embedding-row GEMM b = LN(W_e Emb[c]) (the same choices enqueue_repr_gather makes).
+int gather_gemm_ctas(const Dims& D) {
+  const int BN = pick_bn(D.r, true);
+  const int m_tiles = (D.M() + 127) / 128, n_tiles = D.r / BN;
+  const int nkb = (D.E + (D.bf16 ? 64 : 32) - 1) / (D.bf16 ? 64 : 32);
+  return m_tiles * n_tiles * pick_split(m_tiles, n_tiles, nkb, BN, sm_count());
+}
+
+// Per-device helper streams (highest priority) and fork/join events for dcoco_cycle; the
 // mutex keeps one enqueue sequence at a time per process.
 struct SideStream {
-  cudaStream_t stream = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr;
+  cudaStream_t stream = nullptr, stream2 = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr, join2 = nullptr;
 };
 std::mutex g_side_mu;
 int side_stream(SideStream** out) {
@@ -342,8 +369,10 @@ int side_stream(SideStream** out) {
     int lo = 0, hi = 0;
     cudaError_t e = cudaDeviceGetStreamPriorityRange(&lo, &hi);
     if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&s.stream, cudaStreamNonBlocking, hi);
+    if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&s.stream2, cudaStreamNonBlocking, hi);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.join2, cudaEventDisableTiming);
     if (e != cudaSuccess) return cuda_fail(e, "helper stream set-up");
   }
   *out = &s;
@@ -351,7 +380,7 @@ int side_stream(SideStream** out) {
 }
 
 int enqueue_pair(const Dims& D, const void* h, const dcoco_weights* w, float* wsp, const PairScratch& s,
-                 cudaStream_t st) {
+                 cudaStream_t st, int max_ctas = 0) {
   const int NB = D.NB(), r = D.r, H = D.H, d = D.d;
   // hp[:, 0:r] = W_pair[:, 0:d] h,  hp[:, r:2r] = W_pair[:, d:2d] h   (every slot once)
   {
@@ -364,7 +393,7 @@ int enqueue_pair(const Dims& D, const void* h, const dcoco_weights* w, float* ws
     DCOCO_TRY(gemm_group(&a.g[0], w->W_pair, D, r, d, 2 * d, BN, s.hp, 2 * r, EPI_F32, a.M));
     DCOCO_TRY(gemm_group(&a.g[1], static_cast<const char*>(w->W_pair) + d * D.esz, D, r, d, 2 * d, BN, s.hp + r,
                          2 * r, EPI_F32, a.M));
-    DCOCO_TRY(run_gemm(a, D, BN, st, "gemm W_pair h"));
+    DCOCO_TRY(run_gemm(a, D, BN, st, "gemm W_pair h", max_ctas));
   }
   // s_p = hp[p, 0:r] + hp[p+1, r:2r]
   {
@@ -681,29 +710,35 @@ int dcoco_cycle(const void* logits, int V, const void* emb, const void* h, const
   cudaStream_t st = as_stream(stream);
 
   const int rows = N * B;
-  // Everything that needs only h (pair states, W s, g, the g half of the fusion) runs on the
-  // helper stream while top-K streams the logits and the embedding rows are gathered.
   std::lock_guard<std::mutex> lock(g_side_mu);
   SideStream* side = nullptr;
   DCOCO_TRY(side_stream(&side));
-  cudaError_t e = cudaEventRecord(side->fork, st);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(side->stream, side->fork, 0);
-  if (e != cudaSuccess) return cuda_fail(e, "fork to helper stream");
-  DCOCO_TRY(enqueue_pair(D, h, w, s.wsp, s.pair, side->stream));
-  DCOCO_TRY(enqueue_repr_slot(D, h, w, s.repr, side->stream));
-  e = cudaEventRecord(side->join, side->stream);
-  if (e != cudaSuccess) return cuda_fail(e, "join from helper stream");
-
-  e = launch_topk(logits, D.bf16, rows, V, K, topk_split(rows, V, D.bf16), o_vals, o_ids, st);
+  cudaError_t e = launch_topk(logits, D.bf16, rows, V, K, topk_split(rows, V, D.bf16), o_vals, o_ids, st);
   if (e != cudaSuccess) return cuda_fail(e, "top-K launch");
+  // Top-K occupies every SM's registers, so the work that needs only h (pair states and W s on
+  // one helper stream; g and the g half of the fusion on another) starts after it, beside the
+  // embedding-row GEMM, with split-K grids sized to the SMs that GEMM leaves free (split-K
+  // clusters wider than two did not find room beside it).  z waits for the g branch; the pair
+  // branch is first needed by the U z / V z GEMM.
+  const int spare = std::max(12, sm_count() - gather_gemm_ctas(D));
+  const int pair_ctas = spare * 2 / 3, slot_ctas = spare - pair_ctas;
+  e = cudaEventRecord(side->fork, st);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(side->stream, side->fork, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(side->stream2, side->fork, 0);
+  if (e != cudaSuccess) return cuda_fail(e, "fork to helper streams");
+  DCOCO_TRY(enqueue_pair(D, h, w, s.wsp, s.pair, side->stream, pair_ctas));
+  DCOCO_TRY(enqueue_repr_slot(D, h, w, s.repr, side->stream2, slot_ctas));
+  e = cudaEventRecord(side->join, side->stream);
+  if (e == cudaSuccess) e = cudaEventRecord(side->join2, side->stream2);
+  if (e != cudaSuccess) return cuda_fail(e, "join from helper streams");
   DCOCO_TRY(enqueue_repr_gather(D, o_ids, emb, V, w, s.repr, st));
-  e = cudaStreamWaitEvent(st, side->join, 0);
-  if (e != cudaSuccess) return cuda_fail(e, "join from helper stream");
+  e = cudaStreamWaitEvent(st, side->join2, 0);
+  if (e != cudaSuccess) return cuda_fail(e, "join from helper streams");
   // From here on each kernel may launch while its predecessor finishes (programmatic
   // dependent launch); each waits for it before touching its data.
   PdlScope pdl;
   // uz/vz scratch holds the scorer's prepared operands P and Q here.
-  DCOCO_TRY(enqueue_repr_fuse(D, w, s.uz, s.vz, s.repr, st, o_vals, s.wsp));
+  DCOCO_TRY(enqueue_repr_fuse(D, w, s.uz, s.vz, s.repr, st, o_vals, s.wsp, side->join));
   DCOCO_TRY(enqueue_scores_prepped(D, s.uz, s.vz, o_vals, w, o_S, st));
   SelectVerifyArgs a = {};
   a.S = o_S;
