@@ -39,8 +39,10 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kU = 4;          // 16-byte vectors per lane per iteration
 constexpr int kMaxSplit = 8;
 constexpr int kMaxK = 64;
-constexpr int kCap = 1024;     // candidate buffer (keys)
-constexpr int kSusCap = 2048;  // lanes that may hold a candidate (per block)
+constexpr int kCap = 1024;     // candidate buffer (keys), kCap / kWarps per warp
+constexpr int kSusCap = 2048;  // lanes that may hold a candidate (per block), kSusCap / kWarps per warp
+constexpr int kCapW = kCap / kWarps;
+constexpr int kSusW = kSusCap / kWarps;
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
 template <bool kBf16>
@@ -123,44 +125,96 @@ __device__ __forceinline__ int count_greater(const uint64_t* list, int n, uint64
   return lo;
 }
 
-// Keep the K largest keys of s_buf[0, cnt) in s_keep[0, K) (descending; 0 where cnt < K).
-// Called by every thread of the block.  Small buffers rank every key against all others;
-// larger ones (up to kCap) are sorted in place with a bitonic network, padded with zeros.
-__device__ __forceinline__ void select_top(uint64_t* s_buf, int cnt, int K, uint64_t* s_keep) {
-  if (threadIdx.x < K) s_keep[threadIdx.x] = 0;
+// Merge the kWarps descending, 0-padded lists of K keys in s_wl[w * K ..] into the K largest,
+// s_keep[0, K) (descending; 0 where fewer exist): every key's rank is the sum of binary-search
+// counts over the lists.  Called by every thread of the block.
+__device__ __forceinline__ void merge_lists(const uint64_t* s_wl, int K, uint64_t* s_keep) {
+  for (int t = threadIdx.x; t < K; t += kThreads) s_keep[t] = 0;
   __syncthreads();
-  if (cnt <= 128) {
-    for (int c = threadIdx.x; c < cnt; c += kThreads) {
-      const uint64_t x = s_buf[c];
-      int above = 0;
-      for (int o = 0; o < cnt; ++o) above += (s_buf[o] > x);
-      if (above < K) s_keep[above] = x;
-    }
-    __syncthreads();
-    return;
+  for (int t = threadIdx.x; t < kWarps * K; t += kThreads) {
+    const uint64_t x = s_wl[t];
+    if (x == 0) continue;
+    int above = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) above += count_greater(s_wl + w * K, K, x);
+    if (above < K) s_keep[above] = x;
   }
-  int n = 256;
-  while (n < cnt) n <<= 1;
-  for (int i = cnt + threadIdx.x; i < n; i += kThreads) s_buf[i] = 0;
   __syncthreads();
-  for (int k = 2; k <= n; k <<= 1) {
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = threadIdx.x; i < n; i += kThreads) {
-        const int l = i ^ j;
-        if (l > i) {
-          const uint64_t a = s_buf[i], b = s_buf[l];
-          const bool desc = (i & k) == 0;  // descending blocks end up first: overall descending
-          if (desc ? (a < b) : (a > b)) {
-            s_buf[i] = b;
-            s_buf[l] = a;
-          }
-        }
-      }
-      __syncthreads();
+}
+
+// Keep the K largest keys of s_buf[0, cnt) (cnt <= kCap) in s_keep[0, K) (descending; 0 where
+// cnt < K).  Called by every thread of the block; s_wl ([kWarps * K]) is scratch and may be
+// s_buf itself.  Thread t holds candidates t, t + kThreads, ... in registers, so each warp owns
+// an eighth of them; a warp extracts its K largest one per round with two warp max reductions
+// (value word, then index word among equal values) and the lists are merged.
+__device__ __forceinline__ void select_top(const uint64_t* s_buf, int cnt, int K, uint64_t* s_wl, uint64_t* s_keep) {
+  constexpr int PER = kCap / kThreads;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint64_t e[PER];
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    const int c = static_cast<int>(threadIdx.x) + j * kThreads;
+    e[j] = c < cnt ? s_buf[c] : 0ull;
+  }
+  __syncthreads();  // every candidate is in registers: s_wl (possibly s_buf) may be overwritten
+  auto lane_best = [&]() {
+    uint64_t b = e[0];
+#pragma unroll
+    for (int j = 1; j < PER; ++j) b = e[j] > b ? e[j] : b;
+    return b;
+  };
+  uint64_t b = lane_best();
+  for (int r = 0; r < K; ++r) {
+    const uint32_t hi = static_cast<uint32_t>(b >> 32), lo = static_cast<uint32_t>(b);
+    const uint32_t mhi = __reduce_max_sync(kFull, hi);
+    const uint32_t tie = __ballot_sync(kFull, hi == mhi);
+    uint32_t mlo = 0;
+    if (hi == mhi) mlo = __reduce_max_sync(tie, lo);
+    mlo = __shfl_sync(kFull, mlo, __ffs(tie) - 1);
+    const uint64_t win = (static_cast<uint64_t>(mhi) << 32) | mlo;  // 0 once the warp runs out
+    if (lane == 0) s_wl[warp * K + r] = win;
+    if (win != 0 && b == win) {  // keys are unique: exactly one lane holds the winner
+#pragma unroll
+      for (int j = 0; j < PER; ++j)
+        if (e[j] == win) e[j] = 0;
+      b = lane_best();
     }
   }
-  if (threadIdx.x < K) s_keep[threadIdx.x] = s_buf[threadIdx.x];
   __syncthreads();
+  merge_lists(s_wl, K, s_keep);
+}
+
+// The K largest of buf[0, cnt) (cnt <= kCapW) into out[0, K) (descending, 0-padded), by one warp:
+// lane l holds buf[l], buf[l + 32], ... in registers and each round extracts the largest key
+// with two warp max reductions (value word, then index word among equal values).
+__device__ __forceinline__ void warp_top(const uint64_t* buf, int cnt, int K, uint64_t* out, int lane) {
+  constexpr int PER = kCapW / 32;
+  uint64_t e[PER];
+#pragma unroll
+  for (int j = 0; j < PER; ++j) e[j] = lane + 32 * j < cnt ? buf[lane + 32 * j] : 0ull;
+  auto lane_best = [&]() {
+    uint64_t b = e[0];
+#pragma unroll
+    for (int j = 1; j < PER; ++j) b = e[j] > b ? e[j] : b;
+    return b;
+  };
+  uint64_t b = lane_best();
+  for (int r = 0; r < K; ++r) {
+    const uint32_t hi = static_cast<uint32_t>(b >> 32), lo = static_cast<uint32_t>(b);
+    const uint32_t mhi = __reduce_max_sync(kFull, hi);
+    const uint32_t tie = __ballot_sync(kFull, hi == mhi);
+    uint32_t mlo = 0;
+    if (hi == mhi) mlo = __reduce_max_sync(tie, lo);
+    mlo = __shfl_sync(kFull, mlo, __ffs(tie) - 1);
+    const uint64_t win = (static_cast<uint64_t>(mhi) << 32) | mlo;  // 0 once the candidates run out
+    if (lane == 0) out[r] = win;
+    if (win != 0 && b == win) {  // keys are unique: exactly one lane holds the winner
+#pragma unroll
+      for (int j = 0; j < PER; ++j)
+        if (e[j] == win) e[j] = 0;
+      b = lane_best();
+    }
+  }
 }
 
 // Exact fallback for rows the threshold cannot thin out: a descending top-K list per warp in
@@ -251,7 +305,7 @@ __device__ __noinline__ void exact_segment_topk(const Segment& g, int K, int ran
     if (idx < K) s_wl[warp * K + idx] = L.e[j];
   }
   __syncthreads();
-  select_top(s_wl, kWarps * K, K, s_keep);
+  select_top(s_wl, kWarps * K, K, s_wl, s_keep);
 }
 
 template <bool kBf16, int KW>
@@ -265,16 +319,14 @@ __global__ void __launch_bounds__(kThreads, 4) topk_kernel(const void* __restric
   __shared__ uint64_t s_cluster[kMaxSplit * kMaxK];
   __shared__ int s_sus[kSusCap];  // first vector index of lanes that may hold a candidate
   __shared__ uint64_t s_thr;
-  __shared__ int s_cnt, s_overflow, s_nsus;
+  __shared__ int s_overflow;
 
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int rank = blockIdx.x;  // == rank in the cluster (the cluster spans grid.x)
   const int64_t row = blockIdx.y;
   if (threadIdx.x == 0) {
-    s_cnt = 0;
     s_overflow = 0;
-    s_nsus = 0;
     s_thr = 0;
   }
 
@@ -344,6 +396,7 @@ __global__ void __launch_bounds__(kThreads, 4) topk_kernel(const void* __restric
 
   // Hot loop: one packed max over the lane's vectors and one compare per iteration.  A lane
   // that may hold a key above the threshold only records where its vectors are.
+  int nsus = 0;  // this warp's suspect lanes so far (warp-uniform)
   for (int it = 0; it < iters; ++it) {
     load(it + 2, c2);
     bool maybe = vidx(it, 0) < g.vend;
@@ -354,75 +407,77 @@ __global__ void __launch_bounds__(kThreads, 4) topk_kernel(const void* __restric
       maybe = !(__uint_as_float(vec_max_bits<kBf16>(mx)) < tval);
     }
     const uint32_t bal = __ballot_sync(kFull, maybe);
-    if (bal) {
-      int base = 0;
-      if (lane == 0) base = atomicAdd(&s_nsus, __popc(bal));
-      base = __shfl_sync(kFull, base, 0);
-      if (maybe) {
-        const int pos = base + __popc(bal & ((1u << lane) - 1));
-        if (pos < kSusCap)
-          s_sus[pos] = vidx(it, 0);
-        else
-          s_overflow = 1;
-      }
+    if (maybe) {
+      const int pos = nsus + __popc(bal & ((1u << lane) - 1));
+      if (pos < kSusW) s_sus[warp * kSusW + pos] = vidx(it, 0);
     }
+    nsus += __popc(bal);
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
       c0[u] = c1[u];
       c1[u] = c2[u];
     }
   }
-  __syncthreads();
-  // Key every element of the suspect lanes' vectors; keep the keys above the threshold.
-  if (!s_overflow) {
-    const int ns = min(s_nsus, kSusCap);
-    for (int j = threadIdx.x; j < ns; j += kThreads) {
-      const int vi0 = s_sus[j];
+
+  // Each warp, without waiting for the others: key every element of its suspect lanes'
+  // vectors, keep the keys above the threshold, and extract its K largest.  Warps that finish
+  // streaming early do this while the others still stream.
+  {
+    uint64_t* wbuf = s_buf + warp * kCapW;
+    int ncand = 0;  // warp-uniform
+    bool over = nsus > kSusW;
+    auto append = [&](bool keep, uint64_t key) {
+      const uint32_t b = __ballot_sync(kFull, keep);
+      if (keep) {
+        const int pos = ncand + __popc(b & ((1u << lane) - 1));
+        if (pos < kCapW) wbuf[pos] = key;
+      }
+      ncand += __popc(b);
+    };
+    if (!over) {
+      for (int j0 = 0; j0 < nsus; j0 += 32) {  // warp-uniform trip count
+        const int j = j0 + lane;
+        const int vi0 = j < nsus ? s_sus[warp * kSusW + j] : g.vend;
+        uint4 v[kU];
 #pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int vi = vi0 + u * 32;
-        if (vi >= g.vend) continue;
-        const uint4 v = ld_stream(g.vp + vi);
+        for (int u = 0; u < kU; ++u) v[u] = vi0 + u * 32 < g.vend ? ld_stream(g.vp + vi0 + u * 32) : neg_inf;
 #pragma unroll
-        for (int e = 0; e < EPV; ++e) {
-          const uint64_t key = make_key(elem_bits<kBf16>(v, e), g.head + vi * EPV + e);
-          if (key > thr) {
-            const int pos = atomicAdd(&s_cnt, 1);
-            if (pos < kCap)
-              s_buf[pos] = key;
-            else
-              s_overflow = 1;
+        for (int u = 0; u < kU; ++u) {
+          const int vi = vi0 + u * 32;
+#pragma unroll
+          for (int e = 0; e < EPV; ++e) {
+            const uint64_t key = make_key(elem_bits<kBf16>(v[u], e), g.head + vi * EPV + e);
+            append(vi < g.vend && key > thr, key);
           }
         }
       }
     }
-  }
-
-  // Unaligned head (rank 0) and tail (last rank) elements, one per lane of warp 0.
-  if (warp == 0) {
-    int idx = -1;
-    if (rank == 0 && lane < g.head) idx = lane;
-    if (rank == S - 1 && lane >= 16 && lane - 16 < g.tail) idx = g.head + g.nvec * EPV + (lane - 16);
-    const bool has = idx >= 0;
-    const uint32_t bal = __ballot_sync(kFull, has);
-    int start = 0;
-    if (lane == 0 && bal) start = atomicAdd(&s_cnt, __popc(bal));
-    start = __shfl_sync(kFull, start, 0);
-    if (has) {
-      const uint32_t bits = kBf16 ? static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(g.rowp)[idx]) << 16
-                                  : reinterpret_cast<const uint32_t*>(g.rowp)[idx];
-      const int pos = start + __popc(bal & ((1u << lane) - 1));
-      if (pos < kCap)
-        s_buf[pos] = make_key(bits, idx);
-      else
-        s_overflow = 1;
+    if (warp == 0) {
+      // Unaligned head (rank 0) and tail (last rank) elements, one per lane.
+      int idx = -1;
+      if (rank == 0 && lane < g.head) idx = lane;
+      if (rank == S - 1 && lane >= 16 && lane - 16 < g.tail) idx = g.head + g.nvec * EPV + (lane - 16);
+      uint64_t key = 0;
+      if (idx >= 0) {
+        const uint32_t bits = kBf16 ? static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(g.rowp)[idx]) << 16
+                                    : reinterpret_cast<const uint32_t*>(g.rowp)[idx];
+        key = make_key(bits, idx);
+      }
+      append(idx >= 0, key);
+    }
+    over = over || ncand > kCapW;
+    if (over) {
+      if (lane == 0) s_overflow = 1;
+    } else {
+      __syncwarp();
+      warp_top(wbuf, ncand, K, s_wl + warp * K, lane);
     }
   }
   __syncthreads();
   if (s_overflow)
     exact_segment_topk<kBf16, KW>(g, K, rank, S, s_wl, s_keep);
   else
-    select_top(s_buf, s_cnt, K, s_keep);
+    merge_lists(s_wl, K, s_keep);
 
   if (S > 1) {
     // Push this block's K keys into block 0 of the cluster; block 0 ranks every key among the
