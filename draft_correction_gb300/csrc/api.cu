@@ -304,7 +304,10 @@ int enqueue_repr_fuse(const Dims& D, const dcoco_weights* w, void* uz, void* vz,
     a.bias = s.gw;
     a.bias_div = D.K;
     a.ld_bias = r;
-    const int BN = pick_bn(r, false);
+    // narrower tiles while the grid would cover less than half of the SMs
+    int BN = pick_bn(r, false);
+    const int m_tiles = (M + 127) / 128;
+    while (BN > 64 && m_tiles * (r / BN) * 2 <= sm_count()) BN /= 2;
     DCOCO_TRY(gemm_group(&a.g[0], w->W_f, D, r, r, 2 * r, BN, s.z, r, EPI_SILU_BIAS, a.M));
     DCOCO_TRY(run_gemm(a, D, BN, st, "gemm z = SiLU(W_f [b; g])"));
   }
@@ -319,7 +322,9 @@ int enqueue_repr_fuse(const Dims& D, const dcoco_weights* w, void* uz, void* vz,
     a.M = M;
     a.K = r;
     a.n_groups = 2;
-    const int BN = pick_bn(H, false);
+    // 512-wide tiles when 256-wide ones would need more than one wave of CTAs
+    const int m_tiles = (M + 127) / 128;
+    const int BN = (H % 512 == 0 && m_tiles * (2 * H / 256) > sm_count()) ? 512 : pick_bn(H, false);
     const int epi = prep_vals != nullptr ? EPI_PREP : EPI_ACT;
     DCOCO_TRY(gemm_group(&a.g[0], w->U, D, H, r, r, BN, uz, H, epi, a.M));
     DCOCO_TRY(gemm_group(&a.g[1], w->V, D, H, r, r, BN, vz, H, epi, a.M));
