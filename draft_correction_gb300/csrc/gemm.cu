@@ -4,11 +4,12 @@
 // corrector is shared across slots and transitions, so each projection is one GEMM over
 // all streams' rows: C[m, n] = sum_k A[m, k] B[n, k] with B a weight stored out x in.
 //
-// Kernel shape (one 128-row x BN-column output tile per CTA, 6 warps):
-//   warp 0     TMA producer.  B tiles come from a 2-D tensor map; A tiles either from a
-//              2-D map (activations) or, for the candidate embeddings, as four-row TMA
-//              gathers (tile::gather4) of Emb[c] rows -- the embedding table is read
-//              straight into the swizzled operand layout, never copied to a dense matrix.
+// Kernel shape (one 128-row x BN-column output tile per CTA, 10 warps):
+//   warp 0     TMA producer.  B tiles come from a 2-D tensor map, and so do A tiles of
+//              activations.  For the candidate embeddings the epilogue warps gather the A
+//              rows Emb[c] themselves while the main loop runs (16-byte asynchronous copies
+//              straight into the swizzled operand layout) -- the embedding table is never
+//              copied to a dense matrix.
 //   warp 1     allocates tensor memory; lane 0 issues tcgen05.mma (bf16 -> kind::f16,
 //              f32 -> kind::tf32) into an fp32 accumulator of 128 lanes x BN columns and
 //              commits each stage back to the producer.
@@ -223,17 +224,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (gather && lane > 0 && nk > 0) {
-      // Meanwhile the other lanes pull each gathered row's K range into L2 as one contiguous
-      // request, so that the 128-byte pieces the gather reads come from L2.
-      const int esz = kBf16 ? 2 : 4;
-      const int k0 = kb0 * T::BK, k1 = min(args.K, (kb0 + nk) * T::BK);
-      for (int r = lane - 1; r < BM; r += 31)
-        if (m_tile * BM + r < args.M)
-          prefetch_l2_bulk(static_cast<const char*>(args.gather_base) +
-                               static_cast<size_t>(s_rows[r]) * args.gather_pitch_bytes + static_cast<size_t>(k0) * esz,
-                           static_cast<uint32_t>((k1 - k0) * esz));
-    }
     if (lane == 0) {
       for (int i = 0; i < nk; ++i) {
         const int s = i % stages;

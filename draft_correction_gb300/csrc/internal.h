@@ -59,10 +59,10 @@ struct GemmGroup {
 };
 
 struct GemmArgs {
-  CUtensorMap a_map;        // A [M, K] tiled (box {BK, 128}), or the gather table [rows, K] (box {BK, 1})
+  CUtensorMap a_map;        // A [M, K] tiled (box {BK, 128}); unused when the rows are gathered
   const int32_t* gather;    // non-null: A row m is table row gather[m]
   int gather_limit;         // rows of the gather table (ids outside [0, limit) are replaced by 0)
-  const void* gather_base;  // the gather table (for L2 prefetch of each gathered row's K range)
+  const void* gather_base;  // the gather table (rows are copied from here by the epilogue warps)
   int gather_pitch_bytes;
   int M, K;
   int n_groups;             // 1 or 2
@@ -76,7 +76,7 @@ struct GemmArgs {
 };
 
 // Encodes a 2-D tensor map over a row-major [rows, cols] matrix with the given row pitch (elements).
-// box_rows = 1 gives a gather4 map.
+// box_rows is the box height (1 for a table that is only gathered from).
 bool make_tmap(CUtensorMap* map, const void* base, bool is_bf16, uint64_t rows, uint64_t cols, uint64_t pitch_elems,
                uint32_t box_rows, const char** err);
 

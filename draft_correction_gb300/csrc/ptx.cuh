@@ -1,4 +1,4 @@
-// Thin inline-PTX wrappers for sm_103a: mbarriers, TMA (tiled and gather4), tcgen05
+// Thin inline-PTX wrappers for sm_103a: mbarriers, TMA (tiled), tcgen05
 // (TMEM allocation, MMA, commit, loads) and thread-block-cluster shared memory.
 //
 // Every wait here is bounded: it gives up after a fixed number of polls and reports
@@ -100,19 +100,6 @@ __device__ __forceinline__ float tanh_approx(float x) {
   float y;
   asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
-}
-// Four rows (y0..y3) of one 128-byte column block x, written as four consecutive 128-byte rows.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int x, int y0, int y1, int y2, int y3,
-                                            uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
-      "%5, %6}], [%7];" ::"r"(dst),
-      "l"(map), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
-      : "memory");
-}
-// Asynchronous prefetch of `bytes` (a multiple of 16) at a 16-byte aligned address into L2.
-__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
