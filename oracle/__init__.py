@@ -4,5 +4,5 @@ Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import this package.  The CUDA library never uses it.
 """
 from .dcoco import (LN_EPS, canonical, candidate_repr, cycle, layer_norm, pair_state,  # noqa: F401
-                    residual_draw, select, silu, topk, transition_scores, verify_greedy,
+                    residual_draw, select, select_discounted, silu, topk, transition_scores, verify_greedy,
                     verify_stochastic)

@@ -164,6 +164,40 @@ def select(S: np.ndarray, vals: np.ndarray, ids: np.ndarray) -> Tuple[np.ndarray
     return k, tokens
 
 
+def select_discounted(S: np.ndarray, vals: np.ndarray, ids: np.ndarray, lam: float
+                      ) -> Tuple[np.ndarray, np.ndarray]:
+    """Whole-path selection rules on the same score grid ([Review] "path choice and ablation",
+    Tab. 3): Global-Sum maximises the path's total score, the geometric discount weights later
+    slots down by lambda (0.75 on the page).  Both formulas were lost in extraction; the reading
+    taken here unifies them (lambda = 1 is Global-Sum):
+
+        maximise  l_0(k_0) + sum_{p=0}^{B-2} lambda^(p+1) S_p(k_p, k_{p+1})   over all K^B paths,
+
+    the weight lambda^i of slot i standing for the chance that its prefix survives.  Computed by
+    the max-sum recursion (Viterbi): V_0(a) = l_0(a), V_{p+1}(b) = max_a V_p(a) + lambda^(p+1)
+    S_p(a, b), each maximum taken by the lowest index among equal values, then backtracked from
+    the lowest maximiser of V_{B-1}.  Returns k [N,B] and the draft tokens [N,B].
+    Pinned by brute force over all paths, the zero-correction identity (per-slot argmax for any
+    lambda) and the small-lambda limit (the prefix-first greedy walk).
+    """
+    N, B, K = vals.shape
+    k = np.empty((N, B), dtype=np.int64)
+    for n in range(N):
+        V = canonical(vals[n, 0])
+        back = np.zeros((B, K), dtype=np.int64)
+        w = 1.0
+        for p in range(B - 1):
+            w *= lam
+            cand = V[:, None] + w * canonical(S[n, p])        # [a, b]
+            back[p + 1] = np.argmax(cand, axis=0)              # lowest a among equal values
+            V = cand[back[p + 1], np.arange(K)]
+        k[n, B - 1] = _argmax_first(V)
+        for p in range(B - 1, 0, -1):
+            k[n, p - 1] = back[p, k[n, p]]
+    tokens = np.take_along_axis(ids, k[:, :, None], axis=2)[:, :, 0]
+    return k, tokens
+
+
 def verify_greedy(draft: np.ndarray, t: np.ndarray) -> Dict[str, np.ndarray]:
     """Greedy verification ([Review] §3.1): slots are judged left to right, slot j is
     accepted while the draft equals the verifier's greedy token; the accept length A

@@ -109,6 +109,21 @@ def _residual_keeps_draft(q, u, exclude):
 
 
 ORIG_SELECT = od.select
+ORIG_SD = od.select_discounted
+
+
+def _sd_wrong_power(S, vals, ids, lam):
+    # weights lam^p instead of lam^(p+1): the first transition is not discounted
+    return ORIG_SD(S / lam, vals, ids, lam) if lam != 1.0 else ORIG_SD(S, vals, ids, lam)
+
+
+def _sd_first_slot_fixed(S, vals, ids, lam):
+    # keeps the drafter's top candidate at slot 0 instead of optimising it with the rest
+    v = np.array(vals, dtype=np.float64, copy=True)
+    top = np.argmax(v[:, 0, :], axis=1)
+    v[:, 0, :] = -1e9
+    v[np.arange(v.shape[0]), 0, top] = 0.0
+    return ORIG_SD(S, v, ids, lam)
 ORIG_VG = od.verify_greedy
 ORIG_VS = od.verify_stochastic
 ORIG_RD = od.residual_draw
@@ -130,6 +145,10 @@ CASES = [
     ("verify_greedy", _verify_greedy_commits_draft, pins.test_greedy_verify_closed_form),
     ("verify_stochastic", _verify_stochastic_non_strict, pins.test_stochastic_verify_hand_cases),
     ("residual_draw", _residual_keeps_draft, pins.test_stochastic_verify_hand_cases),
+    ("select_discounted", _sd_wrong_power,
+     lambda: [pins.test_discounted_path_matches_brute_force(i, 0.5) for i in range(10)]),
+    ("select_discounted", _sd_first_slot_fixed,
+     lambda: [pins.test_discounted_path_matches_brute_force(i, 1.0) for i in range(10)]),
 ]
 
 

@@ -314,6 +314,70 @@ def test_greedy_is_not_global_sum():
 
 
 # ---------------------------------------------------------------------------
+# Whole-path rules: Global-Sum (lambda = 1) and the geometric discount (lambda = 0.75)
+# ---------------------------------------------------------------------------
+
+
+def brute_discounted(S, vals, lam):
+    """Every path's score l_0(k_0) + sum_p lam^(p+1) S_p(k_p, k_{p+1}); the best one, ties broken
+    towards the lowest last index, then the lowest index before it, and so on."""
+    B, K = vals.shape
+    best, best_key = None, None
+    for path in itertools.product(range(K), repeat=B):
+        total = vals[0, path[0]] + sum(lam ** (p + 1) * S[p, path[p], path[p + 1]] for p in range(B - 1))
+        key = (total, tuple(-c for c in reversed(path)))
+        if best_key is None or key > best_key:
+            best, best_key = path, key
+    return list(best)
+
+
+@pytest.mark.parametrize("seed", range(10))
+@pytest.mark.parametrize("lam", [1.0, 0.75, 0.5])
+def test_discounted_path_matches_brute_force(seed, lam):
+    rng = np.random.default_rng(300 + seed)
+    B, K, N = int(rng.integers(2, 6)), int(rng.integers(1, 5)), 3
+    vals = rng.integers(-6, 7, (N, B, K)) * 0.5     # dyadic values: every total is exact
+    S = rng.integers(-6, 7, (N, B - 1, K, K)) * 0.5
+    ids = rng.integers(0, 1000, (N, B, K))
+    k, tokens = oracle.select_discounted(S, vals, ids, lam)
+    for n in range(N):
+        assert list(k[n]) == brute_discounted(S[n], vals[n], lam)
+        assert list(tokens[n]) == [ids[n, i, k[n, i]] for i in range(B)]
+
+
+@pytest.mark.parametrize("lam", [1.0, 0.75])
+def test_discounted_path_with_zero_correction_is_per_slot_argmax(lam):
+    rng = np.random.default_rng(21)
+    N, B, K = 4, 7, 5
+    vals = rng.normal(0, 1, (N, B, K))
+    S = np.broadcast_to(vals[:, 1:, None, :], (N, B - 1, K, K))
+    k, _ = oracle.select_discounted(S, vals, np.zeros((N, B, K), dtype=np.int64), lam)
+    np.testing.assert_array_equal(k, np.argmax(vals, axis=2))
+
+
+def test_discounted_path_small_lambda_is_the_greedy_walk():
+    """As lambda -> 0 the objective orders the slots lexicographically: the prefix-first walk."""
+    rng = np.random.default_rng(22)
+    N, B, K = 50, 5, 4
+    vals = rng.normal(0, 1, (N, B, K))
+    S = rng.normal(0, 1, (N, B - 1, K, K))
+    k_greedy, _ = oracle.select(S, vals, np.zeros((N, B, K), dtype=np.int64))
+    k_disc, _ = oracle.select_discounted(S, vals, np.zeros((N, B, K), dtype=np.int64), 1e-3)
+    np.testing.assert_array_equal(k_disc, k_greedy)
+
+
+def test_global_sum_trades_an_early_score_for_a_later_one():
+    """On the grid where the prefix-first walk keeps [0, 0, 0], the whole-path sum takes the
+    candidate that unlocks the large later score."""
+    vals = np.array([[1.0, 0.0], [0.0, 0.0], [0.0, 0.0]])
+    S = np.zeros((2, 2, 2))
+    S[0, 0] = [1.0, 0.9]
+    S[1, 1] = [5.0, 0.0]
+    k, _ = oracle.select_discounted(S[None], vals[None], np.zeros((1, 3, 2), dtype=np.int64), 1.0)
+    assert list(k[0]) == [0, 1, 0]
+
+
+# ---------------------------------------------------------------------------
 # The pages' worked example (B=4, K=3)
 # ---------------------------------------------------------------------------
 
