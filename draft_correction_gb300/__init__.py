@@ -51,6 +51,7 @@ _SIGNATURES = {
     "dcoco_pair_state_noalloc": ([_P, _WP, _I, _I, _P, _P], _I),
     "dcoco_score_transitions": ([_P, _P, _P, _P, _WP, _I, _I, _I, _P, _P], _I),
     "dcoco_select": ([_P, _P, _P, _I, _I, _I, _P, _P, _P], _I),
+    "dcoco_select_path": ([_P, _P, _P, _I, _I, _I, _I, ctypes.c_float, _P, _P, _P], _I),
     "dcoco_verify": ([_I, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P], _I),
     "dcoco_cycle_workspace_size": ([_WP, _I, _I, _I], _Z),
     "dcoco_cycle": ([_P, _I, _P, _P, _WP, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _Z,
@@ -225,6 +226,22 @@ def select(S, vals, ids):
     k_sel = _empty((N, B), torch.int32, vals)
     tokens = _empty((N, B), torch.int32, vals)
     _check(lib().dcoco_select(_ptr(S), _ptr(vals), _ptr(ids), N, B, K, _ptr(k_sel), _ptr(tokens), _stream()))
+    return k_sel, tokens
+
+
+PATH_GREEDY, PATH_DISCOUNTED = 0, 1
+
+
+def select_path(S, vals, ids, rule: str = "greedy", lam: float = 0.75):
+    """Path rules on the score grid: 'greedy' (the prefix-first walk), 'global_sum' (maximise the
+    whole path's score) or 'geometric' (slot i weighted by lam^i) -> k_sel, tokens."""
+    code, l = {"greedy": (PATH_GREEDY, 1.0), "global_sum": (PATH_DISCOUNTED, 1.0),
+               "geometric": (PATH_DISCOUNTED, lam)}[rule]
+    N, B, K = vals.shape
+    k_sel = _empty((N, B), torch.int32, vals)
+    tokens = _empty((N, B), torch.int32, vals)
+    _check(lib().dcoco_select_path(_ptr(S), _ptr(vals), _ptr(ids), N, B, K, code, float(l), _ptr(k_sel),
+                                   _ptr(tokens), _stream()))
     return k_sel, tokens
 
 

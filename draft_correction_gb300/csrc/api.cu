@@ -603,6 +603,36 @@ int dcoco_select(const float* S, const float* vals, const int32_t* ids, int N, i
   return DCOCO_OK;
 }
 
+int dcoco_select_path(const float* S, const float* vals, const int32_t* ids, int N, int B, int K, int rule,
+                      float lambda, int32_t* k_sel, int32_t* tokens, void* stream) {
+  clear_err();
+  if (rule != DCOCO_PATH_GREEDY && rule != DCOCO_PATH_DISCOUNTED) return fail(DCOCO_ERR_INVALID_ARG, "path rule %d", rule);
+  if (rule == DCOCO_PATH_DISCOUNTED && !(lambda > 0.f && lambda <= 1.f))
+    return fail(DCOCO_ERR_INVALID_ARG, "discount lambda=%g outside (0, 1]", static_cast<double>(lambda));
+  DCOCO_TRY(check_block(N, B, K));
+  DCOCO_TRY(check_ptr(S, "S"));
+  DCOCO_TRY(check_ptr(vals, "vals"));
+  DCOCO_TRY(check_ptr(ids, "ids"));
+  DCOCO_TRY(check_ptr(k_sel, "k_sel"));
+  DCOCO_TRY(check_ptr(tokens, "tokens"));
+  SelectVerifyArgs a = {};
+  a.S = S;
+  a.vals = vals;
+  a.ids = ids;
+  a.k_sel = k_sel;
+  a.tokens = tokens;
+  a.rule = rule;
+  a.lam = lambda;
+  a.mode = -1;
+  a.N = N;
+  a.B = B;
+  a.K = K;
+  a.V = 0;
+  const cudaError_t e = launch_select_verify(a, as_stream(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "select launch");
+  return DCOCO_OK;
+}
+
 static int check_verify(int mode, const int32_t* draft, const int32_t* t, const float* q, const float* u, int N, int B,
                         int V, int32_t* accept_len, int32_t* committed, int32_t* n_commit, bool need_draft) {
   if (mode != DCOCO_VERIFY_GREEDY && mode != DCOCO_VERIFY_STOCHASTIC)

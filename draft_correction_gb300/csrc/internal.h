@@ -115,6 +115,8 @@ struct SelectVerifyArgs {
   const int32_t* ids;
   int32_t* k_sel;
   int32_t* tokens;       // written by the walk, read by verification
+  int rule;              // 0 prefix-first greedy walk, 1 discounted max-sum over whole paths
+  float lam;             // rule 1: the discount (1 = Global-Sum)
   // verification (skipped when mode < 0)
   int mode;              // 0 greedy, 1 stochastic, -1 none
   const int32_t* draft;  // block to verify when there is no walk

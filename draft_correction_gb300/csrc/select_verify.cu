@@ -36,6 +36,7 @@ __device__ __forceinline__ int warp_argmax_ord(uint32_t a, uint32_t b, int lane)
   if (ba) return __ffs(ba) - 1;
   return 32 + __ffs(__ballot_sync(kFull, b == m)) - 1;
 }
+__device__ __forceinline__ float canon(float x) { return x != x ? -INFINITY : x; }  // NaN ranks lowest
 __device__ __forceinline__ int warp_argmax(const float* row, int K, int lane) {
   const uint32_t a = lane < K ? ord32(__float_as_uint(row[lane])) : 0u;
   const uint32_t b = lane + 32 < K ? ord32(__float_as_uint(row[lane + 32])) : 0u;
@@ -46,6 +47,8 @@ __global__ void __launch_bounds__(kThreads) select_verify_kernel(const SelectVer
   __shared__ uint32_t s_S[kStageFloats];  // order codes of the stream's scores
   __shared__ int32_t s_draft[kMaxB];
   __shared__ int32_t s_k[kMaxB];       // walk: chosen candidate per slot
+  __shared__ float s_V[64];            // whole-path rule: best path score ending at each candidate
+  __shared__ uint8_t s_back[kMaxB][64];  // whole-path rule: best predecessor of each candidate
   __shared__ int32_t s_t[kMaxB + 1];   // greedy verification: the verifier's tokens
   __shared__ int s_A;
   __shared__ double s_part[kThreads];
@@ -64,11 +67,60 @@ __global__ void __launch_bounds__(kThreads) select_verify_kernel(const SelectVer
     const size_t grid_floats = static_cast<size_t>(B - 1) * K * K;
     const float* Sn = a.S + static_cast<size_t>(n) * grid_floats;
     const bool staged = grid_floats <= static_cast<size_t>(kStageFloats);
+    const bool greedy = a.rule == 0;
     if (staged) {
-      for (size_t i = threadIdx.x; i < grid_floats; i += kThreads) s_S[i] = ord32(__float_as_uint(Sn[i]));
+      // greedy walk: order codes (argmax by integer max); whole-path rule: values, NaN as -inf
+      for (size_t i = threadIdx.x; i < grid_floats; i += kThreads)
+        s_S[i] = greedy ? ord32(__float_as_uint(Sn[i])) : __float_as_uint(canon(Sn[i]));
     }
     __syncthreads();
-    if (warp == 0) {
+    if (warp == 0 && !greedy) {
+      // Discounted max-sum over all paths (lambda = 1: Global-Sum): lane l owns candidates l and
+      // l + 32; V_{p+1}(b) = max_a V_p(a) + lambda^(p+1) S_p(a, b), lowest a among equal values.
+      float v0 = lane < K ? canon(a.vals[static_cast<size_t>(n) * B * K + lane]) : -INFINITY;
+      float v1 = lane + 32 < K ? canon(a.vals[static_cast<size_t>(n) * B * K + lane + 32]) : -INFINITY;
+      float w = 1.f;
+      for (int p = 0; p + 1 < B; ++p) {
+        w *= a.lam;
+        s_V[lane] = v0;
+        s_V[lane + 32] = v1;
+        __syncwarp();
+        const size_t base = static_cast<size_t>(p) * K * K;
+        float best[2] = {-INFINITY, -INFINITY};
+        int arg[2] = {0, 0};
+        for (int q = 0; q < K; ++q) {
+          const float vq = s_V[q];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int b = lane + 32 * h;
+            if (b < K) {
+              const float sv = staged ? __uint_as_float(s_S[base + static_cast<size_t>(q) * K + b])
+                                      : canon(Sn[base + static_cast<size_t>(q) * K + b]);
+              const float c = vq + w * sv;
+              if (c > best[h]) {
+                best[h] = c;
+                arg[h] = q;
+              }
+            }
+          }
+        }
+        if (lane < K) s_back[p + 1][lane] = static_cast<uint8_t>(arg[0]);
+        if (lane + 32 < K) s_back[p + 1][lane + 32] = static_cast<uint8_t>(arg[1]);
+        v0 = lane < K ? best[0] : -INFINITY;
+        v1 = lane + 32 < K ? best[1] : -INFINITY;
+        __syncwarp();
+      }
+      int k = warp_argmax_ord(lane < K ? ord32(__float_as_uint(v0)) : 0u, lane + 32 < K ? ord32(__float_as_uint(v1)) : 0u,
+                              lane);
+      if (lane == 0) {
+        s_k[B - 1] = k;
+        for (int p = B - 1; p > 0; --p) {
+          k = s_back[p][k];
+          s_k[p - 1] = k;
+        }
+      }
+      __syncwarp();
+    } else if (warp == 0) {
       // The chain of argmaxes touches only shared memory (and registers); the token ids of
       // the chosen candidates are looked up together afterwards.
       int k = warp_argmax(a.vals + static_cast<size_t>(n) * B * K, K, lane);
@@ -85,6 +137,8 @@ __global__ void __launch_bounds__(kThreads) select_verify_kernel(const SelectVer
         if (lane == 0) s_k[p + 1] = k;
       }
       __syncwarp();
+    }
+    if (warp == 0) {
       const int32_t* idn = a.ids + static_cast<size_t>(n) * B * K;
       for (int j = lane; j < B; j += 32) {
         const int kj = s_k[j];

@@ -174,6 +174,23 @@ int dcoco_score_transitions(const void* uz, const void* vz, const float* ws_pair
 int dcoco_select(const float* S, const float* vals, const int32_t* ids, int N, int B, int K, int32_t* k_sel,
                  int32_t* tokens, void* stream);
 
+/* Path rules for dcoco_select_path. */
+enum { DCOCO_PATH_GREEDY = 0, DCOCO_PATH_DISCOUNTED = 1 };
+
+/*
+ * Whole-path selection rules on the same score grid, for comparison with the prefix-first walk
+ * (review of arXiv 2610.12570, "path choice and ablation", Tab. 3: Global-Sum and a geometric
+ * discount with lambda = 0.75).  Both formulas were lost from the page; the reading implemented
+ * maximises, over all K^B paths,
+ *   vals[n,0,k_0] + sum_{p=0}^{B-2} lambda^(p+1) S[n,p,k_p,k_{p+1}]        (lambda = 1: Global-Sum)
+ * by the max-sum recursion in float32, each maximum taken by the lowest candidate index among
+ * equal values (NaN ranks lowest).  rule DCOCO_PATH_GREEDY is dcoco_select (lambda unused);
+ * DCOCO_PATH_DISCOUNTED needs 0 < lambda <= 1.  Outputs as for dcoco_select.  Errors:
+ * DCOCO_ERR_INVALID_ARG for an unknown rule, lambda outside (0, 1] or a bad shape or pointer.
+ */
+int dcoco_select_path(const float* S, const float* vals, const int32_t* ids, int N, int B, int K, int rule,
+                      float lambda, int32_t* k_sel, int32_t* tokens, void* stream);
+
 /*
  * a6. Verification of the corrected draft (review §3.1 and App. D).
  *  GREEDY: t [N, B+1] int32 verifier greedy tokens; slot j is accepted while

@@ -101,3 +101,12 @@ def test_verify_errors(L):
 def test_topk_split_knob(L):
     prev = L.dcoco_set_topk_split(3)
     assert L.dcoco_set_topk_split(prev) == 3
+
+
+def test_select_path_argument_errors(L):
+    fake = ctypes.c_void_p(0x10000)
+    rc = L.dcoco_select_path(fake, fake, fake, 1, 4, 3, 7, ctypes.c_float(1.0), fake, fake, None)
+    assert rc == 1 and b"path rule" in L.dcoco_last_error()
+    for lam in (0.0, -0.5, 1.5, float("nan")):
+        rc = L.dcoco_select_path(fake, fake, fake, 1, 4, 3, 1, ctypes.c_float(lam), fake, fake, None)
+        assert rc == 1 and b"lambda" in L.dcoco_last_error()

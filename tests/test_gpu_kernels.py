@@ -108,6 +108,60 @@ def test_select_matches_oracle(N, B, K):
     np.testing.assert_array_equal(tok.cpu().numpy(), rt)
 
 
+def _path_score(S, vals, path, lam):
+    return vals[0, path[0]] + sum(lam ** (p + 1) * S[p, path[p], path[p + 1]] for p in range(len(path) - 1))
+
+
+@pytest.mark.parametrize("lam", [1.0, 0.75, 0.5])
+@pytest.mark.parametrize("seed", range(4))
+def test_select_path_exact_on_dyadic_grids(seed, lam):
+    """Half-integer scores and power-of-two-friendly discounts make every path score exact in
+    float32 as well, so the GPU recursion must pick exactly the oracle's path (ties included)."""
+    rng = np.random.default_rng(500 + seed)
+    N, B, K = 40, int(rng.integers(2, 9)), int(rng.integers(1, 17))
+    vals = (rng.integers(-6, 7, (N, B, K)) * 0.5).astype(np.float32)
+    S = (rng.integers(-6, 7, (N, B - 1, K, K)) * 0.5).astype(np.float32)
+    ids = rng.integers(0, 10 ** 6, (N, B, K)).astype(np.int32)
+    rule = "global_sum" if lam == 1.0 else "geometric"
+    k, tok = dc.select_path(dc.to_device(S, "f32"), dc.to_device(vals, "f32"), dc.to_device(ids, "i32"), rule, lam)
+    rk, rt = oracle.select_discounted(S.astype(np.float64), vals.astype(np.float64), ids, lam)
+    np.testing.assert_array_equal(k.cpu().numpy(), rk)
+    np.testing.assert_array_equal(tok.cpu().numpy(), rt)
+
+
+@pytest.mark.parametrize("rule,lam", [("global_sum", 1.0), ("geometric", 0.75)])
+@pytest.mark.parametrize("N,B,K", [(32, 16, 16), (5, 64, 64), (3, 9, 33)])
+def test_select_path_matches_oracle(rule, lam, N, B, K):
+    """Continuous scores: where the float32 recursion picks another path than the float64 one,
+    that path must score within the float32 accumulation error of the optimum (with lambda < 1
+    the late slots weigh lambda^p, far below that error at B = 64, so many paths tie there)."""
+    rng = np.random.default_rng(N + B + K)
+    vals = rng.normal(0, 3, (N, B, K)).astype(np.float32)
+    S = rng.normal(0, 3, (N, B - 1, K, K)).astype(np.float32)
+    ids = rng.integers(0, 10 ** 6, (N, B, K)).astype(np.int32)
+    k, tok = dc.select_path(dc.to_device(S, "f32"), dc.to_device(vals, "f32"), dc.to_device(ids, "i32"), rule, lam)
+    k = k.cpu().numpy()
+    S64, v64 = S.astype(np.float64), vals.astype(np.float64)
+    rk, _ = oracle.select_discounted(S64, v64, ids, lam)
+    for n in range(N):
+        if (k[n] == rk[n]).all():
+            continue
+        best, got = _path_score(S64[n], v64[n], rk[n], lam), _path_score(S64[n], v64[n], k[n], lam)
+        assert got >= best - 1e-5 * (1.0 + abs(best)), (n, got, best)
+    np.testing.assert_array_equal(tok.cpu().numpy(), np.take_along_axis(ids, k[:, :, None], axis=2)[:, :, 0])
+
+
+def test_select_path_greedy_rule_is_the_walk():
+    rng = np.random.default_rng(9)
+    N, B, K = 20, 12, 8
+    vals = dc.to_device(rng.normal(0, 1, (N, B, K)).astype(np.float32), "f32")
+    S = dc.to_device(rng.normal(0, 1, (N, B - 1, K, K)).astype(np.float32), "f32")
+    ids = dc.to_device(rng.integers(0, 1000, (N, B, K)).astype(np.int32), "i32")
+    k1, t1 = dc.select(S, vals, ids)
+    k2, t2 = dc.select_path(S, vals, ids, "greedy")
+    assert torch.equal(k1, k2) and torch.equal(t1, t2)
+
+
 @pytest.mark.parametrize("N,B", [(1, 1), (50, 16), (7, 64), (9, 33)])
 def test_verify_greedy_matches_oracle(N, B):
     rng = np.random.default_rng(B)
