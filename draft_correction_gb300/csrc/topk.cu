@@ -56,6 +56,13 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
   return v;
 }
 
+// 32 bytes at a 32-byte aligned address, streamed (not kept in L1).
+__device__ __forceinline__ void ld_stream32(const uint4* p, uint4& a, uint4& b) {
+  asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
+               : "l"(p));
+}
+
 __device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
   uint32_t d;
   asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
@@ -188,6 +195,11 @@ __device__ __forceinline__ void select_top(const uint64_t* s_buf, int cnt, int K
 // lane l holds buf[l], buf[l + 32], ... in registers and each round extracts the largest key
 // with two warp max reductions (value word, then index word among equal values).
 __device__ __forceinline__ void warp_top(const uint64_t* buf, int cnt, int K, uint64_t* out, int lane) {
+  if (cnt <= 32) {  // the common case: one key per lane, one warp sort
+    const uint64_t x = warp_sort_desc(lane < cnt ? buf[lane] : 0ull, lane);
+    for (int r = lane; r < K; r += 32) out[r] = r < 32 ? (r == lane ? x : 0ull) : 0ull;
+    return;
+  }
   constexpr int PER = kCapW / 32;
   uint64_t e[PER];
 #pragma unroll
@@ -270,8 +282,8 @@ struct WarpTopK {
 
 struct Segment {
   const char* rowp;  // first element of the row
-  const uint4* vp;   // first 16-byte aligned vector of the row
-  int head, nvec, tail, vbeg, vend;
+  const uint4* vp;   // first 32-byte aligned vector of the row
+  int head, nvec, tail, vbeg, vend;  // nvec (the row's vectors) and every split point are even
 };
 
 template <bool kBf16, int KW>
@@ -333,16 +345,21 @@ __global__ void __launch_bounds__(kThreads, 4) topk_kernel(const void* __restric
   Segment g;
   const int64_t e0 = row * static_cast<int64_t>(V);
   g.rowp = static_cast<const char*>(logits) + e0 * (kBf16 ? 2 : 4);
-  g.head = static_cast<int>((EPV - (e0 % EPV)) % EPV);
+  // Elements before the first 32-byte boundary form the head, and the last odd vector plus the
+  // leftover elements the tail (each at most 15 elements), so that every lane can fetch its 64
+  // contiguous bytes with two 32-byte loads.
+  constexpr int ESZ = kBf16 ? 2 : 4;
+  g.head = static_cast<int>(((32 - (reinterpret_cast<uintptr_t>(g.rowp) & 31)) & 31) / ESZ);
   if (g.head > V) g.head = V;
-  g.nvec = (V - g.head) / EPV;
+  g.nvec = ((V - g.head) / EPV) & ~1;
   g.tail = V - g.head - g.nvec * EPV;
-  g.vp = reinterpret_cast<const uint4*>(g.rowp + static_cast<int64_t>(g.head) * (kBf16 ? 2 : 4));
-  g.vbeg = static_cast<int>(static_cast<int64_t>(rank) * g.nvec / S);
-  g.vend = static_cast<int>(static_cast<int64_t>(rank + 1) * g.nvec / S);
+  g.vp = reinterpret_cast<const uint4*>(g.rowp + static_cast<int64_t>(g.head) * ESZ);
+  g.vbeg = 2 * static_cast<int>(static_cast<int64_t>(rank) * (g.nvec / 2) / S);
+  g.vend = 2 * static_cast<int>(static_cast<int64_t>(rank + 1) * (g.nvec / 2) / S);
   constexpr int CH = kWarps * kU * 32;  // vectors per block iteration
   const int iters = (g.vend - g.vbeg + CH - 1) / CH;
-  auto vidx = [&](int it, int u) { return g.vbeg + it * CH + (warp * kU + u) * 32 + lane; };
+  // lane t of the block owns kU consecutive vectors (64 bytes) of every iteration
+  auto vidx = [&](int it, int u) { return g.vbeg + it * CH + static_cast<int>(threadIdx.x) * kU + u; };
 
   // Lanes past the end of the segment see -inf.
   const uint4 neg_inf = kBf16 ? make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u)
@@ -350,10 +367,13 @@ __global__ void __launch_bounds__(kThreads, 4) topk_kernel(const void* __restric
   // Three iterations of vectors in registers: the current one and two in flight.
   uint4 c0[kU], c1[kU], c2[kU];
   auto load = [&](int it, uint4(&v)[kU]) {
+    const int vi0 = vidx(it, 0);
+    if (it < iters && vi0 + kU <= g.vend) {
+      ld_stream32(g.vp + vi0, v[0], v[1]);
+      ld_stream32(g.vp + vi0 + 2, v[2], v[3]);
+    } else {
 #pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      const int vi = vidx(it, u);
-      v[u] = (it < iters && vi < g.vend) ? ld_stream(g.vp + vi) : neg_inf;
+      for (int u = 0; u < kU; ++u) v[u] = (it < iters && vi0 + u < g.vend) ? ld_stream(g.vp + vi0 + u) : neg_inf;
     }
   };
 
@@ -439,15 +459,23 @@ __global__ void __launch_bounds__(kThreads, 4) topk_kernel(const void* __restric
         const int j = j0 + lane;
         const int vi0 = j < nsus ? s_sus[warp * kSusW + j] : g.vend;
         uint4 v[kU];
+        if (vi0 + kU <= g.vend) {  // the lane's 64 contiguous bytes, one burst
+          ld_stream32(g.vp + vi0, v[0], v[1]);
+          ld_stream32(g.vp + vi0 + 2, v[2], v[3]);
+        } else {
 #pragma unroll
-        for (int u = 0; u < kU; ++u) v[u] = vi0 + u * 32 < g.vend ? ld_stream(g.vp + vi0 + u * 32) : neg_inf;
+          for (int u = 0; u < kU; ++u) v[u] = vi0 + u < g.vend ? ld_stream(g.vp + vi0 + u) : neg_inf;
+        }
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
-          const int vi = vi0 + u * 32;
+          const int vi = vi0 + u;
 #pragma unroll
           for (int e = 0; e < EPV; ++e) {
-            const uint64_t key = make_key(elem_bits<kBf16>(v[u], e), g.head + vi * EPV + e);
-            append(vi < g.vend && key > thr, key);
+            const uint32_t bits = elem_bits<kBf16>(v[u], e);
+            // only values reaching the threshold value can have a key above it
+            const bool reach = vi < g.vend && !(__uint_as_float(bits) < tval);
+            const uint64_t key = reach ? make_key(bits, g.head + vi * EPV + e) : 0ull;
+            append(reach && key > thr, key);
           }
         }
       }
