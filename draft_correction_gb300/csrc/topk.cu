@@ -119,6 +119,30 @@ __device__ __forceinline__ uint64_t warp_sort_desc(uint64_t x, int lane) {
   return x;
 }
 
+// Descending bitonic sort of 64 keys across a warp, two per lane: key i = lane + 32 h is x[h];
+// afterwards x[0] of lane r is the r-th largest.
+__device__ __forceinline__ void warp_sort64_desc(uint64_t (&x)[2], int lane) {
+#pragma unroll
+  for (int k = 2; k <= 64; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      if (j == 32) {  // partners in the same lane (k == 64: the larger goes to the lower index)
+        const uint64_t hi = x[0] > x[1] ? x[0] : x[1], lo = x[0] > x[1] ? x[1] : x[0];
+        x[0] = hi;
+        x[1] = lo;
+      } else {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int i = lane + 32 * h;
+          const uint64_t y = __shfl_xor_sync(kFull, x[h], j);
+          const bool keep_max = ((i & j) == 0) == ((i & k) == 0);
+          x[h] = keep_max ? (x[h] > y ? x[h] : y) : (x[h] < y ? x[h] : y);
+        }
+      }
+    }
+  }
+}
+
 // Number of entries greater than x in a descending list of n keys.
 __device__ __forceinline__ int count_greater(const uint64_t* list, int n, uint64_t x) {
   int lo = 0, hi = n;
@@ -198,6 +222,12 @@ __device__ __forceinline__ void warp_top(const uint64_t* buf, int cnt, int K, ui
   if (cnt <= 32) {  // the common case: one key per lane, one warp sort
     const uint64_t x = warp_sort_desc(lane < cnt ? buf[lane] : 0ull, lane);
     for (int r = lane; r < K; r += 32) out[r] = r < 32 ? (r == lane ? x : 0ull) : 0ull;
+    return;
+  }
+  if (cnt <= 64) {  // two keys per lane, one 64-key warp sort
+    uint64_t x[2] = {buf[lane], lane + 32 < cnt ? buf[lane + 32] : 0ull};
+    warp_sort64_desc(x, lane);
+    for (int r = lane; r < K; r += 32) out[r] = r < 32 ? x[0] : x[1];
     return;
   }
   constexpr int PER = kCapW / 32;
