@@ -244,7 +244,7 @@ def gpu_arm(args, cfg):
 
     stream = torch.cuda.current_stream()
     flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
-    flush_clean = torch.zeros(2 * L2_BYTES // 4, dtype=torch.int32, device=dev)
+    flush_clean = torch.zeros(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)  # float: no widening copy
 
     def flush_l2():
         # Writing a buffer larger than L2 evicts everything useful; reading a second one then
