@@ -5,4 +5,4 @@ Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 """
 from .dcoco import (LN_EPS, canonical, candidate_repr, cycle, layer_norm, pair_state,  # noqa: F401
                     residual_draw, select, select_discounted, silu, topk, transition_scores, verify_greedy,
-                    verify_stochastic)
+                    verify_speculative, verify_stochastic)

@@ -220,6 +220,22 @@ def verify_greedy(draft: np.ndarray, t: np.ndarray) -> Dict[str, np.ndarray]:
     return {"accept_len": acc, "committed": com, "n_commit": acc + 1}
 
 
+def _inverse_cdf(r: np.ndarray, u: float, fallback: int) -> Tuple[int, bool]:
+    """The smallest v (vocabulary order) whose running sum of the residual mass r exceeds u * R,
+    R = sum(r), and whether u * R lies within 1e-9 R of a step of that running sum (a draw that
+    another summation order may resolve differently).  R <= 0 returns `fallback`."""
+    cum = np.cumsum(r)
+    R = cum[-1]
+    if not R > 0.0:
+        return fallback, True
+    target = float(u) * R
+    v = int(np.searchsorted(cum, target, side="right"))
+    if v >= len(r):  # only reachable through rounding of u * R
+        v = int(np.flatnonzero(r > 0)[-1])
+    near = abs(cum[v] - target) <= 1e-9 * R or (v > 0 and abs(cum[v - 1] - target) <= 1e-9 * R)
+    return v, bool(near)
+
+
 def residual_draw(q: np.ndarray, u: float, exclude: int) -> Tuple[int, bool]:
     """Inverse-CDF draw from r(v) = q(v) 1[v != exclude] / R with R = sum_{v != exclude} q(v)
     ([Review] App. D; exclude = -1 draws from q itself).
@@ -232,16 +248,7 @@ def residual_draw(q: np.ndarray, u: float, exclude: int) -> Tuple[int, bool]:
     r = np.asarray(q, dtype=np.float64).copy()
     if exclude >= 0:
         r[exclude] = 0.0
-    cum = np.cumsum(r)
-    R = cum[-1]
-    if not R > 0.0:
-        return exclude, True
-    target = float(u) * R
-    v = int(np.searchsorted(cum, target, side="right"))
-    if v >= len(r):  # only reachable through rounding of u * R
-        v = int(np.flatnonzero(r > 0)[-1])
-    near = abs(cum[v] - target) <= 1e-9 * R or (v > 0 and abs(cum[v - 1] - target) <= 1e-9 * R)
-    return v, bool(near)
+    return _inverse_cdf(r, u, exclude)
 
 
 def verify_stochastic(draft: np.ndarray, q: np.ndarray, u: np.ndarray) -> Dict[str, np.ndarray]:
@@ -266,6 +273,40 @@ def verify_stochastic(draft: np.ndarray, q: np.ndarray, u: np.ndarray) -> Dict[s
             A += 1
         if A < B:
             v, nt = residual_draw(q[n, A], u[n, A, 1], int(draft[n, A]))
+        else:
+            v, nt = residual_draw(q[n, B], u[n, B, 1], -1)
+        com[n, A] = v
+        acc[n] = A
+        near[n] = nt
+    return {"accept_len": acc, "committed": com, "n_commit": acc + 1, "near_tie": near}
+
+
+def verify_speculative(draft: np.ndarray, p: np.ndarray, q: np.ndarray, u: np.ndarray) -> Dict[str, np.ndarray]:
+    """Speculative sampling with a general draft distribution ([Review] §3.1, the standard rule
+    that App. D specialises to a point mass): the draft token y_j was drawn from p_j; slot j is
+    accepted with probability min{1, q_j(y_j) / p_j(y_j)}, here iff u[j,0] p_j(y_j) < q_j(y_j)
+    (the product of two float32 values, exact in float64); at the first rejection the committed
+    token is drawn from the residual max(0, q_j - p_j) / R, R its total, by inverse CDF in
+    vocabulary order with u[j,1] (R <= 0 keeps the draft token); if all B slots are accepted the
+    bonus token is drawn from q_{B+1}.  A one-hot p_j at y_j gives exactly verify_stochastic.
+
+    draft [N,B], p [N,B,V], q [N,B+1,V], u [N,B+1,2] -> accept_len, committed, n_commit, near_tie.
+    """
+    N, B = draft.shape
+    acc = np.zeros(N, dtype=np.int64)
+    com = np.full((N, B + 1), -1, dtype=np.int64)
+    near = np.zeros(N, dtype=bool)
+    for n in range(N):
+        A = 0
+        while A < B:
+            y = int(draft[n, A])
+            if not float(u[n, A, 0]) * float(p[n, A, y]) < float(q[n, A, y]):
+                break
+            com[n, A] = y
+            A += 1
+        if A < B:
+            r = np.maximum(0.0, np.asarray(q[n, A], dtype=np.float64) - np.asarray(p[n, A], dtype=np.float64))
+            v, nt = _inverse_cdf(r, u[n, A, 1], int(draft[n, A]))
         else:
             v, nt = residual_draw(q[n, B], u[n, B, 1], -1)
         com[n, A] = v

@@ -127,6 +127,25 @@ def _sd_first_slot_fixed(S, vals, ids, lam):
 ORIG_VG = od.verify_greedy
 ORIG_VS = od.verify_stochastic
 ORIG_RD = od.residual_draw
+ORIG_VSP = od.verify_speculative
+
+
+def _vsp_ignores_p(draft, p, q, u):
+    # accepts on u < q(y), as if the draft were a point mass
+    return ORIG_VSP(draft, np.ones_like(np.asarray(p, dtype=np.float64)), q, u)
+
+
+def _vsp_unclamped_residual(draft, p, q, u):
+    # residual q - p without the clamp at zero: negative mass enters the draw
+    p = np.asarray(p, dtype=np.float64)
+    q = np.asarray(q, dtype=np.float64)
+    N, B = draft.shape
+    out = ORIG_VSP(draft, p, q, u)
+    for n in range(N):
+        A = int(out["accept_len"][n])
+        if A < B:
+            out["committed"][n, A] = od._inverse_cdf(q[n, A] - p[n, A], u[n, A, 1], int(draft[n, A]))[0]
+    return out
 
 CASES = [
     ("layer_norm", _unbiased_ln, pins.test_layer_norm_spike_closed_form),
@@ -145,6 +164,8 @@ CASES = [
     ("verify_greedy", _verify_greedy_commits_draft, pins.test_greedy_verify_closed_form),
     ("verify_stochastic", _verify_stochastic_non_strict, pins.test_stochastic_verify_hand_cases),
     ("residual_draw", _residual_keeps_draft, pins.test_stochastic_verify_hand_cases),
+    ("verify_speculative", _vsp_ignores_p, pins.test_speculative_hand_cases),
+    ("verify_speculative", _vsp_unclamped_residual, pins.test_speculative_hand_cases),
     ("select_discounted", _sd_wrong_power,
      lambda: [pins.test_discounted_path_matches_brute_force(i, 0.5) for i in range(10)]),
     ("select_discounted", _sd_first_slot_fixed,

@@ -515,6 +515,72 @@ def test_stochastic_verify_preserves_verifier_distribution():
 
 
 # ---------------------------------------------------------------------------
+# Speculative sampling with a general draft distribution
+# ---------------------------------------------------------------------------
+
+
+def _softmax_rows(x):
+    e = np.exp(x - x.max(axis=-1, keepdims=True))
+    return e / e.sum(axis=-1, keepdims=True)
+
+
+def test_speculative_hand_cases():
+    p = np.array([[[0.5, 0.5, 0.0, 0.0]]])            # B = 1, V = 4
+    q = np.array([[[0.25, 0.25, 0.25, 0.25], [0.1, 0.2, 0.3, 0.4]]])
+    draft = np.array([[0]])
+    # accept iff u0 * p(y) < q(y): 0.4 * 0.5 = 0.2 < 0.25; then the bonus from q_2 with u[1,1]
+    out = oracle.verify_speculative(draft, p, q, np.array([[[0.4, 0.0], [0.0, 0.75]]]))
+    assert out["accept_len"][0] == 1 and list(out["committed"][0]) == [0, 3]
+    # 0.5 * 0.5 = 0.25 is not below 0.25: reject; residual max(0, q - p) = [0, 0, .25, .25]
+    out = oracle.verify_speculative(draft, p, q, np.array([[[0.5, 0.5], [0.0, 0.0]]]))
+    assert out["accept_len"][0] == 0 and list(out["committed"][0]) == [3, -1]
+    out = oracle.verify_speculative(draft, p, q, np.array([[[0.9, 0.4], [0.0, 0.0]]]))
+    assert list(out["committed"][0]) == [2, -1]
+
+
+def test_speculative_point_mass_is_the_stochastic_rule():
+    rng = np.random.default_rng(31)
+    N, B, V = 40, 6, 50
+    q = _softmax_rows(rng.normal(0, 2, (N, B + 1, V)))
+    draft = rng.integers(0, V, (N, B))
+    u = rng.random((N, B + 1, 2))
+    p = np.zeros((N, B, V))
+    np.put_along_axis(p, draft[:, :, None], 1.0, axis=2)
+    a = oracle.verify_speculative(draft, p, q, u)
+    b = oracle.verify_stochastic(draft, q, u)
+    for k in ("accept_len", "committed", "n_commit"):
+        np.testing.assert_array_equal(a[k], b[k])
+
+
+def test_speculative_equal_distributions_accept_everything():
+    rng = np.random.default_rng(32)
+    N, B, V = 30, 5, 40
+    q = _softmax_rows(rng.normal(0, 1, (N, B + 1, V)))
+    draft = np.array([[rng.choice(V, p=q[n, j]) for j in range(B)] for n in range(N)])
+    out = oracle.verify_speculative(draft, q[:, :B], q, rng.random((N, B + 1, 2)))
+    assert (out["accept_len"] == B).all()
+
+
+def test_speculative_preserves_target_distribution():
+    """Drafts drawn from p, verified against q: the committed first token is distributed as q."""
+    from scipy.stats import chi2
+    V, T = 6, 60000
+    p1 = np.array([0.3, 0.05, 0.25, 0.1, 0.2, 0.1])
+    q1 = np.array([0.05, 0.3, 0.1, 0.25, 0.2, 0.1])
+    rng = np.random.default_rng(2025)
+    draft = rng.choice(V, size=(T, 1), p=p1)
+    p = np.broadcast_to(p1, (T, 1, V))
+    q = np.broadcast_to(np.stack([q1, q1]), (T, 2, V))
+    out = oracle.verify_speculative(draft, p, q, rng.random((T, 2, 2)))
+    counts = np.bincount(out["committed"][:, 0], minlength=V)
+    exp = q1 * T
+    assert chi2.sf(((counts - exp) ** 2 / exp).sum(), V - 1) > 1e-4, (counts, exp)
+    # the acceptance rate is sum_v min(p(v), q(v))
+    rate = np.minimum(p1, q1).sum()
+    assert abs((out["accept_len"] > 0).mean() - rate) < 4 * math.sqrt(0.25 / T)
+
+
+# ---------------------------------------------------------------------------
 # Synthetic verifier statistic
 # ---------------------------------------------------------------------------
 
