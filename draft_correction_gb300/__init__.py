@@ -53,6 +53,7 @@ _SIGNATURES = {
     "dcoco_select": ([_P, _P, _P, _I, _I, _I, _P, _P, _P], _I),
     "dcoco_select_path": ([_P, _P, _P, _I, _I, _I, _I, ctypes.c_float, _P, _P, _P], _I),
     "dcoco_verify": ([_I, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P], _I),
+    "dcoco_verify_speculative": ([_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P], _I),
     "dcoco_cycle_workspace_size": ([_WP, _I, _I, _I], _Z),
     "dcoco_cycle": ([_P, _I, _P, _P, _WP, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _Z,
                      _P], _I),
@@ -254,6 +255,19 @@ def verify(draft, t=None, q=None, u=None, mode: int = VERIFY_GREEDY):
                                                                                  device=draft.device)}
     _check(lib().dcoco_verify(mode, _ptr(draft), _ptr(t), _ptr(q), _ptr(u), N, B, V, _ptr(out["accept_len"]),
                               _ptr(out["committed"]), _ptr(out["n_commit"]), _ptr(out["near_tie"]), _stream()))
+    return out
+
+
+def verify_speculative(draft, p, q, u):
+    """Speculative sampling with a draft distribution p [N, B, V]: q [N, B+1, V], u [N, B+1, 2]."""
+    N, B = draft.shape
+    V = q.shape[2]
+    out = {"accept_len": _empty((N,), torch.int32, draft), "committed": _empty((N, B + 1), torch.int32, draft),
+           "n_commit": _empty((N,), torch.int32, draft), "near_tie": torch.zeros((N,), dtype=torch.int32,
+                                                                                 device=draft.device)}
+    _check(lib().dcoco_verify_speculative(_ptr(draft), _ptr(p), _ptr(q), _ptr(u), N, B, V, _ptr(out["accept_len"]),
+                                          _ptr(out["committed"]), _ptr(out["n_commit"]), _ptr(out["near_tie"]),
+                                          _stream()))
     return out
 
 

@@ -675,6 +675,31 @@ int dcoco_verify(int mode, const int32_t* draft, const int32_t* t, const float* 
   return DCOCO_OK;
 }
 
+int dcoco_verify_speculative(const int32_t* draft, const float* p, const float* q, const float* u, int N, int B, int V,
+                             int32_t* accept_len, int32_t* committed, int32_t* n_commit, int32_t* near_tie,
+                             void* stream) {
+  clear_err();
+  DCOCO_TRY(check_verify(DCOCO_VERIFY_STOCHASTIC, draft, nullptr, q, u, N, B, V, accept_len, committed, n_commit, true));
+  DCOCO_TRY(check_ptr(p, "p"));
+  SelectVerifyArgs a = {};
+  a.mode = 2;
+  a.draft = draft;
+  a.p = p;
+  a.q = q;
+  a.u = u;
+  a.accept_len = accept_len;
+  a.committed = committed;
+  a.n_commit = n_commit;
+  a.near_tie = near_tie;
+  a.N = N;
+  a.B = B;
+  a.K = 1;
+  a.V = V;
+  const cudaError_t e = launch_select_verify(a, as_stream(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "verify launch");
+  return DCOCO_OK;
+}
+
 namespace {
 struct CycleScratch {
   float* vals;

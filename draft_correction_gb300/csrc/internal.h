@@ -118,10 +118,11 @@ struct SelectVerifyArgs {
   int rule;              // 0 prefix-first greedy walk, 1 discounted max-sum over whole paths
   float lam;             // rule 1: the discount (1 = Global-Sum)
   // verification (skipped when mode < 0)
-  int mode;              // 0 greedy, 1 stochastic, -1 none
+  int mode;              // 0 greedy, 1 stochastic (point mass), 2 speculative (draft distribution p), -1 none
   const int32_t* draft;  // block to verify when there is no walk
   const int32_t* t;
   const float* q;
+  const float* p;        // mode 2: [N, B, V] draft distribution
   const float* u;
   int32_t* accept_len;
   int32_t* committed;

@@ -172,7 +172,12 @@ __global__ void __launch_bounds__(kThreads) select_verify_kernel(const SelectVer
         } else {
           const float uq = a.u[(static_cast<size_t>(n) * (B + 1) + j) * 2];
           const float qy = (y >= 0 && y < V) ? a.q[(static_cast<size_t>(n) * (B + 1) + j) * V + y] : 0.f;
-          ok = uq < qy;
+          if (a.mode == 1) {
+            ok = uq < qy;
+          } else {  // general draft distribution: u p(y) < q(y), the product exact in float64
+            const float py = (y >= 0 && y < V) ? a.p[(static_cast<size_t>(n) * B + j) * V + y] : 0.f;
+            ok = static_cast<double>(uq) * static_cast<double>(py) < static_cast<double>(qy);
+          }
         }
       }
       acc_mask |= static_cast<uint64_t>(__ballot_sync(kFull, ok)) << base;
@@ -198,16 +203,22 @@ __global__ void __launch_bounds__(kThreads) select_verify_kernel(const SelectVer
   }
 
   // ------------------------------------------------------------------ stochastic draw
-  // Row A of q: the residual at the first rejected slot (excluding its draft token), or the
-  // bonus position B (nothing excluded) when every slot was accepted.
-  const int excl = A < B ? s_draft[A] : -1;
+  // Row A of q: the residual at the first rejected slot, or the bonus position B (q itself) when
+  // every slot was accepted.  Point-mass proposal: q without the draft token; general draft
+  // distribution: max(0, q - p), each difference exact in float64.
+  const int fallback = A < B ? s_draft[A] : -1;  // kept when there is no residual mass
+  const int excl = (A < B && a.mode == 1) ? s_draft[A] : -1;
   const float* row = a.q + (static_cast<size_t>(n) * (B + 1) + A) * V;
+  const float* prow = (A < B && a.mode == 2) ? a.p + (static_cast<size_t>(n) * B + A) * V : nullptr;
+  auto mass = [&](int v) -> double {
+    if (prow != nullptr) return fmax(0.0, static_cast<double>(row[v]) - static_cast<double>(prow[v]));
+    return v == excl ? 0.0 : static_cast<double>(row[v]);
+  };
   const double u1 = static_cast<double>(a.u[(static_cast<size_t>(n) * (B + 1) + A) * 2 + 1]);
   const int chunk = (V + kThreads - 1) / kThreads;
   const int c0 = min(V, static_cast<int>(threadIdx.x) * chunk), c1 = min(V, c0 + chunk);
   double part = 0.0;
-  for (int v = c0; v < c1; ++v)
-    if (v != excl) part += static_cast<double>(row[v]);
+  for (int v = c0; v < c1; ++v) part += mass(v);
   s_part[threadIdx.x] = part;
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -240,9 +251,10 @@ __global__ void __launch_bounds__(kThreads) select_verify_kernel(const SelectVer
     double run = 0.0, before = 0.0;
     int v_pick = c1 - 1;
     for (int v = c0; v < c1; ++v) {
-      if (v == excl) continue;
+      const double m = mass(v);
+      if (m == 0.0) continue;  // no mass: cannot be the crossing (the running sum is unchanged)
       before = run;
-      run += static_cast<double>(row[v]);
+      run += m;
       if (run > d) {
         v_pick = v;
         break;
@@ -253,12 +265,12 @@ __global__ void __launch_bounds__(kThreads) select_verify_kernel(const SelectVer
     com[A] = v_pick;
     if (a.near_tie) a.near_tie[n] = near ? 1 : 0;
   } else if (pick < 0 && threadIdx.x == 0) {
-    // R <= 0: no residual mass, the excluded token stays.  Otherwise the crossing was lost to
+    // R <= 0: no residual mass, the draft token stays.  Otherwise the crossing was lost to
     // rounding at the end of the row: the last token with mass.
-    int v = excl;
+    int v = fallback;
     if (R > 0.0) {
       for (int w = V - 1; w >= 0; --w)
-        if (w != excl && row[w] > 0.f) {
+        if (mass(w) > 0.0) {
           v = w;
           break;
         }

@@ -210,6 +210,21 @@ int dcoco_verify(int mode, const int32_t* draft, const int32_t* t, const float* 
                  int32_t* accept_len, int32_t* committed, int32_t* n_commit, int32_t* near_tie, void* stream);
 
 /*
+ * Speculative sampling with a general draft distribution (review §3.1: the standard rule that
+ * App. D specialises to the corrected draft's point mass).  draft [N, B] int32 are tokens drawn
+ * from p [N, B, V] f32; q [N, B+1, V] f32 and u [N, B+1, 2] f32 as for STOCHASTIC.  Slot j is
+ * accepted iff u[j,0] * p[j, draft[j]] < q[j, draft[j]] (float32 operands, product and
+ * comparison in float64); at the first rejection j the committed token is the smallest v whose
+ * running mass of max(0, q[j,v] - p[j,v]) (float64, vocabulary order) exceeds u[j,1] * R, R the
+ * total (R <= 0 keeps draft[j]); if all B are accepted the bonus token is drawn from q[B] as for
+ * STOCHASTIC.  A one-hot p at the draft token reproduces STOCHASTIC exactly.  Outputs and errors
+ * as for dcoco_verify.
+ */
+int dcoco_verify_speculative(const int32_t* draft, const float* p, const float* q, const float* u, int N, int B, int V,
+                             int32_t* accept_len, int32_t* committed, int32_t* n_commit, int32_t* near_tie,
+                             void* stream);
+
+/*
  * One whole correction cycle a1..a6: top-K, candidate representation, pair state,
  * transition scores, walk and verification, with intermediates in the workspace.  Inputs as
  * above; `t` (greedy) or `q`,`u` (stochastic) per `mode`.

@@ -110,3 +110,11 @@ def test_select_path_argument_errors(L):
     for lam in (0.0, -0.5, 1.5, float("nan")):
         rc = L.dcoco_select_path(fake, fake, fake, 1, 4, 3, 1, ctypes.c_float(lam), fake, fake, None)
         assert rc == 1 and b"lambda" in L.dcoco_last_error()
+
+
+def test_verify_speculative_argument_errors(L):
+    fake = ctypes.c_void_p(0x10000)
+    rc = L.dcoco_verify_speculative(fake, None, fake, fake, 2, 4, 10, fake, fake, fake, None, None)
+    assert rc == 1 and b"p is NULL" in L.dcoco_last_error()
+    rc = L.dcoco_verify_speculative(fake, fake, fake, fake, 2, 65, 10, fake, fake, fake, None, None)
+    assert rc == 1

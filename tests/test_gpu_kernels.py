@@ -174,6 +174,47 @@ def test_verify_greedy_matches_oracle(N, B):
         np.testing.assert_array_equal(out[k].cpu().numpy(), ref[k])
 
 
+def _softmax32(x):
+    x = x - x.max(axis=-1, keepdims=True)
+    e = np.exp(x)
+    return (e / e.sum(axis=-1, keepdims=True)).astype(np.float32)
+
+
+@pytest.mark.parametrize("N,B,V", [(64, 16, 1000), (8, 8, 151936), (16, 4, 5)])
+def test_verify_speculative_matches_oracle(N, B, V):
+    rng = np.random.default_rng(V + B)
+    p = _softmax32(rng.normal(0, 2, (N, B, V)))
+    q = _softmax32(rng.normal(0, 2, (N, B + 1, V)))
+    q[:, :B] = 0.5 * q[:, :B] + 0.5 * p        # overlap, so that drafts are often accepted
+    cum = np.cumsum(p.astype(np.float64), axis=2)           # drafts drawn from p by inverse CDF
+    draft = np.minimum((cum < rng.random((N, B, 1)) * cum[:, :, -1:]).sum(axis=2), V - 1).astype(np.int32)
+    u = rng.random((N, B + 1, 2)).astype(np.float32)
+    out = dc.verify_speculative(dc.to_device(draft, "i32"), dc.to_device(p, "f32"), dc.to_device(q, "f32"),
+                                dc.to_device(u, "f32"))
+    ref = oracle.verify_speculative(draft, p, q, u)
+    np.testing.assert_array_equal(out["accept_len"].cpu().numpy(), ref["accept_len"])
+    np.testing.assert_array_equal(out["n_commit"].cpu().numpy(), ref["n_commit"])
+    com, rcom, tie = out["committed"].cpu().numpy(), ref["committed"], ref["near_tie"]
+    for n in range(N):
+        if not tie[n]:
+            np.testing.assert_array_equal(com[n], rcom[n])
+
+
+def test_verify_speculative_point_mass_equals_stochastic():
+    rng = np.random.default_rng(77)
+    N, B, V = 32, 8, 3000
+    q = _softmax32(rng.normal(0, 2, (N, B + 1, V)))
+    draft = rng.integers(0, V, (N, B)).astype(np.int32)
+    u = rng.random((N, B + 1, 2)).astype(np.float32)
+    p = np.zeros((N, B, V), dtype=np.float32)
+    np.put_along_axis(p, draft[:, :, None].astype(np.int64), 1.0, axis=2)
+    d_draft, d_q, d_u = dc.to_device(draft, "i32"), dc.to_device(q, "f32"), dc.to_device(u, "f32")
+    a = dc.verify_speculative(d_draft, dc.to_device(p, "f32"), d_q, d_u)
+    b = dc.verify(d_draft, q=d_q, u=d_u, mode=dc.VERIFY_STOCHASTIC)
+    for k in ("accept_len", "committed", "n_commit"):
+        assert torch.equal(a[k], b[k]), k
+
+
 @pytest.mark.parametrize("N,B,V", [(64, 16, 1000), (8, 8, 151936), (16, 4, 5)])
 def test_verify_stochastic_matches_oracle(N, B, V):
     cfg = wl.HEADLINE.replace(N=N, B=B, V=V)
