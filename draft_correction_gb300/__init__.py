@@ -57,6 +57,10 @@ _SIGNATURES = {
     "dcoco_cycle_workspace_size": ([_WP, _I, _I, _I], _Z),
     "dcoco_cycle": ([_P, _I, _P, _P, _WP, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _Z,
                      _P], _I),
+    "dcoco_cycle_table": ([_P, _I, _P, _P, _WP, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                           _Z, _P], _I),
+    "dcoco_embedding_table_bytes": ([_WP, _I], _Z),
+    "dcoco_embedding_table": ([_P, _I, _WP, _P, _P], _I),
 }
 
 _lib = None
@@ -271,6 +275,14 @@ def verify_speculative(draft, p, q, u):
     return out
 
 
+def embedding_table(emb, w):
+    """b(v) = LN(W_e Emb[v]) for every token v: [V, r] in the activation dtype."""
+    V = emb.shape[0]
+    table = torch.empty((V, w.r), dtype=w.act_dtype, device=emb.device)
+    _check(lib().dcoco_embedding_table(_ptr(emb), V, w.ref, _ptr(table), _stream()))
+    return table
+
+
 class Cycle:
     """Preallocated outputs and workspace for repeated whole cycles (a1..a6) of one shape."""
 
@@ -287,9 +299,13 @@ class Cycle:
         self.ws_bytes = lib().dcoco_cycle_workspace_size(w.ref, N, B, K)
         self.ws = e((self.ws_bytes,), torch.uint8)
 
-    def run(self, logits, emb, h, mode=VERIFY_GREEDY, t=None, q=None, u=None):
+    def run(self, logits, emb, h, mode=VERIFY_GREEDY, t=None, q=None, u=None, table=None):
+        """One cycle.  With `table` (from embedding_table) the candidate rows come from it and
+        `emb` is not read."""
         o = self.out
-        _check(lib().dcoco_cycle(_ptr(logits), self.V, _ptr(emb), _ptr(h), self.w.ref, self.N, self.B, self.K, mode,
+        fn = lib().dcoco_cycle_table if table is not None else lib().dcoco_cycle
+        src = table if table is not None else emb
+        _check(fn(_ptr(logits), self.V, _ptr(src), _ptr(h), self.w.ref, self.N, self.B, self.K, mode,
                                  _ptr(t), _ptr(q), _ptr(u), _ptr(o.get("vals")), _ptr(o.get("ids")),
                                  _ptr(o.get("S")), _ptr(o.get("k_sel")), _ptr(o["tokens"]), _ptr(o["accept_len"]),
                                  _ptr(o["committed"]), _ptr(o["n_commit"]), _ptr(o["near_tie"]), _ptr(self.ws),

@@ -290,14 +290,25 @@ int enqueue_repr_gather(const Dims& D, const int32_t* ids, const void* emb, int 
 // With prep_vals set, the U z / V z epilogue writes the scorer's operands instead:
 // uz <- (U z + b1 + W s + u_a l)/2 and vz <- (V z + u_b l)/2 (W s from prep_wsp).
 // before_uv, when set, is an event the U z / V z GEMM waits for (the producer of prep_wsp).
+// table, when set, replaces b: the A rows of the z GEMM are gathered as table[ids[m]] (V rows).
 int enqueue_repr_fuse(const Dims& D, const dcoco_weights* w, void* uz, void* vz, const ReprScratch& s,
                       cudaStream_t st, const float* prep_vals = nullptr, const float* prep_wsp = nullptr,
-                      cudaEvent_t before_uv = nullptr) {
+                      cudaEvent_t before_uv = nullptr, const void* table = nullptr, const int32_t* ids = nullptr,
+                      int V = 0) {
   const int M = D.M(), r = D.r, H = D.H;
   // z = SiLU(W_f[:, 0:r] b + gw[slot])
   {
     GemmArgs a = {};
-    DCOCO_TRY(a_map_tiled(a, s.b, D, M, r, r));
+    if (table != nullptr) {
+      const char* err = nullptr;
+      if (!make_tmap(&a.a_map, table, D.bf16, V, r, r, 1, &err)) return fail(DCOCO_ERR_CUDA, "%s", err);
+      a.gather = ids;
+      a.gather_limit = V;
+      a.gather_base = table;
+      a.gather_pitch_bytes = static_cast<int>(r * D.esz);
+    } else {
+      DCOCO_TRY(a_map_tiled(a, s.b, D, M, r, r));
+    }
     a.M = M;
     a.K = r;
     a.n_groups = 1;
@@ -736,17 +747,21 @@ size_t dcoco_cycle_workspace_size(const dcoco_weights* w, int N, int B, int K) {
   return c.used;
 }
 
-int dcoco_cycle(const void* logits, int V, const void* emb, const void* h, const dcoco_weights* w, int N, int B, int K,
-                int mode, const int32_t* t, const float* q, const float* u, float* vals, int32_t* ids, float* S,
-                int32_t* k_sel, int32_t* tokens, int32_t* accept_len, int32_t* committed, int32_t* n_commit,
-                int32_t* near_tie, void* workspace, size_t workspace_bytes, void* stream) {
-  clear_err();
+}  // extern "C"
+
+namespace {
+// One cycle; exactly one of emb (gathered and projected every cycle) and table (rows of
+// LN(W_e Emb) precomputed by dcoco_embedding_table) is set.
+int cycle_impl(const void* logits, int V, const void* emb, const void* table, const void* h, const dcoco_weights* w,
+               int N, int B, int K, int mode, const int32_t* t, const float* q, const float* u, float* vals,
+               int32_t* ids, float* S, int32_t* k_sel, int32_t* tokens, int32_t* accept_len, int32_t* committed,
+               int32_t* n_commit, int32_t* near_tie, void* workspace, size_t workspace_bytes, void* stream) {
   DCOCO_TRY(check_weights(w));
   DCOCO_TRY(check_block(N, B, K));
   if (V < K) return fail(DCOCO_ERR_INVALID_ARG, "V=%d < K=%d", V, K);
   if (static_cast<int64_t>(N) * B > 65535) return fail(DCOCO_ERR_UNSUPPORTED, "N*B > 65535");
   DCOCO_TRY(check_ptr(logits, "logits"));
-  DCOCO_TRY(check_ptr(emb, "emb"));
+  DCOCO_TRY(check_ptr(emb != nullptr ? emb : table, emb != nullptr ? "emb" : "table"));
   DCOCO_TRY(check_ptr(h, "h"));
   DCOCO_TRY(check_ptr(tokens, "tokens"));
   DCOCO_TRY(check_verify(mode, nullptr, t, q, u, N, B, V, accept_len, committed, n_commit, false));
@@ -780,7 +795,7 @@ int dcoco_cycle(const void* logits, int V, const void* emb, const void* h, const
   // embedding-row GEMM, with split-K grids sized to the SMs that GEMM leaves free (split-K
   // clusters wider than two did not find room beside it).  z waits for the g branch; the pair
   // branch is first needed by the U z / V z GEMM.
-  const int spare = std::max(12, sm_count() - gather_gemm_ctas(D));
+  const int spare = std::max(12, sm_count() - (table != nullptr ? 0 : gather_gemm_ctas(D)));
   const int pair_ctas = spare * 2 / 3, slot_ctas = spare - pair_ctas;
   e = cudaEventRecord(side->fork, st);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(side->stream, side->fork, 0);
@@ -791,14 +806,14 @@ int dcoco_cycle(const void* logits, int V, const void* emb, const void* h, const
   e = cudaEventRecord(side->join, side->stream);
   if (e == cudaSuccess) e = cudaEventRecord(side->join2, side->stream2);
   if (e != cudaSuccess) return cuda_fail(e, "join from helper streams");
-  DCOCO_TRY(enqueue_repr_gather(D, o_ids, emb, V, w, s.repr, st));
+  if (table == nullptr) DCOCO_TRY(enqueue_repr_gather(D, o_ids, emb, V, w, s.repr, st));
   e = cudaStreamWaitEvent(st, side->join2, 0);
   if (e != cudaSuccess) return cuda_fail(e, "join from helper streams");
   // From here on each kernel may launch while its predecessor finishes (programmatic
   // dependent launch); each waits for it before touching its data.
   PdlScope pdl;
   // uz/vz scratch holds the scorer's prepared operands P and Q here.
-  DCOCO_TRY(enqueue_repr_fuse(D, w, s.uz, s.vz, s.repr, st, o_vals, s.wsp, side->join));
+  DCOCO_TRY(enqueue_repr_fuse(D, w, s.uz, s.vz, s.repr, st, o_vals, s.wsp, side->join, table, o_ids, V));
   DCOCO_TRY(enqueue_scores_prepped(D, s.uz, s.vz, o_vals, w, o_S, st));
   SelectVerifyArgs a = {};
   a.S = o_S;
@@ -821,6 +836,53 @@ int dcoco_cycle(const void* logits, int V, const void* emb, const void* h, const
   e = launch_select_verify(a, st);
   if (e != cudaSuccess) return cuda_fail(e, "walk/verify launch");
   return DCOCO_OK;
+}
+}  // namespace
+
+extern "C" {
+
+int dcoco_cycle(const void* logits, int V, const void* emb, const void* h, const dcoco_weights* w, int N, int B, int K,
+                int mode, const int32_t* t, const float* q, const float* u, float* vals, int32_t* ids, float* S,
+                int32_t* k_sel, int32_t* tokens, int32_t* accept_len, int32_t* committed, int32_t* n_commit,
+                int32_t* near_tie, void* workspace, size_t workspace_bytes, void* stream) {
+  clear_err();
+  if (emb == nullptr) return fail(DCOCO_ERR_INVALID_ARG, "emb is NULL");
+  return cycle_impl(logits, V, emb, nullptr, h, w, N, B, K, mode, t, q, u, vals, ids, S, k_sel, tokens, accept_len,
+                    committed, n_commit, near_tie, workspace, workspace_bytes, stream);
+}
+
+int dcoco_cycle_table(const void* logits, int V, const void* table, const void* h, const dcoco_weights* w, int N,
+                      int B, int K, int mode, const int32_t* t, const float* q, const float* u, float* vals,
+                      int32_t* ids, float* S, int32_t* k_sel, int32_t* tokens, int32_t* accept_len,
+                      int32_t* committed, int32_t* n_commit, int32_t* near_tie, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+  clear_err();
+  if (table == nullptr) return fail(DCOCO_ERR_INVALID_ARG, "table is NULL");
+  return cycle_impl(logits, V, nullptr, table, h, w, N, B, K, mode, t, q, u, vals, ids, S, k_sel, tokens, accept_len,
+                    committed, n_commit, near_tie, workspace, workspace_bytes, stream);
+}
+
+size_t dcoco_embedding_table_bytes(const dcoco_weights* w, int V) {
+  if (w == nullptr || V < 1) return 0;
+  return static_cast<size_t>(V) * w->r * (w->dtype == DCOCO_BF16 ? 2 : 4);
+}
+
+int dcoco_embedding_table(const void* emb, int V, const dcoco_weights* w, void* table, void* stream) {
+  clear_err();
+  DCOCO_TRY(check_weights(w));
+  if (V < 1) return fail(DCOCO_ERR_INVALID_ARG, "V=%d", V);
+  DCOCO_TRY(check_ptr(emb, "emb"));
+  DCOCO_TRY(check_ptr(table, "table"));
+  const Dims D = dims_of(w, 1, 1, 1);
+  GemmArgs a = {};
+  DCOCO_TRY(a_map_tiled(a, emb, D, V, D.E, D.E));
+  a.M = V;
+  a.K = D.E;
+  a.n_groups = 1;
+  const int BN = pick_bn(D.r, true);
+  if (BN != D.r) return fail(DCOCO_ERR_UNSUPPORTED, "r=%d", D.r);
+  DCOCO_TRY(gemm_group(&a.g[0], w->W_e, D, D.r, D.E, D.E, BN, table, D.r, EPI_LN, a.M));
+  return run_gemm(a, D, BN, as_stream(stream), "gemm LN(W_e Emb) table");
 }
 
 }  // extern "C"

@@ -228,11 +228,11 @@ int dcoco_verify_speculative(const int32_t* draft, const float* p, const float* 
  * One whole correction cycle a1..a6: top-K, candidate representation, pair state,
  * transition scores, walk and verification, with intermediates in the workspace.  Inputs as
  * above; `t` (greedy) or `q`,`u` (stochastic) per `mode`.
- * The projections that need only h (pair states, W s, g and its fusion half) run on a
- * library-owned helper stream of the current device (created on the first call, highest
- * priority) that forks from and joins back into `stream` through events, so they overlap
- * top-K; the call can be captured into a CUDA graph after that first call.  Enqueueing is
- * serialised per process by a mutex.
+ * The projections that need only h (pair states and W s; g and its fusion half) run on two
+ * library-owned helper streams of the current device (created on the first call, highest
+ * priority) that fork from `stream` after top-K and join back into it through events, so they
+ * overlap the embedding-row projection; the call can be captured into a CUDA graph after that
+ * first call.  Enqueueing is serialised per process by a mutex.
  * Outputs (any may be NULL except tokens, accept_len, committed, n_commit):
  *   vals, ids [N,B,K]; S [N,B-1,K,K]; k_sel, tokens [N,B]; accept_len, n_commit [N];
  *   committed [N,B+1]; near_tie [N].
@@ -242,6 +242,22 @@ int dcoco_cycle(const void* logits, int V, const void* emb, const void* h, const
                 int mode, const int32_t* t, const float* q, const float* u, float* vals, int32_t* ids, float* S,
                 int32_t* k_sel, int32_t* tokens, int32_t* accept_len, int32_t* committed, int32_t* n_commit,
                 int32_t* near_tie, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Per-vocabulary candidate table (a builder-proposed variant; the pages have no counterpart):
+ * Emb and W_e are frozen at inference, so b(v) = LN(W_e Emb[v]) can be computed once for every
+ * token v.  table [V, r] in w->dtype (dcoco_embedding_table_bytes bytes), one tcgen05 GEMM with
+ * the LayerNorm epilogue over Emb [V, E].  dcoco_cycle_table is dcoco_cycle with the rows
+ * table[c] gathered in place of the per-cycle projection of Emb[c] (512 bytes instead of 2E per
+ * candidate); same outputs, workspace and errors.
+ */
+size_t dcoco_embedding_table_bytes(const dcoco_weights* w, int V);
+int dcoco_embedding_table(const void* emb, int V, const dcoco_weights* w, void* table, void* stream);
+int dcoco_cycle_table(const void* logits, int V, const void* table, const void* h, const dcoco_weights* w, int N,
+                      int B, int K, int mode, const int32_t* t, const float* q, const float* u, float* vals,
+                      int32_t* ids, float* S, int32_t* k_sel, int32_t* tokens, int32_t* accept_len,
+                      int32_t* committed, int32_t* n_commit, int32_t* near_tie, void* workspace,
+                      size_t workspace_bytes, void* stream);
 
 #ifdef __cplusplus
 }

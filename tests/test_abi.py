@@ -118,3 +118,11 @@ def test_verify_speculative_argument_errors(L):
     assert rc == 1 and b"p is NULL" in L.dcoco_last_error()
     rc = L.dcoco_verify_speculative(fake, fake, fake, fake, 2, 65, 10, fake, fake, fake, None, None)
     assert rc == 1
+
+
+def test_table_argument_errors(L):
+    fake = ctypes.c_void_p(0x10000)
+    w = dc._Weights(dc.DCOCO_BF16, 4096, 4096, 256, 512, *([0x20000] * len(dc.WEIGHT_FIELDS)))
+    assert L.dcoco_embedding_table_bytes(ctypes.byref(w), 151936) == 151936 * 256 * 2
+    assert L.dcoco_embedding_table(None, 10, ctypes.byref(w), fake, None) == 1
+    assert L.dcoco_embedding_table(fake, 10, ctypes.byref(w), None, None) == 1

@@ -33,7 +33,7 @@ def sample_streams(N):
     return list(range(N)) if N <= 4 else sorted({0, N // 2, N - 1})
 
 
-def run_cycle_and_compare(cfg, variant=None, logits=None, mode=dc.VERIFY_GREEDY):
+def run_cycle_and_compare(cfg, variant=None, logits=None, mode=dc.VERIFY_GREEDY, use_table=False):
     c = case(cfg, variant)
     logits = c["logits"] if logits is None else logits
     W = w64(c["w"], cfg)
@@ -65,8 +65,10 @@ def run_cycle_and_compare(cfg, variant=None, logits=None, mode=dc.VERIFY_GREEDY)
 
     w = dc.CorrectorWeights.from_numpy(c["w"], cfg.dtype)
     cyc = dc.Cycle(w, cfg.N, cfg.B, cfg.K, cfg.V)
-    out = cyc.run(dc.to_device(logits, cfg.dtype), dc.to_device(c["emb"], cfg.dtype), dc.to_device(c["h"], cfg.dtype),
-                  mode=mode, **extra)
+    emb = dc.to_device(c["emb"], cfg.dtype)
+    table = dc.embedding_table(emb, w) if use_table else None
+    out = cyc.run(dc.to_device(logits, cfg.dtype), emb, dc.to_device(c["h"], cfg.dtype), mode=mode, table=table,
+                  **extra)
     torch.cuda.synchronize()
     g = {k: v.cpu().numpy() for k, v in out.items()}
 
@@ -145,3 +147,30 @@ def test_cycle_sweep_points(n, b, k, mode):
 @pytest.mark.slow
 def test_cycle_large():
     run_cycle_and_compare(wl.LARGE)
+
+
+# ---------------------------------------------------------------------------
+# The per-vocabulary table variant (LN(W_e Emb) precomputed once)
+# ---------------------------------------------------------------------------
+
+
+@pytest.mark.parametrize("cfg", [wl.TINY, SMALL_BF16, SMALL_R256, SMALL_R512], ids=lambda c: c.name)
+def test_embedding_table_rows(cfg):
+    from helpers import assert_intermediate_close
+    c = case(cfg)
+    W = w64(c["w"], cfg)
+    w = dc.CorrectorWeights.from_numpy(c["w"], cfg.dtype)
+    table = dc.embedding_table(dc.to_device(c["emb"], cfg.dtype), w).float().cpu().numpy()
+    rows = np.unique(np.random.default_rng(0).integers(0, cfg.V, 300))
+    ref = oracle.layer_norm(f64(c["emb"][rows], cfg) @ W["W_e"].T)
+    assert_intermediate_close(table[rows], ref, "LN(W_e Emb) table")
+
+
+@pytest.mark.parametrize("cfg", [wl.TINY, SMALL_BF16, SMALL_R256, SMALL_R512], ids=lambda c: c.name)
+@pytest.mark.parametrize("variant", [None, "amplified"])
+def test_cycle_with_table(cfg, variant):
+    run_cycle_and_compare(cfg, variant, use_table=True)
+
+
+def test_cycle_with_table_headline():
+    run_cycle_and_compare(wl.HEADLINE, use_table=True)
