@@ -300,6 +300,26 @@ def gpu_arm(args, cfg):
     value = blocks / (total_ms / 1e3)
     assert dc.device_status() == 0, "device status word reports a fault"
 
+    # Variant: the per-vocabulary candidate table (LN(W_e Emb) computed once, outside the timed
+    # region, as a weight preprocessing step); the same cycle otherwise.  Reported beside the
+    # headline, which keeps the per-cycle projection of the gathered embedding rows.
+    variants = {}
+    if world == 1 and cfg.dtype == "bf16":
+        table = dc.embedding_table(emb, w)
+        for _ in range(2):
+            cyc.run(logits, emb, hidden, t=t_dev, table=table)
+        torch.cuda.synchronize()
+        graph_t = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_t):
+            cyc.run(logits, emb, hidden, t=t_dev, table=table)
+        torch.cuda.synchronize()
+        ms_t = timed_loop(graph_t.replay, args.steps, args.warmup)
+        variants["precomputed_embedding_table"] = {
+            "value": round(cfg.N * len(ms_t) / (sum(ms_t) / 1e3), 1), "unit": "blocks/s",
+            "ms_per_step": round(sum(ms_t) / len(ms_t), 4),
+            "note": "dcoco_cycle_table: rows of LN(W_e Emb), computed once per weights, gathered per cycle"}
+        del table
+
     # Per-stage device times (same inputs, same launch configuration, L2 flushed).
     ids, vals = cyc.out["ids"], cyc.out["vals"]
     uz = torch.empty((cfg.N, cfg.B, cfg.K, cfg.H), dtype=w.act_dtype, device=dev)
@@ -372,7 +392,8 @@ def gpu_arm(args, cfg):
                         "d2h_bytes_per_step": d2h},
                 "gpu_launches": 11 * args.steps, "clocks": clk.summary(),
                 "stages_us": {k: round(v, 2) for k, v in stage_us.items()},
-                "step_ms_p10_p50_p90": [round(float(np.percentile(ms, q)), 4) for q in (10, 50, 90)]}
+                "step_ms_p10_p50_p90": [round(float(np.percentile(ms, q)), 4) for q in (10, 50, 90)],
+                "variants": variants}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()
