@@ -335,6 +335,17 @@ def gpu_arm(args, cfg):
     stages["score_transitions"] = lambda: dc.score_transitions(uzv[0], uzv[1], wsp, vals, w)
     stages["select"] = lambda: dc.select(S, vals, ids)
     stages["verify"] = lambda: dc.verify(cyc.out["tokens"], t=t_dev)
+    # the scope table's next rows at the same shape: whole-path rules and speculative sampling
+    stages["select_path_global_sum"] = lambda: dc.select_path(S, vals, ids, "global_sum")
+    stages["select_path_geometric"] = lambda: dc.select_path(S, vals, ids, "geometric", 0.75)
+    if rank == 0:
+        prng = np.random.default_rng(11)
+        spec_V = cfg.V
+        p_d = torch.softmax(torch.randn((cfg.N, cfg.B, spec_V), device=dev) * 2, dim=-1)
+        q_d = torch.softmax(torch.randn((cfg.N, cfg.B + 1, spec_V), device=dev) * 2, dim=-1)
+        u_d = torch.from_numpy(prng.random((cfg.N, cfg.B + 1, 2), dtype=np.float32)).to(dev)
+        draft_d = torch.multinomial(p_d.reshape(-1, spec_V), 1).reshape(cfg.N, cfg.B).to(torch.int32)
+        stages["verify_speculative"] = lambda: dc.verify_speculative(draft_d, p_d, q_d, u_d)
     del uz
     stage_us = {k: 1e3 * statistics.mean(timed_loop(fn, stage_steps, 2)) for k, fn in stages.items()}
 

@@ -11,10 +11,12 @@
 //              accepted prefix and the verifier's token at the first rejection.
 //  stochastic  the corrected draft is a point-mass proposal, so slot j is accepted with
 //              probability q_j(y_j) (u < q), and the first rejection draws from the residual
-//              q(v) 1[v != y_j] / (1 - q(y_j)) by inverse CDF in vocabulary order.  Running
-//              sums are in float64: each thread sums one contiguous chunk of the row, the
-//              chunk totals are prefixed in chunk order, and only the chunk holding the
-//              crossing is rescanned, with the same additions.
+//              q(v) 1[v != y_j] / (1 - q(y_j)) by inverse CDF in vocabulary order.
+//  speculative a general draft distribution p: accept iff u p(y) < q(y) (exact in float64),
+//              residual max(0, q - p).
+// Residual masses are summed exactly in 62-bit fixed point (integer additions, so the order
+// does not matter and float64 -- slow on this GPU -- is not needed): super-block sums with
+// coalesced loads, one warp's prefix over them, and one warp scan of the crossing super-block.
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -37,6 +39,53 @@ __device__ __forceinline__ int warp_argmax_ord(uint32_t a, uint32_t b, int lane)
   return 32 + __ffs(__ballot_sync(kFull, b == m)) - 1;
 }
 __device__ __forceinline__ float canon(float x) { return x != x ? -INFINITY : x; }  // NaN ranks lowest
+
+constexpr int kMaxSB = 1024;  // super-blocks of a vocabulary row in the residual draw
+constexpr int kDrawU = 8;     // loads per row in flight per lane while summing them
+
+// A probability as unsigned fixed point with 62 fractional bits (range [0, 4)): exact for every
+// float32 at or above 2^-38; smaller values round down (by less than 2^-62); NaN, negatives and
+// zero give 0; values of 4 or more saturate.
+__device__ __forceinline__ uint64_t to_fx(float x) {
+  if (!(x > 0.f)) return 0;
+  if (x >= 4.f) return ~0ull >> 1;
+  const uint32_t b = __float_as_uint(x);
+  const int e = static_cast<int>((b >> 23) & 0xFFu);
+  const uint64_t m = (b & 0x7FFFFFu) | (e != 0 ? 0x800000u : 0u);
+  const int sh = (e != 0 ? e : 1) - 150 + 62;  // x = m 2^(e-150); fixed = m 2^(e-150+62)
+  return sh >= 0 ? (m << sh) : (sh <= -64 ? 0ull : (m >> -sh));
+}
+// floor(R u) for u in [0, 1) given as float32 (exact: 64 x 24-bit product).
+__device__ __forceinline__ uint64_t mul_floor(uint64_t R, float u) {
+  if (!(u > 0.f)) return 0;
+  const uint32_t b = __float_as_uint(u);
+  const int e = static_cast<int>((b >> 23) & 0xFFu);
+  const uint64_t m = (b & 0x7FFFFFu) | (e != 0 ? 0x800000u : 0u);
+  const int s = 150 - (e != 0 ? e : 1);  // u = m 2^-s, s >= 24 for u < 1
+  const uint64_t lo = R * m, hi = __umul64hi(R, m);
+  if (s >= 128) return 0;
+  if (s >= 64) return hi >> (s - 64);
+  return (hi << (64 - s)) | (lo >> s);
+}
+__device__ __forceinline__ uint64_t warp_sum_u64(uint64_t x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, o);
+  return x;
+}
+__device__ __forceinline__ float warp_sum_f32(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, o);
+  return x;
+}
+// inclusive prefix sum across the warp
+__device__ __forceinline__ uint64_t warp_scan_u64(uint64_t x, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint64_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+    if (lane >= o) x += y;
+  }
+  return x;
+}
 __device__ __forceinline__ int warp_argmax(const float* row, int K, int lane) {
   const uint32_t a = lane < K ? ord32(__float_as_uint(row[lane])) : 0u;
   const uint32_t b = lane + 32 < K ? ord32(__float_as_uint(row[lane + 32])) : 0u;
@@ -47,14 +96,11 @@ __global__ void __launch_bounds__(kThreads) select_verify_kernel(const SelectVer
   __shared__ uint32_t s_S[kStageFloats];  // order codes of the stream's scores
   __shared__ int32_t s_draft[kMaxB];
   __shared__ int32_t s_k[kMaxB];       // walk: chosen candidate per slot
-  __shared__ float s_V[64];            // whole-path rule: best path score ending at each candidate
   __shared__ uint8_t s_back[kMaxB][64];  // whole-path rule: best predecessor of each candidate
   __shared__ int32_t s_t[kMaxB + 1];   // greedy verification: the verifier's tokens
   __shared__ int s_A;
-  __shared__ double s_part[kThreads];
-  __shared__ double s_pre[kThreads];
-  __shared__ int s_pick;
-  __shared__ double s_R, s_target;
+  __shared__ uint64_t s_sb[kMaxSB];       // residual mass of each super-block (fixed point)
+  __shared__ float s_fsum[kThreads / 32];
 
   const int n = blockIdx.x;
   const int B = a.B, K = a.K, V = a.V;
@@ -82,21 +128,31 @@ __global__ void __launch_bounds__(kThreads) select_verify_kernel(const SelectVer
       float w = 1.f;
       for (int p = 0; p + 1 < B; ++p) {
         w *= a.lam;
-        s_V[lane] = v0;
-        s_V[lane + 32] = v1;
-        __syncwarp();
         const size_t base = static_cast<size_t>(p) * K * K;
         float best[2] = {-INFINITY, -INFINITY};
         int arg[2] = {0, 0};
-        for (int q = 0; q < K; ++q) {
-          const float vq = s_V[q];
+        auto S_at = [&](int q, int b) -> float {
+          return staged ? __uint_as_float(s_S[base + static_cast<size_t>(q) * K + b])
+                        : canon(Sn[base + static_cast<size_t>(q) * K + b]);
+        };
+        if (K <= 32) {
+#pragma unroll 4
+          for (int q = 0; q < K; ++q) {
+            const float vq = __shfl_sync(kFull, v0, q);  // the best score ending at candidate q
+            const float c = vq + w * (lane < K ? S_at(q, lane) : 0.f);
+            if (c > best[0]) {
+              best[0] = c;
+              arg[0] = q;
+            }
+          }
+        } else {
+#pragma unroll 2
+          for (int q = 0; q < K; ++q) {
+            const float vq = __shfl_sync(kFull, q < 32 ? v0 : v1, q & 31);
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int b = lane + 32 * h;
-            if (b < K) {
-              const float sv = staged ? __uint_as_float(s_S[base + static_cast<size_t>(q) * K + b])
-                                      : canon(Sn[base + static_cast<size_t>(q) * K + b]);
-              const float c = vq + w * sv;
+            for (int h = 0; h < 2; ++h) {
+              const int b = lane + 32 * h;
+              const float c = vq + w * (b < K ? S_at(q, b) : 0.f);
               if (c > best[h]) {
                 best[h] = c;
                 arg[h] = q;
@@ -108,8 +164,8 @@ __global__ void __launch_bounds__(kThreads) select_verify_kernel(const SelectVer
         if (lane + 32 < K) s_back[p + 1][lane + 32] = static_cast<uint8_t>(arg[1]);
         v0 = lane < K ? best[0] : -INFINITY;
         v1 = lane + 32 < K ? best[1] : -INFINITY;
-        __syncwarp();
       }
+      __syncwarp();
       int k = warp_argmax_ord(lane < K ? ord32(__float_as_uint(v0)) : 0u, lane + 32 < K ? ord32(__float_as_uint(v1)) : 0u,
                               lane);
       if (lane == 0) {
@@ -205,78 +261,110 @@ __global__ void __launch_bounds__(kThreads) select_verify_kernel(const SelectVer
   // ------------------------------------------------------------------ stochastic draw
   // Row A of q: the residual at the first rejected slot, or the bonus position B (q itself) when
   // every slot was accepted.  Point-mass proposal: q without the draft token; general draft
-  // distribution: max(0, q - p), each difference exact in float64.
+  // distribution: max(0, q - p).  Masses are summed exactly in 62-bit fixed point (every
+  // probability at or above 2^-38 converts exactly, smaller ones round down by less than 2^-62),
+  // so any order of addition gives the same sums: coalesced super-block sums, one warp's prefix
+  // over them, then one warp scans the crossing super-block.
   const int fallback = A < B ? s_draft[A] : -1;  // kept when there is no residual mass
   const int excl = (A < B && a.mode == 1) ? s_draft[A] : -1;
   const float* row = a.q + (static_cast<size_t>(n) * (B + 1) + A) * V;
   const float* prow = (A < B && a.mode == 2) ? a.p + (static_cast<size_t>(n) * B + A) * V : nullptr;
-  auto mass = [&](int v) -> double {
-    if (prow != nullptr) return fmax(0.0, static_cast<double>(row[v]) - static_cast<double>(prow[v]));
-    return v == excl ? 0.0 : static_cast<double>(row[v]);
-  };
-  const double u1 = static_cast<double>(a.u[(static_cast<size_t>(n) * (B + 1) + A) * 2 + 1]);
-  const int chunk = (V + kThreads - 1) / kThreads;
-  const int c0 = min(V, static_cast<int>(threadIdx.x) * chunk), c1 = min(V, c0 + chunk);
-  double part = 0.0;
-  for (int v = c0; v < c1; ++v) part += mass(v);
-  s_part[threadIdx.x] = part;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    double run = 0.0;
-    for (int t = 0; t < kThreads; ++t) {
-      s_pre[t] = run;
-      run += s_part[t];
+  auto mass = [&](int v) -> uint64_t {
+    if (v >= V) return 0;
+    const uint64_t qq = to_fx(row[v]);
+    if (prow != nullptr) {
+      const uint64_t pp = to_fx(prow[v]);
+      return qq > pp ? qq - pp : 0;
     }
-    const double R = run, target = u1 * R;
-    int pick = -1;
-    if (R > 0.0) {
-      for (int t = 0; t < kThreads; ++t) {
-        if (s_part[t] > 0.0 && target - s_pre[t] < s_part[t]) {
-          pick = t;
-          break;
+    return v == excl ? 0 : qq;
+  };
+  const int sb_len = max(1024, (V + kMaxSB - 1) / kMaxSB + 31) & ~31;  // elements per super-block
+  const int nsb = (V + sb_len - 1) / sb_len;                             // <= kMaxSB
+  float fsum = 0.f;  // plain float total, to flag rows that are not probability vectors
+  for (int sb = warp; sb < nsb; sb += kThreads / 32) {
+    uint64_t acc = 0;
+    for (int k = 0; k < sb_len; k += 32 * kDrawU) {  // kDrawU loads of each row in flight per lane
+      float qv[kDrawU], pv[kDrawU];
+#pragma unroll
+      for (int i = 0; i < kDrawU; ++i) {
+        const int v = sb * sb_len + k + i * 32 + lane;
+        qv[i] = (k + i * 32 < sb_len && v < V) ? row[v] : 0.f;
+        pv[i] = (prow != nullptr && k + i * 32 < sb_len && v < V) ? prow[v] : 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < kDrawU; ++i) {
+        const int v = sb * sb_len + k + i * 32 + lane;
+        const uint64_t qq = to_fx(qv[i]);
+        uint64_t m;
+        if (prow != nullptr) {
+          const uint64_t pp = to_fx(pv[i]);
+          m = qq > pp ? qq - pp : 0;
+        } else {
+          m = v == excl ? 0 : qq;
         }
+        acc += m;
+        fsum += qv[i];
       }
     }
-    s_R = R;
-    s_target = target;
-    s_pick = pick;
+    acc = warp_sum_u64(acc);
+    if (lane == 0) s_sb[sb] = acc;
   }
+  fsum = warp_sum_f32(fsum);
+  if (lane == 0) s_fsum[warp] = fsum;
   __syncthreads();
-  const int pick = s_pick;
-  const double R = s_R, target = s_target;
-  if (pick >= 0 && static_cast<int>(threadIdx.x) == pick) {
-    // Rescan the crossing chunk with the same additions as its partial sum: a crossing exists
-    // because the chunk's full sum exceeds target - prefix.
-    const double d = target - s_pre[pick];
-    double run = 0.0, before = 0.0;
-    int v_pick = c1 - 1;
-    for (int v = c0; v < c1; ++v) {
-      const double m = mass(v);
-      if (m == 0.0) continue;  // no mass: cannot be the crossing (the running sum is unchanged)
-      before = run;
-      run += m;
-      if (run > d) {
-        v_pick = v;
+  if (warp == 0) {
+    // prefix over the super-blocks: lane l takes a contiguous run of them
+    const int per = (nsb + 31) / 32, s0 = min(nsb, lane * per), s1 = min(nsb, s0 + per);
+    uint64_t mine = 0;
+    for (int i = s0; i < s1; ++i) mine += s_sb[i];
+    const uint64_t incl = warp_scan_u64(mine, lane);
+    const uint64_t R = __shfl_sync(kFull, incl, 31);
+    float ftot = lane < kThreads / 32 ? s_fsum[lane] : 0.f;
+    ftot = warp_sum_f32(ftot);
+    const uint64_t T = mul_floor(R, a.u[(static_cast<size_t>(n) * (B + 1) + A) * 2 + 1]);
+    // the first super-block whose inclusive prefix exceeds T
+    uint64_t run = incl - mine;
+    int found = -1;
+    uint64_t found_base = 0;
+    for (int i = s0; i < s1 && R > 0; ++i) {
+      if (run + s_sb[i] > T) {
+        found = i;
+        found_base = run;
         break;
       }
+      run += s_sb[i];
     }
-    const double tol = 1e-9 * R;
-    const bool near = fabs(s_pre[pick] + run - target) <= tol || fabs(s_pre[pick] + before - target) <= tol;
-    com[A] = v_pick;
-    if (a.near_tie) a.near_tie[n] = near ? 1 : 0;
-  } else if (pick < 0 && threadIdx.x == 0) {
-    // R <= 0: no residual mass, the draft token stays.  Otherwise the crossing was lost to
-    // rounding at the end of the row: the last token with mass.
-    int v = fallback;
-    if (R > 0.0) {
-      for (int w = V - 1; w >= 0; --w)
-        if (mass(w) > 0.0) {
-          v = w;
+    const uint32_t has = __ballot_sync(kFull, found >= 0);
+    int v_pick = fallback;
+    bool near = true;
+    if (has) {
+      const int src = __ffs(has) - 1;
+      const int sb = __shfl_sync(kFull, found, src);
+      uint64_t base = __shfl_sync(kFull, found_base, src);
+      const uint64_t tol = R >> 30;  // about 0.93e-9 R
+      for (int k = 0; k < sb_len; k += 32) {
+        const int v = sb * sb_len + k + lane;
+        const uint64_t m = mass(v);
+        const uint64_t in = warp_scan_u64(m, lane);
+        const uint32_t cross = __ballot_sync(kFull, m > 0 && base + in > T);
+        if (cross) {
+          const int l = __ffs(cross) - 1;
+          const uint64_t after = base + __shfl_sync(kFull, in, l);
+          const uint64_t before = after - __shfl_sync(kFull, m, l);
+          v_pick = sb * sb_len + k + l;
+          near = (after - T <= tol) || (T >= before ? T - before <= tol : before - T <= tol);
           break;
         }
+        base += __shfl_sync(kFull, in, 31);
+      }
+      // residual mass below 2^-15 (relative truncation error above 1e-9) or rows that are not
+      // probability vectors (sums beyond the fixed-point range) are flagged, not trusted
+      if (R < (1ull << 47) || !(ftot < 3.5f)) near = true;
     }
-    com[A] = v;
-    if (a.near_tie) a.near_tie[n] = 1;
+    if (lane == 0) {
+      com[A] = v_pick;
+      if (a.near_tie) a.near_tie[n] = near ? 1 : 0;
+    }
   }
   if (threadIdx.x == 0) {
     a.accept_len[n] = A;

@@ -198,12 +198,15 @@ int dcoco_select_path(const float* S, const float* vals, const int32_t* ids, int
  *  STOCHASTIC (point-mass proposal): q [N, B+1, V] f32 verifier probabilities,
  *    u [N, B+1, 2] f32 uniforms in [0,1).  Slot j is accepted iff u[j,0] < q[j, draft[j]];
  *    at the first rejection j the committed token is the smallest v != draft[j] whose
- *    running residual mass (float64, vocabulary order) exceeds u[j,1] * R with
+ *    running residual mass (vocabulary order) exceeds u[j,1] * R with
  *    R = sum_{v != draft[j]} q[j, v]; if all B are accepted the bonus token is drawn the
- *    same way from q[B] (no exclusion) with u[B,1].  R <= 0 commits draft[j].
+ *    same way from q[B] (no exclusion) with u[B,1].  R <= 0 commits draft[j].  Masses are
+ *    summed exactly in 62-bit fixed point (probabilities below 2^-38 round down by less than
+ *    2^-62); rows of q must be probability vectors (summing to less than 3.5).
  *  Outputs: accept_len [N], committed [N, B+1] (-1 after the last committed token),
  *    n_commit [N] = accept_len + 1, all int32.  near_tie [N] int32 (may be NULL,
- *    stochastic only): 1 where u*R lay within 1e-9 R of a step of the running sum.
+ *    stochastic only): 1 where u*R lay within 2^-30 R (about 1e-9 R) of a step of the running
+ *    sum, where R < 2^-15 (truncation could matter), or where the row sums to 3.5 or more.
  *  Unused inputs of the other mode may be NULL.
  */
 int dcoco_verify(int mode, const int32_t* draft, const int32_t* t, const float* q, const float* u, int N, int B, int V,
@@ -215,7 +218,7 @@ int dcoco_verify(int mode, const int32_t* draft, const int32_t* t, const float* 
  * from p [N, B, V] f32; q [N, B+1, V] f32 and u [N, B+1, 2] f32 as for STOCHASTIC.  Slot j is
  * accepted iff u[j,0] * p[j, draft[j]] < q[j, draft[j]] (float32 operands, product and
  * comparison in float64); at the first rejection j the committed token is the smallest v whose
- * running mass of max(0, q[j,v] - p[j,v]) (float64, vocabulary order) exceeds u[j,1] * R, R the
+ * running mass of max(0, q[j,v] - p[j,v]) (exact fixed point, vocabulary order) exceeds u[j,1] * R, R the
  * total (R <= 0 keeps draft[j]); if all B are accepted the bonus token is drawn from q[B] as for
  * STOCHASTIC.  A one-hot p at the draft token reproduces STOCHASTIC exactly.  Outputs and errors
  * as for dcoco_verify.
