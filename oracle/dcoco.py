@@ -64,6 +64,28 @@ def topk(logits: np.ndarray, K: int) -> Tuple[np.ndarray, np.ndarray]:
     return np.take_along_axis(x, order, axis=-1), order.astype(np.int64)
 
 
+def lm_logits(h: np.ndarray, W_lm: np.ndarray) -> np.ndarray:
+    """The drafter's output projection: l[..., v] = sum_k h[..., k] W_lm[v, k].
+
+    [Blog] "Score neighboring candidates in parallel": the corrector reuses what the
+    drafter's own pass produced, and the logits l_i(k) it keeps are that pass's vocabulary
+    projection of the drafter's final hidden state at slot i.  W_lm is stored [V, d]
+    (one row per token).  Pinned by per-logit loops and one-hot rows in the tests.
+    """
+    h = np.asarray(h, dtype=np.float64)
+    W_lm = np.asarray(W_lm, dtype=np.float64)
+    return h @ W_lm.T
+
+
+def lm_head_topk(h: np.ndarray, W_lm: np.ndarray, K: int) -> Tuple[np.ndarray, np.ndarray]:
+    """Top-K of the drafter's logits computed from its hidden state: topk(lm_logits(h, W_lm)).
+
+    The plain definition of the fused LM-head/top-K kernel: the logits exist here in full,
+    in float64; the GPU never stores them.
+    """
+    return topk(lm_logits(h, W_lm), K)
+
+
 def layer_norm(x: np.ndarray, eps: float = LN_EPS) -> np.ndarray:
     """Non-affine layer normalisation over the last axis ([Review] §3.2: the embedding
     and hidden-state projections are normalised without affine parameters because
@@ -324,3 +346,11 @@ def cycle(logits: np.ndarray, emb: np.ndarray, h: np.ndarray, w: Dict[str, np.nd
     S = transition_scores(rep["z"], s, vals, w)
     k, tokens = select(S, vals, ids)
     return {"vals": vals, "ids": ids, "s": s, "S": S, "k": k, "tokens": tokens, **rep}
+
+
+def cycle_lm(h: np.ndarray, W_lm: np.ndarray, emb: np.ndarray, w: Dict[str, np.ndarray], K: int
+             ) -> Dict[str, np.ndarray]:
+    """One correction pass starting from the drafter's hidden state: its logits are
+    lm_logits(h, W_lm), then the same pass as ``cycle``.  The one hidden state h feeds both
+    the output projection and the corrector (g and the pair states)."""
+    return cycle(lm_logits(h, W_lm), emb, h, w, K)

@@ -147,6 +147,16 @@ def _vsp_unclamped_residual(draft, p, q, u):
             out["committed"][n, A] = od._inverse_cdf(q[n, A] - p[n, A], u[n, A, 1], int(draft[n, A]))[0]
     return out
 
+def _lm_transposed(h, W_lm):
+    return np.asarray(h, dtype=np.float64) @ np.asarray(W_lm, dtype=np.float64)
+
+
+def _lm_drops_last_unit(h, W_lm):
+    h = np.asarray(h, dtype=np.float64)
+    W_lm = np.asarray(W_lm, dtype=np.float64)
+    return h[..., :-1] @ W_lm[:, :-1].T
+
+
 CASES = [
     ("layer_norm", _unbiased_ln, pins.test_layer_norm_spike_closed_form),
     ("layer_norm", _eps_outside_ln, pins.test_layer_norm_spike_closed_form),
@@ -168,6 +178,8 @@ CASES = [
     ("verify_speculative", _vsp_unclamped_residual, pins.test_speculative_hand_cases),
     ("select_discounted", _sd_wrong_power,
      lambda: [pins.test_discounted_path_matches_brute_force(i, 0.5) for i in range(10)]),
+    ("lm_logits", _lm_transposed, lambda: [pins.test_lm_head_topk_matches_scalar_loops(i) for i in range(5)]),
+    ("lm_logits", _lm_drops_last_unit, lambda: [pins.test_lm_head_topk_matches_scalar_loops(i) for i in range(5)]),
     ("select_discounted", _sd_first_slot_fixed,
      lambda: [pins.test_discounted_path_matches_brute_force(i, 1.0) for i in range(10)]),
 ]

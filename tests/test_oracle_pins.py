@@ -80,6 +80,65 @@ def test_topk_batched_rows_independent():
 
 
 # ---------------------------------------------------------------------------
+# Drafter output projection + top-K: scalar loops, one-hot rows, ties
+# ---------------------------------------------------------------------------
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_lm_head_topk_matches_scalar_loops(seed):
+    """Each logit as an explicit scalar sum over the hidden units, then brute-force top-K.
+    Square shapes (V == d) catch a transposed projection; dyadic values keep every sum exact."""
+    rng = np.random.default_rng(100 + seed)
+    rows, d = int(rng.integers(1, 4)), int(rng.integers(2, 9))
+    V = d if seed % 2 == 0 else int(rng.integers(d + 1, 3 * d + 2))
+    K = int(rng.integers(1, V + 1))
+    h = rng.integers(-4, 5, (rows, d)) / 4.0
+    W = rng.integers(-4, 5, (V, d)) / 8.0
+    vals, ids = oracle.lm_head_topk(h, W, K)
+    for i in range(rows):
+        row = []
+        for v in range(V):
+            acc = 0.0
+            for k in range(d):
+                acc += float(h[i, k]) * float(W[v, k])
+            row.append(acc)
+        want = brute_topk(row, K)
+        assert list(ids[i]) == want
+        assert list(vals[i]) == [row[v] for v in want]
+
+
+def test_lm_head_topk_one_hot_rows_select_hidden_units():
+    """Row v of W_lm = c_v e_{pi(v)} (c_v > 0, V <= d) makes logit v = c_v h[pi(v)]: the
+    top-K follows the scaled hidden units through the permutation."""
+    rng = np.random.default_rng(7)
+    d, V, K = 12, 9, 4
+    pi = rng.permutation(d)[:V]
+    c = rng.integers(1, 4, V).astype(np.float64)
+    W = np.zeros((V, d))
+    W[np.arange(V), pi] = c
+    h = rng.integers(-8, 9, (2, d)).astype(np.float64)
+    vals, ids = oracle.lm_head_topk(h, W, K)
+    for i in range(2):
+        scaled = [c[v] * h[i, pi[v]] for v in range(V)]
+        assert list(ids[i]) == brute_topk(scaled, K)
+        assert list(vals[i]) == sorted(scaled, reverse=True)[:K]
+
+
+def test_lm_head_topk_duplicate_rows_tie_to_lower_id():
+    """Tokens with identical output rows have equal logits; the lower id ranks first."""
+    rng = np.random.default_rng(3)
+    base = rng.integers(-3, 4, (4, 6)).astype(np.float64)
+    W = np.concatenate([base, base[::-1]])   # ids 0..3 and 7..4 repeat the same rows
+    h = rng.integers(-3, 4, (1, 6)).astype(np.float64)
+    _, ids = oracle.lm_head_topk(h, W, 8)
+    logit = {v: float(h[0] @ W[v]) for v in range(8)}
+    assert list(ids[0]) == brute_topk([logit[v] for v in range(8)], 8)
+    for a, b in zip(ids[0][:-1], ids[0][1:]):
+        if logit[a] == logit[b]:
+            assert a < b
+
+
+# ---------------------------------------------------------------------------
 # LayerNorm and SiLU: closed forms and invariants
 # ---------------------------------------------------------------------------
 

@@ -36,6 +36,9 @@ def test_distributions():
     assert u.dtype == np.float32 and u.min() >= 0 and u.max() < 1
     q = wl.verifier_probs(cfg.replace(N=2, V=1000))
     np.testing.assert_allclose(q.sum(axis=2), 1.0, rtol=1e-5)
+    W = wl.to_f64(wl.lm_head(cfg), "bf16")
+    assert W.shape == (cfg.V, cfg.d)
+    assert abs(W.std() - 3.0 / np.sqrt(cfg.d)) < 0.002
 
 
 def test_grid_logits():

@@ -114,7 +114,7 @@ def scaled(cfg: Config, **kw) -> Config:
 # Seeded draws
 # ----------------------------------------------------------------------------
 
-TAG_LOGITS, TAG_HIDDEN, TAG_EMB, TAG_WEIGHTS, TAG_VERIFIER, TAG_PROBS = 1, 2, 3, 4, 5, 6
+TAG_LOGITS, TAG_HIDDEN, TAG_EMB, TAG_WEIGHTS, TAG_VERIFIER, TAG_PROBS, TAG_LM_HEAD = 1, 2, 3, 4, 5, 6, 7
 _CHUNK = 1 << 24
 
 
@@ -180,6 +180,15 @@ def hidden(cfg: Config) -> np.ndarray:
 def embedding(cfg: Config) -> np.ndarray:
     """Frozen token-embedding table, shape [V, E], ~N(0, emb_sigma^2)."""
     return _normal(cfg.base_seed, TAG_EMB, 0, (cfg.V, cfg.E), cfg.emb_sigma, cfg.dtype)
+
+
+def lm_head(cfg: Config) -> np.ndarray:
+    """Drafter output projection W_lm, shape [V, d], ~N(0, (logit_sigma / sqrt(d))^2).
+
+    With h ~ N(0, 1) this gives logits h . W_lm[v] ~ N(0, logit_sigma^2), the spread of the
+    stored-logit workloads (without their Zipf boost).
+    """
+    return _normal(cfg.base_seed, TAG_LM_HEAD, 0, (cfg.V, cfg.d), cfg.logit_sigma / np.sqrt(cfg.d), cfg.dtype)
 
 
 WEIGHT_NAMES = ("W_e", "W_h", "W_f", "W_pair", "U", "V", "W", "u_a", "u_b", "b1", "w2", "b2")
