@@ -59,6 +59,12 @@ _SIGNATURES = {
                      _P], _I),
     "dcoco_cycle_table": ([_P, _I, _P, _P, _WP, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                            _Z, _P], _I),
+    "dcoco_lm_head_topk_workspace_size": ([_I, _I, _I, _I, _I], _Z),
+    "dcoco_lm_head_topk": ([_P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _Z, _P], _I),
+    "dcoco_set_lm_cluster": ([_I], _I),
+    "dcoco_cycle_lm_workspace_size": ([_WP, _I, _I, _I, _I], _Z),
+    "dcoco_cycle_lm": ([_P, _I, _P, _P, _WP, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _Z,
+                        _P], _I),
     "dcoco_embedding_table_bytes": ([_WP, _I], _Z),
     "dcoco_embedding_table": ([_P, _I, _WP, _P, _P], _I),
 }
@@ -275,6 +281,26 @@ def verify_speculative(draft, p, q, u):
     return out
 
 
+def set_lm_cluster(ctas: int) -> int:
+    return lib().dcoco_set_lm_cluster(int(ctas))
+
+
+def lm_head_topk(h: torch.Tensor, W_lm: torch.Tensor, K: int, vals=None, ids=None, ws=None):
+    """Fused drafter output projection + top-K: h [N, B, d], W_lm [V, d] (same dtype) ->
+    vals [N, B, K] f32 (the fp32 logits), ids [N, B, K] i32; the logits are never stored."""
+    N, B, d = h.shape
+    V = W_lm.shape[0]
+    code = _dtype_code(h)
+    vals = _empty((N, B, K), torch.float32, h) if vals is None else vals
+    ids = _empty((N, B, K), torch.int32, h) if ids is None else ids
+    nbytes = lib().dcoco_lm_head_topk_workspace_size(code, N, B, V, K)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.empty((max(nbytes, 16),), dtype=torch.uint8, device=h.device)
+    _check(lib().dcoco_lm_head_topk(_ptr(h), _ptr(W_lm), code, N, B, d, V, K, _ptr(vals), _ptr(ids), _ptr(ws),
+                                    ws.numel(), _stream()))
+    return vals, ids
+
+
 def embedding_table(emb, w):
     """b(v) = LN(W_e Emb[v]) for every token v: [V, r] in the activation dtype."""
     V = emb.shape[0]
@@ -298,11 +324,24 @@ class Cycle:
                              "S": e((N, B - 1, K, K), torch.float32), "k_sel": e((N, B), torch.int32)})
         self.ws_bytes = lib().dcoco_cycle_workspace_size(w.ref, N, B, K)
         self.ws = e((self.ws_bytes,), torch.uint8)
+        self.ws_lm = None
 
-    def run(self, logits, emb, h, mode=VERIFY_GREEDY, t=None, q=None, u=None, table=None):
+    def run(self, logits, emb, h, mode=VERIFY_GREEDY, t=None, q=None, u=None, table=None, W_lm=None):
         """One cycle.  With `table` (from embedding_table) the candidate rows come from it and
-        `emb` is not read."""
+        `emb` is not read.  With `W_lm` [V, d] the logits are not an input: top-K is the fused
+        output projection of `h` (dcoco_cycle_lm) and `logits` is not read."""
         o = self.out
+        if W_lm is not None:
+            if self.ws_lm is None:
+                nbytes = lib().dcoco_cycle_lm_workspace_size(self.w.ref, self.N, self.B, self.K, self.V)
+                self.ws_lm = torch.empty((max(nbytes, 16),), dtype=torch.uint8, device=self.ws.device)
+            ws = self.ws_lm
+            _check(lib().dcoco_cycle_lm(_ptr(W_lm), self.V, _ptr(emb), _ptr(h), self.w.ref, self.N, self.B, self.K,
+                                        mode, _ptr(t), _ptr(q), _ptr(u), _ptr(o.get("vals")), _ptr(o.get("ids")),
+                                        _ptr(o.get("S")), _ptr(o.get("k_sel")), _ptr(o["tokens"]),
+                                        _ptr(o["accept_len"]), _ptr(o["committed"]), _ptr(o["n_commit"]),
+                                        _ptr(o["near_tie"]), _ptr(ws), ws.numel(), _stream()))
+            return o
         fn = lib().dcoco_cycle_table if table is not None else lib().dcoco_cycle
         src = table if table is not None else emb
         _check(fn(_ptr(logits), self.V, _ptr(src), _ptr(h), self.w.ref, self.N, self.B, self.K, mode,

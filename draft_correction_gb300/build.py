@@ -12,7 +12,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libdcoco.so")
-SOURCES = ("api.cu", "topk.cu", "gemm.cu", "score.cu", "select_verify.cu")
+SOURCES = ("api.cu", "topk.cu", "lm_topk.cu", "gemm.cu", "score.cu", "select_verify.cu")
 HEADERS = ("ptx.cuh", "internal.h")
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 

@@ -38,6 +38,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
 int g_topk_split = 0;  // 0 = automatic
+int g_lm_cluster = 0;  // 0 = automatic
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -487,6 +488,12 @@ int dcoco_set_topk_split(int ctas_per_row) {
   return prev;
 }
 
+int dcoco_set_lm_cluster(int ctas) {
+  const int prev = g_lm_cluster;
+  g_lm_cluster = (ctas == 1 || ctas == 2 || ctas == 4) ? ctas : 0;
+  return prev;
+}
+
 int dcoco_device_status(void* stream, uint32_t* bits) {
   clear_err();
   int rc;
@@ -517,6 +524,41 @@ int dcoco_topk(const void* logits, int dtype, int N, int B, int V, int K, float*
   const int rows = N * B;
   const cudaError_t e = launch_topk(logits, bf16, rows, V, K, topk_split(rows, V, bf16), vals, ids, as_stream(stream));
   if (e != cudaSuccess) return cuda_fail(e, "top-K launch");
+  return DCOCO_OK;
+}
+
+size_t dcoco_lm_head_topk_workspace_size(int dtype, int N, int B, int V, int K) {
+  if ((dtype != DCOCO_BF16 && dtype != DCOCO_F32) || N < 1 || B < 1 || V < 1 || K < 1 || K > 64 || K > V ||
+      static_cast<int64_t>(N) * B > 65535)
+    return 0;
+  return lm_topk_partial_bytes(dtype == DCOCO_BF16, N * B, V, K, g_lm_cluster);
+}
+
+int dcoco_lm_head_topk(const void* h, const void* W_lm, int dtype, int N, int B, int d, int V, int K, float* vals,
+                       int32_t* ids, void* workspace, size_t workspace_bytes, void* stream) {
+  clear_err();
+  if (dtype != DCOCO_BF16 && dtype != DCOCO_F32) return fail(DCOCO_ERR_UNSUPPORTED, "dtype %d", dtype);
+  if (N < 1 || B < 1 || V < 1 || K < 1 || K > 64 || K > V || d < 1)
+    return fail(DCOCO_ERR_INVALID_ARG, "shape N=%d B=%d d=%d V=%d K=%d (need 1<=K<=min(64,V))", N, B, d, V, K);
+  if (static_cast<int64_t>(N) * B > 65535) return fail(DCOCO_ERR_UNSUPPORTED, "N*B=%lld rows > 65535", (long long)N * B);
+  const bool bf16 = dtype == DCOCO_BF16;
+  if ((static_cast<size_t>(d) * (bf16 ? 2 : 4)) % 16 != 0)
+    return fail(DCOCO_ERR_INVALID_ARG, "d=%d: rows of h and W_lm must be a multiple of 16 bytes", d);
+  DCOCO_TRY(check_ptr(h, "h"));
+  DCOCO_TRY(check_ptr(W_lm, "W_lm"));
+  DCOCO_TRY(check_ptr(vals, "vals"));
+  DCOCO_TRY(check_ptr(ids, "ids"));
+  const size_t need = lm_topk_partial_bytes(bf16, N * B, V, K, g_lm_cluster);
+  if (need == 0) return fail(DCOCO_ERR_CUDA, "no launch plan for the fused LM-head top-K on this device");
+  if (workspace == nullptr || workspace_bytes < need)
+    return fail(DCOCO_ERR_WORKSPACE, "workspace %zu bytes < %zu required", workspace_bytes, need);
+  if (!aligned16(workspace)) return fail(DCOCO_ERR_INVALID_ARG, "workspace is not 16-byte aligned");
+  int rc;
+  unsigned int* status = status_word(&rc);
+  if (rc != DCOCO_OK) return rc;
+  const cudaError_t e = launch_lm_topk(h, W_lm, bf16, N * B, d, V, K, g_lm_cluster, vals, ids, workspace,
+                                       workspace_bytes, status, as_stream(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "LM-head top-K launch");
   return DCOCO_OK;
 }
 
@@ -752,15 +794,15 @@ size_t dcoco_cycle_workspace_size(const dcoco_weights* w, int N, int B, int K) {
 namespace {
 // One cycle; exactly one of emb (gathered and projected every cycle) and table (rows of
 // LN(W_e Emb) precomputed by dcoco_embedding_table) is set.
-int cycle_impl(const void* logits, int V, const void* emb, const void* table, const void* h, const dcoco_weights* w,
-               int N, int B, int K, int mode, const int32_t* t, const float* q, const float* u, float* vals,
+int cycle_impl(const void* logits, const void* W_lm, int V, const void* emb, const void* table, const void* h,
+               const dcoco_weights* w, int N, int B, int K, int mode, const int32_t* t, const float* q, const float* u, float* vals,
                int32_t* ids, float* S, int32_t* k_sel, int32_t* tokens, int32_t* accept_len, int32_t* committed,
                int32_t* n_commit, int32_t* near_tie, void* workspace, size_t workspace_bytes, void* stream) {
   DCOCO_TRY(check_weights(w));
   DCOCO_TRY(check_block(N, B, K));
   if (V < K) return fail(DCOCO_ERR_INVALID_ARG, "V=%d < K=%d", V, K);
   if (static_cast<int64_t>(N) * B > 65535) return fail(DCOCO_ERR_UNSUPPORTED, "N*B > 65535");
-  DCOCO_TRY(check_ptr(logits, "logits"));
+  DCOCO_TRY(check_ptr(W_lm != nullptr ? W_lm : logits, W_lm != nullptr ? "W_lm" : "logits"));
   DCOCO_TRY(check_ptr(emb != nullptr ? emb : table, emb != nullptr ? "emb" : "table"));
   DCOCO_TRY(check_ptr(h, "h"));
   DCOCO_TRY(check_ptr(tokens, "tokens"));
@@ -771,13 +813,22 @@ int cycle_impl(const void* logits, int V, const void* emb, const void* table, co
   if ((ids && !aligned16(ids)) || (k_sel && !aligned16(k_sel)))
     return fail(DCOCO_ERR_INVALID_ARG, "an optional output is not 16-byte aligned");
   const Dims D = dims_of(w, N, B, K);
-  const size_t need = dcoco_cycle_workspace_size(w, N, B, K);
+  const size_t base_need = dcoco_cycle_workspace_size(w, N, B, K);
+  size_t lm_bytes = 0;
+  if (W_lm != nullptr) {
+    if ((static_cast<size_t>(D.d) * D.esz) % 16 != 0)
+      return fail(DCOCO_ERR_INVALID_ARG, "d=%d: rows of h and W_lm must be a multiple of 16 bytes", D.d);
+    lm_bytes = lm_topk_partial_bytes(D.bf16, N * B, V, K, g_lm_cluster);
+    if (lm_bytes == 0) return fail(DCOCO_ERR_CUDA, "no launch plan for the fused LM-head top-K on this device");
+  }
+  const size_t need = base_need + round256(lm_bytes);
   if (workspace == nullptr || workspace_bytes < need)
     return fail(DCOCO_ERR_WORKSPACE, "workspace %zu bytes < %zu required", workspace_bytes, need);
   if (!aligned16(workspace)) return fail(DCOCO_ERR_INVALID_ARG, "workspace is not 16-byte aligned");
   Carve c(workspace);
   CycleScratch s;
   cycle_scratch(D, c, &s);
+  void* lm_partial = W_lm != nullptr ? c.take<void>(lm_bytes) : nullptr;
   float* o_vals = vals ? vals : s.vals;
   int32_t* o_ids = ids ? ids : s.ids;
   float* o_S = S ? S : s.S;
@@ -788,7 +839,15 @@ int cycle_impl(const void* logits, int V, const void* emb, const void* table, co
   std::lock_guard<std::mutex> lock(g_side_mu);
   SideStream* side = nullptr;
   DCOCO_TRY(side_stream(&side));
-  cudaError_t e = launch_topk(logits, D.bf16, rows, V, K, topk_split(rows, V, D.bf16), o_vals, o_ids, st);
+  cudaError_t e;
+  if (W_lm != nullptr) {
+    int rc;
+    unsigned int* status = status_word(&rc);
+    if (rc != DCOCO_OK) return rc;
+    e = launch_lm_topk(h, W_lm, D.bf16, rows, D.d, V, K, g_lm_cluster, o_vals, o_ids, lm_partial, lm_bytes, status, st);
+  } else {
+    e = launch_topk(logits, D.bf16, rows, V, K, topk_split(rows, V, D.bf16), o_vals, o_ids, st);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "top-K launch");
   // Top-K occupies every SM's registers, so the work that needs only h (pair states and W s on
   // one helper stream; g and the g half of the fusion on another) starts after it, beside the
@@ -847,7 +906,7 @@ int dcoco_cycle(const void* logits, int V, const void* emb, const void* h, const
                 int32_t* near_tie, void* workspace, size_t workspace_bytes, void* stream) {
   clear_err();
   if (emb == nullptr) return fail(DCOCO_ERR_INVALID_ARG, "emb is NULL");
-  return cycle_impl(logits, V, emb, nullptr, h, w, N, B, K, mode, t, q, u, vals, ids, S, k_sel, tokens, accept_len,
+  return cycle_impl(logits, nullptr, V, emb, nullptr, h, w, N, B, K, mode, t, q, u, vals, ids, S, k_sel, tokens, accept_len,
                     committed, n_commit, near_tie, workspace, workspace_bytes, stream);
 }
 
@@ -858,8 +917,26 @@ int dcoco_cycle_table(const void* logits, int V, const void* table, const void* 
                       size_t workspace_bytes, void* stream) {
   clear_err();
   if (table == nullptr) return fail(DCOCO_ERR_INVALID_ARG, "table is NULL");
-  return cycle_impl(logits, V, nullptr, table, h, w, N, B, K, mode, t, q, u, vals, ids, S, k_sel, tokens, accept_len,
+  return cycle_impl(logits, nullptr, V, nullptr, table, h, w, N, B, K, mode, t, q, u, vals, ids, S, k_sel, tokens, accept_len,
                     committed, n_commit, near_tie, workspace, workspace_bytes, stream);
+}
+
+size_t dcoco_cycle_lm_workspace_size(const dcoco_weights* w, int N, int B, int K, int V) {
+  const size_t base = dcoco_cycle_workspace_size(w, N, B, K);
+  if (base == 0 || (w->dtype != DCOCO_BF16 && w->dtype != DCOCO_F32)) return 0;
+  const size_t lm = dcoco_lm_head_topk_workspace_size(w->dtype, N, B, V, K);
+  return lm == 0 ? 0 : base + round256(lm);
+}
+
+int dcoco_cycle_lm(const void* W_lm, int V, const void* emb, const void* h, const dcoco_weights* w, int N, int B,
+                   int K, int mode, const int32_t* t, const float* q, const float* u, float* vals, int32_t* ids,
+                   float* S, int32_t* k_sel, int32_t* tokens, int32_t* accept_len, int32_t* committed,
+                   int32_t* n_commit, int32_t* near_tie, void* workspace, size_t workspace_bytes, void* stream) {
+  clear_err();
+  if (W_lm == nullptr) return fail(DCOCO_ERR_INVALID_ARG, "W_lm is NULL");
+  if (emb == nullptr) return fail(DCOCO_ERR_INVALID_ARG, "emb is NULL");
+  return cycle_impl(nullptr, W_lm, V, emb, nullptr, h, w, N, B, K, mode, t, q, u, vals, ids, S, k_sel, tokens,
+                    accept_len, committed, n_commit, near_tie, workspace, workspace_bytes, stream);
 }
 
 size_t dcoco_embedding_table_bytes(const dcoco_weights* w, int V) {

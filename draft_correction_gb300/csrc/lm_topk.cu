@@ -1,0 +1,438 @@
+// Fused drafter output projection and top-K on the 5th-generation tensor cores.
+//
+// [Blog] "Score neighboring candidates in parallel" and "Keep the leading candidates": the
+// corrector starts from what the drafter's own pass produced, whose last step projects the
+// final hidden state h of every slot onto the vocabulary (l[v] = h . W_lm[v]) and keeps the K
+// largest logits.  Here both happen in one pass over W_lm: the [rows, V] logits exist only in
+// tensor memory and never reach HBM.
+//
+// Kernel shape (persistent, one CTA per SM, 10 warps):
+//   A cluster of CM CTAs (CM = 1, 2 or 4) covers CM consecutive 128-row tiles of h and walks
+//   one contiguous range of 256-token vocabulary tiles.  Every CTA of the cluster multiplies
+//   by the same W_lm tile, so each CTA loads 1/CM of it and multicasts that slice to all.
+//   warp 0     TMA producer: this CTA's h tile and its slice of the W_lm tile per k-block.
+//   warp 1     allocates 512 TMEM columns (two 128 x 256 fp32 accumulators) and issues
+//              tcgen05.mma; each stage is released to every CTA of the cluster by a multicast
+//              commit, so no CTA refills a stage that another CTA still reads.
+//   warps 2-9  epilogue: while the next tile accumulates in the other buffer, each thread
+//              reads 128 columns of its row and keeps a running top-K of everything it has
+//              seen (a sorted list of keys in shared memory, entered only by values that reach
+//              its current K-th key).
+// Each (row, cluster, column half) leaves a sorted list of K keys; lm_merge_kernel merges the
+// lists of a row.  Keys are ordered value bits << 32 | ~token, as in the top-K kernel, so the
+// selection is exact on the fp32 logits and deterministic.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace dcoco {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;  // vocabulary entries per tile: one accumulator of 256 fp32 columns
+constexpr int kThreads = 320;
+constexpr int kEpiThreads = 256;
+constexpr int kMaxStages = 4;
+constexpr int A_BYTES = BM * 128;
+constexpr int B_BYTES = BN * 128;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int kSmemLimit = 227 * 1024;  // per CTA, static + dynamic
+constexpr int kMaxListsPerLane = 16;    // merge: up to 512 lists per row
+
+struct LmArgs {
+  CUtensorMap a_map;  // h [rows, d], box {128 bytes, 128 rows}
+  CUtensorMap b_map;  // W_lm [V, d], box {128 bytes, BN / cm rows}
+  unsigned long long* partial;  // [rows, n_lists, K] keys, each list descending
+  int rows, d, V, K;
+  int n_vt;    // vocabulary tiles, ceil(V / BN)
+  int nclus;   // clusters per row group (vocabulary ranges); n_lists = 2 * nclus
+  int cm;      // CTAs per cluster (row tiles sharing the W_lm tile)
+  int stages;  // pipeline depth
+  unsigned int* status;
+};
+
+// Enters `key` into the descending list my[0], my[256], ..., my[(K-1)*256] if it beats the
+// last entry; returns the value of the (new) last entry, NaN while the list is not full.
+__device__ __noinline__ float list_insert(unsigned long long* my, unsigned long long key, int K) {
+  if (key > my[(K - 1) * 256]) {
+    int j = K - 1;
+    while (j > 0) {
+      const unsigned long long p = my[(j - 1) * 256];
+      if (p >= key) break;
+      my[j * 256] = p;
+      --j;
+    }
+    my[j * 256] = key;
+  }
+  return key_value(my[(K - 1) * 256]);
+}
+
+template <bool kBf16>
+__global__ void __launch_bounds__(kThreads, 1) lm_topk_kernel(const __grid_constant__ LmArgs args) {
+  constexpr int BK = kBf16 ? 64 : 32;  // elements per 128-byte row of a stage
+  constexpr int UK = kBf16 ? 16 : 8;   // K of one MMA instruction
+  constexpr uint32_t IDESC = mma_idesc(kBf16 ? 1u : 2u, BM, BN);
+
+  extern __shared__ uint8_t dyn_smem[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
+  __shared__ __align__(8) uint64_t full_bar[kMaxStages];
+  __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
+  __shared__ __align__(8) uint64_t acc_full[2];
+  __shared__ __align__(8) uint64_t acc_empty[2];
+  __shared__ uint32_t tmem_base_s;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int cm = args.cm, S = args.stages, K = args.K;
+  const uint32_t rank = cm > 1 ? cluster_rank() : 0u;
+  const int clus = blockIdx.x / cm;
+  const int m_tile = blockIdx.y * cm + static_cast<int>(rank);
+  const int t0 = static_cast<int>(static_cast<long long>(clus) * args.n_vt / args.nclus);
+  const int t1 = static_cast<int>(static_cast<long long>(clus + 1) * args.n_vt / args.nclus);
+  const int ntile = t1 - t0;
+  const int nkb = (args.d + BK - 1) / BK;
+  const uint16_t mask = static_cast<uint16_t>((1u << cm) - 1u);
+  unsigned long long* lists = reinterpret_cast<unsigned long long*>(smem + S * STAGE_BYTES);  // [K][256]
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_u32(&full_bar[s]), 1);
+      mbar_init(smem_u32(&empty_bar[s]), cm);  // one MMA commit from every CTA of the cluster
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&acc_full[b]), 1);
+      mbar_init(smem_u32(&acc_empty[b]), kEpiThreads / 32);
+    }
+    fence_mbar_init();
+    prefetch_tmap(&args.a_map);
+    prefetch_tmap(&args.b_map);
+  }
+  if (warp == 1) tmem_alloc(smem_u32(&tmem_base_s), 2 * BN);
+  if (threadIdx.x >= 64)
+    for (int j = 0; j < K; ++j) lists[j * 256 + (threadIdx.x - 64)] = 0ull;  // below every real key
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (cm > 1) cluster_sync();  // every CTA's barriers exist before the first multicast lands
+  const uint32_t tmem = tmem_base_s;
+  const uint32_t smem0 = smem_u32(smem);
+  const int total = ntile * nkb;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const int slice = BN / cm;
+      for (int i = 0; i < total; ++i) {
+        const int s = i % S;
+        const uint32_t ph = (i / S) & 1;
+        if (!mbar_wait(smem_u32(&empty_bar[s]), ph ^ 1)) {
+          atomicOr(args.status, DEV_TIMEOUT_MMA);
+          break;
+        }
+        const uint32_t fb = smem_u32(&full_bar[s]);
+        const uint32_t a_s = smem0 + s * STAGE_BYTES;
+        const uint32_t b_s = a_s + A_BYTES;
+        const int tile = t0 + i / nkb;
+        const int kx = (i % nkb) * BK;
+        mbar_expect_tx(fb, STAGE_BYTES);  // own h tile + every CTA's W_lm slice
+        tma_load_2d(a_s, &args.a_map, kx, m_tile * BM, fb);
+        if (cm > 1)
+          tma_load_2d_multicast(b_s + rank * slice * 128, &args.b_map, kx, tile * BN + static_cast<int>(rank) * slice, fb,
+                                mask);
+        else
+          tma_load_2d(b_s, &args.b_map, kx, tile * BN, fb);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int i = 0;
+      bool ok = true;
+      for (int t = 0; t < ntile && ok; ++t) {
+        const int buf = t & 1;
+        if (!mbar_wait(smem_u32(&acc_empty[buf]), ((t >> 1) & 1) ^ 1)) {
+          atomicOr(args.status, DEV_TIMEOUT_ACC);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + buf * BN;
+        for (int kb = 0; kb < nkb; ++kb, ++i) {
+          const int s = i % S;
+          const uint32_t ph = (i / S) & 1;
+          if (!mbar_wait(smem_u32(&full_bar[s]), ph)) {
+            atomicOr(args.status, DEV_TIMEOUT_TMA);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_s = smem0 + s * STAGE_BYTES;
+          const uint32_t b_s = a_s + A_BYTES;
+#pragma unroll
+          for (int j = 0; j < BK / UK; ++j)
+            tc_mma<!kBf16>(d_tmem, sw128_desc(a_s + j * 32), sw128_desc(b_s + j * 32), IDESC,
+                           (kb > 0 || j > 0) ? 1u : 0u);
+          if (cm > 1)
+            tc_commit_multicast(smem_u32(&empty_bar[s]), mask);
+          else
+            tc_commit(smem_u32(&empty_bar[s]));
+        }
+        if (ok) tc_commit(smem_u32(&acc_full[buf]));
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 2..9)
+    const int e = threadIdx.x - 64;
+    const int q = warp & 3;            // TMEM lane quarter this warp may access
+    const int half = (warp - 2) >> 2;  // which 128 columns of each tile
+    const int row = m_tile * BM + q * 32 + lane;
+    const bool live = row < args.rows;
+    unsigned long long* my = lists + e;
+    // NaN while the list is not full (every value then reaches the key test); rows past the
+    // end see only zero-filled inputs and +inf keeps them out.
+    float thr = live ? __uint_as_float(0xFFFFFFFFu) : __int_as_float(0x7F800000);
+    for (int t = 0; t < ntile; ++t) {
+      const int buf = t & 1;
+      const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&acc_full[buf]), (t >> 1) & 1));
+      if (!ok) {
+        if (lane == 0) atomicOr(args.status, DEV_TIMEOUT_ACC);
+        break;
+      }
+      tc_fence_after();
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * BN + half * 128;
+      const int col0 = (t0 + t) * BN + half * 128;
+      for (int c = 0; c < 128; c += 32) {
+        float v[32];
+        tmem_ld32(taddr + c, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int col = col0 + c + i;
+          // columns past V hold products with zero-filled W_lm rows
+          if (!(v[i] < thr) && col < args.V) thr = list_insert(my, make_key(__float_as_uint(v[i]), col), K);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&acc_empty[buf]));
+    }
+    if (live) {
+      unsigned long long* dst =
+          args.partial + (static_cast<size_t>(row) * (2 * args.nclus) + clus * 2 + half) * static_cast<size_t>(K);
+      for (int j = 0; j < K; ++j) dst[j] = my[j * 256];
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 2 * BN);
+  }
+  if (cm > 1) cluster_sync();  // no CTA leaves while a multicast commit may still arrive in it
+}
+
+// One warp per row: K rounds of "largest head among the row's sorted lists".
+__global__ void __launch_bounds__(256) lm_merge_kernel(const unsigned long long* __restrict__ partial, int rows,
+                                                       int n_lists, int K, float* __restrict__ vals,
+                                                       int32_t* __restrict__ ids) {
+  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const unsigned long long* base = partial + static_cast<size_t>(row) * n_lists * K;
+  unsigned long long head[kMaxListsPerLane];
+  int pos[kMaxListsPerLane];
+#pragma unroll
+  for (int j = 0; j < kMaxListsPerLane; ++j) {
+    const int l = lane + 32 * j;
+    pos[j] = 0;
+    head[j] = l < n_lists ? base[static_cast<size_t>(l) * K] : 0ull;
+  }
+  for (int r = 0; r < K; ++r) {
+    unsigned long long best = 0ull;
+    int bj = -1;
+#pragma unroll
+    for (int j = 0; j < kMaxListsPerLane; ++j)
+      if (head[j] > best) {
+        best = head[j];
+        bj = j;
+      }
+    unsigned long long wmax = best;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, wmax, o);
+      wmax = other > wmax ? other : wmax;
+    }
+    // keys of one row are distinct (each token sits in exactly one list), so one lane advances
+    if (bj >= 0 && best == wmax) {
+#pragma unroll
+      for (int j = 0; j < kMaxListsPerLane; ++j)
+        if (j == bj) {
+          ++pos[j];
+          head[j] = pos[j] < K ? base[static_cast<size_t>(lane + 32 * j) * K + pos[j]] : 0ull;
+        }
+    }
+    if (lane == 0) {
+      vals[static_cast<size_t>(row) * K + r] = key_value(wmax);
+      ids[static_cast<size_t>(row) * K + r] = static_cast<int32_t>(key_index(wmax));
+    }
+  }
+}
+
+struct Plan {
+  int cm, m_groups, nclus, n_vt, stages, smem;
+};
+
+int stages_for(int K) {
+  const int lists = K * kEpiThreads * 8;
+  return std::min(kMaxStages, (kSmemLimit - 2048 - lists) / STAGE_BYTES);
+}
+
+template <bool kBf16>
+cudaError_t configure(int smem) {
+  static int configured[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (smem > configured[dev]) {
+    e = cudaFuncSetAttribute(lm_topk_kernel<kBf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured[dev] = smem;
+  }
+  return cudaSuccess;
+}
+
+// Clusters of `cm` CTAs of this kernel that fit on the device at once (0 on failure).
+template <bool kBf16>
+int active_clusters(int cm, int smem) {
+  if (configure<kBf16>(smem) != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cm * 64, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cm;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, lm_topk_kernel<kBf16>, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+// The launch plan: cluster size (forced, or the one that keeps the most CTAs resident, larger
+// clusters on ties), then as many vocabulary ranges as fit in one wave.
+template <bool kBf16>
+cudaError_t plan_for(int rows, int V, int K, int force_cm, Plan* p) {
+  const int m_tiles = (rows + BM - 1) / BM;
+  p->n_vt = (V + BN - 1) / BN;
+  p->stages = stages_for(K);
+  if (p->stages < 2) return cudaErrorInvalidValue;
+  p->smem = p->stages * STAGE_BYTES + K * kEpiThreads * 8 + 1024;
+  struct Key {
+    int dev, cm, smem;
+  };
+  static Key cache_key[64][3];
+  static int cache_val[64][3];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  auto active = [&](int cm) {
+    const int slot = cm == 4 ? 2 : cm == 2 ? 1 : 0;
+    Key& k = cache_key[dev][slot];
+    if (k.cm != cm || k.smem != p->smem) {
+      cache_val[dev][slot] = active_clusters<kBf16>(cm, p->smem);
+      k = Key{dev, cm, p->smem};
+    }
+    return cache_val[dev][slot];
+  };
+  int best_cm = 1, best_ctas = -1;
+  for (int cm : {4, 2, 1}) {
+    if (force_cm > 0 && cm != force_cm) continue;
+    if (force_cm == 0 && cm > 1 && m_tiles < cm) continue;
+    const int ctas = active(cm) * cm;
+    if (ctas > best_ctas) {
+      best_ctas = ctas;
+      best_cm = cm;
+    }
+  }
+  p->cm = best_cm;
+  p->m_groups = (m_tiles + p->cm - 1) / p->cm;
+  const int fit = std::max(1, active(p->cm));
+  p->nclus = std::max(1, std::min(p->n_vt, fit / p->m_groups));
+  return cudaSuccess;
+}
+
+template <bool kBf16>
+cudaError_t launch_t(const void* h, const void* W_lm, int rows, int d, int V, int K, int force_cm, float* vals,
+                     int32_t* ids, void* partial, size_t partial_bytes, unsigned int* status, cudaStream_t stream) {
+  Plan p;
+  cudaError_t e = plan_for<kBf16>(rows, V, K, force_cm, &p);
+  if (e != cudaSuccess) return e;
+  const int n_lists = 2 * p.nclus;
+  if (n_lists > 32 * kMaxListsPerLane) return cudaErrorInvalidValue;
+  if (static_cast<size_t>(rows) * n_lists * K * 8 > partial_bytes) return cudaErrorInvalidValue;
+  LmArgs a;
+  const char* err = nullptr;
+  if (!make_tmap(&a.a_map, h, kBf16, static_cast<uint64_t>(rows), static_cast<uint64_t>(d), static_cast<uint64_t>(d), BM,
+                 &err) ||
+      !make_tmap(&a.b_map, W_lm, kBf16, static_cast<uint64_t>(V), static_cast<uint64_t>(d), static_cast<uint64_t>(d),
+                 static_cast<uint32_t>(BN / p.cm), &err))
+    return cudaErrorInvalidValue;
+  a.partial = static_cast<unsigned long long*>(partial);
+  a.rows = rows;
+  a.d = d;
+  a.V = V;
+  a.K = K;
+  a.n_vt = p.n_vt;
+  a.nclus = p.nclus;
+  a.cm = p.cm;
+  a.stages = p.stages;
+  a.status = status;
+  e = configure<kBf16>(p.smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.cm * p.nclus, p.m_groups, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = p.smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = p.cm;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, lm_topk_kernel<kBf16>, a);
+  if (e != cudaSuccess) return e;
+  lm_merge_kernel<<<(rows + 7) / 8, 256, 0, stream>>>(static_cast<const unsigned long long*>(partial), rows, n_lists, K,
+                                                      vals, ids);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t lm_topk_partial_bytes(bool is_bf16, int rows, int V, int K, int force_cm) {
+  Plan p;
+  const cudaError_t e = is_bf16 ? plan_for<true>(rows, V, K, force_cm, &p) : plan_for<false>(rows, V, K, force_cm, &p);
+  if (e != cudaSuccess) return 0;
+  return static_cast<size_t>(rows) * (2 * p.nclus) * K * 8;
+}
+
+cudaError_t launch_lm_topk(const void* h, const void* W_lm, bool is_bf16, int rows, int d, int V, int K, int force_cm,
+                           float* vals, int32_t* ids, void* partial, size_t partial_bytes, unsigned int* status,
+                           cudaStream_t stream) {
+  return is_bf16 ? launch_t<true>(h, W_lm, rows, d, V, K, force_cm, vals, ids, partial, partial_bytes, status, stream)
+                 : launch_t<false>(h, W_lm, rows, d, V, K, force_cm, vals, ids, partial, partial_bytes, status, stream);
+}
+
+}  // namespace dcoco

@@ -262,6 +262,44 @@ int dcoco_cycle_table(const void* logits, int V, const void* table, const void* 
                       int32_t* committed, int32_t* n_commit, int32_t* near_tie, void* workspace,
                       size_t workspace_bytes, void* stream);
 
+/*
+ * Fused drafter output projection and top-K (Two Delta blog, "Score neighboring candidates in
+ * parallel": the corrector reuses the drafter's own pass; its logits are that pass's projection
+ * of the final hidden state onto the vocabulary).  For every row (n,i) of h [N, B, d] the
+ * logits l[v] = sum_k h[n,i,k] W_lm[v,k], v in [0, V), are formed on the tensor cores (bf16
+ * products or tf32 for f32 inputs, fp32 accumulation) and reduced to the K largest in the
+ * same kernel; the [N, B, V] logits are never written.  W_lm [V, d] row-major (one row per
+ * token), same dtype as h; d a multiple of 16 bytes' worth of elements; 1 <= K <= min(64, V).
+ *   vals [N, B, K] float32  the kept fp32 logits, descending, equal values by ascending id
+ *   ids  [N, B, K] int32
+ * Workspace: dcoco_lm_head_topk_workspace_size bytes (per-row partial lists; the size depends
+ * on the current device and on dcoco_set_lm_cluster), 16-byte aligned, caller-owned.
+ * Selection is exact on the fp32 logits it computes and deterministic.  The fp32 logits differ
+ * from exact dot products by accumulation rounding, so two tokens whose exact logits lie within
+ * that rounding may rank in either order.
+ */
+size_t dcoco_lm_head_topk_workspace_size(int dtype, int N, int B, int V, int K);
+int dcoco_lm_head_topk(const void* h, const void* W_lm, int dtype, int N, int B, int d, int V, int K, float* vals,
+                       int32_t* ids, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Tuning knob: CTAs per thread-block cluster in dcoco_lm_head_topk (1, 2 or 4 row tiles that
+ * share each W_lm tile by multicast; 0 = automatic, the size that keeps the most CTAs
+ * resident).  Process-wide; returns the previous value.  Query workspace sizes after setting it.
+ */
+int dcoco_set_lm_cluster(int ctas);
+
+/*
+ * dcoco_cycle starting from the drafter's hidden state instead of its logits: top-K is
+ * dcoco_lm_head_topk of h with W_lm [V, d] (w->dtype), and the same h feeds the corrector.
+ * Same outputs and errors as dcoco_cycle; workspace dcoco_cycle_lm_workspace_size bytes.
+ */
+size_t dcoco_cycle_lm_workspace_size(const dcoco_weights* w, int N, int B, int K, int V);
+int dcoco_cycle_lm(const void* W_lm, int V, const void* emb, const void* h, const dcoco_weights* w, int N, int B,
+                   int K, int mode, const int32_t* t, const float* q, const float* u, float* vals, int32_t* ids,
+                   float* S, int32_t* k_sel, int32_t* tokens, int32_t* accept_len, int32_t* committed,
+                   int32_t* n_commit, int32_t* near_tie, void* workspace, size_t workspace_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -126,3 +126,38 @@ def test_table_argument_errors(L):
     assert L.dcoco_embedding_table_bytes(ctypes.byref(w), 151936) == 151936 * 256 * 2
     assert L.dcoco_embedding_table(None, 10, ctypes.byref(w), fake, None) == 1
     assert L.dcoco_embedding_table(fake, 10, ctypes.byref(w), None, None) == 1
+
+
+def test_lm_head_topk_argument_errors(L):
+    # h, W_lm, dtype, N, B, d, V, K, vals, ids, ws, ws_bytes, stream
+    ok = dict(h=FAKE, W=FAKE, dt=dc.DCOCO_BF16, N=1, B=4, d=64, V=1000, K=8)
+
+    def call(**kw):
+        a = {**ok, **kw}
+        return L.dcoco_lm_head_topk(a["h"], a["W"], a["dt"], a["N"], a["B"], a["d"], a["V"], a["K"], FAKE, FAKE,
+                                    FAKE, 1 << 20, None)
+
+    assert call(dt=7) == 2
+    assert call(K=65) == 1 and call(K=0) == 1 and call(V=7) == 1
+    assert call(d=12) == 1 and b"16 bytes" in L.dcoco_last_error()        # 24-byte bf16 rows
+    assert call(dt=dc.DCOCO_F32, d=6) == 1                                  # 24-byte f32 rows
+    assert call(h=None) == 1 and b"h is NULL" in L.dcoco_last_error()
+    assert call(W=MISALIGNED) == 1 and b"W_lm" in L.dcoco_last_error()
+    assert call(N=4096, B=17) == 2                                          # rows > 65535
+    assert L.dcoco_lm_head_topk_workspace_size(7, 1, 4, 1000, 8) == 0
+    assert L.dcoco_lm_head_topk_workspace_size(dc.DCOCO_BF16, 1, 4, 1000, 65) == 0
+
+
+def test_lm_cluster_knob(L):
+    prev = L.dcoco_set_lm_cluster(2)
+    assert L.dcoco_set_lm_cluster(3) == 2        # 3 is not a cluster size: automatic
+    assert L.dcoco_set_lm_cluster(prev) == 0
+
+
+def test_cycle_lm_argument_errors(L):
+    w = _weights()
+    args = [1000, FAKE, FAKE, ctypes.byref(w), 1, 4, 3, 0, FAKE, None, None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+            FAKE, FAKE, None, FAKE, 1 << 30, None]
+    assert L.dcoco_cycle_lm(None, *args) == 1 and b"W_lm is NULL" in L.dcoco_last_error()
+    assert L.dcoco_cycle_lm(MISALIGNED, *args) == 1 and b"W_lm" in L.dcoco_last_error()
+    assert L.dcoco_cycle_lm_workspace_size(None, 1, 4, 3, 1000) == 0
