@@ -16,8 +16,11 @@
 //              commit, so no CTA refills a stage that another CTA still reads.
 //   warps 2-9  epilogue: while the next tile accumulates in the other buffer, each thread
 //              reads 128 columns of its row and keeps a running top-K of everything it has
-//              seen (a sorted list of keys in shared memory, entered only by values that reach
-//              its current K-th key).
+//              seen: a descending list of KR >= K keys in registers.  Per 32 columns each lane
+//              marks the values that reach its list's last key and parks the 32 values in
+//              shared memory; then every pass of a loop inserts each lane's next marked value
+//              with one compare-exchange pass over the lists, the whole warp together (lanes
+//              with nothing left pass a null key), until no lane has marks left.
 // Each (row, cluster, column half) leaves a sorted list of K keys; lm_merge_kernel merges the
 // lists of a row.  Keys are ordered value bits << 32 | ~token, as in the top-K kernel, so the
 // selection is exact on the fp32 logits and deterministic.
@@ -39,8 +42,9 @@ constexpr int kMaxStages = 4;
 constexpr int A_BYTES = BM * 128;
 constexpr int B_BYTES = BN * 128;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int kSmemLimit = 227 * 1024;  // per CTA, static + dynamic
-constexpr int kMaxListsPerLane = 16;    // merge: up to 512 lists per row
+constexpr int kMaxListsPerLane = 16;  // merge: up to 512 lists per row
+constexpr int kStageValsBytes = kEpiThreads * 32 * 4;  // one 32-column chunk per epilogue thread
+constexpr int kSmem = kMaxStages * STAGE_BYTES + kStageValsBytes + 1024;
 
 struct LmArgs {
   CUtensorMap a_map;  // h [rows, d], box {128 bytes, 128 rows}
@@ -50,27 +54,37 @@ struct LmArgs {
   int n_vt;    // vocabulary tiles, ceil(V / BN)
   int nclus;   // clusters per row group (vocabulary ranges); n_lists = 2 * nclus
   int cm;      // CTAs per cluster (row tiles sharing the W_lm tile)
-  int stages;  // pipeline depth
   unsigned int* status;
 };
 
-// Enters `key` into the descending list my[0], my[256], ..., my[(K-1)*256] if it beats the
-// last entry; returns the value of the (new) last entry, NaN while the list is not full.
-__device__ __noinline__ float list_insert(unsigned long long* my, unsigned long long key, int K) {
-  if (key > my[(K - 1) * 256]) {
-    int j = K - 1;
-    while (j > 0) {
-      const unsigned long long p = my[(j - 1) * 256];
-      if (p >= key) break;
-      my[j * 256] = p;
-      --j;
-    }
-    my[j * 256] = key;
+// Inserts x into the descending list a[0..KR-1] and drops the smallest key: one
+// compare-exchange pass (x = 0, below every real key, leaves the list unchanged).
+template <int KR>
+__device__ __forceinline__ void list_insert(unsigned long long (&a)[KR], unsigned long long x) {
+#pragma unroll
+  for (int j = 0; j < KR; ++j) {
+    const unsigned long long hi = a[j] > x ? a[j] : x;
+    x = a[j] > x ? x : a[j];
+    a[j] = hi;
   }
-  return key_value(my[(K - 1) * 256]);
 }
 
-template <bool kBf16>
+// 16 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, "
+      "[%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// KR: list length kept per thread (K rounded up to 4, 8, 16, 32 or 64).
+template <bool kBf16, int KR>
 __global__ void __launch_bounds__(kThreads, 1) lm_topk_kernel(const __grid_constant__ LmArgs args) {
   constexpr int BK = kBf16 ? 64 : 32;  // elements per 128-byte row of a stage
   constexpr int UK = kBf16 ? 16 : 8;   // K of one MMA instruction
@@ -86,7 +100,9 @@ __global__ void __launch_bounds__(kThreads, 1) lm_topk_kernel(const __grid_const
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int cm = args.cm, S = args.stages, K = args.K;
+  constexpr int S = kMaxStages;
+  constexpr int CW = KR >= 64 ? 16 : 32;  // columns per TMEM load (fewer registers beside a long list)
+  const int cm = args.cm, K = args.K;
   const uint32_t rank = cm > 1 ? cluster_rank() : 0u;
   const int clus = blockIdx.x / cm;
   const int m_tile = blockIdx.y * cm + static_cast<int>(rank);
@@ -95,7 +111,6 @@ __global__ void __launch_bounds__(kThreads, 1) lm_topk_kernel(const __grid_const
   const int ntile = t1 - t0;
   const int nkb = (args.d + BK - 1) / BK;
   const uint16_t mask = static_cast<uint16_t>((1u << cm) - 1u);
-  unsigned long long* lists = reinterpret_cast<unsigned long long*>(smem + S * STAGE_BYTES);  // [K][256]
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -111,8 +126,6 @@ __global__ void __launch_bounds__(kThreads, 1) lm_topk_kernel(const __grid_const
     prefetch_tmap(&args.b_map);
   }
   if (warp == 1) tmem_alloc(smem_u32(&tmem_base_s), 2 * BN);
-  if (threadIdx.x >= 64)
-    for (int j = 0; j < K; ++j) lists[j * 256 + (threadIdx.x - 64)] = 0ull;  // below every real key
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -185,14 +198,17 @@ __global__ void __launch_bounds__(kThreads, 1) lm_topk_kernel(const __grid_const
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue (warps 2..9)
-    const int e = threadIdx.x - 64;
     const int q = warp & 3;            // TMEM lane quarter this warp may access
     const int half = (warp - 2) >> 2;  // which 128 columns of each tile
     const int row = m_tile * BM + q * 32 + lane;
     const bool live = row < args.rows;
-    unsigned long long* my = lists + e;
-    // NaN while the list is not full (every value then reaches the key test); rows past the
-    // end see only zero-filled inputs and +inf keeps them out.
+    // this warp's staging area: column i of the current chunk at sv[i * 32] (lanes interleaved)
+    float* sv = reinterpret_cast<float*>(smem + kMaxStages * STAGE_BYTES) + (warp - 2) * 32 * 32 + lane;
+    unsigned long long a[KR];
+#pragma unroll
+    for (int j = 0; j < KR; ++j) a[j] = 0ull;  // below every real key
+    // The last key's value: NaN while the list is not full (every value then reaches the key
+    // test); rows past the end see only zero-filled inputs and +inf keeps them out.
     float thr = live ? __uint_as_float(0xFFFFFFFFu) : __int_as_float(0x7F800000);
     for (int t = 0; t < ntile; ++t) {
       const int buf = t & 1;
@@ -204,14 +220,33 @@ __global__ void __launch_bounds__(kThreads, 1) lm_topk_kernel(const __grid_const
       tc_fence_after();
       const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * BN + half * 128;
       const int col0 = (t0 + t) * BN + half * 128;
-      for (int c = 0; c < 128; c += 32) {
-        float v[32];
-        tmem_ld32(taddr + c, v);
+      for (int c = 0; c < 128; c += CW) {
+        // Which of these CW columns reach this lane's threshold (columns past V hold products
+        // with zero-filled W_lm rows and never count).
+        uint32_t m = 0;
+        {
+          float v[CW];
+          if constexpr (CW == 32)
+            tmem_ld32(taddr + c, v);
+          else
+            tmem_ld16(taddr + c, v);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int col = col0 + c + i;
-          // columns past V hold products with zero-filled W_lm rows
-          if (!(v[i] < thr) && col < args.V) thr = list_insert(my, make_key(__float_as_uint(v[i]), col), K);
+          for (int i = 0; i < CW; ++i) {
+            m |= (v[i] < thr ? 0u : 1u) << i;
+            sv[i * 32] = v[i];
+          }
+        }
+        const int valid = args.V - (col0 + c);
+        if (valid < CW) m &= valid > 0 ? (1u << valid) - 1u : 0u;
+        // Each pass inserts every lane's next marked value (the lowest marked column left), so
+        // the warp runs as many passes as its busiest lane has marks, in a loop (not unrolled).
+        while (__any_sync(0xFFFFFFFFu, m != 0u)) {
+          const int i = m != 0u ? __ffs(m) - 1 : 0;
+          const float x = sv[i * 32];
+          const bool pass = m != 0u && !(x < thr);
+          m &= m - 1u;
+          list_insert<KR>(a, pass ? make_key(__float_as_uint(x), static_cast<uint32_t>(col0 + c + i)) : 0ull);
+          thr = key_value(a[KR - 1]);
         }
       }
       tc_fence_before();
@@ -221,7 +256,9 @@ __global__ void __launch_bounds__(kThreads, 1) lm_topk_kernel(const __grid_const
     if (live) {
       unsigned long long* dst =
           args.partial + (static_cast<size_t>(row) * (2 * args.nclus) + clus * 2 + half) * static_cast<size_t>(K);
-      for (int j = 0; j < K; ++j) dst[j] = my[j * 256];
+#pragma unroll
+      for (int j = 0; j < KR; ++j)
+        if (j < K) dst[j] = a[j];
     }
   }
 
@@ -282,37 +319,51 @@ __global__ void __launch_bounds__(256) lm_merge_kernel(const unsigned long long*
 }
 
 struct Plan {
-  int cm, m_groups, nclus, n_vt, stages, smem;
+  int cm, m_groups, nclus, n_vt;
 };
 
-int stages_for(int K) {
-  const int lists = K * kEpiThreads * 8;
-  return std::min(kMaxStages, (kSmemLimit - 2048 - lists) / STAGE_BYTES);
-}
+int list_len(int K) { return K <= 4 ? 4 : K <= 8 ? 8 : K <= 16 ? 16 : K <= 32 ? 32 : 64; }
+
+using KernelFn = void (*)(LmArgs);
 
 template <bool kBf16>
-cudaError_t configure(int smem) {
-  static int configured[64] = {};
+KernelFn kernel_for(int KR) {
+  switch (KR) {
+    case 4: return lm_topk_kernel<kBf16, 4>;
+    case 8: return lm_topk_kernel<kBf16, 8>;
+    case 16: return lm_topk_kernel<kBf16, 16>;
+    case 32: return lm_topk_kernel<kBf16, 32>;
+    default: return lm_topk_kernel<kBf16, 64>;
+  }
+}
+
+// Sets the dynamic shared-memory size once per kernel instance and device.
+cudaError_t configure(KernelFn fn, int slot) {
+  static bool done[64][10] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (smem > configured[dev]) {
-    e = cudaFuncSetAttribute(lm_topk_kernel<kBf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (!done[dev][slot]) {
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
-    configured[dev] = smem;
+    done[dev][slot] = true;
   }
   return cudaSuccess;
 }
 
+int slot_of(bool is_bf16, int KR) {
+  const int k = KR == 4 ? 0 : KR == 8 ? 1 : KR == 16 ? 2 : KR == 32 ? 3 : 4;
+  return (is_bf16 ? 5 : 0) + k;
+}
+
 // Clusters of `cm` CTAs of this kernel that fit on the device at once (0 on failure).
-template <bool kBf16>
-int active_clusters(int cm, int smem) {
-  if (configure<kBf16>(smem) != cudaSuccess) return 0;
+int active_clusters(KernelFn fn, int slot, int cm) {
+  if (configure(fn, slot) != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(cm * 64, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = kSmem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = cm;
@@ -321,7 +372,7 @@ int active_clusters(int cm, int smem) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, lm_topk_kernel<kBf16>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(fn), &cfg) != cudaSuccess) {
     (void)cudaGetLastError();
     return 0;
   }
@@ -330,30 +381,21 @@ int active_clusters(int cm, int smem) {
 
 // The launch plan: cluster size (forced, or the one that keeps the most CTAs resident, larger
 // clusters on ties), then as many vocabulary ranges as fit in one wave.
-template <bool kBf16>
-cudaError_t plan_for(int rows, int V, int K, int force_cm, Plan* p) {
+cudaError_t plan_for(bool is_bf16, int rows, int V, int K, int force_cm, Plan* p) {
+  const int KR = list_len(K);
+  const int slot = slot_of(is_bf16, KR);
+  const KernelFn fn = is_bf16 ? kernel_for<true>(KR) : kernel_for<false>(KR);
   const int m_tiles = (rows + BM - 1) / BM;
   p->n_vt = (V + BN - 1) / BN;
-  p->stages = stages_for(K);
-  if (p->stages < 2) return cudaErrorInvalidValue;
-  p->smem = p->stages * STAGE_BYTES + K * kEpiThreads * 8 + 1024;
-  struct Key {
-    int dev, cm, smem;
-  };
-  static Key cache_key[64][3];
-  static int cache_val[64][3];
+  static int cache[64][10][3];  // active clusters + 1 per device, instance and cluster size (0 = unknown)
   int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  const cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   auto active = [&](int cm) {
-    const int slot = cm == 4 ? 2 : cm == 2 ? 1 : 0;
-    Key& k = cache_key[dev][slot];
-    if (k.cm != cm || k.smem != p->smem) {
-      cache_val[dev][slot] = active_clusters<kBf16>(cm, p->smem);
-      k = Key{dev, cm, p->smem};
-    }
-    return cache_val[dev][slot];
+    int& c = cache[dev][slot][cm == 4 ? 2 : cm == 2 ? 1 : 0];
+    if (c == 0) c = active_clusters(fn, slot, cm) + 1;
+    return c - 1;
   };
   int best_cm = 1, best_ctas = -1;
   for (int cm : {4, 2, 1}) {
@@ -372,20 +414,28 @@ cudaError_t plan_for(int rows, int V, int K, int force_cm, Plan* p) {
   return cudaSuccess;
 }
 
-template <bool kBf16>
-cudaError_t launch_t(const void* h, const void* W_lm, int rows, int d, int V, int K, int force_cm, float* vals,
-                     int32_t* ids, void* partial, size_t partial_bytes, unsigned int* status, cudaStream_t stream) {
+}  // namespace
+
+size_t lm_topk_partial_bytes(bool is_bf16, int rows, int V, int K, int force_cm) {
   Plan p;
-  cudaError_t e = plan_for<kBf16>(rows, V, K, force_cm, &p);
+  if (plan_for(is_bf16, rows, V, K, force_cm, &p) != cudaSuccess) return 0;
+  return static_cast<size_t>(rows) * (2 * p.nclus) * K * 8;
+}
+
+cudaError_t launch_lm_topk(const void* h, const void* W_lm, bool is_bf16, int rows, int d, int V, int K, int force_cm,
+                           float* vals, int32_t* ids, void* partial, size_t partial_bytes, unsigned int* status,
+                           cudaStream_t stream) {
+  Plan p;
+  cudaError_t e = plan_for(is_bf16, rows, V, K, force_cm, &p);
   if (e != cudaSuccess) return e;
   const int n_lists = 2 * p.nclus;
   if (n_lists > 32 * kMaxListsPerLane) return cudaErrorInvalidValue;
   if (static_cast<size_t>(rows) * n_lists * K * 8 > partial_bytes) return cudaErrorInvalidValue;
   LmArgs a;
   const char* err = nullptr;
-  if (!make_tmap(&a.a_map, h, kBf16, static_cast<uint64_t>(rows), static_cast<uint64_t>(d), static_cast<uint64_t>(d), BM,
-                 &err) ||
-      !make_tmap(&a.b_map, W_lm, kBf16, static_cast<uint64_t>(V), static_cast<uint64_t>(d), static_cast<uint64_t>(d),
+  if (!make_tmap(&a.a_map, h, is_bf16, static_cast<uint64_t>(rows), static_cast<uint64_t>(d), static_cast<uint64_t>(d),
+                 BM, &err) ||
+      !make_tmap(&a.b_map, W_lm, is_bf16, static_cast<uint64_t>(V), static_cast<uint64_t>(d), static_cast<uint64_t>(d),
                  static_cast<uint32_t>(BN / p.cm), &err))
     return cudaErrorInvalidValue;
   a.partial = static_cast<unsigned long long*>(partial);
@@ -396,14 +446,15 @@ cudaError_t launch_t(const void* h, const void* W_lm, int rows, int d, int V, in
   a.n_vt = p.n_vt;
   a.nclus = p.nclus;
   a.cm = p.cm;
-  a.stages = p.stages;
   a.status = status;
-  e = configure<kBf16>(p.smem);
+  const int KR = list_len(K);
+  const KernelFn fn = is_bf16 ? kernel_for<true>(KR) : kernel_for<false>(KR);
+  e = configure(fn, slot_of(is_bf16, KR));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.cm * p.nclus, p.m_groups, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = p.smem;
+  cfg.dynamicSmemBytes = kSmem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -412,27 +463,11 @@ cudaError_t launch_t(const void* h, const void* W_lm, int rows, int d, int V, in
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, lm_topk_kernel<kBf16>, a);
+  e = cudaLaunchKernelEx(&cfg, fn, a);
   if (e != cudaSuccess) return e;
   lm_merge_kernel<<<(rows + 7) / 8, 256, 0, stream>>>(static_cast<const unsigned long long*>(partial), rows, n_lists, K,
                                                       vals, ids);
   return cudaGetLastError();
-}
-
-}  // namespace
-
-size_t lm_topk_partial_bytes(bool is_bf16, int rows, int V, int K, int force_cm) {
-  Plan p;
-  const cudaError_t e = is_bf16 ? plan_for<true>(rows, V, K, force_cm, &p) : plan_for<false>(rows, V, K, force_cm, &p);
-  if (e != cudaSuccess) return 0;
-  return static_cast<size_t>(rows) * (2 * p.nclus) * K * 8;
-}
-
-cudaError_t launch_lm_topk(const void* h, const void* W_lm, bool is_bf16, int rows, int d, int V, int K, int force_cm,
-                           float* vals, int32_t* ids, void* partial, size_t partial_bytes, unsigned int* status,
-                           cudaStream_t stream) {
-  return is_bf16 ? launch_t<true>(h, W_lm, rows, d, V, K, force_cm, vals, ids, partial, partial_bytes, status, stream)
-                 : launch_t<false>(h, W_lm, rows, d, V, K, force_cm, vals, ids, partial, partial_bytes, status, stream);
 }
 
 }  // namespace dcoco
