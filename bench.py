@@ -320,6 +320,49 @@ def gpu_arm(args, cfg):
             "note": "dcoco_cycle_table: rows of LN(W_e Emb), computed once per weights, gathered per cycle"}
         del table
 
+        # Variant: the cycle from the drafter's hidden state.  Top-K is the fused output
+        # projection (h [N,B,d] x W_lm [V,d]^T) and selection, so the logits never reach HBM;
+        # the same hidden states feed the corrector.  W_lm is synthetic, ~N(0, (3/sqrt(d))^2).
+        W_lm = dc.to_device(wl.lm_head(cfg), cfg.dtype, dev)
+        for _ in range(2):
+            cyc.run(None, emb, hidden, t=t_dev, W_lm=W_lm)
+        torch.cuda.synchronize()
+        graph_l = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_l):
+            cyc.run(None, emb, hidden, t=t_dev, W_lm=W_lm)
+        torch.cuda.synchronize()
+        ms_l = timed_loop(graph_l.replay, args.steps, args.warmup)
+        # the fused kernel pair alone (projection + per-range lists, then the merge)
+        lm_vals = torch.empty((cfg.N, cfg.B, cfg.K), dtype=torch.float32, device=dev)
+        lm_ids = torch.empty((cfg.N, cfg.B, cfg.K), dtype=torch.int32, device=dev)
+        lm_ws = torch.empty((max(16, dc.lib().dcoco_lm_head_topk_workspace_size(1, cfg.N, cfg.B, cfg.V, cfg.K)),),
+                            dtype=torch.uint8, device=dev)
+        lm_steps = max(5, min(args.steps, 20))
+        lm_ms = timed_loop(lambda: dc.lm_head_topk(hidden, W_lm, cfg.K, lm_vals, lm_ids, lm_ws), lm_steps, 2)
+        lm_us = 1e3 * statistics.mean(lm_ms)
+        lm_flops = 2.0 * cfg.N * cfg.B * cfg.V * cfg.d
+        _, bf16_peak, peak_kind_t = peaks()
+        lm_tf = lm_flops / (lm_us * 1e-6) / 1e12
+        # for comparison: the unfused path, a cuBLAS projection writing bf16 logits, then top-K
+        h2 = hidden.reshape(cfg.N * cfg.B, cfg.d)
+        lg = torch.empty((cfg.N * cfg.B, cfg.V), dtype=hidden.dtype, device=dev)
+
+        def unfused():
+            torch.matmul(h2, W_lm.t(), out=lg)
+            dc.topk(lg.view(cfg.N, cfg.B, cfg.V), cfg.K, vals=lm_vals, ids=lm_ids)
+
+        un_us = 1e3 * statistics.mean(timed_loop(unfused, lm_steps, 2))
+        variants["fused_lm_head_topk"] = {
+            "value": round(cfg.N * len(ms_l) / (sum(ms_l) / 1e3), 1), "unit": "blocks/s",
+            "ms_per_step": round(sum(ms_l) / len(ms_l), 4),
+            "kernel_us": round(lm_us, 1),
+            "roofline": {"bound": "tensor", "kernel": "lm_topk_kernel + lm_merge_kernel", "achieved": round(lm_tf, 1),
+                         "peak": bf16_peak, "unit": "TFLOP/s", "frac": round(lm_tf / bf16_peak, 4), "traffic": None,
+                         "peak_source": f"{peak_kind_t} bf16_tflops (burst)", "algorithmic_flops_per_launch": lm_flops},
+            "unfused_cublas_projection_then_topk_us": round(un_us, 1),
+            "note": "dcoco_cycle_lm: the cycle from the drafter's hidden state; W_lm [V, d] synthetic"}
+        del W_lm, lg, lm_ws
+
     # Per-stage device times (same inputs, same launch configuration, L2 flushed).
     ids, vals = cyc.out["ids"], cyc.out["vals"]
     uz = torch.empty((cfg.N, cfg.B, cfg.K, cfg.H), dtype=w.act_dtype, device=dev)
