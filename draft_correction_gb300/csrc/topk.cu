@@ -413,6 +413,16 @@ __global__ void __launch_bounds__(kThreads, 4) topk_kernel(const void* __restric
   // (already in registers).  K elements reach that value, so nothing below it is in the top K.
   load(0, c0);
   load(1, c1);
+  // While the block ranks its lane maxima (two barriers, no loads in flight), keep HBM busy:
+  // ask L2 for the next two iterations, which the hot loop then reads from L2.
+#pragma unroll
+  for (int it = 2; it < 4; ++it) {
+    const int vi0 = vidx(it, 0);
+    if (it < iters && vi0 < g.vend) {
+      prefetch_l2(g.vp + vi0);
+      if (vi0 + kU - 1 < g.vend) prefetch_l2(g.vp + vi0 + kU - 1);
+    }
+  }
   {
     uint32_t mb = 0xFF800000u;  // -inf
     bool any = false;
