@@ -389,6 +389,7 @@ def gpu_arm(args, cfg):
         u_d = torch.from_numpy(prng.random((cfg.N, cfg.B + 1, 2), dtype=np.float32)).to(dev)
         draft_d = torch.multinomial(p_d.reshape(-1, spec_V), 1).reshape(cfg.N, cfg.B).to(torch.int32)
         stages["verify_speculative"] = lambda: dc.verify_speculative(draft_d, p_d, q_d, u_d)
+        stages["verify_stochastic"] = lambda: dc.verify(draft_d, q=q_d, u=u_d, mode=dc.VERIFY_STOCHASTIC)
     del uz
     stage_us = {k: 1e3 * statistics.mean(timed_loop(fn, stage_steps, 2)) for k, fn in stages.items()}
 

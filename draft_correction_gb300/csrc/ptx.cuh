@@ -219,6 +219,11 @@ __device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t caddr) {
                : "memory");
   return v;
 }
+__device__ __forceinline__ uint64_t ld_cluster_u64(uint32_t caddr) {
+  uint64_t v;
+  asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(caddr) : "memory");
+  return v;
+}
 __device__ __forceinline__ void st_cluster_u64(uint32_t caddr, uint64_t v) {
   asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(caddr), "l"(v) : "memory");
 }

@@ -17,6 +17,9 @@
 // Residual masses are summed exactly in 62-bit fixed point (integer additions, so the order
 // does not matter and float64 -- slow on this GPU -- is not needed): super-block sums with
 // coalesced loads, one warp's prefix over them, and one warp scan of the crossing super-block.
+// For the two sampling modes a stream's vocabulary row is shared by a cluster of up to 8 CTAs,
+// each summing a contiguous range of super-blocks; rank 0 reads the others' sums through
+// distributed shared memory and makes the draw (integer sums: the same result for any split).
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -101,8 +104,10 @@ __global__ void __launch_bounds__(kThreads) select_verify_kernel(const SelectVer
   __shared__ int s_A;
   __shared__ uint64_t s_sb[kMaxSB];       // residual mass of each super-block (fixed point)
   __shared__ float s_fsum[kThreads / 32];
+  __shared__ uint64_t s_draw[6];  // R, T, found, crossing super-block, mass before it, flag
 
-  const int n = blockIdx.x;
+  const int n = blockIdx.y;
+  const int C = gridDim.x, rank = blockIdx.x;  // CTAs of this stream's cluster (1 unless sampling)
   const int B = a.B, K = a.K, V = a.V;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   grid_dep_wait();  // scores, logits and ids come from preceding kernels
@@ -200,8 +205,10 @@ __global__ void __launch_bounds__(kThreads) select_verify_kernel(const SelectVer
         const int kj = s_k[j];
         const int32_t tok = idn[static_cast<size_t>(j) * K + kj];
         s_draft[j] = tok;
-        a.k_sel[static_cast<size_t>(n) * B + j] = kj;
-        a.tokens[static_cast<size_t>(n) * B + j] = tok;
+        if (rank == 0) {
+          a.k_sel[static_cast<size_t>(n) * B + j] = kj;
+          a.tokens[static_cast<size_t>(n) * B + j] = tok;
+        }
       }
     } else if (warp == 1 && a.mode == 0) {
       // the verifier's greedy tokens, fetched while the walk runs
@@ -280,8 +287,11 @@ __global__ void __launch_bounds__(kThreads) select_verify_kernel(const SelectVer
   };
   const int sb_len = max(1024, (V + kMaxSB - 1) / kMaxSB + 31) & ~31;  // elements per super-block
   const int nsb = (V + sb_len - 1) / sb_len;                             // <= kMaxSB
+  auto sb_owner = [&](int sb) { return static_cast<int>((static_cast<int64_t>(sb) * C) / nsb); };
+  const int sb_lo = static_cast<int>((static_cast<int64_t>(rank) * nsb + C - 1) / C);  // first sb with owner rank
+  const int sb_hi = static_cast<int>((static_cast<int64_t>(rank + 1) * nsb + C - 1) / C);
   float fsum = 0.f;  // plain float total, to flag rows that are not probability vectors
-  for (int sb = warp; sb < nsb; sb += kThreads / 32) {
+  for (int sb = sb_lo + warp; sb < sb_hi; sb += kThreads / 32) {
     uint64_t acc = 0;
     for (int k = 0; k < sb_len; k += 32 * kDrawU) {  // kDrawU loads of each row in flight per lane
       float qv[kDrawU], pv[kDrawU];
@@ -312,6 +322,24 @@ __global__ void __launch_bounds__(kThreads) select_verify_kernel(const SelectVer
   fsum = warp_sum_f32(fsum);
   if (lane == 0) s_fsum[warp] = fsum;
   __syncthreads();
+  if (C > 1) {
+    // rank 0 collects the other ranks' super-block sums and float partial totals
+    cluster_sync();
+    if (rank == 0) {
+      for (int sb = threadIdx.x; sb < nsb; sb += kThreads) {
+        const int o = sb_owner(sb);
+        if (o != 0) s_sb[sb] = ld_cluster_u64(map_to_rank(smem_u32(&s_sb[sb]), o));
+      }
+      if (threadIdx.x < kThreads / 32) {
+        float f = s_fsum[threadIdx.x];
+        for (int o = 1; o < C; ++o) f += ld_cluster_f32(map_to_rank(smem_u32(&s_fsum[threadIdx.x]), o));
+        s_fsum[threadIdx.x] = f;
+      }
+    }
+    cluster_sync();  // no rank leaves while rank 0 reads its shared memory
+    if (rank != 0) return;
+    __syncthreads();
+  }
   if (warp == 0) {
     // prefix over the super-blocks: lane l takes a contiguous run of them
     const int per = (nsb + 31) / 32, s0 = min(nsb, lane * per), s1 = min(nsb, s0 + per);
@@ -335,15 +363,69 @@ __global__ void __launch_bounds__(kThreads) select_verify_kernel(const SelectVer
       run += s_sb[i];
     }
     const uint32_t has = __ballot_sync(kFull, found >= 0);
-    int v_pick = fallback;
-    bool near = true;
+    if (lane == 0) {
+      s_draw[0] = R;
+      s_draw[1] = T;
+      s_draw[2] = has ? 1u : 0u;
+      s_draw[5] = (R < (1ull << 47) || !(ftot < 3.5f)) ? 1u : 0u;  // flag: tiny mass or not a distribution
+    }
     if (has) {
       const int src = __ffs(has) - 1;
       const int sb = __shfl_sync(kFull, found, src);
-      uint64_t base = __shfl_sync(kFull, found_base, src);
+      const uint64_t base = __shfl_sync(kFull, found_base, src);
+      if (lane == 0) {
+        s_draw[3] = static_cast<uint64_t>(sb);
+        s_draw[4] = base;
+      }
+    }
+  }
+  __syncthreads();
+  if (s_draw[2] != 0) {
+    // The crossing super-block: every warp sums 32-element chunks of it (one memory round trip
+    // each, in parallel), warp 0 scans the chunk sums and then the one chunk that crosses.
+    const uint64_t R = s_draw[0], T = s_draw[1];
+    const int sb = static_cast<int>(s_draw[3]);
+    const int nch = sb_len / 32;
+    if (nch <= kMaxSB) {
+      for (int c = warp; c < nch; c += kThreads / 32) {
+        const uint64_t cs = warp_sum_u64(mass(sb * sb_len + c * 32 + lane));
+        if (lane == 0) s_sb[c] = cs;
+      }
+    }
+    __syncthreads();
+    if (warp == 0) {
+      uint64_t base = s_draw[4];
+      int v_pick = fallback;
+      bool near = true;
       const uint64_t tol = R >> 30;  // about 0.93e-9 R
-      for (int k = 0; k < sb_len; k += 32) {
-        const int v = sb * sb_len + k + lane;
+      int c_lo = 0, c_hi = nch;
+      if (nch <= kMaxSB) {
+        // first chunk whose inclusive prefix exceeds T (lane l takes a contiguous run)
+        const int per = (nch + 31) / 32, s0 = min(nch, lane * per), s1 = min(nch, s0 + per);
+        uint64_t mine = 0;
+        for (int i = s0; i < s1; ++i) mine += s_sb[i];
+        const uint64_t incl = warp_scan_u64(mine, lane);
+        uint64_t run = base + incl - mine;
+        int found = -1;
+        uint64_t fb = 0;
+        for (int i = s0; i < s1; ++i) {
+          if (run + s_sb[i] > T) {
+            found = i;
+            fb = run;
+            break;
+          }
+          run += s_sb[i];
+        }
+        const uint32_t hc = __ballot_sync(kFull, found >= 0);
+        if (hc) {
+          const int src = __ffs(hc) - 1;
+          c_lo = __shfl_sync(kFull, found, src);
+          c_hi = c_lo + 1;
+          base = __shfl_sync(kFull, fb, src);
+        }
+      }
+      for (int c = c_lo; c < c_hi; ++c) {
+        const int v = sb * sb_len + c * 32 + lane;
         const uint64_t m = mass(v);
         const uint64_t in = warp_scan_u64(m, lane);
         const uint32_t cross = __ballot_sync(kFull, m > 0 && base + in > T);
@@ -351,7 +433,7 @@ __global__ void __launch_bounds__(kThreads) select_verify_kernel(const SelectVer
           const int l = __ffs(cross) - 1;
           const uint64_t after = base + __shfl_sync(kFull, in, l);
           const uint64_t before = after - __shfl_sync(kFull, m, l);
-          v_pick = sb * sb_len + k + l;
+          v_pick = sb * sb_len + c * 32 + l;
           near = (after - T <= tol) || (T >= before ? T - before <= tol : before - T <= tol);
           break;
         }
@@ -359,12 +441,15 @@ __global__ void __launch_bounds__(kThreads) select_verify_kernel(const SelectVer
       }
       // residual mass below 2^-15 (relative truncation error above 1e-9) or rows that are not
       // probability vectors (sums beyond the fixed-point range) are flagged, not trusted
-      if (R < (1ull << 47) || !(ftot < 3.5f)) near = true;
+      if (s_draw[5] != 0) near = true;
+      if (lane == 0) {
+        com[A] = v_pick;
+        if (a.near_tie) a.near_tie[n] = near ? 1 : 0;
+      }
     }
-    if (lane == 0) {
-      com[A] = v_pick;
-      if (a.near_tie) a.near_tie[n] = near ? 1 : 0;
-    }
+  } else if (threadIdx.x == 0) {
+    com[A] = fallback;
+    if (a.near_tie) a.near_tie[n] = 1;
   }
   if (threadIdx.x == 0) {
     a.accept_len[n] = A;
@@ -377,13 +462,31 @@ __global__ void __launch_bounds__(kThreads) select_verify_kernel(const SelectVer
 }  // namespace
 
 cudaError_t launch_select_verify(const SelectVerifyArgs& a, cudaStream_t stream) {
+  // Sampling modes read whole vocabulary rows: spread each stream over a cluster so that up to
+  // two CTAs per SM (what registers allow) stream them.  The walk and greedy verification stay
+  // one CTA per stream.
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        sms <= 0)
+      sms = 152;
+  }
+  int C = 1;
+  if (a.mode >= 1)
+    while (C < 8 && static_cast<int64_t>(a.N) * C * 2 <= 2 * static_cast<int64_t>(sms)) C *= 2;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.N, 1, 1);
+  cfg.gridDim = dim3(C, a.N, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = pdl_attr(&attr[0]);
+  cfg.numAttrs = C > 1 ? 1 : 0;
+  cfg.numAttrs += pdl_attr(&attr[cfg.numAttrs]);
   return cudaLaunchKernelEx(&cfg, select_verify_kernel, a);
 }
 
