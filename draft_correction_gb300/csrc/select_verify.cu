@@ -95,6 +95,9 @@ __device__ __forceinline__ int warp_argmax(const float* row, int K, int lane) {
   return warp_argmax_ord(a, b, lane);
 }
 
+// kSampling: the instance that also holds the stochastic and speculative draw (modes 1, 2); the
+// other instance (walk, path rules, greedy verification) is compiled without it.
+template <bool kSampling>
 __global__ void __launch_bounds__(kThreads) select_verify_kernel(const SelectVerifyArgs a) {
   __shared__ uint32_t s_S[kStageFloats];  // order codes of the stream's scores
   __shared__ int32_t s_draft[kMaxB];
@@ -264,7 +267,7 @@ __global__ void __launch_bounds__(kThreads) select_verify_kernel(const SelectVer
     }
     return;
   }
-
+  if constexpr (kSampling) {
   // ------------------------------------------------------------------ stochastic draw
   // Row A of q: the residual at the first rejected slot, or the bonus position B (q itself) when
   // every slot was accepted.  Point-mass proposal: q without the draft token; general draft
@@ -457,6 +460,7 @@ __global__ void __launch_bounds__(kThreads) select_verify_kernel(const SelectVer
   }
   for (int j = threadIdx.x; j < A; j += kThreads) com[j] = s_draft[j];
   for (int j = A + 1 + static_cast<int>(threadIdx.x); j <= B; j += kThreads) com[j] = -1;
+  }
 }
 
 }  // namespace
@@ -487,7 +491,8 @@ cudaError_t launch_select_verify(const SelectVerifyArgs& a, cudaStream_t stream)
   cfg.attrs = attr;
   cfg.numAttrs = C > 1 ? 1 : 0;
   cfg.numAttrs += pdl_attr(&attr[cfg.numAttrs]);
-  return cudaLaunchKernelEx(&cfg, select_verify_kernel, a);
+  return a.mode >= 1 ? cudaLaunchKernelEx(&cfg, select_verify_kernel<true>, a)
+                     : cudaLaunchKernelEx(&cfg, select_verify_kernel<false>, a);
 }
 
 }  // namespace dcoco
