@@ -456,6 +456,86 @@ def gpu_arm(args, cfg):
     return 0
 
 
+def sweep_arm(args):
+    """The 42-point draft-correct-verify sweep on the headline shapes: corrected draft blocks/s of
+    the whole cycle with greedy and with stochastic verification at every (N, B, K), one CUDA
+    graph per point, L2 flushed before every step.  Prints one JSON line with every point."""
+    import torch
+
+    import draft_correction_gb300 as dc
+    from draft_correction_gb300 import build as dcb
+
+    dcb.build()
+    dc.lib()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    base = wl.HEADLINE
+    emb = dc.to_device(wl.embedding(base), base.dtype, dev)
+    w = dc.CorrectorWeights.from_numpy(wl.weights(base), base.dtype, dev)
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    flush_clean = torch.zeros(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def timed(fn, steps, warmup):
+        for _ in range(warmup):
+            flush.fill_(1)
+            flush_clean.sum()
+            fn()
+        torch.cuda.synchronize()
+        ms = []
+        for _ in range(steps):
+            flush.fill_(1)
+            flush_clean.sum()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            ms.append(a.elapsed_time(b))
+        return ms
+
+    points = []
+    hbm, _, _ = peaks()
+    for n in wl.SWEEP_STREAMS:
+        for b in wl.SWEEP_B:
+            cfg_nb = base.replace(N=n, B=b)
+            logits = dc.to_device(wl.logits(cfg_nb), base.dtype, dev)
+            hidden = dc.to_device(wl.hidden(cfg_nb), base.dtype, dev)
+            q = dc.to_device(wl.verifier_probs(cfg_nb), "f32", dev)
+            u = dc.to_device(wl.uniforms(cfg_nb), "f32", dev)
+            for k in wl.SWEEP_K:
+                cfg = cfg_nb.replace(name=f"sweep_n{n}_b{b}_k{k}", K=k)
+                cyc = dc.Cycle(w, n, b, k, cfg.V, device=dev, keep_intermediates=False)
+                out = cyc.run(logits, emb, hidden, t=torch.zeros((n, b + 1), dtype=torch.int32, device=dev))
+                torch.cuda.synchronize()
+                t = dc.to_device(wl.verifier_tokens(cfg, out["tokens"].cpu().numpy()), "i32", dev)
+                pt = {"workload": cfg.name, "streams": n, "B": b, "K": k}
+                for mode, name, kw in ((dc.VERIFY_GREEDY, "greedy", {"t": t}),
+                                       (dc.VERIFY_STOCHASTIC, "stochastic", {"q": q, "u": u})):
+                    for _ in range(2):
+                        cyc.run(logits, emb, hidden, mode=mode, **kw)
+                    torch.cuda.synchronize()
+                    g = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(g):
+                        cyc.run(logits, emb, hidden, mode=mode, **kw)
+                    torch.cuda.synchronize()
+                    ms = timed(g.replay, args.steps, args.warmup)
+                    pt[f"{name}_blocks_per_s"] = round(n * len(ms) / (sum(ms) / 1e3), 1)
+                    pt[f"{name}_ms_per_cycle"] = round(sum(ms) / len(ms), 4)
+                    del g
+                # top-K share of the HBM roofline at this point (bf16 logits)
+                pt["logits_mb"] = round(n * b * cfg.V * 2 / 1e6, 1)
+                points.append(pt)
+                del cyc
+            del logits, hidden, q, u
+    assert dc.device_status() == 0, "device status word reports a fault"
+    print(json.dumps({"metric": METRIC, "sweep": points, "unit": "blocks/s", "n_gpus": 1, "steps": args.steps,
+                      "warmup": args.warmup, "dtype": base.dtype, "data": "synthetic",
+                      "l2": "flushed before every timed step", "hbm_peak_gbs": hbm}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -464,8 +544,11 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default=wl.HEADLINE.name, choices=sorted(wl.CONFIGS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true", help="the 42-point (streams, B, K) sweep instead of one workload")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
+    if args.sweep and args.impl == "ours":
+        return sweep_arm(args)
     cfg = wl.CONFIGS[args.config]
     if args.impl == "reference":
         return reference_arm(args, cfg)
