@@ -102,6 +102,16 @@ def _ptr(t: Optional[torch.Tensor]):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _ptr_logits(t: Optional[torch.Tensor]):
+    """Logits may also be a host tensor: page-locked host memory is read by top-K through its
+    device mapping; the library refuses pageable memory."""
+    if t is None or t.is_cuda:
+        return _ptr(t)
+    if not t.is_contiguous():
+        raise ValueError("dcoco: tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
 def _stream():
     return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
 
@@ -179,11 +189,12 @@ def _empty(shape, dtype, like):
 
 
 def topk(logits: torch.Tensor, K: int, vals=None, ids=None):
-    """a1: top-K of every row of logits [N, B, V] -> vals [N, B, K] f32, ids [N, B, K] i32."""
+    """a1: top-K of every row of logits [N, B, V] -> vals [N, B, K] f32, ids [N, B, K] i32.
+    logits may be a pinned host tensor (pass vals and ids on the GPU then)."""
     N, B, V = logits.shape
     vals = _empty((N, B, K), torch.float32, logits) if vals is None else vals
     ids = _empty((N, B, K), torch.int32, logits) if ids is None else ids
-    _check(lib().dcoco_topk(_ptr(logits), _dtype_code(logits), N, B, V, K, _ptr(vals), _ptr(ids), _stream()))
+    _check(lib().dcoco_topk(_ptr_logits(logits), _dtype_code(logits), N, B, V, K, _ptr(vals), _ptr(ids), _stream()))
     return vals, ids
 
 
@@ -344,7 +355,7 @@ class Cycle:
             return o
         fn = lib().dcoco_cycle_table if table is not None else lib().dcoco_cycle
         src = table if table is not None else emb
-        _check(fn(_ptr(logits), self.V, _ptr(src), _ptr(h), self.w.ref, self.N, self.B, self.K, mode,
+        _check(fn(_ptr_logits(logits), self.V, _ptr(src), _ptr(h), self.w.ref, self.N, self.B, self.K, mode,
                                  _ptr(t), _ptr(q), _ptr(u), _ptr(o.get("vals")), _ptr(o.get("ids")),
                                  _ptr(o.get("S")), _ptr(o.get("k_sel")), _ptr(o["tokens"]), _ptr(o["accept_len"]),
                                  _ptr(o["committed"]), _ptr(o["n_commit"]), _ptr(o["near_tie"]), _ptr(self.ws),

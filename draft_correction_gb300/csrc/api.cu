@@ -89,6 +89,27 @@ int check_ptr(const void* p, const char* name) {
   return DCOCO_OK;
 }
 
+// Logits may live in device memory or in page-locked host memory that is mapped into the
+// device's address space (then top-K streams them once over the host link instead of after a
+// bulk copy).  *dev receives the address kernels use; pageable host memory is rejected.
+int resolve_readable(const void* p, const char* name, const void** dev) {
+  cudaPointerAttributes at{};
+  const cudaError_t e = cudaPointerGetAttributes(&at, p);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return cuda_fail(e, name);
+  }
+  if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) {
+    *dev = p;
+    return 0;
+  }
+  if (at.type == cudaMemoryTypeHost && at.devicePointer != nullptr) {
+    *dev = at.devicePointer;
+    return 0;
+  }
+  return fail(DCOCO_ERR_INVALID_ARG, "%s is neither device memory nor page-locked host memory mapped for the device", name);
+}
+
 #define DCOCO_TRY(x)             \
   do {                           \
     const int _rc = (x);         \
@@ -520,6 +541,7 @@ int dcoco_topk(const void* logits, int dtype, int N, int B, int V, int K, float*
   DCOCO_TRY(check_ptr(logits, "logits"));
   DCOCO_TRY(check_ptr(vals, "vals"));
   DCOCO_TRY(check_ptr(ids, "ids"));
+  DCOCO_TRY(resolve_readable(logits, "logits", &logits));
   const bool bf16 = dtype == DCOCO_BF16;
   const int rows = N * B;
   const cudaError_t e = launch_topk(logits, bf16, rows, V, K, topk_split(rows, V, bf16), vals, ids, as_stream(stream));
@@ -836,6 +858,7 @@ int cycle_impl(const void* logits, const void* W_lm, int V, const void* emb, con
   cudaStream_t st = as_stream(stream);
 
   const int rows = N * B;
+  if (W_lm == nullptr) DCOCO_TRY(resolve_readable(logits, "logits", &logits));
   std::lock_guard<std::mutex> lock(g_side_mu);
   SideStream* side = nullptr;
   DCOCO_TRY(side_stream(&side));

@@ -106,6 +106,9 @@ int dcoco_set_topk_split(int ctas_per_row);
  *   vals [N, B, K] float32   the kept logits l_i(k) (exact widening of the input)
  *   ids  [N, B, K] int32     the token ids c_ik
  * Deterministic: the result does not depend on scheduling.  No workspace.
+ * `logits` may be device memory or page-locked host memory mapped for the device (read once over
+ * the host link; on GB300 that streams at about 100 GB/s, so a bulk copy into HBM first is faster);
+ * pageable host memory gives DCOCO_ERR_INVALID_ARG.  The same holds for dcoco_cycle's logits.
  */
 int dcoco_topk(const void* logits, int dtype, int N, int B, int V, int K, float* vals, int32_t* ids, void* stream);
 
