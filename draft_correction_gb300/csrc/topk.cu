@@ -143,17 +143,28 @@ __device__ __forceinline__ void warp_sort64_desc(uint64_t (&x)[2], int lane) {
   }
 }
 
-// Number of entries greater than x in a descending list of n keys.
-__device__ __forceinline__ int count_greater(const uint64_t* list, int n, uint64_t x) {
-  int lo = 0, hi = n;
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (list[mid] > x)
-      lo = mid + 1;
-    else
-      hi = mid;
+// Number of keys above x in nl (<= NL) descending lists of len keys each (list w at
+// lists[w * len]).  The binary searches of all lists advance together, one probe of each per
+// step, so their shared-memory loads overlap; in a descending list the keys above x form a
+// prefix, and pos[w] grows to its length.
+template <int NL>
+__device__ __forceinline__ int rank_in_lists(const uint64_t* lists, int nl, int len, uint64_t x) {
+  int top = 1;  // the largest power of two not above len
+  while (top * 2 <= len) top *= 2;
+  int pos[NL];
+#pragma unroll
+  for (int w = 0; w < NL; ++w) pos[w] = 0;
+  for (int step = top; step > 0; step >>= 1) {
+#pragma unroll
+    for (int w = 0; w < NL; ++w) {
+      const int i = pos[w] + step - 1;
+      if (w < nl && i < len && lists[w * len + i] > x) pos[w] += step;
+    }
   }
-  return lo;
+  int above = 0;
+#pragma unroll
+  for (int w = 0; w < NL; ++w) above += pos[w];
+  return above;
 }
 
 // Merge the kWarps descending, 0-padded lists of K keys in s_wl[w * K ..] into the K largest,
@@ -165,9 +176,7 @@ __device__ __forceinline__ void merge_lists(const uint64_t* s_wl, int K, uint64_
   for (int t = threadIdx.x; t < kWarps * K; t += kThreads) {
     const uint64_t x = s_wl[t];
     if (x == 0) continue;
-    int above = 0;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) above += count_greater(s_wl + w * K, K, x);
+    const int above = rank_in_lists<kWarps>(s_wl, kWarps, K, x);
     if (above < K) s_keep[above] = x;
   }
   __syncthreads();
@@ -443,9 +452,7 @@ __global__ void __launch_bounds__(kThreads, 4) topk_kernel(const void* __restric
     __syncthreads();
     const uint64_t x = s_sorted[threadIdx.x];
     if (x != 0 && K <= kThreads) {
-      int above = 0;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) above += count_greater(s_sorted + w * 32, 32, x);
+      const int above = rank_in_lists<kWarps>(s_sorted, kWarps, 32, x);
       if (above == K - 1) s_thr = x & 0xFFFFFFFF00000000ull;  // value part only: keeps ties
     }
     __syncthreads();
@@ -559,8 +566,7 @@ __global__ void __launch_bounds__(kThreads, 4) topk_kernel(const void* __restric
     for (int c = threadIdx.x; c < S * K; c += kThreads) {
       const uint64_t x = s_cluster[c];
       if (x == 0) continue;
-      int above = 0;
-      for (int w = 0; w < S; ++w) above += count_greater(s_cluster + w * K, K, x);
+      const int above = rank_in_lists<kMaxSplit>(s_cluster, S, K, x);
       if (above < K) {
         vals[row * K + above] = key_value(x);
         ids[row * K + above] = static_cast<int32_t>(key_index(x));
