@@ -502,16 +502,29 @@ __global__ void __launch_bounds__(kThreads, 4) topk_kernel(const void* __restric
       ncand += __popc(b);
     };
     if (!over) {
-      for (int j0 = 0; j0 < nsus; j0 += 32) {  // warp-uniform trip count
-        const int j = j0 + lane;
-        const int vi0 = j < nsus ? s_sus[warp * kSusW + j] : g.vend;
-        uint4 v[kU];
+      // one suspect per lane per round; the next round's 64 bytes are requested before this
+      // round's are keyed, so the rounds' memory latencies overlap
+      auto fetch = [&](int vi0, uint4(&v)[kU]) {
         if (vi0 + kU <= g.vend) {  // the lane's 64 contiguous bytes, one burst
           ld_stream32(g.vp + vi0, v[0], v[1]);
           ld_stream32(g.vp + vi0 + 2, v[2], v[3]);
         } else {
 #pragma unroll
           for (int u = 0; u < kU; ++u) v[u] = vi0 + u < g.vend ? ld_stream(g.vp + vi0 + u) : neg_inf;
+        }
+      };
+      int vi_next = lane < nsus ? s_sus[warp * kSusW + lane] : g.vend;
+      uint4 v_next[kU];
+      if (nsus > 0) fetch(vi_next, v_next);
+      for (int j0 = 0; j0 < nsus; j0 += 32) {  // warp-uniform trip count
+        const int vi0 = vi_next;
+        uint4 v[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) v[u] = v_next[u];
+        if (j0 + 32 < nsus) {
+          const int jn = j0 + 32 + lane;
+          vi_next = jn < nsus ? s_sus[warp * kSusW + jn] : g.vend;
+          fetch(vi_next, v_next);
         }
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
