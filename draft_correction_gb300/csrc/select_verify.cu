@@ -123,9 +123,20 @@ __global__ void __launch_bounds__(kThreads) select_verify_kernel(const SelectVer
     const bool staged = grid_floats <= static_cast<size_t>(kStageFloats);
     const bool greedy = a.rule == 0;
     if (staged) {
-      // greedy walk: order codes (argmax by integer max); whole-path rule: values, NaN as -inf
-      for (size_t i = threadIdx.x; i < grid_floats; i += kThreads)
-        s_S[i] = greedy ? ord32(__float_as_uint(Sn[i])) : __float_as_uint(canon(Sn[i]));
+      // greedy walk: order codes (argmax by integer max); whole-path rule: values, NaN as -inf.
+      // Every thread issues all its loads before storing any, so they are in flight together.
+      constexpr int kPer = kStageFloats / kThreads;
+      float x[kPer];
+#pragma unroll
+      for (int q = 0; q < kPer; ++q) {
+        const size_t i = threadIdx.x + static_cast<size_t>(q) * kThreads;
+        x[q] = i < grid_floats ? Sn[i] : 0.f;
+      }
+#pragma unroll
+      for (int q = 0; q < kPer; ++q) {
+        const size_t i = threadIdx.x + static_cast<size_t>(q) * kThreads;
+        if (i < grid_floats) s_S[i] = greedy ? ord32(__float_as_uint(x[q])) : __float_as_uint(canon(x[q]));
+      }
     }
     __syncthreads();
     if (warp == 0 && !greedy) {
