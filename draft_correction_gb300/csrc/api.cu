@@ -270,6 +270,8 @@ int enqueue_repr_slot(const Dims& D, const void* h, const dcoco_weights* w, cons
     DCOCO_TRY(gemm_group(&a.g[0], w->W_h, D, r, D.d, D.d, BN, s.g, r, EPI_LN, a.M));
     DCOCO_TRY(run_gemm(a, D, BN, st, "gemm g = LN(W_h h)", max_ctas));
   }
+  // gw follows this library's own g GEMM: it may launch early
+  PdlScope pdl_chain;
   // gw = W_f[:, r:2r] g   (the g half of the fusion, once per slot)
   {
     GemmArgs a = {};
@@ -433,6 +435,8 @@ int enqueue_pair(const Dims& D, const void* h, const dcoco_weights* w, float* ws
                          2 * r, EPI_F32, a.M));
     DCOCO_TRY(run_gemm(a, D, BN, st, "gemm W_pair h", max_ctas));
   }
+  // the rest of the chain follows this library's own kernels: each may launch early
+  PdlScope pdl_chain;
   // s_p = hp[p, 0:r] + hp[p+1, r:2r]
   {
     const cudaError_t e = launch_pair_combine(s.hp, s.s, D.bf16, D.N, D.B, r, st);

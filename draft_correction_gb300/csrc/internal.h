@@ -9,8 +9,9 @@ namespace dcoco {
 
 // Kernels enqueued by this thread while set carry the programmatic-stream-serialization launch
 // attribute, so that each may start (prologue, weight loads) while its predecessor finishes.
-// Only the cycle sets it: there every predecessor is one of this library's kernels, none of
-// which writes the weights, and every kernel waits (grid_dep_wait) before touching its data.
+// It is set only where every predecessor is one of this library's kernels, none of which writes
+// the weights (the cycle after its helper streams join, and the second and later kernels of the
+// pair-state and slot chains), and every kernel waits (grid_dep_wait) before touching its data.
 extern thread_local bool g_pdl;
 struct PdlScope {
   PdlScope() { g_pdl = true; }
