@@ -352,6 +352,16 @@ def gpu_arm(args, cfg):
             dc.topk(lg.view(cfg.N, cfg.B, cfg.V), cfg.K, vals=lm_vals, ids=lm_ids)
 
         un_us = 1e3 * statistics.mean(timed_loop(unfused, lm_steps, 2))
+        # for comparison: the same fused kernel with one-CTA MMAs instead of CTA pairs
+        prev_pair = dc.set_lm_pair(-1)
+        try:
+            ws1 = torch.empty((max(16, dc.lib().dcoco_lm_head_topk_workspace_size(1, cfg.N, cfg.B, cfg.V, cfg.K)),),
+                              dtype=torch.uint8, device=dev)
+            one_us = 1e3 * statistics.mean(
+                timed_loop(lambda: dc.lm_head_topk(hidden, W_lm, cfg.K, lm_vals, lm_ids, ws1), lm_steps, 2))
+        finally:
+            dc.set_lm_pair(prev_pair)
+        del ws1
         # the binding roof: W_lm streams once (HBM), the projection is a dense contraction (tensor)
         lm_bytes = cfg.V * cfg.d * (2 if cfg.dtype == "bf16" else 4) + cfg.N * cfg.B * cfg.d * 2
         hbm_peak, _, _ = peaks()
@@ -371,6 +381,7 @@ def gpu_arm(args, cfg):
             "kernel_us": round(lm_us, 1),
             "roofline": lm_roof,
             "unfused_cublas_projection_then_topk_us": round(un_us, 1),
+            "one_cta_mma_kernel_us": round(one_us, 1),
             "note": "dcoco_cycle_lm: the cycle from the drafter's hidden state; W_lm [V, d] synthetic"}
         del W_lm, lg, lm_ws
 

@@ -62,6 +62,7 @@ _SIGNATURES = {
     "dcoco_lm_head_topk_workspace_size": ([_I, _I, _I, _I, _I], _Z),
     "dcoco_lm_head_topk": ([_P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _Z, _P], _I),
     "dcoco_set_lm_cluster": ([_I], _I),
+    "dcoco_set_lm_pair": ([_I], _I),
     "dcoco_cycle_lm_workspace_size": ([_WP, _I, _I, _I, _I], _Z),
     "dcoco_cycle_lm": ([_P, _I, _P, _P, _WP, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _Z,
                         _P], _I),
@@ -294,6 +295,10 @@ def verify_speculative(draft, p, q, u):
 
 def set_lm_cluster(ctas: int) -> int:
     return lib().dcoco_set_lm_cluster(int(ctas))
+
+
+def set_lm_pair(mode: int) -> int:
+    return lib().dcoco_set_lm_pair(int(mode))
 
 
 def lm_head_topk(h: torch.Tensor, W_lm: torch.Tensor, K: int, vals=None, ids=None, ws=None):

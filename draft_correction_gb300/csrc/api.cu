@@ -39,6 +39,7 @@ cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
 int g_topk_split = 0;  // 0 = automatic
 int g_lm_cluster = 0;  // 0 = automatic
+int g_lm_pair = 0;     // 0 = automatic, 1 = always (bf16), -1 = never
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -519,6 +520,12 @@ int dcoco_set_lm_cluster(int ctas) {
   return prev;
 }
 
+int dcoco_set_lm_pair(int mode) {
+  const int prev = g_lm_pair;
+  g_lm_pair = mode > 0 ? 1 : mode < 0 ? -1 : 0;
+  return prev;
+}
+
 int dcoco_device_status(void* stream, uint32_t* bits) {
   clear_err();
   int rc;
@@ -557,7 +564,7 @@ size_t dcoco_lm_head_topk_workspace_size(int dtype, int N, int B, int V, int K) 
   if ((dtype != DCOCO_BF16 && dtype != DCOCO_F32) || N < 1 || B < 1 || V < 1 || K < 1 || K > 64 || K > V ||
       static_cast<int64_t>(N) * B > 65535)
     return 0;
-  return lm_topk_partial_bytes(dtype == DCOCO_BF16, N * B, V, K, g_lm_cluster);
+  return lm_topk_partial_bytes(dtype == DCOCO_BF16, N * B, V, K, g_lm_cluster, g_lm_pair);
 }
 
 int dcoco_lm_head_topk(const void* h, const void* W_lm, int dtype, int N, int B, int d, int V, int K, float* vals,
@@ -574,7 +581,7 @@ int dcoco_lm_head_topk(const void* h, const void* W_lm, int dtype, int N, int B,
   DCOCO_TRY(check_ptr(W_lm, "W_lm"));
   DCOCO_TRY(check_ptr(vals, "vals"));
   DCOCO_TRY(check_ptr(ids, "ids"));
-  const size_t need = lm_topk_partial_bytes(bf16, N * B, V, K, g_lm_cluster);
+  const size_t need = lm_topk_partial_bytes(bf16, N * B, V, K, g_lm_cluster, g_lm_pair);
   if (need == 0) return fail(DCOCO_ERR_CUDA, "no launch plan for the fused LM-head top-K on this device");
   if (workspace == nullptr || workspace_bytes < need)
     return fail(DCOCO_ERR_WORKSPACE, "workspace %zu bytes < %zu required", workspace_bytes, need);
@@ -582,7 +589,7 @@ int dcoco_lm_head_topk(const void* h, const void* W_lm, int dtype, int N, int B,
   int rc;
   unsigned int* status = status_word(&rc);
   if (rc != DCOCO_OK) return rc;
-  const cudaError_t e = launch_lm_topk(h, W_lm, bf16, N * B, d, V, K, g_lm_cluster, vals, ids, workspace,
+  const cudaError_t e = launch_lm_topk(h, W_lm, bf16, N * B, d, V, K, g_lm_cluster, g_lm_pair, vals, ids, workspace,
                                        workspace_bytes, status, as_stream(stream));
   if (e != cudaSuccess) return cuda_fail(e, "LM-head top-K launch");
   return DCOCO_OK;
@@ -844,7 +851,7 @@ int cycle_impl(const void* logits, const void* W_lm, int V, const void* emb, con
   if (W_lm != nullptr) {
     if ((static_cast<size_t>(D.d) * D.esz) % 16 != 0)
       return fail(DCOCO_ERR_INVALID_ARG, "d=%d: rows of h and W_lm must be a multiple of 16 bytes", D.d);
-    lm_bytes = lm_topk_partial_bytes(D.bf16, N * B, V, K, g_lm_cluster);
+    lm_bytes = lm_topk_partial_bytes(D.bf16, N * B, V, K, g_lm_cluster, g_lm_pair);
     if (lm_bytes == 0) return fail(DCOCO_ERR_CUDA, "no launch plan for the fused LM-head top-K on this device");
   }
   const size_t need = base_need + round256(lm_bytes);
@@ -871,7 +878,7 @@ int cycle_impl(const void* logits, const void* W_lm, int V, const void* emb, con
     int rc;
     unsigned int* status = status_word(&rc);
     if (rc != DCOCO_OK) return rc;
-    e = launch_lm_topk(h, W_lm, D.bf16, rows, D.d, V, K, g_lm_cluster, o_vals, o_ids, lm_partial, lm_bytes, status, st);
+    e = launch_lm_topk(h, W_lm, D.bf16, rows, D.d, V, K, g_lm_cluster, g_lm_pair, o_vals, o_ids, lm_partial, lm_bytes, status, st);
   } else {
     e = launch_topk(logits, D.bf16, rows, V, K, topk_split(rows, V, D.bf16), o_vals, o_ids, st);
   }

@@ -21,6 +21,13 @@
 //              shared memory; then every pass of a loop inserts each lane's next marked value
 //              with one compare-exchange pass over the lists, the whole warp together (lanes
 //              with nothing left pass a null key), until no lane has marks left.
+// CTA-pair variant (bf16): the two CTAs of a cluster of 2 act as one MMA unit.  Each holds its
+// own 128-row h tile and one half (128 tokens) of the W_lm tile; the even CTA issues
+// 256 x 256 x 16 MMAs (cta_group::2) that read A and B from both CTAs' shared memory and leave
+// each CTA's 128 rows in its own TMEM.  Per SM that halves the W_lm bytes the tensor core reads
+// and TMA writes per flop, the shared-memory traffic that bounds the one-CTA 128 x 256 MMAs.
+// Both CTAs' loads count on the even CTA's stage barrier; its commits release the stages and
+// accumulators in both CTAs; both CTAs' epilogues release an accumulator to the even CTA.
 // Each (row, cluster, column half) leaves a sorted list of K keys; lm_merge_kernel merges the
 // lists of a row.  Keys are ordered value bits << 32 | ~token, as in the top-K kernel, so the
 // selection is exact on the fp32 logits and deterministic.
@@ -38,13 +45,21 @@ constexpr int BM = 128;
 constexpr int BN = 256;  // vocabulary entries per tile: one accumulator of 256 fp32 columns
 constexpr int kThreads = 320;
 constexpr int kEpiThreads = 256;
-constexpr int kMaxStages = 4;
 constexpr int A_BYTES = BM * 128;
 constexpr int B_BYTES = BN * 128;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int kMaxListsPerLane = 16;  // merge: up to 512 lists per row
 constexpr int kStageValsBytes = kEpiThreads * 32 * 4;  // one 32-column chunk per epilogue thread
-constexpr int kSmem = kMaxStages * STAGE_BYTES + kStageValsBytes + 1024;
+// One-CTA MMAs: 4 stages of the h tile and the whole W_lm tile.  CTA pairs: 6 stages of the h
+// tile and half the W_lm tile.
+template <bool kPair>
+struct Pipe {
+  static constexpr int kStages = kPair ? 6 : 4;
+  static constexpr int kBStage = kPair ? B_BYTES / 2 : B_BYTES;
+  static constexpr int kStageBytes = A_BYTES + kBStage;
+  static constexpr int kSmem = kStages * kStageBytes + kStageValsBytes + 1024;
+};
+constexpr int kMaxStages = 6;
+static_assert(Pipe<true>::kSmem <= 227 * 1024 - 256, "pair pipeline exceeds shared memory");
 
 struct LmArgs {
   CUtensorMap a_map;  // h [rows, d], box {128 bytes, 128 rows}
@@ -83,12 +98,16 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// KR: list length kept per thread (K rounded up to 4, 8, 16, 32 or 64).
-template <bool kBf16, int KR>
+// KR: list length kept per thread (K rounded up to 4, 8, 16, 32 or 64).  kPair: CTA-pair MMAs
+// (bf16 only; clusters of exactly 2).
+template <bool kBf16, int KR, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1) lm_topk_kernel(const __grid_constant__ LmArgs args) {
+  static_assert(!kPair || kBf16, "CTA-pair MMAs are built for bf16 inputs");
   constexpr int BK = kBf16 ? 64 : 32;  // elements per 128-byte row of a stage
   constexpr int UK = kBf16 ? 16 : 8;   // K of one MMA instruction
-  constexpr uint32_t IDESC = mma_idesc(kBf16 ? 1u : 2u, BM, BN);
+  constexpr uint32_t IDESC = mma_idesc(kBf16 ? 1u : 2u, kPair ? 2 * BM : BM, BN);
+  constexpr int S = Pipe<kPair>::kStages;
+  constexpr int STAGE_BYTES = Pipe<kPair>::kStageBytes;
 
   extern __shared__ uint8_t dyn_smem[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
@@ -100,10 +119,11 @@ __global__ void __launch_bounds__(kThreads, 1) lm_topk_kernel(const __grid_const
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  constexpr int S = kMaxStages;
   constexpr int CW = KR >= 64 ? 16 : 32;  // columns per TMEM load (fewer registers beside a long list)
-  const int cm = args.cm, K = args.K;
+  const int cm = kPair ? 2 : args.cm;
+  const int K = args.K;
   const uint32_t rank = cm > 1 ? cluster_rank() : 0u;
+  const bool leader = rank == 0;  // pairs: the CTA that issues the MMAs
   const int clus = blockIdx.x / cm;
   const int m_tile = blockIdx.y * cm + static_cast<int>(rank);
   const int t0 = static_cast<int>(static_cast<long long>(clus) * args.n_vt / args.nclus);
@@ -115,21 +135,27 @@ __global__ void __launch_bounds__(kThreads, 1) lm_topk_kernel(const __grid_const
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(smem_u32(&full_bar[s]), 1);
-      mbar_init(smem_u32(&empty_bar[s]), cm);  // one MMA commit from every CTA of the cluster
+      // pairs: the even CTA's commit; otherwise one MMA commit from every CTA of the cluster
+      mbar_init(smem_u32(&empty_bar[s]), kPair ? 1 : cm);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&acc_full[b]), 1);
-      mbar_init(smem_u32(&acc_empty[b]), kEpiThreads / 32);
+      mbar_init(smem_u32(&acc_empty[b]), (kPair ? 2 : 1) * (kEpiThreads / 32));  // pairs: both CTAs' epilogue warps
     }
     fence_mbar_init();
     prefetch_tmap(&args.a_map);
     prefetch_tmap(&args.b_map);
   }
-  if (warp == 1) tmem_alloc(smem_u32(&tmem_base_s), 2 * BN);
+  if (warp == 1) {
+    if constexpr (kPair)
+      tmem_alloc_pair(smem_u32(&tmem_base_s), 2 * BN);
+    else
+      tmem_alloc(smem_u32(&tmem_base_s), 2 * BN);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (cm > 1) cluster_sync();  // every CTA's barriers exist before the first multicast lands
+  if (cm > 1) cluster_sync();  // every CTA's barriers exist before the first remote arrival lands
   const uint32_t tmem = tmem_base_s;
   const uint32_t smem0 = smem_u32(smem);
   const int total = ntile * nkb;
@@ -150,23 +176,33 @@ __global__ void __launch_bounds__(kThreads, 1) lm_topk_kernel(const __grid_const
         const uint32_t b_s = a_s + A_BYTES;
         const int tile = t0 + i / nkb;
         const int kx = (i % nkb) * BK;
-        mbar_expect_tx(fb, STAGE_BYTES);  // own h tile + every CTA's W_lm slice
-        tma_load_2d(a_s, &args.a_map, kx, m_tile * BM, fb);
-        if (cm > 1)
-          tma_load_2d_multicast(b_s + rank * slice * 128, &args.b_map, kx, tile * BN + static_cast<int>(rank) * slice, fb,
-                                mask);
-        else
-          tma_load_2d(b_s, &args.b_map, kx, tile * BN, fb);
+        if constexpr (kPair) {
+          // both CTAs' h tiles and W_lm halves count on the even CTA's barrier
+          const uint32_t fb_lead = leader ? fb : map_to_rank(fb, 0);
+          if (leader) mbar_expect_tx(fb, 2 * STAGE_BYTES);
+          tma_load_2d_pair(a_s, &args.a_map, kx, m_tile * BM, fb_lead);
+          tma_load_2d_pair(b_s, &args.b_map, kx, tile * BN + static_cast<int>(rank) * slice, fb_lead);
+        } else {
+          mbar_expect_tx(fb, STAGE_BYTES);  // own h tile + every CTA's W_lm slice
+          tma_load_2d(a_s, &args.a_map, kx, m_tile * BM, fb);
+          if (cm > 1)
+            tma_load_2d_multicast(b_s + rank * slice * 128, &args.b_map, kx, tile * BN + static_cast<int>(rank) * slice,
+                                  fb, mask);
+          else
+            tma_load_2d(b_s, &args.b_map, kx, tile * BN, fb);
+        }
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && (!kPair || leader)) {
       int i = 0;
       bool ok = true;
       for (int t = 0; t < ntile && ok; ++t) {
         const int buf = t & 1;
-        if (!mbar_wait(smem_u32(&acc_empty[buf]), ((t >> 1) & 1) ^ 1)) {
+        const bool freed = kPair ? mbar_wait_cluster(smem_u32(&acc_empty[buf]), ((t >> 1) & 1) ^ 1)
+                                 : mbar_wait(smem_u32(&acc_empty[buf]), ((t >> 1) & 1) ^ 1);
+        if (!freed) {
           atomicOr(args.status, DEV_TIMEOUT_ACC);
           break;
         }
@@ -175,7 +211,8 @@ __global__ void __launch_bounds__(kThreads, 1) lm_topk_kernel(const __grid_const
         for (int kb = 0; kb < nkb; ++kb, ++i) {
           const int s = i % S;
           const uint32_t ph = (i / S) & 1;
-          if (!mbar_wait(smem_u32(&full_bar[s]), ph)) {
+          const bool landed = kPair ? mbar_wait_cluster(smem_u32(&full_bar[s]), ph) : mbar_wait(smem_u32(&full_bar[s]), ph);
+          if (!landed) {
             atomicOr(args.status, DEV_TIMEOUT_TMA);
             ok = false;
             break;
@@ -184,15 +221,26 @@ __global__ void __launch_bounds__(kThreads, 1) lm_topk_kernel(const __grid_const
           const uint32_t a_s = smem0 + s * STAGE_BYTES;
           const uint32_t b_s = a_s + A_BYTES;
 #pragma unroll
-          for (int j = 0; j < BK / UK; ++j)
-            tc_mma<!kBf16>(d_tmem, sw128_desc(a_s + j * 32), sw128_desc(b_s + j * 32), IDESC,
-                           (kb > 0 || j > 0) ? 1u : 0u);
-          if (cm > 1)
+          for (int j = 0; j < BK / UK; ++j) {
+            const uint32_t acc = (kb > 0 || j > 0) ? 1u : 0u;
+            if constexpr (kPair)
+              tc_mma_pair_f16(d_tmem, sw128_desc(a_s + j * 32), sw128_desc(b_s + j * 32), IDESC, acc);
+            else
+              tc_mma<!kBf16>(d_tmem, sw128_desc(a_s + j * 32), sw128_desc(b_s + j * 32), IDESC, acc);
+          }
+          if constexpr (kPair)
+            tc_commit_pair_multicast(smem_u32(&empty_bar[s]), mask);
+          else if (cm > 1)
             tc_commit_multicast(smem_u32(&empty_bar[s]), mask);
           else
             tc_commit(smem_u32(&empty_bar[s]));
         }
-        if (ok) tc_commit(smem_u32(&acc_full[buf]));
+        if (ok) {
+          if constexpr (kPair)
+            tc_commit_pair_multicast(smem_u32(&acc_full[buf]), mask);
+          else
+            tc_commit(smem_u32(&acc_full[buf]));
+        }
       }
     }
     __syncwarp();
@@ -203,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1) lm_topk_kernel(const __grid_const
     const int row = m_tile * BM + q * 32 + lane;
     const bool live = row < args.rows;
     // this warp's staging area: column i of the current chunk at sv[i * 32] (lanes interleaved)
-    float* sv = reinterpret_cast<float*>(smem + kMaxStages * STAGE_BYTES) + (warp - 2) * 32 * 32 + lane;
+    float* sv = reinterpret_cast<float*>(smem + S * STAGE_BYTES) + (warp - 2) * 32 * 32 + lane;
     unsigned long long a[KR];
 #pragma unroll
     for (int j = 0; j < KR; ++j) a[j] = 0ull;  // below every real key
@@ -251,7 +299,12 @@ __global__ void __launch_bounds__(kThreads, 1) lm_topk_kernel(const __grid_const
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&acc_empty[buf]));
+      if (lane == 0) {
+        if (kPair && !leader)
+          mbar_arrive_cluster(map_to_rank(smem_u32(&acc_empty[buf]), 0));
+        else
+          mbar_arrive(smem_u32(&acc_empty[buf]));
+      }
     }
     if (live) {
       unsigned long long* dst =
@@ -264,7 +317,14 @@ __global__ void __launch_bounds__(kThreads, 1) lm_topk_kernel(const __grid_const
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if constexpr (kPair) {
+    // the pair's TMEM is released together, once neither CTA reads it any more
+    cluster_sync();
+    if (warp == 1) {
+      tc_fence_after();
+      tmem_dealloc_pair(tmem, 2 * BN);
+    }
+  } else if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 2 * BN);
   }
@@ -320,50 +380,59 @@ __global__ void __launch_bounds__(256) lm_merge_kernel(const unsigned long long*
 
 struct Plan {
   int cm, m_groups, nclus, n_vt;
+  bool pair;
 };
 
 int list_len(int K) { return K <= 4 ? 4 : K <= 8 ? 8 : K <= 16 ? 16 : K <= 32 ? 32 : 64; }
 
 using KernelFn = void (*)(LmArgs);
 
-template <bool kBf16>
+template <bool kBf16, bool kPair>
 KernelFn kernel_for(int KR) {
   switch (KR) {
-    case 4: return lm_topk_kernel<kBf16, 4>;
-    case 8: return lm_topk_kernel<kBf16, 8>;
-    case 16: return lm_topk_kernel<kBf16, 16>;
-    case 32: return lm_topk_kernel<kBf16, 32>;
-    default: return lm_topk_kernel<kBf16, 64>;
+    case 4: return lm_topk_kernel<kBf16, 4, kPair>;
+    case 8: return lm_topk_kernel<kBf16, 8, kPair>;
+    case 16: return lm_topk_kernel<kBf16, 16, kPair>;
+    case 32: return lm_topk_kernel<kBf16, 32, kPair>;
+    default: return lm_topk_kernel<kBf16, 64, kPair>;
   }
 }
 
+// Kernel instances: f32, bf16 (one-CTA MMAs), bf16 CTA pairs; five list lengths each.
+constexpr int kSlots = 15;
+struct Instance {
+  KernelFn fn;
+  int slot, smem;
+};
+Instance instance(bool is_bf16, bool pair, int KR) {
+  const int k = KR == 4 ? 0 : KR == 8 ? 1 : KR == 16 ? 2 : KR == 32 ? 3 : 4;
+  if (pair) return {kernel_for<true, true>(KR), 10 + k, Pipe<true>::kSmem};
+  if (is_bf16) return {kernel_for<true, false>(KR), 5 + k, Pipe<false>::kSmem};
+  return {kernel_for<false, false>(KR), k, Pipe<false>::kSmem};
+}
+
 // Sets the dynamic shared-memory size once per kernel instance and device.
-cudaError_t configure(KernelFn fn, int slot) {
-  static bool done[64][10] = {};
+cudaError_t configure(const Instance& in) {
+  static bool done[64][kSlots] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!done[dev][slot]) {
-    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (!done[dev][in.slot]) {
+    e = cudaFuncSetAttribute(in.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, in.smem);
     if (e != cudaSuccess) return e;
-    done[dev][slot] = true;
+    done[dev][in.slot] = true;
   }
   return cudaSuccess;
 }
 
-int slot_of(bool is_bf16, int KR) {
-  const int k = KR == 4 ? 0 : KR == 8 ? 1 : KR == 16 ? 2 : KR == 32 ? 3 : 4;
-  return (is_bf16 ? 5 : 0) + k;
-}
-
 // Clusters of `cm` CTAs of this kernel that fit on the device at once (0 on failure).
-int active_clusters(KernelFn fn, int slot, int cm) {
-  if (configure(fn, slot) != cudaSuccess) return 0;
+int active_clusters(const Instance& in, int cm) {
+  if (configure(in) != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(cm * 64, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmem;
+  cfg.dynamicSmemBytes = in.smem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = cm;
@@ -372,39 +441,44 @@ int active_clusters(KernelFn fn, int slot, int cm) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(fn), &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(in.fn), &cfg) != cudaSuccess) {
     (void)cudaGetLastError();
     return 0;
   }
   return n;
 }
 
-// The launch plan: cluster size (forced, or the one that keeps the most CTAs resident, larger
-// clusters on ties), then as many vocabulary ranges as fit in one wave.
-cudaError_t plan_for(bool is_bf16, int rows, int V, int K, int force_cm, Plan* p) {
+// The launch plan.  CTA pairs (bf16) when pair_mode > 0, or when pair_mode == 0, no cluster size
+// is forced and h has at least two row tiles; otherwise the one-CTA kernel with the cluster size
+// that is forced, or that keeps the most CTAs resident (larger clusters on ties).  Then as many
+// vocabulary ranges as fit in one wave.
+cudaError_t plan_for(bool is_bf16, int rows, int V, int K, int force_cm, int pair_mode, Plan* p) {
   const int KR = list_len(K);
-  const int slot = slot_of(is_bf16, KR);
-  const KernelFn fn = is_bf16 ? kernel_for<true>(KR) : kernel_for<false>(KR);
   const int m_tiles = (rows + BM - 1) / BM;
   p->n_vt = (V + BN - 1) / BN;
-  static int cache[64][10][3];  // active clusters + 1 per device, instance and cluster size (0 = unknown)
+  p->pair = is_bf16 && (pair_mode > 0 || (pair_mode == 0 && force_cm == 0 && m_tiles >= 2));
+  static int cache[64][kSlots][3];  // active clusters + 1 per device, instance and cluster size (0 = unknown)
   int dev = 0;
   const cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  const Instance in = instance(is_bf16, p->pair, KR);
   auto active = [&](int cm) {
-    int& c = cache[dev][slot][cm == 4 ? 2 : cm == 2 ? 1 : 0];
-    if (c == 0) c = active_clusters(fn, slot, cm) + 1;
+    int& c = cache[dev][in.slot][cm == 4 ? 2 : cm == 2 ? 1 : 0];
+    if (c == 0) c = active_clusters(in, cm) + 1;
     return c - 1;
   };
-  int best_cm = 1, best_ctas = -1;
-  for (int cm : {4, 2, 1}) {
-    if (force_cm > 0 && cm != force_cm) continue;
-    if (force_cm == 0 && cm > 1 && m_tiles < cm) continue;
-    const int ctas = active(cm) * cm;
-    if (ctas > best_ctas) {
-      best_ctas = ctas;
-      best_cm = cm;
+  int best_cm = 2;
+  if (!p->pair) {
+    int best_ctas = -1;
+    for (int cm : {4, 2, 1}) {
+      if (force_cm > 0 && cm != force_cm) continue;
+      if (force_cm == 0 && cm > 1 && m_tiles < cm) continue;
+      const int ctas = active(cm) * cm;
+      if (ctas > best_ctas) {
+        best_ctas = ctas;
+        best_cm = cm;
+      }
     }
   }
   p->cm = best_cm;
@@ -416,17 +490,17 @@ cudaError_t plan_for(bool is_bf16, int rows, int V, int K, int force_cm, Plan* p
 
 }  // namespace
 
-size_t lm_topk_partial_bytes(bool is_bf16, int rows, int V, int K, int force_cm) {
+size_t lm_topk_partial_bytes(bool is_bf16, int rows, int V, int K, int force_cm, int pair_mode) {
   Plan p;
-  if (plan_for(is_bf16, rows, V, K, force_cm, &p) != cudaSuccess) return 0;
+  if (plan_for(is_bf16, rows, V, K, force_cm, pair_mode, &p) != cudaSuccess) return 0;
   return static_cast<size_t>(rows) * (2 * p.nclus) * K * 8;
 }
 
 cudaError_t launch_lm_topk(const void* h, const void* W_lm, bool is_bf16, int rows, int d, int V, int K, int force_cm,
-                           float* vals, int32_t* ids, void* partial, size_t partial_bytes, unsigned int* status,
-                           cudaStream_t stream) {
+                           int pair_mode, float* vals, int32_t* ids, void* partial, size_t partial_bytes,
+                           unsigned int* status, cudaStream_t stream) {
   Plan p;
-  cudaError_t e = plan_for(is_bf16, rows, V, K, force_cm, &p);
+  cudaError_t e = plan_for(is_bf16, rows, V, K, force_cm, pair_mode, &p);
   if (e != cudaSuccess) return e;
   const int n_lists = 2 * p.nclus;
   if (n_lists > 32 * kMaxListsPerLane) return cudaErrorInvalidValue;
@@ -447,14 +521,13 @@ cudaError_t launch_lm_topk(const void* h, const void* W_lm, bool is_bf16, int ro
   a.nclus = p.nclus;
   a.cm = p.cm;
   a.status = status;
-  const int KR = list_len(K);
-  const KernelFn fn = is_bf16 ? kernel_for<true>(KR) : kernel_for<false>(KR);
-  e = configure(fn, slot_of(is_bf16, KR));
+  const Instance in = instance(is_bf16, p.pair, list_len(K));
+  e = configure(in);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.cm * p.nclus, p.m_groups, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmem;
+  cfg.dynamicSmemBytes = in.smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -463,7 +536,7 @@ cudaError_t launch_lm_topk(const void* h, const void* W_lm, bool is_bf16, int ro
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, fn, a);
+  e = cudaLaunchKernelEx(&cfg, in.fn, a);
   if (e != cudaSuccess) return e;
   lm_merge_kernel<<<(rows + 7) / 8, 256, 0, stream>>>(static_cast<const unsigned long long*>(partial), rows, n_lists, K,
                                                       vals, ids);

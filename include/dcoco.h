@@ -276,7 +276,8 @@ int dcoco_cycle_table(const void* logits, int V, const void* table, const void* 
  *   vals [N, B, K] float32  the kept fp32 logits, descending, equal values by ascending id
  *   ids  [N, B, K] int32
  * Workspace: dcoco_lm_head_topk_workspace_size bytes (per-row partial lists; the size depends
- * on the current device and on dcoco_set_lm_cluster), 16-byte aligned, caller-owned.
+ * on the current device, dcoco_set_lm_cluster and dcoco_set_lm_pair), 16-byte aligned,
+ * caller-owned.
  * Selection is exact on the fp32 logits it computes and deterministic.  The fp32 logits differ
  * from exact dot products by accumulation rounding, so two tokens whose exact logits lie within
  * that rounding may rank in either order.
@@ -291,6 +292,15 @@ int dcoco_lm_head_topk(const void* h, const void* W_lm, int dtype, int N, int B,
  * resident).  Process-wide; returns the previous value.  Query workspace sizes after setting it.
  */
 int dcoco_set_lm_cluster(int ctas);
+
+/*
+ * Tuning knob: CTA-pair MMAs in dcoco_lm_head_topk for bf16 inputs (two CTAs of a cluster
+ * issue one 256-row MMA together, each holding half of every W_lm tile).  0 = automatic
+ * (pairs when h has at least two 128-row tiles and no cluster size is forced), 1 = always,
+ * -1 = never (dcoco_set_lm_cluster then applies).  f32 inputs never use pairs.  Process-wide;
+ * returns the previous value.  Query workspace sizes after setting it.
+ */
+int dcoco_set_lm_pair(int mode);
 
 /*
  * dcoco_cycle starting from the drafter's hidden state instead of its logits: top-K is

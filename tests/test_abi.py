@@ -154,6 +154,12 @@ def test_lm_cluster_knob(L):
     assert L.dcoco_set_lm_cluster(prev) == 0
 
 
+def test_lm_pair_knob(L):
+    prev = L.dcoco_set_lm_pair(5)                # any positive value: always
+    assert L.dcoco_set_lm_pair(-3) == 1          # any negative value: never
+    assert L.dcoco_set_lm_pair(prev) == -1
+
+
 def test_cycle_lm_argument_errors(L):
     w = _weights()
     args = [1000, FAKE, FAKE, ctypes.byref(w), 1, 4, 3, 0, FAKE, None, None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,

@@ -38,6 +38,7 @@ def built():
     dc.lib()
     yield
     dc.set_lm_cluster(0)
+    dc.set_lm_pair(0)
     assert dc.device_status() == 0, "a kernel reported a timeout or a bad index"
 
 
@@ -137,6 +138,33 @@ def test_lm_head_topk_same_result_for_every_cluster_size(shape):
         np.testing.assert_array_equal(v, res[0][0])
 
 
+PAIR_CASES = [
+    (1, 1, 64, 300, 1),      # one row: the odd CTA of the pair holds only zero-filled rows
+    (2, 16, 200, 4097, 16),  # one row tile, ragged k-block and vocabulary tail
+    (3, 43, 520, 2500, 33),  # two row tiles: one full pair
+    (1, 520, 64, 777, 8),    # five row tiles: three pairs, the last one half empty
+    (2, 150, 136, 5000, 64), # three row tiles, K = 64
+]
+
+
+@pytest.mark.parametrize("mode", [1, -1], ids=["pairs", "one-cta"])
+@pytest.mark.parametrize("N,B,d,V,K", PAIR_CASES, ids=[f"{c[0]}x{c[1]}-d{c[2]}-V{c[3]}-K{c[4]}" for c in PAIR_CASES])
+def test_lm_head_topk_cta_pairs_and_single_ctas(N, B, d, V, K, mode):
+    """CTA-pair MMAs (one 256-row MMA over two CTAs' shared memory) forced on, and forced off,
+    against exact float64 logits under the rule of this file."""
+    cfg = lm_cfg("bf16", N, B, d, V, K)
+    h, W = lm_inputs(cfg)
+    prev = dc.set_lm_pair(mode)
+    try:
+        vals, ids = dc.lm_head_topk(dc.to_device(h, "bf16"), dc.to_device(W, "bf16"), K)
+        torch.cuda.synchronize()
+    finally:
+        dc.set_lm_pair(prev)
+    h64 = f64(h, cfg).reshape(N * B, d)
+    L, A = exact_logits(h64, W, cfg)
+    check_rows(vals.cpu().numpy().reshape(N * B, K), ids.cpu().numpy().reshape(N * B, K), L, A, K, rel_tol(cfg))
+
+
 def test_lm_head_topk_duplicate_rows_tie_to_lower_id():
     """Tokens with identical W_lm rows get bit-identical logits; the lower id ranks first."""
     cfg = lm_cfg("bf16", 1, 8, 128, 1500, 12)
@@ -158,13 +186,19 @@ def headline_inputs():
     return wl.hidden(cfg), wl.lm_head(cfg)
 
 
-def test_lm_head_topk_headline_size():
-    """512 rows x V = 151936 x d = 4096 in the launch configuration the benchmark times: all
-    rows for order and distinctness, sampled rows against exact float64 logits."""
+@pytest.mark.parametrize("mode", [0, -1], ids=["automatic", "one-cta"])
+def test_lm_head_topk_headline_size(mode):
+    """512 rows x V = 151936 x d = 4096 in the launch configuration the benchmark times (the
+    automatic plan: CTA pairs), and with one-CTA MMAs: all rows for order and distinctness,
+    sampled rows against exact float64 logits."""
     cfg = wl.HEADLINE
     h, W = headline_inputs()
-    vals, ids = dc.lm_head_topk(dc.to_device(h, "bf16"), dc.to_device(W, "bf16"), cfg.K)
-    torch.cuda.synchronize()
+    prev = dc.set_lm_pair(mode)
+    try:
+        vals, ids = dc.lm_head_topk(dc.to_device(h, "bf16"), dc.to_device(W, "bf16"), cfg.K)
+        torch.cuda.synchronize()
+    finally:
+        dc.set_lm_pair(prev)
     g_v = vals.cpu().numpy().reshape(-1, cfg.K).astype(np.float64)
     g_i = ids.cpu().numpy().reshape(-1, cfg.K)
     assert np.all(np.diff(g_v, axis=1) <= 0)
