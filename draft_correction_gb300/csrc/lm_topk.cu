@@ -278,10 +278,17 @@ __global__ void __launch_bounds__(kThreads, 1) lm_topk_kernel(const __grid_const
             tmem_ld32(taddr + c, v);
           else
             tmem_ld16(taddr + c, v);
+          // Most chunks hold nothing that reaches the list: one max, one compare.  (fmaxf skips
+          // NaN, which ranks below every number; NaN thr, a list not yet full, takes every chunk.)
+          float mx = v[0];
 #pragma unroll
-          for (int i = 0; i < CW; ++i) {
-            m |= (v[i] < thr ? 0u : 1u) << i;
-            sv[i * 32] = v[i];
+          for (int i = 1; i < CW; ++i) mx = fmaxf(mx, v[i]);
+          if (!(mx < thr)) {
+#pragma unroll
+            for (int i = 0; i < CW; ++i) {
+              m |= (v[i] < thr ? 0u : 1u) << i;
+              sv[i * 32] = v[i];
+            }
           }
         }
         const int valid = args.V - (col0 + c);

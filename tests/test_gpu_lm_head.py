@@ -118,21 +118,29 @@ def test_lm_head_topk_matches_oracle(dtype, N, B, d, V, K):
 
 @pytest.mark.parametrize("shape", [(3, 43, 520, 2500, 16), (4, 32, 128, 3000, 16)], ids=["3-row-tiles", "4-row-tiles"])
 def test_lm_head_topk_same_result_for_every_cluster_size(shape):
-    """Each CTA accumulates its whole 128 x 256 tile in the same order whatever the cluster
-    size, so the logits and the selection are bit-identical."""
+    """Each CTA accumulates its whole 128 x 256 tile in the same order (k ascending, 16 per MMA)
+    whatever the cluster size, and so does each CTA of a pair with 256-row MMAs, so the logits
+    and the selection are bit-identical."""
     N, B, d, V, K = shape
     cfg = lm_cfg("bf16", N, B, d, V, K)
     h, W = lm_inputs(cfg)
     hd, Wd = dc.to_device(h, "bf16"), dc.to_device(W, "bf16")
     res = []
     try:
+        dc.set_lm_pair(-1)
         for cm in (1, 2, 4):
             dc.set_lm_cluster(cm)
             v, i = dc.lm_head_topk(hd, Wd, K)
             torch.cuda.synchronize()
             res.append((v.cpu().numpy(), i.cpu().numpy()))
+        dc.set_lm_cluster(0)
+        dc.set_lm_pair(1)
+        v, i = dc.lm_head_topk(hd, Wd, K)
+        torch.cuda.synchronize()
+        res.append((v.cpu().numpy(), i.cpu().numpy()))
     finally:
         dc.set_lm_cluster(0)
+        dc.set_lm_pair(0)
     for v, i in res[1:]:
         np.testing.assert_array_equal(i, res[0][1])
         np.testing.assert_array_equal(v, res[0][0])
