@@ -16,16 +16,17 @@
 //              commit, so no CTA refills a stage that another CTA still reads.
 //   warps 2-9  epilogue: while the next tile accumulates in the other buffer, each thread
 //              reads 128 columns of its row and keeps a running top-K of everything it has
-//              seen: a descending list of KR >= K keys in registers.  Per 32 columns each lane
-//              marks the values that reach its list's last key and parks the 32 values in
-//              shared memory; then every pass of a loop inserts each lane's next marked value
+//              seen: a descending list of KR >= K keys in registers.  Per 32 columns a lane
+//              compares their maximum with its list's last key and, if it reaches it, marks
+//              the values that do and parks the 32 values in shared memory; then every pass
+//              of a loop inserts each lane's next marked value
 //              with one compare-exchange pass over the lists, the whole warp together (lanes
 //              with nothing left pass a null key), until no lane has marks left.
 // CTA-pair variant (bf16): the two CTAs of a cluster of 2 act as one MMA unit.  Each holds its
 // own 128-row h tile and one half (128 tokens) of the W_lm tile; the even CTA issues
 // 256 x 256 x 16 MMAs (cta_group::2) that read A and B from both CTAs' shared memory and leave
 // each CTA's 128 rows in its own TMEM.  Per SM that halves the W_lm bytes the tensor core reads
-// and TMA writes per flop, the shared-memory traffic that bounds the one-CTA 128 x 256 MMAs.
+// and TMA writes per flop; the smaller stages (32 KB) also leave room for 6 of them.
 // Both CTAs' loads count on the even CTA's stage barrier; its commits release the stages and
 // accumulators in both CTAs; both CTAs' epilogues release an accumulator to the even CTA.
 // Each (row, cluster, column half) leaves a sorted list of K keys; lm_merge_kernel merges the
