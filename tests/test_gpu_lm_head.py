@@ -253,3 +253,50 @@ def test_cycle_lm_matches_oracle(cfg):
             np.testing.assert_array_equal(g["tokens"][n], ref["tokens"][n])
             assert g["accept_len"][n] == ver["accept_len"][n]
             np.testing.assert_array_equal(g["committed"][n], ver["committed"][n])
+
+
+@pytest.mark.slow
+def test_cycle_lm_headline_size():
+    """dcoco_cycle_lm at the headline shapes (512 rows, V = 151936, d = 4096, CTA-pair MMAs):
+    three sampled streams through the whole cycle against the oracle, whose top-K comes from
+    exact float64 logits of those streams' rows.  A stream with a near-tie swap among its
+    candidates is checked for that swap only (the rule of this file)."""
+    cfg = wl.HEADLINE
+    h, W_lm = headline_inputs()
+    emb = emb_table(cfg)
+    w = wl.weights(cfg)
+    W = w64(w, cfg)
+    sam = [0, cfg.N // 2, cfg.N - 1]
+    h64 = f64(h[sam], cfg)
+    L, A = exact_logits(h64.reshape(-1, cfg.d), W_lm, cfg)
+    vals_r, ids_r = oracle.topk(L, cfg.K)
+    vals_r = vals_r.reshape(len(sam), cfg.B, cfg.K)
+    ids_r = ids_r.reshape(len(sam), cfg.B, cfg.K)
+    uniq, inv = np.unique(ids_r, return_inverse=True)
+    rep = oracle.candidate_repr(inv.reshape(ids_r.shape), f64(emb[uniq], cfg), h64, W)
+    S_ref = oracle.transition_scores(rep["z"], oracle.pair_state(h64, W), vals_r, W)
+    k_ref, tok_ref = oracle.select(S_ref, vals_r, ids_r)
+    draft = np.zeros((cfg.N, cfg.B), dtype=np.int64)  # streams the oracle does not walk: any draft
+    draft[sam] = tok_ref
+    t = wl.verifier_tokens(cfg, draft)
+    ver = oracle.verify_greedy(tok_ref, t[sam])
+
+    cw = dc.CorrectorWeights.from_numpy(w, cfg.dtype)
+    cyc = dc.Cycle(cw, cfg.N, cfg.B, cfg.K, cfg.V)
+    out = cyc.run(None, dc.to_device(emb, cfg.dtype), dc.to_device(h, cfg.dtype), t=dc.to_device(t, "i32"),
+                  W_lm=dc.to_device(W_lm, cfg.dtype))
+    torch.cuda.synchronize()
+    g = {k: v.cpu().numpy()[sam] for k, v in out.items()}
+
+    check_rows(g["vals"].reshape(-1, cfg.K), g["ids"].reshape(-1, cfg.K), L, A, cfg.K, rel_tol(cfg))
+    full = 0
+    for i in range(len(sam)):
+        if not np.array_equal(g["ids"][i], ids_r[i]):
+            continue
+        assert_scores_close(g["S"][i][None], S_ref[i][None])
+        if compare_walk(g["k_sel"][i][None], k_ref[i][None], S_ref[i][None], vals_r[i][None]) == 0:
+            np.testing.assert_array_equal(g["tokens"][i], tok_ref[i])
+            assert g["accept_len"][i] == ver["accept_len"][i]
+            np.testing.assert_array_equal(g["committed"][i], ver["committed"][i])
+            full += 1
+    assert full >= 2, f"only {full} of {len(sam)} sampled streams compared in full"
