@@ -43,6 +43,32 @@ def peaks():
         return FALLBACK_HBM_GBS, 1900.0, "fallback"
 
 
+# ----------------------------------------------------------------------------- replicas (N ranks)
+
+
+def rank_workload(cfg, rank: int):
+    """Rank r runs its own replica on its own N streams: the input seeds are offset by r * N
+    (the weights and the embedding table are the same on every rank)."""
+    return cfg.replace(base_seed=cfg.base_seed + rank * cfg.N) if rank else cfg
+
+
+def max_over_ranks(ms: float, world: int, device=None) -> float:
+    """The job's time for a region that every rank timed: the slowest rank's.  A collective
+    (every rank calls it); with one rank, ms itself."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world: int, n_streams: int, steps: int, ms: float) -> float:
+    """Corrected draft blocks per second of the whole job: every rank's streams over the job's time."""
+    return world * n_streams * steps / (ms / 1e3)
+
+
 # ----------------------------------------------------------------------------- CPU oracle arm
 
 ORACLE_SNIPPET = r"""
@@ -226,7 +252,7 @@ def gpu_arm(args, cfg):
     dc.lib()
 
     # Inputs: every rank owns its own N streams (seeds offset by rank); table and weights shared.
-    rcfg = cfg.replace(base_seed=cfg.base_seed + rank * cfg.N) if rank else cfg
+    rcfg = rank_workload(cfg, rank)
     logits_h = wl.logits(rcfg)
     hidden_h = wl.hidden(rcfg)
     emb = dc.to_device(wl.embedding(cfg), cfg.dtype, dev)
@@ -291,13 +317,8 @@ def gpu_arm(args, cfg):
         ms = timed_loop(graph.replay, args.steps, args.warmup)
         clk.mark()
     torch.cuda.synchronize()
-    total_ms = sum(ms)
-    if world > 1:
-        tt = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
-    blocks = world * cfg.N * args.steps
-    value = blocks / (total_ms / 1e3)
+    total_ms = max_over_ranks(sum(ms), world, dev)
+    value = whole_job_rate(world, cfg.N, args.steps, total_ms)
     assert dc.device_status() == 0, "device status word reports a fault"
 
     # Variant: the per-vocabulary candidate table (LN(W_e Emb) computed once, outside the timed
@@ -478,7 +499,7 @@ def gpu_arm(args, cfg):
     e2e_run(e2e_steps)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_val = cfg.N * e2e_steps / (e0.elapsed_time(e1) / 1e3) * world
+    e2e_val = whole_job_rate(world, cfg.N, e2e_steps, max_over_ranks(e0.elapsed_time(e1), world, dev))
     h2d = logits_h.nbytes + hidden_h.nbytes + t_host.nbytes
     d2h = com_pin.numel() * 4 + acc_pin.numel() * 4
 
