@@ -35,6 +35,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -496,10 +497,14 @@ cudaError_t plan_for(bool is_bf16, int rows, int V, int K, int force_cm, int pai
   return cudaSuccess;
 }
 
+// Guards the per-device plan and attribute caches against concurrent calls.
+std::mutex g_plan_mu;
+
 }  // namespace
 
 size_t lm_topk_partial_bytes(bool is_bf16, int rows, int V, int K, int force_cm, int pair_mode) {
   Plan p;
+  std::lock_guard<std::mutex> lock(g_plan_mu);
   if (plan_for(is_bf16, rows, V, K, force_cm, pair_mode, &p) != cudaSuccess) return 0;
   return static_cast<size_t>(rows) * (2 * p.nclus) * K * 8;
 }
@@ -508,6 +513,7 @@ cudaError_t launch_lm_topk(const void* h, const void* W_lm, bool is_bf16, int ro
                            int pair_mode, float* vals, int32_t* ids, void* partial, size_t partial_bytes,
                            unsigned int* status, cudaStream_t stream) {
   Plan p;
+  std::unique_lock<std::mutex> lock(g_plan_mu);
   cudaError_t e = plan_for(is_bf16, rows, V, K, force_cm, pair_mode, &p);
   if (e != cudaSuccess) return e;
   const int n_lists = 2 * p.nclus;
@@ -531,6 +537,7 @@ cudaError_t launch_lm_topk(const void* h, const void* W_lm, bool is_bf16, int ro
   a.status = status;
   const Instance in = instance(is_bf16, p.pair, list_len(K));
   e = configure(in);
+  lock.unlock();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.cm * p.nclus, p.m_groups, 1);
