@@ -50,6 +50,10 @@ constexpr int kEpiThreads = 256;
 constexpr int A_BYTES = BM * 128;
 constexpr int B_BYTES = BN * 128;
 constexpr int kMaxListsPerLane = 16;  // merge: up to 512 lists per row
+// Epilogue warps that share one row's 256 columns of a tile (each keeps its own list of its
+// 256 / kColSplit columns); 4 * kColSplit epilogue warps work, the others stay idle.
+constexpr int kColSplit = 2;
+constexpr int kEpiWorkWarps = 4 * kColSplit;
 constexpr int kStageValsBytes = kEpiThreads * 32 * 4;  // one 32-column chunk per epilogue thread
 // One-CTA MMAs: 4 stages of the h tile and the whole W_lm tile.  CTA pairs: 6 stages of the h
 // tile and half the W_lm tile.
@@ -69,7 +73,7 @@ struct LmArgs {
   unsigned long long* partial;  // [rows, n_lists, K] keys, each list descending
   int rows, d, V, K;
   int n_vt;    // vocabulary tiles, ceil(V / BN)
-  int nclus;   // clusters per row group (vocabulary ranges); n_lists = 2 * nclus
+  int nclus;   // clusters per row group (vocabulary ranges); n_lists = kColSplit * nclus
   int cm;      // CTAs per cluster (row tiles sharing the W_lm tile)
   unsigned int* status;
 };
@@ -142,7 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1) lm_topk_kernel(const __grid_const
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&acc_full[b]), 1);
-      mbar_init(smem_u32(&acc_empty[b]), (kPair ? 2 : 1) * (kEpiThreads / 32));  // pairs: both CTAs' epilogue warps
+      mbar_init(smem_u32(&acc_empty[b]), (kPair ? 2 : 1) * kEpiWorkWarps);  // pairs: both CTAs' epilogue warps
     }
     fence_mbar_init();
     prefetch_tmap(&args.a_map);
@@ -246,10 +250,11 @@ __global__ void __launch_bounds__(kThreads, 1) lm_topk_kernel(const __grid_const
       }
     }
     __syncwarp();
-  } else {
-    // ------------------------------------------------------------ epilogue (warps 2..9)
+  } else if (warp < 2 + kEpiWorkWarps) {
+    // ------------------------------------------------------------ epilogue (warps 2..)
+    constexpr int CPW = BN / kColSplit;  // columns of each tile per warp
     const int q = warp & 3;            // TMEM lane quarter this warp may access
-    const int half = (warp - 2) >> 2;  // which 128 columns of each tile
+    const int half = (warp - 2) >> 2;  // which CPW columns of each tile
     const int row = m_tile * BM + q * 32 + lane;
     const bool live = row < args.rows;
     // this warp's staging area: column i of the current chunk at sv[i * 32] (lanes interleaved)
@@ -268,9 +273,9 @@ __global__ void __launch_bounds__(kThreads, 1) lm_topk_kernel(const __grid_const
         break;
       }
       tc_fence_after();
-      const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * BN + half * 128;
-      const int col0 = (t0 + t) * BN + half * 128;
-      for (int c = 0; c < 128; c += CW) {
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * BN + half * CPW;
+      const int col0 = (t0 + t) * BN + half * CPW;
+      for (int c = 0; c < CPW; c += CW) {
         // Which of these CW columns reach this lane's threshold (columns past V hold products
         // with zero-filled W_lm rows and never count).
         uint32_t m = 0;
@@ -317,7 +322,8 @@ __global__ void __launch_bounds__(kThreads, 1) lm_topk_kernel(const __grid_const
     }
     if (live) {
       unsigned long long* dst =
-          args.partial + (static_cast<size_t>(row) * (2 * args.nclus) + clus * 2 + half) * static_cast<size_t>(K);
+          args.partial + (static_cast<size_t>(row) * (kColSplit * args.nclus) + clus * kColSplit + half) *
+                             static_cast<size_t>(K);
 #pragma unroll
       for (int j = 0; j < KR; ++j)
         if (j < K) dst[j] = a[j];
@@ -506,7 +512,7 @@ size_t lm_topk_partial_bytes(bool is_bf16, int rows, int V, int K, int force_cm,
   Plan p;
   std::lock_guard<std::mutex> lock(g_plan_mu);
   if (plan_for(is_bf16, rows, V, K, force_cm, pair_mode, &p) != cudaSuccess) return 0;
-  return static_cast<size_t>(rows) * (2 * p.nclus) * K * 8;
+  return static_cast<size_t>(rows) * (kColSplit * p.nclus) * K * 8;
 }
 
 cudaError_t launch_lm_topk(const void* h, const void* W_lm, bool is_bf16, int rows, int d, int V, int K, int force_cm,
@@ -516,7 +522,7 @@ cudaError_t launch_lm_topk(const void* h, const void* W_lm, bool is_bf16, int ro
   std::unique_lock<std::mutex> lock(g_plan_mu);
   cudaError_t e = plan_for(is_bf16, rows, V, K, force_cm, pair_mode, &p);
   if (e != cudaSuccess) return e;
-  const int n_lists = 2 * p.nclus;
+  const int n_lists = kColSplit * p.nclus;
   if (n_lists > 32 * kMaxListsPerLane) return cudaErrorInvalidValue;
   if (static_cast<size_t>(rows) * n_lists * K * 8 > partial_bytes) return cudaErrorInvalidValue;
   LmArgs a;
