@@ -348,8 +348,9 @@ class Cycle:
         output projection of `h` (dcoco_cycle_lm) and `logits` is not read."""
         o = self.out
         if W_lm is not None:
-            if self.ws_lm is None:
-                nbytes = lib().dcoco_cycle_lm_workspace_size(self.w.ref, self.N, self.B, self.K, self.V)
+            # the size depends on the LM-head knobs (set_lm_cluster, set_lm_pair): grow if needed
+            nbytes = lib().dcoco_cycle_lm_workspace_size(self.w.ref, self.N, self.B, self.K, self.V)
+            if self.ws_lm is None or self.ws_lm.numel() < nbytes:
                 self.ws_lm = torch.empty((max(nbytes, 16),), dtype=torch.uint8, device=self.ws.device)
             ws = self.ws_lm
             _check(lib().dcoco_cycle_lm(_ptr(W_lm), self.V, _ptr(emb), _ptr(h), self.w.ref, self.N, self.B, self.K,
