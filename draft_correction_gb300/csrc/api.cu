@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -14,6 +15,18 @@
 
 namespace dcoco {
 thread_local bool g_pdl = false;
+
+int sm_count() {
+  static std::atomic<int> sms[64];  // per device, 0 until first asked
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+  int n = sms[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
+    sms[dev].store(n, std::memory_order_relaxed);
+  }
+  return n;
+}
 }  // namespace dcoco
 
 using namespace dcoco;
@@ -146,15 +159,6 @@ int pick_bn(int n, bool allow512) {
   return 32;
 }
 
-int sm_count() {
-  static int sms[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
-  if (sms[dev] == 0 && (cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-                        sms[dev] <= 0))
-    sms[dev] = 152;
-  return sms[dev];
-}
 
 // Split-K factor for long reductions only (>= 16 K blocks): double it while the grid stays
 // within max_ctas (the SM count by default) and every split keeps at least 8 K blocks.  Short

@@ -25,6 +25,9 @@ inline unsigned pdl_attr(cudaLaunchAttribute* attr) {
   return 1;
 }
 
+// Streaming multiprocessors of the current device (152 if the query fails); cached per device.
+int sm_count();
+
 // ------------------------------------------------------------------ top-K
 // Rows of `logits` ([rows, V], bf16 bits if is_bf16 else f32); ctas_per_row in 1..8.
 cudaError_t launch_topk(const void* logits, bool is_bf16, int rows, int V, int K, int ctas_per_row, float* vals,

@@ -480,13 +480,7 @@ cudaError_t launch_select_verify(const SelectVerifyArgs& a, cudaStream_t stream)
   // Sampling modes read whole vocabulary rows: spread each stream over a cluster so that up to
   // two CTAs per SM (what registers allow) stream them.  The walk and greedy verification stay
   // one CTA per stream.
-  static int sms = 0;
-  if (sms == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        sms <= 0)
-      sms = 152;
-  }
+  const int sms = sm_count();
   int C = 1;
   if (a.mode >= 1)
     while (C < 8 && static_cast<int64_t>(a.N) * C * 2 <= 2 * static_cast<int64_t>(sms)) C *= 2;
