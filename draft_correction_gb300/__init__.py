@@ -61,7 +61,6 @@ _SIGNATURES = {
                            _Z, _P], _I),
     "dcoco_lm_head_topk_workspace_size": ([_I, _I, _I, _I, _I], _Z),
     "dcoco_lm_head_topk": ([_P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _Z, _P], _I),
-    "dcoco_set_lm_cluster": ([_I], _I),
     "dcoco_set_lm_pair": ([_I], _I),
     "dcoco_cycle_lm_workspace_size": ([_WP, _I, _I, _I, _I], _Z),
     "dcoco_cycle_lm": ([_P, _I, _P, _P, _WP, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _Z,
@@ -293,10 +292,6 @@ def verify_speculative(draft, p, q, u):
     return out
 
 
-def set_lm_cluster(ctas: int) -> int:
-    return lib().dcoco_set_lm_cluster(int(ctas))
-
-
 def set_lm_pair(mode: int) -> int:
     return lib().dcoco_set_lm_pair(int(mode))
 
@@ -348,7 +343,7 @@ class Cycle:
         output projection of `h` (dcoco_cycle_lm) and `logits` is not read."""
         o = self.out
         if W_lm is not None:
-            # the size depends on the LM-head knobs (set_lm_cluster, set_lm_pair): grow if needed
+            # the size depends on the LM-head knobs (set_lm_pair): grow if needed
             nbytes = lib().dcoco_cycle_lm_workspace_size(self.w.ref, self.N, self.B, self.K, self.V)
             if self.ws_lm is None or self.ws_lm.numel() < nbytes:
                 self.ws_lm = torch.empty((max(nbytes, 16),), dtype=torch.uint8, device=self.ws.device)

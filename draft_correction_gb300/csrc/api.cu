@@ -50,9 +50,10 @@ void clear_err() { g_err[0] = '\0'; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
-int g_topk_split = 0;  // 0 = automatic
-int g_lm_cluster = 0;  // 0 = automatic
-int g_lm_pair = 0;     // 0 = automatic, 1 = always (bf16), -1 = never
+// Process-wide tuning knobs.  Each entry point reads a knob once and uses that one value for
+// both its workspace check and its launch, so a concurrent change cannot split the two.
+std::atomic<int> g_topk_split{0};  // 0 = automatic
+std::atomic<int> g_lm_pair{0};     // 0 = automatic, 1 = always (bf16), -1 = never
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -502,7 +503,7 @@ int enqueue_scores_prepped(const Dims& D, const void* P, const void* Q, const fl
 }
 
 // 0 lets the top-K launcher choose the split from the device's occupancy.
-int topk_split(int, int, bool) { return g_topk_split; }
+int topk_split(int, int, bool) { return g_topk_split.load(); }
 
 }  // namespace
 
@@ -513,22 +514,10 @@ int dcoco_version(void) { return 100; }
 const char* dcoco_last_error(void) { return g_err; }
 
 int dcoco_set_topk_split(int ctas_per_row) {
-  const int prev = g_topk_split;
-  g_topk_split = std::max(0, std::min(8, ctas_per_row));
-  return prev;
+  return g_topk_split.exchange(std::max(0, std::min(8, ctas_per_row)));
 }
 
-int dcoco_set_lm_cluster(int ctas) {
-  const int prev = g_lm_cluster;
-  g_lm_cluster = (ctas == 1 || ctas == 2 || ctas == 4) ? ctas : 0;
-  return prev;
-}
-
-int dcoco_set_lm_pair(int mode) {
-  const int prev = g_lm_pair;
-  g_lm_pair = mode > 0 ? 1 : mode < 0 ? -1 : 0;
-  return prev;
-}
+int dcoco_set_lm_pair(int mode) { return g_lm_pair.exchange(mode > 0 ? 1 : mode < 0 ? -1 : 0); }
 
 int dcoco_device_status(void* stream, uint32_t* bits) {
   clear_err();
@@ -568,7 +557,7 @@ size_t dcoco_lm_head_topk_workspace_size(int dtype, int N, int B, int V, int K) 
   if ((dtype != DCOCO_BF16 && dtype != DCOCO_F32) || N < 1 || B < 1 || V < 1 || K < 1 || K > 64 || K > V ||
       static_cast<int64_t>(N) * B > 65535)
     return 0;
-  return lm_topk_partial_bytes(dtype == DCOCO_BF16, N * B, V, K, g_lm_cluster, g_lm_pair);
+  return lm_topk_partial_bytes(dtype == DCOCO_BF16, N * B, V, K, g_lm_pair.load());
 }
 
 int dcoco_lm_head_topk(const void* h, const void* W_lm, int dtype, int N, int B, int d, int V, int K, float* vals,
@@ -585,7 +574,8 @@ int dcoco_lm_head_topk(const void* h, const void* W_lm, int dtype, int N, int B,
   DCOCO_TRY(check_ptr(W_lm, "W_lm"));
   DCOCO_TRY(check_ptr(vals, "vals"));
   DCOCO_TRY(check_ptr(ids, "ids"));
-  const size_t need = lm_topk_partial_bytes(bf16, N * B, V, K, g_lm_cluster, g_lm_pair);
+  const int pair_mode = g_lm_pair.load();
+  const size_t need = lm_topk_partial_bytes(bf16, N * B, V, K, pair_mode);
   if (need == 0) return fail(DCOCO_ERR_CUDA, "no launch plan for the fused LM-head top-K on this device");
   if (workspace == nullptr || workspace_bytes < need)
     return fail(DCOCO_ERR_WORKSPACE, "workspace %zu bytes < %zu required", workspace_bytes, need);
@@ -593,7 +583,7 @@ int dcoco_lm_head_topk(const void* h, const void* W_lm, int dtype, int N, int B,
   int rc;
   unsigned int* status = status_word(&rc);
   if (rc != DCOCO_OK) return rc;
-  const cudaError_t e = launch_lm_topk(h, W_lm, bf16, N * B, d, V, K, g_lm_cluster, g_lm_pair, vals, ids, workspace,
+  const cudaError_t e = launch_lm_topk(h, W_lm, bf16, N * B, d, V, K, pair_mode, vals, ids, workspace,
                                        workspace_bytes, status, as_stream(stream));
   if (e != cudaSuccess) return cuda_fail(e, "LM-head top-K launch");
   return DCOCO_OK;
@@ -852,10 +842,11 @@ int cycle_impl(const void* logits, const void* W_lm, int V, const void* emb, con
   const Dims D = dims_of(w, N, B, K);
   const size_t base_need = dcoco_cycle_workspace_size(w, N, B, K);
   size_t lm_bytes = 0;
+  const int pair_mode = g_lm_pair.load();
   if (W_lm != nullptr) {
     if ((static_cast<size_t>(D.d) * D.esz) % 16 != 0)
       return fail(DCOCO_ERR_INVALID_ARG, "d=%d: rows of h and W_lm must be a multiple of 16 bytes", D.d);
-    lm_bytes = lm_topk_partial_bytes(D.bf16, N * B, V, K, g_lm_cluster, g_lm_pair);
+    lm_bytes = lm_topk_partial_bytes(D.bf16, N * B, V, K, pair_mode);
     if (lm_bytes == 0) return fail(DCOCO_ERR_CUDA, "no launch plan for the fused LM-head top-K on this device");
   }
   const size_t need = base_need + round256(lm_bytes);
@@ -882,7 +873,7 @@ int cycle_impl(const void* logits, const void* W_lm, int V, const void* emb, con
     int rc;
     unsigned int* status = status_word(&rc);
     if (rc != DCOCO_OK) return rc;
-    e = launch_lm_topk(h, W_lm, D.bf16, rows, D.d, V, K, g_lm_cluster, g_lm_pair, o_vals, o_ids, lm_partial, lm_bytes, status, st);
+    e = launch_lm_topk(h, W_lm, D.bf16, rows, D.d, V, K, pair_mode, o_vals, o_ids, lm_partial, lm_bytes, status, st);
   } else {
     e = launch_topk(logits, D.bf16, rows, V, K, topk_split(rows, V, D.bf16), o_vals, o_ids, st);
   }

@@ -34,14 +34,13 @@ cudaError_t launch_topk(const void* logits, bool is_bf16, int rows, int V, int K
                         int32_t* ids, cudaStream_t stream);
 
 // ------------------------------------------------------------------ fused LM head + top-K
-// Bytes of the per-row partial lists launch_lm_topk needs (0 if no plan exists).  force_cm 0
-// picks the cluster size of the one-CTA kernel; pair_mode 0 uses CTA-pair MMAs for bf16 with at
-// least two row tiles when no cluster size is forced, 1 always for bf16, -1 never.
-size_t lm_topk_partial_bytes(bool is_bf16, int rows, int V, int K, int force_cm, int pair_mode);
+// Bytes of the per-row partial lists launch_lm_topk needs (0 if no plan exists).  pair_mode 0
+// uses CTA-pair MMAs for bf16 with at least two row tiles, 1 always for bf16, -1 never.
+size_t lm_topk_partial_bytes(bool is_bf16, int rows, int V, int K, int pair_mode);
 // h [rows, d], W_lm [V, d] (bf16 bits if is_bf16 else f32) -> vals, ids [rows, K].
-cudaError_t launch_lm_topk(const void* h, const void* W_lm, bool is_bf16, int rows, int d, int V, int K, int force_cm,
-                           int pair_mode, float* vals, int32_t* ids, void* partial, size_t partial_bytes,
-                           unsigned int* status, cudaStream_t stream);
+cudaError_t launch_lm_topk(const void* h, const void* W_lm, bool is_bf16, int rows, int d, int V, int K, int pair_mode,
+                           float* vals, int32_t* ids, void* partial, size_t partial_bytes, unsigned int* status,
+                           cudaStream_t stream);
 
 // ------------------------------------------------------------------ GEMM
 // C[m, n] = sum_k A[m, k] * B[n, k] on tcgen05 tensor cores (bf16 -> kind::f16, f32 -> kind::tf32),

@@ -7,13 +7,11 @@
 // tensor memory and never reach HBM.
 //
 // Kernel shape (persistent, one CTA per SM, 10 warps):
-//   A cluster of CM CTAs (CM = 1, 2 or 4) covers CM consecutive 128-row tiles of h and walks
-//   one contiguous range of 256-token vocabulary tiles.  Every CTA of the cluster multiplies
-//   by the same W_lm tile, so each CTA loads 1/CM of it and multicasts that slice to all.
-//   warp 0     TMA producer: this CTA's h tile and its slice of the W_lm tile per k-block.
+//   Each CTA covers one 128-row tile of h and walks one contiguous range of 256-token
+//   vocabulary tiles.
+//   warp 0     TMA producer: this CTA's h tile and the W_lm tile per k-block.
 //   warp 1     allocates 512 TMEM columns (two 128 x 256 fp32 accumulators) and issues
-//              tcgen05.mma; each stage is released to every CTA of the cluster by a multicast
-//              commit, so no CTA refills a stage that another CTA still reads.
+//              tcgen05.mma; each stage is released back to the producer by a commit.
 //   warps 2-5  epilogue (one per TMEM lane quarter; warps 6-9 idle): while the next tile
 //              accumulates in the other buffer, each thread reads the 256 columns of its row
 //              and keeps a running top-K of everything it has seen: a descending list of
@@ -28,7 +26,9 @@
 // each CTA's 128 rows in its own TMEM.  Per SM that halves the W_lm bytes the tensor core reads
 // and TMA writes per flop; the smaller stages (32 KB) also leave room for 6 of them.
 // Both CTAs' loads count on the even CTA's stage barrier; its commits release the stages and
-// accumulators in both CTAs; both CTAs' epilogues release an accumulator to the even CTA.
+// accumulators in both CTAs (one commit arriving on the same barrier offset in each CTA); both
+// CTAs' epilogues release an accumulator to the even CTA.  Every TMA load writes only the
+// issuing CTA's own shared memory.
 // Each (row, cluster) leaves a sorted list of K keys; lm_merge_kernel merges the lists of a
 // row.  Keys are ordered value bits << 32 | ~token, as in the top-K kernel, so the
 // selection is exact on the fp32 logits and deterministic.
@@ -72,12 +72,12 @@ static_assert(Pipe<true>::kSmem <= 227 * 1024 - 256, "pair pipeline exceeds shar
 
 struct LmArgs {
   CUtensorMap a_map;  // h [rows, d], box {128 bytes, 128 rows}
-  CUtensorMap b_map;  // W_lm [V, d], box {128 bytes, BN / cm rows}
+  CUtensorMap b_map;  // W_lm [V, d], box {128 bytes, BN / cm rows} (each CTA of a pair loads half)
   unsigned long long* partial;  // [rows, n_lists, K] keys, each list descending
   int rows, d, V, K;
   int n_vt;    // vocabulary tiles, ceil(V / BN)
   int nclus;   // clusters per row group (vocabulary ranges); n_lists = kColSplit * nclus
-  int cm;      // CTAs per cluster (row tiles sharing the W_lm tile)
+  int cm;      // CTAs per cluster: 2 for CTA pairs, else 1
   unsigned int* status;
 };
 
@@ -129,7 +129,7 @@ __global__ void __launch_bounds__(kThreads, 1) lm_topk_kernel(const __grid_const
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   constexpr int CW = KR >= 64 ? 16 : 32;  // columns per TMEM load (fewer registers beside a long list)
-  const int cm = kPair ? 2 : args.cm;
+  constexpr int cm = kPair ? 2 : 1;
   const int K = args.K;
   const uint32_t rank = cm > 1 ? cluster_rank() : 0u;
   const bool leader = rank == 0;  // pairs: the CTA that issues the MMAs
@@ -144,8 +144,7 @@ __global__ void __launch_bounds__(kThreads, 1) lm_topk_kernel(const __grid_const
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(smem_u32(&full_bar[s]), 1);
-      // pairs: the even CTA's commit; otherwise one MMA commit from every CTA of the cluster
-      mbar_init(smem_u32(&empty_bar[s]), kPair ? 1 : cm);
+      mbar_init(smem_u32(&empty_bar[s]), 1);  // pairs: the even CTA's commit
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&acc_full[b]), 1);
@@ -164,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1) lm_topk_kernel(const __grid_const
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (cm > 1) cluster_sync();  // every CTA's barriers exist before the first remote arrival lands
+  if constexpr (kPair) cluster_sync();  // both CTAs' barriers exist before the first remote arrival lands
   const uint32_t tmem = tmem_base_s;
   const uint32_t smem0 = smem_u32(smem);
   const int total = ntile * nkb;
@@ -192,13 +191,9 @@ __global__ void __launch_bounds__(kThreads, 1) lm_topk_kernel(const __grid_const
           tma_load_2d_pair(a_s, &args.a_map, kx, m_tile * BM, fb_lead);
           tma_load_2d_pair(b_s, &args.b_map, kx, tile * BN + static_cast<int>(rank) * slice, fb_lead);
         } else {
-          mbar_expect_tx(fb, STAGE_BYTES);  // own h tile + every CTA's W_lm slice
+          mbar_expect_tx(fb, STAGE_BYTES);  // the h tile and the whole W_lm tile
           tma_load_2d(a_s, &args.a_map, kx, m_tile * BM, fb);
-          if (cm > 1)
-            tma_load_2d_multicast(b_s + rank * slice * 128, &args.b_map, kx, tile * BN + static_cast<int>(rank) * slice,
-                                  fb, mask);
-          else
-            tma_load_2d(b_s, &args.b_map, kx, tile * BN, fb);
+          tma_load_2d(b_s, &args.b_map, kx, tile * BN, fb);
         }
       }
     }
@@ -239,8 +234,6 @@ __global__ void __launch_bounds__(kThreads, 1) lm_topk_kernel(const __grid_const
           }
           if constexpr (kPair)
             tc_commit_pair_multicast(smem_u32(&empty_bar[s]), mask);
-          else if (cm > 1)
-            tc_commit_multicast(smem_u32(&empty_bar[s]), mask);
           else
             tc_commit(smem_u32(&empty_bar[s]));
         }
@@ -346,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1) lm_topk_kernel(const __grid_const
     tc_fence_after();
     tmem_dealloc(tmem, 2 * BN);
   }
-  if (cm > 1) cluster_sync();  // no CTA leaves while a multicast commit may still arrive in it
+  if constexpr (kPair) cluster_sync();  // neither CTA leaves while a pair commit may still arrive in it
 }
 
 // One warp per row: K rounds of "largest head among the row's sorted lists".
@@ -466,42 +459,25 @@ int active_clusters(const Instance& in, int cm) {
   return n;
 }
 
-// The launch plan.  CTA pairs (bf16) when pair_mode > 0, or when pair_mode == 0, no cluster size
-// is forced and h has at least two row tiles; otherwise the one-CTA kernel with the cluster size
-// that is forced, or that keeps the most CTAs resident (larger clusters on ties).  Then as many
-// vocabulary ranges as fit in one wave.
-cudaError_t plan_for(bool is_bf16, int rows, int V, int K, int force_cm, int pair_mode, Plan* p) {
+// The launch plan.  CTA pairs (bf16) when pair_mode > 0, or when pair_mode == 0 and h has at
+// least two row tiles; otherwise the one-CTA kernel (clusters of 1).  Then as many vocabulary
+// ranges as fit in one wave.
+cudaError_t plan_for(bool is_bf16, int rows, int V, int K, int pair_mode, Plan* p) {
   const int KR = list_len(K);
   const int m_tiles = (rows + BM - 1) / BM;
   p->n_vt = (V + BN - 1) / BN;
-  p->pair = is_bf16 && (pair_mode > 0 || (pair_mode == 0 && force_cm == 0 && m_tiles >= 2));
-  static int cache[64][kSlots][3];  // active clusters + 1 per device, instance and cluster size (0 = unknown)
+  p->pair = is_bf16 && (pair_mode > 0 || (pair_mode == 0 && m_tiles >= 2));
+  static int cache[64][kSlots];  // active clusters + 1 per device and instance (0 = unknown)
   int dev = 0;
   const cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   const Instance in = instance(is_bf16, p->pair, KR);
-  auto active = [&](int cm) {
-    int& c = cache[dev][in.slot][cm == 4 ? 2 : cm == 2 ? 1 : 0];
-    if (c == 0) c = active_clusters(in, cm) + 1;
-    return c - 1;
-  };
-  int best_cm = 2;
-  if (!p->pair) {
-    int best_ctas = -1;
-    for (int cm : {4, 2, 1}) {
-      if (force_cm > 0 && cm != force_cm) continue;
-      if (force_cm == 0 && cm > 1 && m_tiles < cm) continue;
-      const int ctas = active(cm) * cm;
-      if (ctas > best_ctas) {
-        best_ctas = ctas;
-        best_cm = cm;
-      }
-    }
-  }
-  p->cm = best_cm;
+  p->cm = p->pair ? 2 : 1;
+  int& c = cache[dev][in.slot];
+  if (c == 0) c = active_clusters(in, p->cm) + 1;
   p->m_groups = (m_tiles + p->cm - 1) / p->cm;
-  const int fit = std::max(1, active(p->cm));
+  const int fit = std::max(1, c - 1);
   p->nclus = std::max(1, std::min(p->n_vt, fit / p->m_groups));
   return cudaSuccess;
 }
@@ -511,19 +487,18 @@ std::mutex g_plan_mu;
 
 }  // namespace
 
-size_t lm_topk_partial_bytes(bool is_bf16, int rows, int V, int K, int force_cm, int pair_mode) {
+size_t lm_topk_partial_bytes(bool is_bf16, int rows, int V, int K, int pair_mode) {
   Plan p;
   std::lock_guard<std::mutex> lock(g_plan_mu);
-  if (plan_for(is_bf16, rows, V, K, force_cm, pair_mode, &p) != cudaSuccess) return 0;
+  if (plan_for(is_bf16, rows, V, K, pair_mode, &p) != cudaSuccess) return 0;
   return static_cast<size_t>(rows) * (kColSplit * p.nclus) * K * 8;
 }
 
-cudaError_t launch_lm_topk(const void* h, const void* W_lm, bool is_bf16, int rows, int d, int V, int K, int force_cm,
-                           int pair_mode, float* vals, int32_t* ids, void* partial, size_t partial_bytes,
+cudaError_t launch_lm_topk(const void* h, const void* W_lm, bool is_bf16, int rows, int d, int V, int K, int pair_mode, float* vals, int32_t* ids, void* partial, size_t partial_bytes,
                            unsigned int* status, cudaStream_t stream) {
   Plan p;
   std::unique_lock<std::mutex> lock(g_plan_mu);
-  cudaError_t e = plan_for(is_bf16, rows, V, K, force_cm, pair_mode, &p);
+  cudaError_t e = plan_for(is_bf16, rows, V, K, pair_mode, &p);
   if (e != cudaSuccess) return e;
   const int n_lists = kColSplit * p.nclus;
   if (n_lists > 32 * kMaxListsPerLane) return cudaErrorInvalidValue;

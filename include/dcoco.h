@@ -276,8 +276,7 @@ int dcoco_cycle_table(const void* logits, int V, const void* table, const void* 
  *   vals [N, B, K] float32  the kept fp32 logits, descending, equal values by ascending id
  *   ids  [N, B, K] int32
  * Workspace: dcoco_lm_head_topk_workspace_size bytes (per-row partial lists; the size depends
- * on the current device, dcoco_set_lm_cluster and dcoco_set_lm_pair), 16-byte aligned,
- * caller-owned.
+ * on the current device and dcoco_set_lm_pair), 16-byte aligned, caller-owned.
  * Selection is exact on the fp32 logits it computes and deterministic.  The fp32 logits differ
  * from exact dot products by accumulation rounding, so two tokens whose exact logits lie within
  * that rounding may rank in either order.
@@ -287,17 +286,10 @@ int dcoco_lm_head_topk(const void* h, const void* W_lm, int dtype, int N, int B,
                        int32_t* ids, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
- * Tuning knob: CTAs per thread-block cluster in dcoco_lm_head_topk (1, 2 or 4 row tiles that
- * share each W_lm tile by multicast; 0 = automatic, the size that keeps the most CTAs
- * resident).  Process-wide; returns the previous value.  Query workspace sizes after setting it.
- */
-int dcoco_set_lm_cluster(int ctas);
-
-/*
  * Tuning knob: CTA-pair MMAs in dcoco_lm_head_topk for bf16 inputs (two CTAs of a cluster
  * issue one 256-row MMA together, each holding half of every W_lm tile).  0 = automatic
- * (pairs when h has at least two 128-row tiles and no cluster size is forced), 1 = always,
- * -1 = never (dcoco_set_lm_cluster then applies).  f32 inputs never use pairs.  Process-wide;
+ * (pairs when h has at least two 128-row tiles), 1 = always, -1 = never (every CTA then loads
+ * whole W_lm tiles and issues 128-row MMAs alone).  f32 inputs never use pairs.  Process-wide;
  * returns the previous value.  Query workspace sizes after setting it.
  */
 int dcoco_set_lm_pair(int mode);

@@ -148,12 +148,6 @@ def test_lm_head_topk_argument_errors(L):
     assert L.dcoco_lm_head_topk_workspace_size(dc.DCOCO_BF16, 1, 4, 1000, 65) == 0
 
 
-def test_lm_cluster_knob(L):
-    prev = L.dcoco_set_lm_cluster(2)
-    assert L.dcoco_set_lm_cluster(3) == 2        # 3 is not a cluster size: automatic
-    assert L.dcoco_set_lm_cluster(prev) == 0
-
-
 def test_lm_pair_knob(L):
     prev = L.dcoco_set_lm_pair(5)                # any positive value: always
     assert L.dcoco_set_lm_pair(-3) == 1          # any negative value: never

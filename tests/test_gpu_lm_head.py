@@ -37,7 +37,6 @@ def built():
     build.build()
     dc.lib()
     yield
-    dc.set_lm_cluster(0)
     dc.set_lm_pair(0)
     assert dc.device_status() == 0, "a kernel reported a timeout or a bad index"
 
@@ -99,7 +98,7 @@ LM_CASES = [
     ("bf16", 2, 16, 200, 4097, 16),   # ragged k-block (200 = 3 x 64 + 8) and vocabulary tail
     ("bf16", 3, 43, 520, 2500, 33),   # two row tiles, K above 32
     ("bf16", 2, 150, 136, 5000, 64),  # three row tiles, K = 64 (two pipeline stages)
-    ("bf16", 1, 520, 64, 777, 8),     # five row tiles: cluster padding rows
+    ("bf16", 1, 520, 64, 777, 8),     # five row tiles: the last pair half empty
     ("f32", 2, 7, 100, 3333, 10),     # f32 with a ragged k-block
 ]
 
@@ -117,33 +116,25 @@ def test_lm_head_topk_matches_oracle(dtype, N, B, d, V, K):
 
 
 @pytest.mark.parametrize("shape", [(3, 43, 520, 2500, 16), (4, 32, 128, 3000, 16)], ids=["3-row-tiles", "4-row-tiles"])
-def test_lm_head_topk_same_result_for_every_cluster_size(shape):
+def test_lm_head_topk_pairs_and_single_ctas_bit_identical(shape):
     """Each CTA accumulates its whole 128 x 256 tile in the same order (k ascending, 16 per MMA)
-    whatever the cluster size, and so does each CTA of a pair with 256-row MMAs, so the logits
-    and the selection are bit-identical."""
+    whether it issues 128-row MMAs alone or 256-row MMAs with its pair, so the logits and the
+    selection are bit-identical."""
     N, B, d, V, K = shape
     cfg = lm_cfg("bf16", N, B, d, V, K)
     h, W = lm_inputs(cfg)
     hd, Wd = dc.to_device(h, "bf16"), dc.to_device(W, "bf16")
     res = []
     try:
-        dc.set_lm_pair(-1)
-        for cm in (1, 2, 4):
-            dc.set_lm_cluster(cm)
+        for mode in (-1, 1):
+            dc.set_lm_pair(mode)
             v, i = dc.lm_head_topk(hd, Wd, K)
             torch.cuda.synchronize()
             res.append((v.cpu().numpy(), i.cpu().numpy()))
-        dc.set_lm_cluster(0)
-        dc.set_lm_pair(1)
-        v, i = dc.lm_head_topk(hd, Wd, K)
-        torch.cuda.synchronize()
-        res.append((v.cpu().numpy(), i.cpu().numpy()))
     finally:
-        dc.set_lm_cluster(0)
         dc.set_lm_pair(0)
-    for v, i in res[1:]:
-        np.testing.assert_array_equal(i, res[0][1])
-        np.testing.assert_array_equal(v, res[0][0])
+    np.testing.assert_array_equal(res[1][1], res[0][1])
+    np.testing.assert_array_equal(res[1][0], res[0][0])
 
 
 PAIR_CASES = [
