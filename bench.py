@@ -77,15 +77,18 @@ sys.path.insert(0, {root!r})
 import numpy as np
 import oracle, workloads as wl
 cfg = wl.CONFIGS[{cfg!r}].replace(N=1)
-n_streams, reps, budget = {n_streams}, {reps}, {budget}
-emb = wl.embedding(cfg)
+n_streams, reps, budget, stream0, emb_path = {n_streams}, {reps}, {budget}, {stream0}, {emb_path!r}
+emb = np.load(emb_path, mmap_mode="r") if emb_path else wl.embedding(cfg)
 w = wl.weights(cfg)
 f = lambda a: wl.to_f64(a, cfg.dtype)
 W = {{k: f(v) for k, v in w.items()}}
 streams = []
-for n in range(n_streams):
+for n in range(stream0, stream0 + n_streams):
     c = cfg.replace(base_seed=cfg.base_seed + n)
     streams.append((wl.logits(c), wl.hidden(c)))
+if {sync}:  # the processes of one run start their timed loops together, on the parent's word
+    print("ready", flush=True)
+    sys.stdin.readline()
 times = []
 while len(times) < reps and (budget <= 0 or sum(times) < budget):
     t0 = time.perf_counter()
@@ -103,35 +106,101 @@ print(json.dumps({{"times": times, "streams": n_streams}}))
 """
 
 
-def run_oracle(cfg_name: str, n_streams: int, reps: int, budget_s: float = 0.0):
-    """Times the oracle in a fresh single-threaded process (no CUDA context, no fork):
-    `reps` repetitions, or fewer once `budget_s` seconds of timed work are done."""
+def _oracle_env():
     env = dict(os.environ)
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
         env[k] = "1"
-    code = ORACLE_SNIPPET.format(root=ROOT, cfg=cfg_name, n_streams=n_streams, reps=reps, budget=budget_s)
-    res = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env)
+    return env
+
+
+def run_oracle(cfg_name: str, n_streams: int, reps: int, budget_s: float = 0.0, emb_path: str = ""):
+    """Times the oracle in a fresh single-threaded process (no CUDA context, no fork):
+    `reps` repetitions, or fewer once `budget_s` seconds of timed work are done."""
+    code = ORACLE_SNIPPET.format(root=ROOT, cfg=cfg_name, n_streams=n_streams, reps=reps, budget=budget_s, stream0=0,
+                                 emb_path=emb_path, sync=False)
+    res = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=_oracle_env())
     if res.returncode != 0:
         raise RuntimeError(f"oracle run failed:\n{res.stderr[-2000:]}")
     return json.loads(res.stdout.strip().splitlines()[-1])
 
 
+def host_cores() -> int:
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+
+
+def run_oracle_all_cores(cfg_name: str, streams_per_proc: int, reps: int, budget_s: float, emb_path: str = "",
+                         procs: int = 0, skip: int = 0):
+    """The oracle on every host core: one single-threaded process per core, each on its own
+    streams (process p owns streams p*s .. p*s+s-1), all starting their timed loops together.
+    Returns the whole host's rate in blocks/s (the first `skip` repetitions of each process
+    left out) and the process count."""
+    procs = procs or host_cores()
+    running = []
+    for p in range(procs):
+        code = ORACLE_SNIPPET.format(root=ROOT, cfg=cfg_name, n_streams=streams_per_proc, reps=reps, budget=budget_s,
+                                     stream0=p * streams_per_proc, emb_path=emb_path, sync=True)
+        running.append(subprocess.Popen([sys.executable, "-c", code], stdin=subprocess.PIPE, stdout=subprocess.PIPE,
+                                        stderr=subprocess.PIPE, text=True, env=_oracle_env()))
+    for pr in running:  # every process has built its inputs
+        if pr.stdout.readline().strip() != "ready":
+            pr.wait()
+    for pr in running:
+        if pr.poll() is None:
+            pr.stdin.write("go\n")
+            pr.stdin.flush()
+    results = []
+    for pr in running:
+        out, err = pr.communicate()
+        if pr.returncode != 0:
+            raise RuntimeError(f"oracle run failed:\n{err[-2000:]}")
+        results.append(json.loads(out.strip().splitlines()[-1]))
+    # each process's timed loop runs concurrently with the others'; the host's rate is every
+    # process's blocks over the longest loop
+    blocks = sum(r["streams"] * len(r["times"][skip:]) for r in results)
+    wall = max(sum(r["times"][skip:]) for r in results)
+    return blocks / wall, procs
+
+
+class EmbeddingFile:
+    """The workload's embedding table written once to a temporary .npy file that every oracle
+    process maps read-only, instead of each process drawing its own 1.2 GB copy."""
+
+    def __init__(self, cfg, table=None):
+        self.cfg, self.table, self.path = cfg, table, ""
+
+    def __enter__(self):
+        import tempfile
+        d = "/dev/shm" if os.path.isdir("/dev/shm") and os.access("/dev/shm", os.W_OK) else tempfile.gettempdir()
+        fd, self.path = tempfile.mkstemp(suffix=".npy", prefix="dcoco_emb_", dir=d)
+        os.close(fd)
+        np.save(self.path, wl.embedding(self.cfg) if self.table is None else self.table)
+        return self.path
+
+    def __exit__(self, *exc):
+        if self.path and os.path.exists(self.path):
+            os.unlink(self.path)
+
+
 def reference_arm(args, cfg):
+    """The oracle on every host core: one single-threaded process per core, one stream each;
+    a step is every process's full cycle over its stream, so each step is a bounded sample of
+    the workload (host cores x 1 of its streams)."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    n_streams = 2
-    r = run_oracle(cfg.name, n_streams, args.warmup + args.steps)
-    timed = r["times"][args.warmup:]
-    sec = sum(timed)
-    value = n_streams * len(timed) / sec
+    with EmbeddingFile(cfg) as emb_path:
+        procs = min(host_cores(), cfg.N)
+        reps = args.warmup + args.steps
+        # warm-up repetitions are timed inside each process but left out of the rate below
+        rate_all, procs = run_oracle_all_cores(cfg.name, 1, reps, 0.0, emb_path, procs=procs, skip=args.warmup)
+    value = rate_all
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "blocks/s", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec / len(timed),
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * procs / value,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config_dict(cfg),
-            "cpu_baseline": {"value": value, "unit": "blocks/s", "cores": 1, "kind": "oracle",
-                             "sample": f"{n_streams} of {cfg.N} streams per step (one full block each), "
-                                       f"same shapes and distributions"},
+            "cpu_baseline": {"value": value, "unit": "blocks/s", "cores": procs, "kind": "oracle",
+                             "sample": f"{procs} of {cfg.N} streams per step (one full block each, one "
+                                       f"single-threaded process per host core), same shapes and distributions"},
             "e2e": {"value": value, "unit": "blocks/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -153,6 +222,58 @@ def captured_traffic(kernel: str):
     except (OSError, KeyError, ValueError):
         return None
 
+
+
+def cycle_work(cfg, w_h):
+    """Algorithmic HBM bytes and tensor flops of one whole cycle (a1..a6, greedy verify).
+
+    Bytes: the logits once, each candidate's embedding row once, the hidden states once, every
+    weight once, the verifier tokens in and the committed tokens, accept lengths and commit
+    counts out.  Flops: 2 x rows x in x out of every projection (W_e on the gathered rows, W_h on
+    the slots, both halves of W_f, U and V on the candidates, W_pair on the slots' two halves,
+    W on the pairs).  The transition MLP (SFU) and the walk are not counted."""
+    esz = 2 if cfg.dtype == "bf16" else 4
+    N, B, K, V, d, E, r, H = cfg.N, cfg.B, cfg.K, cfg.V, cfg.d, cfg.E, cfg.r, cfg.H
+    weights = sum(int(np.asarray(v).size) for v in w_h.values()) * esz
+    nbytes = (N * B * V * esz + N * B * K * E * esz + N * B * d * esz + weights
+              + N * (B + 1) * 4 + N * (B + 1) * 4 + 2 * N * 4)
+    M, NB, NP = N * B * K, N * B, N * (B - 1)
+    flops = 2.0 * (M * E * r + NB * d * r + M * r * r + NB * r * r + 2 * M * r * H + NB * 2 * d * r + NP * r * H)
+    return nbytes, flops
+
+
+def cycle_roofline(cfg, ms_per_step, w_h):
+    """The cycle's roofline: whichever of the HBM time and the tensor time of its algorithmic
+    work is longer binds; achieved = that work over the measured step time."""
+    hbm, bf16, kind = peaks()
+    nbytes, flops = cycle_work(cfg, w_h)
+    t_hbm, t_tensor = nbytes / (hbm * 1e9), flops / (bf16 * 1e12)
+    sec = ms_per_step * 1e-3
+    if t_hbm >= t_tensor:
+        out = {"bound": "hbm", "achieved": round(nbytes / sec / 1e9, 1), "peak": hbm, "unit": "GB/s",
+               "frac": round(t_hbm / sec, 4), "peak_source": f"{kind} hbm_gbs (burst)"}
+    else:
+        out = {"bound": "tensor", "achieved": round(flops / sec / 1e12, 1), "peak": bf16, "unit": "TFLOP/s",
+               "frac": round(t_tensor / sec, 4), "peak_source": f"{kind} bf16_tflops (burst)"}
+    out.update({"kernel": "whole cycle (one CUDA graph, a1..a6)", "traffic": None,
+                "algorithmic_bytes_per_step": nbytes, "algorithmic_tensor_flops_per_step": flops,
+                "hbm_time_us_at_peak": round(t_hbm * 1e6, 2), "tensor_time_us_at_peak": round(t_tensor * 1e6, 2),
+                "measured_us_per_step": round(ms_per_step * 1e3, 2)})
+    return out
+
+
+def arithmetic(cfg):
+    """The precision each part of the path computes in (the line's dtype names the inputs)."""
+    if cfg.dtype == "bf16":
+        return {"inputs": "bf16 logits, embeddings, hidden states and weights",
+                "topk": "exact comparison of the bf16 values (64-bit value/index keys)",
+                "projections": "bf16 operands on tcgen05, fp32 accumulation in tensor memory; LayerNorm and "
+                               "SiLU epilogues in fp32; b, z, U z / V z stored in bf16",
+                "scorer": "pre-activations, tanh.approx.f16x2 and 8-term partial sums in f16; per-output "
+                          "totals in fp32 (stages_us.score_transitions_fp32 times the all-fp32 path)",
+                "walk_verify": "fp32 comparisons; residual draws in exact 62-bit fixed point"}
+    return {"inputs": "f32", "projections": "tf32 operands on tcgen05, fp32 accumulation",
+            "scorer": "fp32 with tanh.approx.f32", "walk_verify": "fp32; residual draws in exact 62-bit fixed point"}
 
 
 def config_dict(cfg):
@@ -255,8 +376,10 @@ def gpu_arm(args, cfg):
     rcfg = rank_workload(cfg, rank)
     logits_h = wl.logits(rcfg)
     hidden_h = wl.hidden(rcfg)
-    emb = dc.to_device(wl.embedding(cfg), cfg.dtype, dev)
-    w = dc.CorrectorWeights.from_numpy(wl.weights(cfg), cfg.dtype, dev)
+    emb_h = wl.embedding(cfg)
+    emb = dc.to_device(emb_h, cfg.dtype, dev)
+    w_h = wl.weights(cfg)
+    w = dc.CorrectorWeights.from_numpy(w_h, cfg.dtype, dev)
     logits = dc.to_device(logits_h, cfg.dtype, dev)
     hidden = dc.to_device(hidden_h, cfg.dtype, dev)
     cyc = dc.Cycle(w, cfg.N, cfg.B, cfg.K, cfg.V, device=dev, keep_intermediates=True)
@@ -420,6 +543,12 @@ def gpu_arm(args, cfg):
     S = dc.score_transitions(uzv[0], uzv[1], wsp, vals, w)
     stages["score_transitions"] = lambda: dc.score_transitions(uzv[0], uzv[1], wsp, vals, w)
     stages["select"] = lambda: dc.select(S, vals, ids)
+    if cfg.dtype == "bf16":
+        # the same scores with float32 operands and arithmetic throughout (tanh.approx.f32), for
+        # comparison with the half-precision transition MLP the bf16 path uses
+        w32 = dc.CorrectorWeights.from_numpy({k: wl.bf16_to_f32(v) for k, v in w_h.items()}, "f32", dev)
+        uz32, vz32 = uzv[0].float(), uzv[1].float()
+        stages["score_transitions_fp32"] = lambda: dc.score_transitions(uz32, vz32, wsp, vals, w32)
     stages["verify"] = lambda: dc.verify(cyc.out["tokens"], t=t_dev)
     # the scope table's next rows at the same shape: whole-path rules and speculative sampling
     stages["select_path_global_sum"] = lambda: dc.select_path(S, vals, ids, "global_sum")
@@ -444,6 +573,8 @@ def gpu_arm(args, cfg):
     roofline = {"bound": "hbm", "kernel": "topk_kernel", "achieved": round(achieved, 1), "peak": hbm,
                 "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": captured_traffic("topk"),
                 "peak_source": f"{peak_kind} hbm_gbs (burst)", "algorithmic_bytes_per_launch": topk_bytes}
+    # The whole cycle (what the metric measures) against its own binding roof.
+    roofline["cycle"] = cycle_roofline(cfg, total_ms / args.steps, w_h)
 
     # End to end through the public API: pinned host inputs -> device, cycle, results -> host.
     def pinned(a):
@@ -503,22 +634,31 @@ def gpu_arm(args, cfg):
     h2d = logits_h.nbytes + hidden_h.nbytes + t_host.nbytes
     d2h = com_pin.numel() * 4 + acc_pin.numel() * 4
 
-    cpu = None
+    cpu = cpu_all = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        # a bounded sample of about 10 s of host work: a few streams, repeated
-        n_streams = min(2, cfg.N)
-        r = run_oracle(cfg.name, n_streams, 200, budget_s=10.0)
-        reps = len(r["times"])
-        sec = statistics.mean(r["times"])
-        cpu = {"value": n_streams / sec, "unit": "blocks/s", "cores": 1, "kind": "oracle",
-               "sample": f"{n_streams} of {cfg.N} streams, full cycle each, {reps} repetitions, "
-                         f"single host thread"}
+        with EmbeddingFile(cfg, emb_h) as emb_path:
+            # a bounded sample of about 10 s of host work: a few streams, repeated
+            n_streams = min(2, cfg.N)
+            r = run_oracle(cfg.name, n_streams, 200, budget_s=10.0, emb_path=emb_path)
+            reps = len(r["times"])
+            sec = statistics.mean(r["times"])
+            cpu = {"value": n_streams / sec, "unit": "blocks/s", "cores": 1, "kind": "oracle",
+                   "sample": f"{n_streams} of {cfg.N} streams, full cycle each, {reps} repetitions, "
+                             f"single host thread"}
+            # every host core: one single-threaded process per core, its own stream each, ~10 s
+            procs = min(host_cores(), cfg.N)
+            rate, procs = run_oracle_all_cores(cfg.name, 1, 200, 10.0, emb_path, procs=procs)
+            cpu_all = {"value": rate, "unit": "blocks/s", "cores": procs, "kind": "oracle",
+                       "sample": f"{procs} of {cfg.N} streams, one single-threaded process per host core "
+                                 f"(of {host_cores()}), full cycle each, repeated for about 10 s"}
+    del emb_h
 
     if rank == 0:
         line = {"metric": METRIC, "value": round(value, 1), "unit": "blocks/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic",
                 "config": config_dict(cfg), "roofline": roofline, "cpu_baseline": cpu,
+                "cpu_baseline_all_cores": cpu_all, "arithmetic": arithmetic(cfg),
                 "e2e": {"value": round(e2e_val, 1), "unit": "blocks/s", "h2d_bytes_per_step": h2d,
                         "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                         "pipeline": "inputs double-buffered: step i+1 copied while step i computes"},

@@ -42,6 +42,7 @@ _SIGNATURES = {
     "dcoco_version": ([], _I),
     "dcoco_last_error": ([], ctypes.c_char_p),
     "dcoco_device_status": ([_P, ctypes.POINTER(ctypes.c_uint32)], _I),
+    "dcoco_selftest_timeout": ([ctypes.c_uint32, _P], _I),
     "dcoco_set_topk_split": ([_I], _I),
     "dcoco_topk": ([_P, _I, _I, _I, _I, _I, _P, _P, _P], _I),
     "dcoco_candidate_repr_workspace_size": ([_WP, _I, _I, _I], _Z),
@@ -178,6 +179,11 @@ def device_status() -> int:
     if rc not in (0, 5):
         _check(rc)
     return int(bits.value)
+
+
+def selftest_timeout(polls: int) -> None:
+    """Enqueue one bounded wait that gives up after `polls` polls and reports it in the status word."""
+    _check(lib().dcoco_selftest_timeout(int(polls), _stream()))
 
 
 def set_topk_split(ctas_per_row: int) -> int:

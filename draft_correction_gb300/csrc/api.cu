@@ -12,6 +12,7 @@
 
 #include "../../include/dcoco.h"
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace dcoco {
 thread_local bool g_pdl = false;
@@ -518,6 +519,38 @@ int dcoco_set_topk_split(int ctas_per_row) {
 }
 
 int dcoco_set_lm_pair(int mode) { return g_lm_pair.exchange(mode > 0 ? 1 : mode < 0 ? -1 : 0); }
+
+}  // extern "C"
+
+namespace {
+// One warp: lane 0 waits on an mbarrier that nothing arrives at, with the same bounded wait the
+// library's pipelines use but at most `polls` polls, records the TMA-wait timeout bit the way a
+// producer whose copy never lands would, and invalidates the barrier.  No copy is in flight.
+__global__ void wait_timeout_kernel(uint32_t polls, unsigned int* status) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+    if (!mbar_wait_n(smem_u32(&bar), 0, polls)) atomicOr(status, DEV_TIMEOUT_TMA);
+    mbar_inval(smem_u32(&bar));
+  }
+  __syncwarp();
+}
+}  // namespace
+
+extern "C" {
+
+int dcoco_selftest_timeout(uint32_t polls, void* stream) {
+  clear_err();
+  if (polls < 1 || polls > 65536) return fail(DCOCO_ERR_INVALID_ARG, "polls=%u outside [1, 65536]", polls);
+  int rc;
+  unsigned int* w = status_word(&rc);
+  if (rc != DCOCO_OK) return rc;
+  wait_timeout_kernel<<<1, 32, 0, as_stream(stream)>>>(polls, w);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+  return DCOCO_OK;
+}
 
 int dcoco_device_status(void* stream, uint32_t* bits) {
   clear_err();

@@ -93,6 +93,17 @@ const char* dcoco_last_error(void);
 int dcoco_device_status(void* stream, uint32_t* bits);
 
 /*
+ * Self-test of the device-side failure path (the pages have no counterpart; it checks this
+ * library's own error reporting).  Enqueues one warp that waits on an mbarrier nothing ever
+ * arrives at, with the bounded wait every pipeline of the library uses but at most `polls`
+ * polls (1..65536), and then sets bit 1 (a TMA wait gave up) in the status word, as a copy that
+ * never lands would.  Nothing faults, no copy is in flight, and the context stays usable; the
+ * next dcoco_device_status returns DCOCO_ERR_TIMEOUT.  Errors: DCOCO_ERR_INVALID_ARG for polls
+ * outside [1, 65536].
+ */
+int dcoco_selftest_timeout(uint32_t polls, void* stream);
+
+/*
  * Tuning knob: thread blocks per logits row in dcoco_topk (1..8; 0 = automatic).
  * Process-wide; returns the previous value.
  */

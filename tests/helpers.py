@@ -11,7 +11,9 @@ most 5e-2; ids, candidate indices, accept lengths and committed tokens are bit-e
 """
 from __future__ import annotations
 
+import concurrent.futures
 import functools
+import os
 
 import numpy as np
 
@@ -91,3 +93,20 @@ def f64(arr, cfg):
 
 def w64(w, cfg):
     return {k: f64(v, cfg) for k, v in w.items()}
+
+
+def oracle_topk_rows(logits, cfg: wl.Config, K: int):
+    """oracle.topk over every row of [N, B, V] logits, rows split over host threads (each
+    thread runs the oracle itself on its own rows; numpy's sort releases the GIL)."""
+    x = np.asarray(logits).reshape(-1, logits.shape[-1])
+    n = x.shape[0]
+    starts = list(range(0, n, 32))  # 32 rows per call bounds the float64 copies in flight
+
+    def part(s0):
+        return oracle.topk(f64(x[s0:s0 + 32], cfg), K)
+
+    with concurrent.futures.ThreadPoolExecutor(max_workers=max(1, min(16, os.cpu_count() or 1))) as ex:
+        parts = list(ex.map(part, starts))
+    vals = np.concatenate([p[0] for p in parts]).reshape(logits.shape[:-1] + (K,))
+    ids = np.concatenate([p[1] for p in parts]).reshape(logits.shape[:-1] + (K,))
+    return vals, ids

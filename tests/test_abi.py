@@ -161,3 +161,8 @@ def test_cycle_lm_argument_errors(L):
     assert L.dcoco_cycle_lm(None, *args) == 1 and b"W_lm is NULL" in L.dcoco_last_error()
     assert L.dcoco_cycle_lm(MISALIGNED, *args) == 1 and b"W_lm" in L.dcoco_last_error()
     assert L.dcoco_cycle_lm_workspace_size(None, 1, 4, 3, 1000) == 0
+
+
+def test_selftest_timeout_argument_errors(L):
+    assert L.dcoco_selftest_timeout(0, None) == 1 and b"polls" in L.dcoco_last_error()
+    assert L.dcoco_selftest_timeout(65537, None) == 1

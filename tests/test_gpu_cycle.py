@@ -1,9 +1,11 @@
 """Whole-cycle parity (a1..a6 through dcoco_cycle) against the float64 oracle.
 
 Small configurations are compared in full.  At the full workload sizes (the launch
-configuration the benchmark times) top-K is compared on every row and the rest on a
-sample of streams that the oracle recomputes end to end.
+configuration the benchmark times) top-K is compared on every row of every stream and the
+rest on a sample of streams that the oracle recomputes end to end.  Every point of the
+streams x B x K sweep is compared, with greedy and with stochastic verification.
 """
+import functools
 import os
 
 import numpy as np
@@ -14,7 +16,7 @@ import draft_correction_gb300 as dc
 import oracle
 import workloads as wl
 from conftest import GOLDEN
-from helpers import assert_scores_close, case, compare_walk, f64, w64
+from helpers import assert_scores_close, case, compare_walk, emb_table, f64, oracle_topk_rows, w64
 from test_gpu_kernels import SMALL_BF16, SMALL_R256, SMALL_R512
 
 pytestmark = pytest.mark.gpu
@@ -33,16 +35,20 @@ def sample_streams(N):
     return list(range(N)) if N <= 4 else sorted({0, N // 2, N - 1})
 
 
-def run_cycle_and_compare(cfg, variant=None, logits=None, mode=dc.VERIFY_GREEDY, use_table=False):
-    c = case(cfg, variant)
+def run_cycle_and_compare(cfg, variant=None, logits=None, mode=dc.VERIFY_GREEDY, use_table=False, inputs=None):
+    """inputs, when given, holds this configuration's host tensors (logits, h, emb, w; q and u
+    for stochastic verification; optionally "topk", the oracle's top-K of every row for some
+    K' >= K, whose first K columns are the top-K)."""
+    c = case(cfg, variant) if inputs is None else inputs
     logits = c["logits"] if logits is None else logits
     W = w64(c["w"], cfg)
     sam = sample_streams(cfg.N)
-    # top-K parity on every row up to 512 rows, on the sampled streams beyond that
-    rows = list(range(cfg.N)) if cfg.N * cfg.B <= 512 else sam
-    vals_r, ids_r = oracle.topk(f64(logits[rows], cfg), cfg.K)
-    pos = [rows.index(n) for n in sam]
-    vals, ids = vals_r[pos], ids_r[pos]
+    # top-K parity on every row of every stream
+    if c.get("topk") is not None and logits is c["logits"]:
+        vals_r, ids_r = c["topk"][0][..., :cfg.K], c["topk"][1][..., :cfg.K]
+    else:
+        vals_r, ids_r = oracle_topk_rows(logits, cfg, cfg.K)
+    vals, ids = vals_r[sam], ids_r[sam]
     h64 = f64(c["h"][sam], cfg)
     # the oracle sees exactly the embedding rows it gathers (never the whole table in float64)
     uniq, inv = np.unique(ids, return_inverse=True)
@@ -58,8 +64,8 @@ def run_cycle_and_compare(cfg, variant=None, logits=None, mode=dc.VERIFY_GREEDY,
         ver_ref = oracle.verify_greedy(tok_ref, t[sam])
         extra = {"t": dc.to_device(t, "i32")}
     else:
-        q = wl.verifier_probs(cfg)
-        u = wl.uniforms(cfg)
+        q = c["q"] if "q" in c else wl.verifier_probs(cfg)
+        u = c["u"] if "u" in c else wl.uniforms(cfg)
         ver_ref = oracle.verify_stochastic(tok_ref, q[sam], u[sam])
         extra = {"q": dc.to_device(q, "f32"), "u": dc.to_device(u, "f32")}
 
@@ -72,8 +78,8 @@ def run_cycle_and_compare(cfg, variant=None, logits=None, mode=dc.VERIFY_GREEDY,
     torch.cuda.synchronize()
     g = {k: v.cpu().numpy() for k, v in out.items()}
 
-    np.testing.assert_array_equal(g["ids"][rows], ids_r)
-    np.testing.assert_array_equal(g["vals"][rows].astype(np.float64), vals_r)
+    np.testing.assert_array_equal(g["ids"], ids_r)
+    np.testing.assert_array_equal(g["vals"].astype(np.float64), vals_r)
     unary = np.broadcast_to(vals[:, 1:, None, :], S_ref.shape) if variant == "amplified" else None
     assert_scores_close(g["S"][sam], S_ref, unary=unary)
     near = compare_walk(g["k_sel"][sam], k_ref, S_ref, vals)
@@ -136,12 +142,29 @@ def test_cycle_full_size(cfg):
     run_cycle_and_compare(cfg)
 
 
+@functools.lru_cache(maxsize=1)
+def sweep_inputs(n, b):
+    """Host inputs of the sweep's (streams, B) point, shared by its three K and two verify modes:
+    the oracle's top-16 of every row gives the top-4 and top-8 as its first columns."""
+    cfg = wl.HEADLINE.replace(name=f"sweep_n{n}_b{b}", N=n, B=b)
+    lg = wl.logits(cfg)
+    return {"logits": lg, "h": wl.hidden(cfg), "emb": emb_table(cfg), "w": wl.weights(cfg),
+            "q": wl.verifier_probs(cfg), "u": wl.uniforms(cfg), "topk": oracle_topk_rows(lg, cfg, max(wl.SWEEP_K))}
+
+
+SWEEP_POINTS = [(n, b, k, mode) for n in wl.SWEEP_STREAMS for b in wl.SWEEP_B for k in wl.SWEEP_K
+                for mode in (dc.VERIFY_GREEDY, dc.VERIFY_STOCHASTIC)]
+
+
 @pytest.mark.slow
-@pytest.mark.parametrize("n,b,k,mode", [(4, 8, 4, dc.VERIFY_STOCHASTIC), (128, 16, 16, dc.VERIFY_GREEDY),
-                                        (16, 8, 16, dc.VERIFY_STOCHASTIC)])
+@pytest.mark.parametrize("n,b,k,mode", SWEEP_POINTS,
+                         ids=[f"n{n}-b{b}-k{k}-{'greedy' if m == dc.VERIFY_GREEDY else 'stochastic'}"
+                              for n, b, k, m in SWEEP_POINTS])
 def test_cycle_sweep_points(n, b, k, mode):
+    """All 42 (streams, B, K) points of the draft-correct-verify sweep, each with greedy and with
+    stochastic verification, in the launch configuration the sweep benchmark times."""
     cfg = wl.HEADLINE.replace(name=f"sweep_n{n}_b{b}_k{k}", N=n, B=b, K=k)
-    run_cycle_and_compare(cfg, mode=mode)
+    run_cycle_and_compare(cfg, mode=mode, inputs=sweep_inputs(n, b))
 
 
 @pytest.mark.slow
