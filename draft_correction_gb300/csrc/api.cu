@@ -245,10 +245,14 @@ int run_gemm(GemmArgs& a, const Dims& D, int BN, cudaStream_t st, const char* wh
   if (rc != DCOCO_OK) return rc;
   a.ln_eps = 1e-5f;
   const int m_tiles = (a.M + 127) / 128;
-  const int n_tiles = a.g[0].n_tiles + (a.n_groups > 1 ? a.g[1].n_tiles : 0);
+  int n_tiles = 0;
+  bool prep = false;
+  for (int i = 0; i < a.n_groups; ++i) {
+    n_tiles += a.g[i].n_tiles;
+    prep = prep || a.g[i].epi == EPI_PREP;
+  }
   const int bk = D.bf16 ? 64 : 32;
   const int nkb = (a.K + bk - 1) / bk;
-  const bool prep = a.g[0].epi == EPI_PREP || (a.n_groups > 1 && a.g[1].epi == EPI_PREP);
   const int split = prep ? 1 : pick_split(m_tiles, n_tiles, nkb, BN, max_ctas > 0 ? max_ctas : sm_count());
   const cudaError_t e = launch_gemm(a, D.bf16, BN, split, st);
   if (e != cudaSuccess) return cuda_fail(e, what);
@@ -327,6 +331,37 @@ int enqueue_repr_fuse(const Dims& D, const dcoco_weights* w, void* uz, void* vz,
                       cudaEvent_t before_uv = nullptr, const void* table = nullptr, const int32_t* ids = nullptr,
                       int V = 0) {
   const int M = D.M(), r = D.r, H = D.H;
+  if (prep_vals != nullptr && table == nullptr && zuv_supported(D.bf16, r, H)) {
+    // z and the scorer operands in one kernel: z stays on chip
+    if (before_uv != nullptr) {
+      const cudaError_t e = cudaStreamWaitEvent(st, before_uv, 0);
+      if (e != cudaSuccess) return cuda_fail(e, "wait for W s");
+    }
+    ZuvArgs z = {};
+    const char* err = nullptr;
+    if (!make_tmap(&z.b_map, s.b, true, M, r, r, 128, &err) || !make_tmap(&z.wf_map, w->W_f, true, r, 2 * r, 2 * r, r, &err) ||
+        !make_tmap(&z.u_map, w->U, true, H, r, r, std::min(H, 256), &err) ||
+        !make_tmap(&z.v_map, w->V, true, H, r, r, std::min(H, 256), &err) ||
+        !make_tmap(&z.p_map, uz, true, M, H, H, 32, &err) || !make_tmap(&z.q_map, vz, true, M, H, H, 32, &err))
+      return fail(DCOCO_ERR_CUDA, "%s", err);
+    z.gw = s.gw;
+    z.wsp = prep_wsp;
+    z.vals = prep_vals;
+    z.b1 = w->b1;
+    z.u_a = w->u_a;
+    z.u_b = w->u_b;
+    z.M = M;
+    z.r = r;
+    z.H = H;
+    z.cand = D.K;
+    z.slots = D.B;
+    int rc;
+    z.status = status_word(&rc);
+    if (rc != DCOCO_OK) return rc;
+    const cudaError_t e = launch_zuv(z, st);
+    if (e != cudaSuccess) return cuda_fail(e, "fused z, U z / V z");
+    return DCOCO_OK;
+  }
   // z = SiLU(W_f[:, 0:r] b + gw[slot])
   {
     GemmArgs a = {};
@@ -459,6 +494,61 @@ int enqueue_pair(const Dims& D, const void* h, const dcoco_weights* w, float* ws
     const int BN = pick_bn(H, false);
     DCOCO_TRY(gemm_group(&a.g[0], w->W, D, H, r, r, BN, wsp, H, EPI_F32, a.M));
     DCOCO_TRY(run_gemm(a, D, BN, st, "gemm W s"));
+  }
+  return DCOCO_OK;
+}
+
+// The cycle's projections that need only h, as one GEMM over h with three output groups:
+// g = LN(W_h h) and the two halves of W_pair applied to every slot (hp).  It lets the next
+// kernel of the stream (top-K, which does not read its outputs) launch as soon as it starts.
+int enqueue_hproj(const Dims& D, const void* h, const dcoco_weights* w, const ReprScratch& rs, const PairScratch& ps,
+                  cudaStream_t st, int max_ctas) {
+  const int NB = D.NB(), r = D.r, d = D.d;
+  GemmArgs a = {};
+  DCOCO_TRY(a_map_tiled(a, h, D, NB, d, d));
+  a.M = NB;
+  a.K = d;
+  a.n_groups = 3;
+  a.early_dependents = 1;
+  const int BN = pick_bn(r, true);  // the LayerNorm group needs its whole row in one tile
+  if (BN != r) return fail(DCOCO_ERR_UNSUPPORTED, "r=%d", r);
+  DCOCO_TRY(gemm_group(&a.g[0], w->W_h, D, r, d, d, BN, rs.g, r, EPI_LN, a.M));
+  DCOCO_TRY(gemm_group(&a.g[1], w->W_pair, D, r, d, 2 * d, BN, ps.hp, 2 * r, EPI_F32, a.M));
+  DCOCO_TRY(gemm_group(&a.g[2], static_cast<const char*>(w->W_pair) + d * D.esz, D, r, d, 2 * d, BN, ps.hp + r, 2 * r,
+                       EPI_F32, a.M));
+  return run_gemm(a, D, BN, st, "gemm g = LN(W_h h), W_pair h", max_ctas);
+}
+
+// The rest of the h-only work after enqueue_hproj, on two streams: s_p = hp[p, 0:r] +
+// hp[p+1, r:2r] and W s_p on st_pair; the g half of the fusion gw = W_f[:, r:2r] g on st_slot.
+int enqueue_h_tail(const Dims& D, const dcoco_weights* w, float* wsp, const ReprScratch& rs, const PairScratch& ps,
+                   cudaStream_t st_pair, cudaStream_t st_slot) {
+  const int r = D.r, H = D.H;
+  {
+    const cudaError_t e = launch_pair_combine(ps.hp, ps.s, D.bf16, D.N, D.B, r, st_pair);
+    if (e != cudaSuccess) return cuda_fail(e, "pair combine");
+  }
+  {
+    GemmArgs a = {};
+    DCOCO_TRY(a_map_tiled(a, rs.g, D, D.NB(), r, r));
+    a.M = D.NB();
+    a.K = r;
+    a.n_groups = 1;
+    const int BN = pick_bn(r, false);
+    DCOCO_TRY(gemm_group(&a.g[0], static_cast<const char*>(w->W_f) + r * D.esz, D, r, r, 2 * r, BN, rs.gw, r, EPI_F32,
+                         a.M));
+    DCOCO_TRY(run_gemm(a, D, BN, st_slot, "gemm gw = W_f,g g"));
+  }
+  PdlScope pdl_chain;  // W s follows this library's own pair-combine kernel
+  {
+    GemmArgs a = {};
+    DCOCO_TRY(a_map_tiled(a, ps.s, D, D.NP(), r, r));
+    a.M = D.NP();
+    a.K = r;
+    a.n_groups = 1;
+    const int BN = pick_bn(H, false);
+    DCOCO_TRY(gemm_group(&a.g[0], w->W, D, H, r, r, BN, wsp, H, EPI_F32, a.M));
+    DCOCO_TRY(run_gemm(a, D, BN, st_pair, "gemm W s"));
   }
   return DCOCO_OK;
 }
@@ -903,30 +993,44 @@ int cycle_impl(const void* logits, const void* W_lm, int V, const void* emb, con
   DCOCO_TRY(side_stream(&side));
   cudaError_t e;
   if (W_lm != nullptr) {
+    // The fused LM-head kernel is persistent over every SM: the h-only work forks after it and
+    // runs beside the embedding-row GEMM, on the SMs that GEMM leaves free.
     int rc;
     unsigned int* status = status_word(&rc);
     if (rc != DCOCO_OK) return rc;
     e = launch_lm_topk(h, W_lm, D.bf16, rows, D.d, V, K, pair_mode, o_vals, o_ids, lm_partial, lm_bytes, status, st);
+    if (e != cudaSuccess) return cuda_fail(e, "top-K launch");
+    const int spare = std::max(12, sm_count() - gather_gemm_ctas(D));
+    const int pair_ctas = spare * 2 / 3, slot_ctas = spare - pair_ctas;
+    e = cudaEventRecord(side->fork, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(side->stream, side->fork, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(side->stream2, side->fork, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "fork to helper streams");
+    DCOCO_TRY(enqueue_pair(D, h, w, s.wsp, s.pair, side->stream, pair_ctas));
+    DCOCO_TRY(enqueue_repr_slot(D, h, w, s.repr, side->stream2, slot_ctas));
+    e = cudaEventRecord(side->join, side->stream);
+    if (e == cudaSuccess) e = cudaEventRecord(side->join2, side->stream2);
+    if (e != cudaSuccess) return cuda_fail(e, "join from helper streams");
   } else {
-    e = launch_topk(logits, D.bf16, rows, V, K, topk_split(rows, V, D.bf16), o_vals, o_ids, st);
+    // The projections that need only h run first, as one GEMM on the SMs top-K leaves free
+    // (top-K holds at most four blocks per SM); top-K launches programmatically behind it, as
+    // soon as its CTAs have started, without waiting for it.  The tail of the h-only chain (pair
+    // sums, W s, the g half of the fusion) runs on a helper stream once that GEMM is done, on
+    // the SMs it frees, while top-K still streams the logits.
+    const int topk_sms = (rows * topk_ctas_per_row(rows, V, D.bf16, topk_split(rows, V, D.bf16)) + 3) / 4;
+    const int spare = std::max(12, sm_count() - topk_sms);
+    DCOCO_TRY(enqueue_hproj(D, h, w, s.repr, s.pair, st, spare));
+    e = cudaEventRecord(side->fork, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(side->stream, side->fork, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(side->stream2, side->fork, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "fork to helper streams");
+    e = launch_topk(logits, D.bf16, rows, V, K, topk_split(rows, V, D.bf16), o_vals, o_ids, st, true);
+    if (e != cudaSuccess) return cuda_fail(e, "top-K launch");
+    DCOCO_TRY(enqueue_h_tail(D, w, s.wsp, s.repr, s.pair, side->stream, side->stream2));
+    e = cudaEventRecord(side->join, side->stream);
+    if (e == cudaSuccess) e = cudaEventRecord(side->join2, side->stream2);
+    if (e != cudaSuccess) return cuda_fail(e, "join from helper streams");
   }
-  if (e != cudaSuccess) return cuda_fail(e, "top-K launch");
-  // Top-K occupies every SM's registers, so the work that needs only h (pair states and W s on
-  // one helper stream; g and the g half of the fusion on another) starts after it, beside the
-  // embedding-row GEMM, with split-K grids sized to the SMs that GEMM leaves free (split-K
-  // clusters wider than two did not find room beside it).  z waits for the g branch; the pair
-  // branch is first needed by the U z / V z GEMM.
-  const int spare = std::max(12, sm_count() - (table != nullptr ? 0 : gather_gemm_ctas(D)));
-  const int pair_ctas = spare * 2 / 3, slot_ctas = spare - pair_ctas;
-  e = cudaEventRecord(side->fork, st);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(side->stream, side->fork, 0);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(side->stream2, side->fork, 0);
-  if (e != cudaSuccess) return cuda_fail(e, "fork to helper streams");
-  DCOCO_TRY(enqueue_pair(D, h, w, s.wsp, s.pair, side->stream, pair_ctas));
-  DCOCO_TRY(enqueue_repr_slot(D, h, w, s.repr, side->stream2, slot_ctas));
-  e = cudaEventRecord(side->join, side->stream);
-  if (e == cudaSuccess) e = cudaEventRecord(side->join2, side->stream2);
-  if (e != cudaSuccess) return cuda_fail(e, "join from helper streams");
   if (table == nullptr) DCOCO_TRY(enqueue_repr_gather(D, o_ids, emb, V, w, s.repr, st));
   e = cudaStreamWaitEvent(st, side->join2, 0);
   if (e != cudaSuccess) return cuda_fail(e, "join from helper streams");

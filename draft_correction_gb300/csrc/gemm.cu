@@ -38,6 +38,7 @@ constexpr int kThreads = 64 + kEpiThreads;
 constexpr int kMaxStages = 8;
 constexpr int kSmemBudget = 200 * 1024;
 constexpr int kGatherThreads = kEpiThreads;  // epilogue warps that gather the A operand
+constexpr int kGatherDepth = 4;              // k-blocks of gathered rows in flight per thread
 constexpr int kBiasStageBytes = 20 * 1024;  // per-slot bias rows of one tile (SiLU epilogue)
 
 __device__ unsigned int g_status_word;
@@ -108,6 +109,20 @@ __device__ __forceinline__ void store_act1(void* out, size_t idx, float v) {
   }
 }
 
+// 32 bytes (two 16-byte halves) from a 32-byte aligned address, not kept in L1.
+__device__ __forceinline__ void ld_nc32(const void* p, uint4& a, uint4& b) {
+  asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
+               : "l"(p));
+}
+__device__ __forceinline__ uint4 ld_nc16(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
@@ -140,9 +155,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   const int lane = threadIdx.x & 31;
   const int m_tile = blockIdx.x;
   int gi = 0, nt = blockIdx.y;
-  if (nt >= args.g[0].n_tiles) {
-    gi = 1;
-    nt -= args.g[0].n_tiles;
+  while (gi + 1 < args.n_groups && nt >= args.g[gi].n_tiles) {
+    nt -= args.g[gi].n_tiles;
+    ++gi;
   }
   const GemmGroup& grp = args.g[gi];
   const int ks = blockIdx.z;
@@ -180,6 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       for (int h = 0; h < NH; ++h) tma_load_2d(b_s + h * NMMA * 128, &grp.b_map, kx, nt * BN + h * NMMA, fb);
     }
   }
+  if (args.early_dependents) grid_dep_launch();
   grid_dep_wait();
   if (args.gather != nullptr && threadIdx.x < BM) {
     const int m = m_tile * BM + threadIdx.x;
@@ -252,49 +268,72 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   } else {
     // ------------------------------------------------------------ epilogue (warps 2..5)
     if (gather) {
-      // Gathered A operand: while the main loop runs these 128 threads copy Emb[c] rows into
-      // the stages with 16-byte asynchronous copies straight into the 128-byte swizzled layout
-      // (eight threads per 128-byte row piece, so global reads stay coalesced), then hand each
-      // stage to the tensor core with a generic-to-async proxy fence and one arrival.
-      constexpr int RPT = BM * 8 / kGatherThreads;  // tile rows per thread (4)
-      constexpr int RSTEP = kGatherThreads / 8;     // rows covered by one pass of the threads
+      // Gathered A operand: while the main loop runs these 256 threads copy Emb[c] rows into the
+      // stages through registers.  Thread t owns the 32-byte piece t % 4 of tile rows t / 4 and
+      // 64 + t / 4 in every k-block (the 8 threads of a row pair cover 2 x 128 bytes, coalesced),
+      // loads kGatherDepth k-blocks ahead with 32-byte non-caching loads, and stores each k-block
+      // into the 128-byte swizzled operand layout once its stage is free; a generic-to-async
+      // proxy fence and one arrival per thread hand the stage to the tensor core.  (Measured on
+      // this GPU: 32-byte register loads reach about 6.4 TB/s on this gather, 16-byte
+      // asynchronous copies about 3 TB/s at any ring depth.)
       const int t = threadIdx.x - 64;
-      const int c = t & 7;                     // 16-byte chunk of the 128-byte row piece
-      const int cs = c ^ ((t >> 3) & 7);       // its swizzled position (row & 7 == (t >> 3) & 7)
-      const int esz = kBf16 ? 2 : 4;
-      const char* rowb[RPT];  // start of the table row behind each of this thread's tile rows
+      const int pc = t & 3;                    // 32-byte piece of the 128-byte row
+      const int rA = t >> 2, rB = 64 + (t >> 2);
+      constexpr int esz = kBf16 ? 2 : 4;
+      constexpr int EPP = 32 / esz;            // elements per piece
+      const char* base = static_cast<const char*>(args.gather_base);
+      const char* pA = base + static_cast<size_t>(s_rows[rA]) * args.gather_pitch_bytes + kb0 * 128 + pc * 32;
+      const char* pB = base + static_cast<size_t>(s_rows[rB]) * args.gather_pitch_bytes + kb0 * 128 + pc * 32;
+      const int kel0 = kb0 * T::BK + pc * EPP;  // first element of this thread's piece in k-block 0
+      // 32-byte loads need 32-byte aligned rows; the ABI promises 16 (then two 16-byte loads)
+      const bool wide = ((reinterpret_cast<uintptr_t>(base) | static_cast<uintptr_t>(args.gather_pitch_bytes)) & 31) == 0;
+      uint4 ra[kGatherDepth][2], rb[kGatherDepth][2];
+      // The piece of k-block i, 16 bytes at a time: a row ends on a 16-byte boundary, so each half
+      // lies wholly inside the row or wholly past its end (zero).
+      auto fetch = [&](int i, uint4(&a)[2], uint4(&b)[2]) {
+        const int kcol = kel0 + i * T::BK;
+        const size_t off = static_cast<size_t>(i) * 128;
+        const bool lo = i < nk && kcol < args.K;
+        const bool hi = i < nk && kcol + EPP / 2 < args.K;
+        if (wide && hi) {
+          ld_nc32(pA + off, a[0], a[1]);
+          ld_nc32(pB + off, b[0], b[1]);
+        } else {
+          const uint4 z = make_uint4(0, 0, 0, 0);
+          a[0] = lo ? ld_nc16(pA + off) : z;
+          b[0] = lo ? ld_nc16(pB + off) : z;
+          a[1] = hi ? ld_nc16(pA + off + 16) : z;
+          b[1] = hi ? ld_nc16(pB + off + 16) : z;
+        }
+      };
+      // swizzled positions of the piece's two 16-byte chunks in rows rA and rB (rA & 7 == rB & 7)
+      const int sw = rA & 7;
+      const uint32_t offA0 = rA * 128 + (((2 * pc) ^ sw) << 4), offA1 = rA * 128 + (((2 * pc + 1) ^ sw) << 4);
+      const uint32_t offB0 = offA0 + 64 * 128, offB1 = offA1 + 64 * 128;
 #pragma unroll
-      for (int it = 0; it < RPT; ++it)
-        rowb[it] = static_cast<const char*>(args.gather_base) +
-                   static_cast<size_t>(s_rows[it * RSTEP + (t >> 3)]) * args.gather_pitch_bytes;
-      const int lag = stages - 1;
+      for (int d = 0; d < kGatherDepth; ++d) fetch(d, ra[d], rb[d]);
       bool alive = true;
-      for (int i = 0; i < nk && alive; ++i) {
-        const int s = i % stages;
-        const uint32_t ph = (i / stages) & 1;
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&empty_bar[s]), ph ^ 1))) {
-          if (lane == 0) atomicOr(args.status, DEV_TIMEOUT_MMA);
-          alive = false;
-          break;
-        }
-        const uint32_t a_s = smem0 + s * STAGE_BYTES;
-        const int kcol = (kb0 + i) * T::BK + c * (16 / esz);  // first element of this chunk
-        const uint32_t nbytes = kcol < args.K ? 16u : 0u;      // K is a multiple of 16 bytes
-        const size_t koff = static_cast<size_t>(kcol) * esz;
+      for (int i0 = 0; i0 < nk && alive; i0 += kGatherDepth) {
 #pragma unroll
-        for (int it = 0; it < RPT; ++it)
-          cp_async16(a_s + (it * RSTEP + (t >> 3)) * 128 + cs * 16, rowb[it] + (nbytes ? koff : 0), nbytes);
-        cp_async_commit();
-        if (i >= lag) {
-          cp_async_wait(lag);
+        for (int d = 0; d < kGatherDepth; ++d) {
+          const int i = i0 + d;
+          if (i >= nk || !alive) break;  // warp-uniform
+          const int s = i % stages;
+          const uint32_t ph = (i / stages) & 1;
+          if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&empty_bar[s]), ph ^ 1))) {
+            if (lane == 0) atomicOr(args.status, DEV_TIMEOUT_MMA);
+            alive = false;
+            break;
+          }
+          uint8_t* a_s = smem + s * STAGE_BYTES;
+          *reinterpret_cast<uint4*>(a_s + offA0) = ra[d][0];
+          *reinterpret_cast<uint4*>(a_s + offA1) = ra[d][1];
+          *reinterpret_cast<uint4*>(a_s + offB0) = rb[d][0];
+          *reinterpret_cast<uint4*>(a_s + offB1) = rb[d][1];
           fence_proxy_async();
-          mbar_arrive(smem_u32(&full_bar[(i - lag) % stages]));
+          mbar_arrive(smem_u32(&full_bar[s]));
+          fetch(i + kGatherDepth, ra[d], rb[d]);
         }
-      }
-      cp_async_wait(0);
-      fence_proxy_async();
-      if (alive) {
-        for (int i = nk > lag ? nk - lag : 0; i < nk; ++i) mbar_arrive(smem_u32(&full_bar[i % stages]));
       }
     }
     const int q = warp & 3;  // TMEM lane quarter this warp may access
@@ -604,14 +643,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 template <bool kBf16, int BN, bool kSplit>
 cudaError_t launch_gemm_t(const GemmArgs& args, int split_k, cudaStream_t stream) {
   // The split-K reduction has no scorer-operand epilogue.
-  if (kSplit && (args.g[0].epi == EPI_PREP || (args.n_groups > 1 && args.g[1].epi == EPI_PREP)))
-    return cudaErrorInvalidValue;
+  auto any_group = [&](auto pred) {
+    for (int i = 0; i < args.n_groups; ++i)
+      if (pred(args.g[i].epi)) return true;
+    return false;
+  };
+  if (args.n_groups < 1 || args.n_groups > 3) return cudaErrorInvalidValue;
+  if (kSplit && any_group([](int epi) { return epi == EPI_PREP; })) return cudaErrorInvalidValue;
   constexpr int STAGE_BYTES = BM * 128 + BN * 128;
   int stages = std::min(kMaxStages, kSmemBudget / STAGE_BYTES);
   // split-K reuses the pipeline buffers: partial tile (BM x LDS) plus this CTA's reduced rows
   const int split_bytes = kSplit ? (BM + BM / 2) * (BN + 4) * 4 : 0;
   auto staged = [](int epi) { return epi == EPI_SILU_BIAS || epi == EPI_PREP; };
-  const bool has_bias = staged(args.g[0].epi) || (args.n_groups > 1 && staged(args.g[1].epi));
+  const bool has_bias = any_group(staged);
   if (has_bias) stages = std::min(stages, 4);
   const int bias_off = std::max(stages * STAGE_BYTES, split_bytes);
   const int smem = bias_off + (has_bias ? kBiasStageBytes : 0) + 1024;
@@ -629,7 +673,9 @@ cudaError_t launch_gemm_t(const GemmArgs& args, int split_k, cudaStream_t stream
     configured[dev] = smem;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((args.M + BM - 1) / BM, args.g[0].n_tiles + (args.n_groups > 1 ? args.g[1].n_tiles : 0), split_k);
+  int n_tiles = 0;
+  for (int i = 0; i < args.n_groups; ++i) n_tiles += args.g[i].n_tiles;
+  cfg.gridDim = dim3((args.M + BM - 1) / BM, n_tiles, split_k);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
@@ -673,11 +719,351 @@ __global__ void pair_combine_kernel(const float* __restrict__ hp, void* __restri
   }
 }
 
+
+// ---------------------------------------------------------------- fused z -> P / Q
+// The candidate fusion z = SiLU(W_f [b; g]) and the candidate blocks of the first MLP layer
+// (U z, V z, folded into the scorer's operands P and Q) for one 128-row tile, in one kernel:
+//   phase 1  acc1 = b W_f[:, 0:r]^T in TMEM (b tile loaded once by TMA, W_f k-blocks through a
+//            two-stage ring); the epilogue warps write z = SiLU(acc1 + gw[slot]) in bf16 over the
+//            b tile, in the 128-byte swizzled operand layout, and hand it to the MMA warp;
+//   phase 2  acc2 = z U^T (grid.y = 0) or z V^T (grid.y = 1), the weight k-blocks through the
+//            same ring; the epilogue adds the logit term (and for P the bias and W s_p), halves,
+//            and stores f16 rows with tensor-map stores.
+// z never leaves shared memory.  Warp roles as in gemm_kernel: 0 TMA producer, 1 MMA issuer,
+// 2-9 epilogue (two per TMEM lane quarter, each with half of the columns).
+constexpr int kZuvRing = 2;
+constexpr int kZuvStage = 512 * 128;  // one k-block of up to 512 weight rows
+constexpr int kZuvConst = 32 * 1024;  // per-tile constants of the epilogues
+
+// tanh of two values in packed half precision (one SFU instruction for both).
+__device__ __forceinline__ float2 tanh2_f16(float a, float b) {
+  const __half2 x = __floats2half2_rn(a, b);
+  uint32_t t;
+  asm("tanh.approx.f16x2 %0, %1;" : "=r"(t) : "r"(*reinterpret_cast<const uint32_t*>(&x)));
+  return __half22float2(*reinterpret_cast<const __half2*>(&t));
+}
+
+__device__ __forceinline__ uint4 pack8_bf16(const float* v) {
+  __nv_bfloat162 t0 = __floats2bfloat162_rn(v[0], v[1]);
+  __nv_bfloat162 t1 = __floats2bfloat162_rn(v[2], v[3]);
+  __nv_bfloat162 t2 = __floats2bfloat162_rn(v[4], v[5]);
+  __nv_bfloat162 t3 = __floats2bfloat162_rn(v[6], v[7]);
+  return make_uint4(*reinterpret_cast<uint32_t*>(&t0), *reinterpret_cast<uint32_t*>(&t1),
+                    *reinterpret_cast<uint32_t*>(&t2), *reinterpret_cast<uint32_t*>(&t3));
+}
+
+template <int R>
+__global__ void __launch_bounds__(kThreads, 1) zuv_kernel(const __grid_constant__ ZuvArgs args) {
+  constexpr int NK = R / 64;      // k-blocks of both products (their K is r)
+  constexpr int A_KB = BM * 128;  // one k-block of the 128-row operand
+  constexpr uint32_t IDESC1 = mma_idesc(1u, BM, R);
+  extern __shared__ uint8_t dyn_smem[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
+  uint8_t* a_reg = smem;            // NK x 16 KB: the b tile, then z
+  uint8_t* ring = smem + NK * A_KB;  // kZuvRing x kZuvStage
+  __shared__ __align__(8) uint64_t full_bar[kZuvRing];
+  __shared__ __align__(8) uint64_t empty_bar[kZuvRing];
+  __shared__ __align__(8) uint64_t a_bar, acc1_bar, z_bar, acc2_bar;
+  __shared__ uint32_t tmem_base_s;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int m_tile = blockIdx.x;
+  const bool is_q = blockIdx.y != 0;
+  const int H = args.H;
+  const int NC = H <= 256 ? H : 256;  // columns per phase-2 MMA
+  const uint32_t idesc2 = mma_idesc(1u, BM, static_cast<uint32_t>(NC));
+  const CUtensorMap* w2_map = is_q ? &args.v_map : &args.u_map;
+  constexpr int total = 2 * NK;  // ring loads: NK k-blocks of W_f, then NK of U or V
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kZuvRing; ++s) {
+      mbar_init(smem_u32(&full_bar[s]), 1);
+      mbar_init(smem_u32(&empty_bar[s]), 1);
+    }
+    mbar_init(smem_u32(&a_bar), 1);
+    mbar_init(smem_u32(&acc1_bar), 1);
+    mbar_init(smem_u32(&z_bar), 1);
+    mbar_init(smem_u32(&acc2_bar), 1);
+    fence_mbar_init();
+    prefetch_tmap(&args.b_map);
+    prefetch_tmap(&args.wf_map);
+    prefetch_tmap(w2_map);
+    prefetch_tmap(is_q ? &args.q_map : &args.p_map);
+  }
+  if (warp == 1) tmem_alloc(smem_u32(&tmem_base_s), 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_s;
+  const uint32_t ring0 = smem_u32(ring), a0 = smem_u32(a_reg);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      auto issue = [&](int i) {
+        const int s = i % kZuvRing;
+        const uint32_t fb = smem_u32(&full_bar[s]);
+        const uint32_t dst = ring0 + s * kZuvStage;
+        if (i < NK) {
+          mbar_expect_tx(fb, R * 128);
+          tma_load_2d(dst, &args.wf_map, i * 64, 0, fb);
+        } else {
+          mbar_expect_tx(fb, H * 128);
+          for (int h0 = 0; h0 < H; h0 += NC) tma_load_2d(dst + h0 * 128, w2_map, (i - NK) * 64, h0, fb);
+        }
+      };
+      // the weight tiles do not depend on the preceding kernels: request them first
+      for (int i = 0; i < kZuvRing && i < total; ++i) issue(i);
+      grid_dep_wait();  // the b rows come from the preceding kernel
+      const uint32_t ab = smem_u32(&a_bar);
+      mbar_expect_tx(ab, NK * A_KB);
+      for (int kb = 0; kb < NK; ++kb) tma_load_2d(a0 + kb * A_KB, &args.b_map, kb * 64, m_tile * BM, ab);
+      for (int i = kZuvRing; i < total; ++i) {
+        const int s = i % kZuvRing;
+        if (!mbar_wait(smem_u32(&empty_bar[s]), ((i / kZuvRing) & 1) ^ 1)) {
+          atomicOr(args.status, DEV_TIMEOUT_MMA);
+          break;
+        }
+        issue(i);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      bool ok = mbar_wait(smem_u32(&a_bar), 0);
+      if (!ok) atomicOr(args.status, DEV_TIMEOUT_TMA);
+      for (int i = 0; ok && i < total; ++i) {
+        if (i == NK) {
+          // phase 2 reads z, which the epilogue writes over b once it has read acc1
+          tc_commit(smem_u32(&acc1_bar));
+          if (!mbar_wait(smem_u32(&z_bar), 0)) {
+            atomicOr(args.status, DEV_TIMEOUT_ACC);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        const int s = i % kZuvRing;
+        if (!mbar_wait(smem_u32(&full_bar[s]), (i / kZuvRing) & 1)) {
+          atomicOr(args.status, DEV_TIMEOUT_TMA);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t b_s = ring0 + s * kZuvStage;
+        const int kb = i < NK ? i : i - NK;
+        const uint32_t a_s = a0 + kb * A_KB;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint64_t ad = sw128_desc(a_s + j * 32);
+          const uint32_t acc = (kb > 0 || j > 0) ? 1u : 0u;
+          if (i < NK) {
+            tc_mma<false>(tmem, ad, sw128_desc(b_s + j * 32), IDESC1, acc);
+          } else {
+            for (int c = 0; c < H; c += NC) tc_mma<false>(tmem + c, ad, sw128_desc(b_s + c * 128 + j * 32), idesc2, acc);
+          }
+        }
+        tc_commit(smem_u32(&empty_bar[s]));
+      }
+      if (ok) tc_commit(smem_u32(&acc2_bar));
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 2..9)
+    const int q = warp & 3;            // TMEM lane quarter
+    const int half = (warp - 2) >> 2;  // which half of the columns
+    const int row = q * 32 + lane;
+    const int m = m_tile * BM + row;
+    const bool live = m < args.M;
+    const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    grid_dep_wait();  // gw, W s and the logits come from earlier kernels
+    const int slot = live ? m / args.cand : 0;  // stream * slots + slot
+    // Per-tile constants, staged in shared memory while the MMAs run (when they fit): the gw rows
+    // of the tile's slots; per slot (b1 + W s_p) / 2 for P (zero for Q); u / 2.
+    const int first_slot = (m_tile * BM) / args.cand;
+    const int nslots = (min(args.M, m_tile * BM + BM) - 1) / args.cand - first_slot + 1;
+    const bool staged = (nslots * (R + H) + H) * 4 <= kZuvConst;
+    float* s_gw = reinterpret_cast<float*>(ring + kZuvRing * kZuvStage);  // [nslots][R]
+    float* s_add = s_gw + nslots * R;                                       // [nslots][H]
+    float* s_u = s_add + nslots * H;                                        // [H]
+    const void* col_u = is_q ? args.u_b : args.u_a;
+    if (staged) {
+      const int et = threadIdx.x - 64;
+      for (int i = et; i < nslots * (R / 4); i += kEpiThreads) {
+        const int sl = i / (R / 4), c4 = i % (R / 4);
+        *reinterpret_cast<float4*>(s_gw + sl * R + c4 * 4) =
+            *reinterpret_cast<const float4*>(args.gw + static_cast<size_t>(first_slot + sl) * R + c4 * 4);
+      }
+      for (int i = et; i < nslots * (H / 4); i += kEpiThreads) {
+        const int sl = i / (H / 4), col = (i % (H / 4)) * 4;
+        float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (!is_q) {
+          a4 = ldw4<true>(args.b1, col);
+          const int qs = first_slot + sl, st = qs / args.slots;
+          if (qs - st * args.slots < args.slots - 1) {
+            const float4 r4 = *reinterpret_cast<const float4*>(args.wsp + static_cast<size_t>(qs - st) * H + col);
+            a4.x += r4.x;
+            a4.y += r4.y;
+            a4.z += r4.z;
+            a4.w += r4.w;
+          }
+        }
+        *reinterpret_cast<float4*>(s_add + sl * H + col) = make_float4(0.5f * a4.x, 0.5f * a4.y, 0.5f * a4.z, 0.5f * a4.w);
+      }
+      for (int i = et; i < H / 4; i += kEpiThreads) {
+        const float4 u4 = ldw4<true>(col_u, i * 4);
+        *reinterpret_cast<float4*>(s_u + i * 4) = make_float4(0.5f * u4.x, 0.5f * u4.y, 0.5f * u4.z, 0.5f * u4.w);
+      }
+    }
+    named_barrier_sync(1, kEpiThreads);
+    // phase 1: z = SiLU(acc1 + gw[slot]) in bf16, over the b tile, swizzled as TMA would load it;
+    // SiLU(x) = h + h tanh(h), h = x / 2, with the tanh in packed half precision (z is rounded to
+    // bf16, whose step is eight times the half-precision tanh's)
+    bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&acc1_bar), 0));
+    if (!ok && lane == 0) atomicOr(args.status, DEV_TIMEOUT_ACC);
+    tc_fence_after();
+    const float* gwr = staged ? s_gw + (slot - first_slot) * R : args.gw + static_cast<size_t>(slot) * R;
+#pragma unroll 1
+    for (int c = half * (R / 2); c < (half + 1) * (R / 2); c += 32) {
+      float v[32];
+      tmem_ld32(trow + c, v);
+#pragma unroll
+      for (int i = 0; i < 32; i += 4) {
+        const float4 g4 = *reinterpret_cast<const float4*>(gwr + c + i);
+        const float h0 = 0.5f * (v[i] + g4.x), h1 = 0.5f * (v[i + 1] + g4.y);
+        const float h2 = 0.5f * (v[i + 2] + g4.z), h3 = 0.5f * (v[i + 3] + g4.w);
+        const float2 t01 = tanh2_f16(h0, h1), t23 = tanh2_f16(h2, h3);
+        v[i] = live ? fmaf(h0, t01.x, h0) : 0.f;
+        v[i + 1] = live ? fmaf(h1, t01.y, h1) : 0.f;
+        v[i + 2] = live ? fmaf(h2, t23.x, h2) : 0.f;
+        v[i + 3] = live ? fmaf(h3, t23.y, h3) : 0.f;
+      }
+      uint8_t* kbase = a_reg + (c / 64) * A_KB + row * 128;
+      const int ch0 = (c % 64) / 8;
+#pragma unroll
+      for (int t = 0; t < 4; ++t)
+        *reinterpret_cast<uint4*>(kbase + (((ch0 + t) ^ (row & 7)) << 4)) = pack8_bf16(v + 8 * t);
+    }
+    fence_proxy_async();  // the tensor core reads z next
+    tc_fence_before();
+    named_barrier_sync(1, kEpiThreads);
+    if (threadIdx.x == 64) mbar_arrive(smem_u32(&z_bar));
+    // phase 2: P or Q
+    ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&acc2_bar), 0));
+    if (!ok && lane == 0) atomicOr(args.status, DEV_TIMEOUT_ACC);
+    grid_dep_launch();  // main loops done: the next kernel may start its prologue
+    tc_fence_after();
+    const float l = live ? args.vals[m] : 0.f;
+    const int stream_i = slot / args.slots, p = slot - stream_i * args.slots;
+    const float* rb = (!is_q && live && p < args.slots - 1) ? args.wsp + static_cast<size_t>(slot - stream_i) * H
+                                                            : nullptr;
+    const float* addr = s_add + (slot - first_slot) * H;
+    const int nsub = H / 64;  // 128-byte (64-column f16) sub-tiles of the row
+    const int halves = nsub >= 2 ? 2 : 1;
+    const int j0 = half * nsub / halves, j1 = (half + 1) * nsub / halves;
+    uint8_t* stg = ring + (warp - 2) * 8192;  // the ring is drained: every MMA has completed
+    const int y0 = m_tile * BM + q * 32;
+    const CUtensorMap* out_map = is_q ? &args.q_map : &args.p_map;
+    for (int j = j0; half < halves && j < j1; ++j) {
+      float v[64];
+      tmem_ld32(trow + j * 64, *reinterpret_cast<float(*)[32]>(v));
+      tmem_ld32(trow + j * 64 + 32, *reinterpret_cast<float(*)[32]>(v + 32));
+      if (staged) {
+#pragma unroll
+        for (int i = 0; i < 64; i += 4) {
+          const int col = j * 64 + i;
+          const float4 u4 = *reinterpret_cast<const float4*>(s_u + col);
+          const float4 a4 = *reinterpret_cast<const float4*>(addr + col);
+          v[i] = fmaf(0.5f, v[i], fmaf(u4.x, l, a4.x));
+          v[i + 1] = fmaf(0.5f, v[i + 1], fmaf(u4.y, l, a4.y));
+          v[i + 2] = fmaf(0.5f, v[i + 2], fmaf(u4.z, l, a4.z));
+          v[i + 3] = fmaf(0.5f, v[i + 3], fmaf(u4.w, l, a4.w));
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 64; i += 4) {
+          const int col = j * 64 + i;
+          const float4 u4 = ldw4<true>(col_u, col);
+          float4 add = (!is_q) ? ldw4<true>(args.b1, col) : make_float4(0.f, 0.f, 0.f, 0.f);
+          if (rb != nullptr) {
+            const float4 r4 = *reinterpret_cast<const float4*>(rb + col);
+            add.x += r4.x;
+            add.y += r4.y;
+            add.z += r4.z;
+            add.w += r4.w;
+          }
+          v[i] = 0.5f * (v[i] + add.x + u4.x * l);
+          v[i + 1] = 0.5f * (v[i + 1] + add.y + u4.y * l);
+          v[i + 2] = 0.5f * (v[i + 2] + add.z + u4.z * l);
+          v[i + 3] = 0.5f * (v[i + 3] + add.w + u4.w * l);
+        }
+      }
+      uint8_t* buf = stg + ((j - j0) & 1) * 4096;
+      if (j - j0 >= 2) {
+        if (lane == 0) bulk_wait_read<1>();  // the store that used this half has read it
+        __syncwarp();
+      }
+      stage_row<2>(buf, lane, v);
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0 && y0 < args.M && ok) {
+        tma_store_2d(out_map, j * 64, y0, smem_u32(buf));
+        bulk_commit();
+      }
+    }
+    if (lane == 0) bulk_wait<0>();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int R>
+cudaError_t launch_zuv_t(const ZuvArgs& a, cudaStream_t stream) {
+  const int smem = (R / 64) * BM * 128 + kZuvRing * kZuvStage + kZuvConst + 1024;
+  static int configured[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    e = cudaFuncSetAttribute(zuv_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured[dev] = 1;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((a.M + BM - 1) / BM, 2, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_attr(&attr[0]);
+  return cudaLaunchKernelEx(&cfg, zuv_kernel<R>, a);
+}
+
 }  // namespace
 
 cudaError_t launch_gemm(const GemmArgs& args, bool is_bf16, int BN, int split_k, cudaStream_t stream) {
   if (split_k < 1 || split_k > 8 || (BM % split_k) != 0) return cudaErrorInvalidValue;
   return is_bf16 ? dispatch_bn<true>(args, BN, split_k, stream) : dispatch_bn<false>(args, BN, split_k, stream);
+}
+
+bool zuv_supported(bool is_bf16, int r, int H) {
+  return is_bf16 && (r == 64 || r == 128 || r == 256) && H % 64 == 0 && H >= 64 && (H <= 256 || H == 512);
+}
+
+cudaError_t launch_zuv(const ZuvArgs& a, cudaStream_t stream) {
+  if (!zuv_supported(true, a.r, a.H)) return cudaErrorInvalidValue;
+  switch (a.r) {
+    case 64: return launch_zuv_t<64>(a, stream);
+    case 128: return launch_zuv_t<128>(a, stream);
+    default: return launch_zuv_t<256>(a, stream);
+  }
 }
 
 cudaError_t launch_pair_combine(const float* hp, void* s, bool is_bf16, int N, int B, int r, cudaStream_t stream) {

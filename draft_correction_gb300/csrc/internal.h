@@ -30,8 +30,14 @@ int sm_count();
 
 // ------------------------------------------------------------------ top-K
 // Rows of `logits` ([rows, V], bf16 bits if is_bf16 else f32); ctas_per_row in 1..8.
+// after_unrelated: the kernel is launched programmatically behind a kernel that does not write
+// the logits (and itself started only after the logits' producer finished), so it does not
+// wait for that kernel to finish.
 cudaError_t launch_topk(const void* logits, bool is_bf16, int rows, int V, int K, int ctas_per_row, float* vals,
-                        int32_t* ids, cudaStream_t stream);
+                        int32_t* ids, cudaStream_t stream, bool after_unrelated = false);
+// Thread blocks per row launch_topk uses (ctas_per_row 0: its automatic choice); at most four
+// blocks of top-K are resident on one SM.
+int topk_ctas_per_row(int rows, int V, bool is_bf16, int ctas_per_row);
 
 // ------------------------------------------------------------------ fused LM head + top-K
 // Bytes of the per-row partial lists launch_lm_topk needs (0 if no plan exists).  pair_mode 0
@@ -75,16 +81,19 @@ struct GemmArgs {
   CUtensorMap a_map;        // A [M, K] tiled (box {BK, 128}); unused when the rows are gathered
   const int32_t* gather;    // non-null: A row m is table row gather[m]
   int gather_limit;         // rows of the gather table (ids outside [0, limit) are replaced by 0)
-  const void* gather_base;  // the gather table (rows are copied from here by the epilogue warps)
+  const void* gather_base;  // the gather table (rows are loaded from here by the epilogue warps)
   int gather_pitch_bytes;
   int M, K;
-  int n_groups;             // 1 or 2
-  GemmGroup g[2];
+  int n_groups;             // 1 to 3 (each group its own B operand, output and epilogue)
+  GemmGroup g[3];
   const float* bias;        // EPI_SILU_BIAS
   int bias_div, ld_bias;
   const float* row_l;       // EPI_PREP: [M] per-row scale
   int slots;                // EPI_PREP: slots per stream
   float ln_eps;
+  // Nonzero: the kernel lets the next kernel of its stream launch as soon as it starts (for a
+  // next kernel that does not read this one's outputs; it must not wait on it either).
+  int early_dependents;
   unsigned int* status;
 };
 
@@ -96,6 +105,33 @@ bool make_tmap(CUtensorMap* map, const void* base, bool is_bf16, uint64_t rows, 
 
 // BN in {32, 64, 128, 256, 512}; split_k >= 1 (BN <= 256 when split_k > 1).
 cudaError_t launch_gemm(const GemmArgs& args, bool is_bf16, int BN, int split_k, cudaStream_t stream);
+
+// The candidate fusion and the candidate blocks of the first MLP layer in one kernel (bf16 only):
+//   z = SiLU(b W_f[:, 0:r]^T + gw[slot])                      kept in shared memory, never stored
+//   P = (z U^T + b1 + W s[pair] + u_a l) / 2,  Q = (z V^T + u_b l) / 2     f16, clamped to +-30000
+// with the row and slot conventions of EPI_SILU_BIAS and EPI_PREP.  Grid (m_tiles, 2): y = 0
+// writes P and y = 1 writes Q; both recompute z for their 128 rows.
+struct ZuvArgs {
+  CUtensorMap b_map;   // b [M, r], box {64, 128}
+  CUtensorMap wf_map;  // W_f [r, 2r] (its first r columns act on b), box {64, r}
+  CUtensorMap u_map;   // U [H, r], box {64, min(H, 256)}
+  CUtensorMap v_map;   // V [H, r], same box
+  CUtensorMap p_map;   // P [M, H] f16, box {64, 32}
+  CUtensorMap q_map;   // Q [M, H] f16, box {64, 32}
+  const float* gw;     // [slots total, r] f32: W_f[:, r:2r] g of each slot
+  const float* wsp;    // [pairs, H] f32: W s_p
+  const float* vals;   // [M] f32: the candidate's logit l
+  const void* b1;      // [H] bf16
+  const void* u_a;     // [H] bf16
+  const void* u_b;     // [H] bf16
+  int M, r, H;
+  int cand;            // candidates per slot (K): row m belongs to slot m / cand
+  int slots;           // slots per stream (B)
+  unsigned int* status;
+};
+// True when launch_zuv supports the shape (bf16, r in {64, 128, 256}, H a multiple of 64 up to 512).
+bool zuv_supported(bool is_bf16, int r, int H);
+cudaError_t launch_zuv(const ZuvArgs& a, cudaStream_t stream);
 
 // s[n, p, :] = act(hp[n, p, 0:r] + hp[n, p+1, r:2r]), hp [N, B, 2r] f32, s [N, B-1, r] activation dtype.
 cudaError_t launch_pair_combine(const float* hp, void* s, bool is_bf16, int N, int B, int r, cudaStream_t stream);

@@ -361,7 +361,8 @@ __device__ __noinline__ void exact_segment_topk(const Segment& g, int K, int ran
 
 template <bool kBf16, int KW>
 __global__ void __launch_bounds__(kThreads, 4) topk_kernel(const void* __restrict__ logits, int V, int K, int S,
-                                                        float* __restrict__ vals, int32_t* __restrict__ ids) {
+                                                        float* __restrict__ vals, int32_t* __restrict__ ids,
+                                                        int wait_prior) {
   constexpr int EPV = kEpv<kBf16>;
   __shared__ uint64_t s_buf[kCap];
   __shared__ uint64_t s_sorted[kThreads];  // each warp's lane maxima, sorted
@@ -416,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 4) topk_kernel(const void* __restric
     }
   };
 
-  grid_dep_wait();  // the logits may come from the preceding kernel
+  if (wait_prior) grid_dep_wait();  // the logits may come from the preceding kernel
   grid_dep_launch();
   // Seed threshold: the K-th largest of the block's lane maxima over the first two iterations
   // (already in registers).  K elements reach that value, so nothing below it is in the top K.
@@ -596,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, 4) topk_kernel(const void* __restric
 
 template <bool kBf16, int KW>
 cudaError_t launch_topk_t(const void* logits, int rows, int V, int K, int S, float* vals, int32_t* ids,
-                          cudaStream_t stream) {
+                          cudaStream_t stream, bool after_unrelated) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(S, rows, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -609,8 +610,14 @@ cudaError_t launch_topk_t(const void* logits, int rows, int V, int K, int S, flo
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = S > 1 ? 1 : 0;
-  cfg.numAttrs += pdl_attr(&attr[cfg.numAttrs]);
-  return cudaLaunchKernelEx(&cfg, topk_kernel<kBf16, KW>, logits, V, K, S, vals, ids);
+  if (after_unrelated) {
+    attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+    ++cfg.numAttrs;
+  } else {
+    cfg.numAttrs += pdl_attr(&attr[cfg.numAttrs]);
+  }
+  return cudaLaunchKernelEx(&cfg, topk_kernel<kBf16, KW>, logits, V, K, S, vals, ids, after_unrelated ? 0 : 1);
 }
 
 // Blocks per row: one block per row once there are at least two rows per SM (more blocks per
@@ -633,16 +640,20 @@ int auto_split(int rows, int V, bool bf16) {
 
 }  // namespace
 
+int topk_ctas_per_row(int rows, int V, bool is_bf16, int ctas_per_row) {
+  const int S = ctas_per_row > 0 ? ctas_per_row : auto_split(rows, V, is_bf16);
+  return S < 1 ? 1 : (S > kMaxSplit ? kMaxSplit : S);
+}
+
 cudaError_t launch_topk(const void* logits, bool is_bf16, int rows, int V, int K, int ctas_per_row, float* vals,
-                        int32_t* ids, cudaStream_t stream) {
+                        int32_t* ids, cudaStream_t stream, bool after_unrelated) {
   if (rows > 65535 || K > kMaxK) return cudaErrorInvalidConfiguration;
-  int S = ctas_per_row > 0 ? ctas_per_row : auto_split(rows, V, is_bf16);
-  S = S < 1 ? 1 : (S > kMaxSplit ? kMaxSplit : S);
+  const int S = topk_ctas_per_row(rows, V, is_bf16, ctas_per_row);
   if (is_bf16)
-    return K <= 32 ? launch_topk_t<true, 1>(logits, rows, V, K, S, vals, ids, stream)
-                   : launch_topk_t<true, 2>(logits, rows, V, K, S, vals, ids, stream);
-  return K <= 32 ? launch_topk_t<false, 1>(logits, rows, V, K, S, vals, ids, stream)
-                 : launch_topk_t<false, 2>(logits, rows, V, K, S, vals, ids, stream);
+    return K <= 32 ? launch_topk_t<true, 1>(logits, rows, V, K, S, vals, ids, stream, after_unrelated)
+                   : launch_topk_t<true, 2>(logits, rows, V, K, S, vals, ids, stream, after_unrelated);
+  return K <= 32 ? launch_topk_t<false, 1>(logits, rows, V, K, S, vals, ids, stream, after_unrelated)
+                 : launch_topk_t<false, 2>(logits, rows, V, K, S, vals, ids, stream, after_unrelated);
 }
 
 }  // namespace dcoco
