@@ -429,8 +429,9 @@ int enqueue_repr(const Dims& D, const int32_t* ids, const void* emb, int V, cons
 
 // CTAs of the embedding-row GEMM b = LN(W_e Emb[c]) (the same choices enqueue_repr_gather makes).
 int gather_gemm_ctas(const Dims& D) {
+  const int m_tiles = (D.M() + 127) / 128;
   const int BN = pick_bn(D.r, true);
-  const int m_tiles = (D.M() + 127) / 128, n_tiles = D.r / BN;
+  const int n_tiles = D.r / BN;
   const int nkb = (D.E + (D.bf16 ? 64 : 32) - 1) / (D.bf16 ? 64 : 32);
   return m_tiles * n_tiles * pick_split(m_tiles, n_tiles, nkb, BN, sm_count());
 }
@@ -1031,7 +1032,10 @@ int cycle_impl(const void* logits, const void* W_lm, int V, const void* emb, con
     if (e == cudaSuccess) e = cudaEventRecord(side->join2, side->stream2);
     if (e != cudaSuccess) return cuda_fail(e, "join from helper streams");
   }
-  if (table == nullptr) DCOCO_TRY(enqueue_repr_gather(D, o_ids, emb, V, w, s.repr, st));
+  if (table == nullptr) {
+    PdlScope pdl_gather;  // behind top-K, whose ids it waits for after its prologue
+    DCOCO_TRY(enqueue_repr_gather(D, o_ids, emb, V, w, s.repr, st));
+  }
   e = cudaStreamWaitEvent(st, side->join2, 0);
   if (e != cudaSuccess) return cuda_fail(e, "join from helper streams");
   // From here on each kernel may launch while its predecessor finishes (programmatic

@@ -109,17 +109,16 @@ __device__ __forceinline__ void store_act1(void* out, size_t idx, float v) {
   }
 }
 
-// 32 bytes (two 16-byte halves) from a 32-byte aligned address, not kept in L1.
+// 32 bytes (two 16-byte halves) from a 32-byte aligned address of data no kernel writes while
+// this one runs, not kept in L1; not volatile, so the compiler may schedule the loads freely.
 __device__ __forceinline__ void ld_nc32(const void* p, uint4& a, uint4& b) {
-  asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-               : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
-               : "l"(p));
+  asm("ld.global.nc.L1::no_allocate.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+      : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
+      : "l"(p));
 }
 __device__ __forceinline__ uint4 ld_nc16(const void* p) {
   uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
   return v;
 }
 
@@ -1045,6 +1044,7 @@ cudaError_t launch_zuv_t(const ZuvArgs& a, cudaStream_t stream) {
   cfg.numAttrs = pdl_attr(&attr[0]);
   return cudaLaunchKernelEx(&cfg, zuv_kernel<R>, a);
 }
+
 
 }  // namespace
 
