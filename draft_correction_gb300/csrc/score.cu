@@ -30,7 +30,7 @@ namespace dcoco {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kAB = 8;    // predecessor rows per block
+constexpr int kAB = 4;    // predecessor rows per block (four: about two waves of blocks at the headline shape)
 constexpr int kTA = 2;    // predecessor rows per thread tile
 constexpr int kTB = 4;    // successor rows per thread tile
 constexpr int kHC = 128;  // hidden units per shared-memory chunk (at most)
@@ -427,12 +427,16 @@ cudaError_t configure_once() {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (configured[dev]) return cudaSuccess;
-  const int most = 227 * 1024;
   const void* fns[] = {reinterpret_cast<const void*>(score_kernel<true>), reinterpret_cast<const void*>(score_kernel<false>),
                        reinterpret_cast<const void*>(score_prepped_kernel<true>),
                        reinterpret_cast<const void*>(score_prepped_kernel<false>)};
   for (const void* f : fns) {
-    e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+    cudaFuncAttributes fa{};
+    e = cudaFuncGetAttributes(&fa, f);
+    if (e != cudaSuccess) return e;
+    // the dynamic ceiling plus the kernel's static shared memory stays within 227 KB
+    e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             227 * 1024 - static_cast<int>(fa.sharedSizeBytes));
     if (e != cudaSuccess) return e;
   }
   configured[dev] = true;
@@ -442,7 +446,7 @@ cudaError_t configure_once() {
 
 cudaError_t launch_scores(const ScoreArgs& a, bool is_bf16, cudaStream_t stream) {
   const size_t smem = score_smem_bytes(a.H, a.K, is_bf16);
-  if (smem > 227 * 1024) return cudaErrorInvalidValue;
+  if (smem > 226 * 1024) return cudaErrorInvalidValue;
   const dim3 grid(a.N * (a.B - 1), (a.K + kAB - 1) / kAB);
   cudaError_t e = configure_once();
   if (e != cudaSuccess) return e;
@@ -459,7 +463,7 @@ cudaError_t launch_scores(const ScoreArgs& a, bool is_bf16, cudaStream_t stream)
 
 cudaError_t launch_scores_prepped(const ScoreArgs& a, bool is_bf16, cudaStream_t stream) {
   const size_t smem = score_prepped_smem_bytes(a.H, a.K, is_bf16);
-  if (smem > 227 * 1024) return cudaErrorInvalidValue;
+  if (smem > 226 * 1024) return cudaErrorInvalidValue;
   const dim3 grid(a.N * (a.B - 1), (a.K + kAB - 1) / kAB);
   cudaError_t e = configure_once();
   if (e != cudaSuccess) return e;
