@@ -43,6 +43,7 @@ _SIGNATURES = {
     "dcoco_last_error": ([], ctypes.c_char_p),
     "dcoco_device_status": ([_P, ctypes.POINTER(ctypes.c_uint32)], _I),
     "dcoco_selftest_timeout": ([ctypes.c_uint32, _P], _I),
+    "dcoco_set_helper_streams": ([_P, _P], _I),
     "dcoco_set_topk_split": ([_I], _I),
     "dcoco_topk": ([_P, _I, _I, _I, _I, _I, _P, _P, _P], _I),
     "dcoco_candidate_repr_workspace_size": ([_WP, _I, _I, _I], _Z),
@@ -184,6 +185,13 @@ def device_status() -> int:
 def selftest_timeout(polls: int) -> None:
     """Enqueue one bounded wait that gives up after `polls` polls and reports it in the status word."""
     _check(lib().dcoco_selftest_timeout(int(polls), _stream()))
+
+
+def set_helper_streams(a: Optional[torch.cuda.Stream], b: Optional[torch.cuda.Stream]) -> None:
+    """Caller-owned helper streams for the cycles enqueued by this host thread (None, None: the
+    library's shared per-device streams)."""
+    _check(lib().dcoco_set_helper_streams(ctypes.c_void_p(a.cuda_stream) if a is not None else None,
+                                          ctypes.c_void_p(b.cuda_stream) if b is not None else None))
 
 
 def set_topk_split(ctas_per_row: int) -> int:

@@ -442,6 +442,15 @@ struct SideStream {
   cudaStream_t stream = nullptr, stream2 = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr, join2 = nullptr;
 };
+int make_events(SideStream& s) {
+  cudaError_t e = cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.join2, cudaEventDisableTiming);
+  if (e != cudaSuccess) return cuda_fail(e, "helper event set-up");
+  return DCOCO_OK;
+}
+// Library-owned helper streams (highest priority) and events, one set per device, shared by
+// every host thread: g_side_mu keeps one enqueue sequence at a time on them.
 std::mutex g_side_mu;
 int side_stream(SideStream** out) {
   static SideStream per_dev[64];
@@ -453,11 +462,31 @@ int side_stream(SideStream** out) {
     cudaError_t e = cudaDeviceGetStreamPriorityRange(&lo, &hi);
     if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&s.stream, cudaStreamNonBlocking, hi);
     if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&s.stream2, cudaStreamNonBlocking, hi);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.join2, cudaEventDisableTiming);
     if (e != cudaSuccess) return cuda_fail(e, "helper stream set-up");
+    DCOCO_TRY(make_events(s));
   }
+  *out = &s;
+  return DCOCO_OK;
+}
+// Caller-owned helper streams of this host thread (dcoco_set_helper_streams) and this thread's
+// own fork/join events, one set per device.
+thread_local cudaStream_t t_helper[2] = {nullptr, nullptr};
+struct ThreadEvents {
+  SideStream dev[64];
+  ~ThreadEvents() {
+    for (SideStream& s : dev)
+      for (cudaEvent_t ev : {s.fork, s.join, s.join2})
+        if (ev != nullptr) (void)cudaEventDestroy(ev);
+  }
+};
+thread_local ThreadEvents t_events;
+int caller_side_stream(SideStream** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return fail(DCOCO_ERR_CUDA, "no current CUDA device");
+  SideStream& s = t_events.dev[dev];
+  if (s.fork == nullptr) DCOCO_TRY(make_events(s));
+  s.stream = t_helper[0];
+  s.stream2 = t_helper[1];
   *out = &s;
   return DCOCO_OK;
 }
@@ -604,6 +633,17 @@ extern "C" {
 int dcoco_version(void) { return 100; }
 
 const char* dcoco_last_error(void) { return g_err; }
+
+int dcoco_set_helper_streams(void* helper_a, void* helper_b) {
+  clear_err();
+  if ((helper_a == nullptr) != (helper_b == nullptr))
+    return fail(DCOCO_ERR_INVALID_ARG, "helper streams: pass two streams or two NULLs");
+  if (helper_a != nullptr && helper_a == helper_b)
+    return fail(DCOCO_ERR_INVALID_ARG, "helper streams: the two streams must differ");
+  t_helper[0] = as_stream(helper_a);
+  t_helper[1] = as_stream(helper_b);
+  return DCOCO_OK;
+}
 
 int dcoco_set_topk_split(int ctas_per_row) {
   return g_topk_split.exchange(std::max(0, std::min(8, ctas_per_row)));
@@ -989,9 +1029,16 @@ int cycle_impl(const void* logits, const void* W_lm, int V, const void* emb, con
 
   const int rows = N * B;
   if (W_lm == nullptr) DCOCO_TRY(resolve_readable(logits, "logits", &logits));
-  std::lock_guard<std::mutex> lock(g_side_mu);
+  // the library's shared helper streams are used by one enqueue sequence at a time; a thread's
+  // own helper streams need no lock
+  std::unique_lock<std::mutex> lock(g_side_mu, std::defer_lock);
   SideStream* side = nullptr;
-  DCOCO_TRY(side_stream(&side));
+  if (t_helper[0] != nullptr) {
+    DCOCO_TRY(caller_side_stream(&side));
+  } else {
+    lock.lock();
+    DCOCO_TRY(side_stream(&side));
+  }
   cudaError_t e;
   if (W_lm != nullptr) {
     // The fused LM-head kernel is persistent over every SM: the h-only work forks after it and

@@ -30,7 +30,8 @@ namespace dcoco {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kAB = 4;    // predecessor rows per block (four: about two waves of blocks at the headline shape)
+constexpr int kAB = 8;    // predecessor rows per block of score_kernel
+constexpr int kABP = 4;   // predecessor rows per block of score_prepped_kernel (about two waves at the headline shape)
 constexpr int kTA = 2;    // predecessor rows per thread tile
 constexpr int kTB = 4;    // successor rows per thread tile
 constexpr int kHC = 128;  // hidden units per shared-memory chunk (at most)
@@ -92,18 +93,19 @@ __device__ __forceinline__ float tanh_fast(float x) {
   return y;
 }
 
-// Thread tiles: OT = (kAB/kTA) x (Kp/kTB); HS threads share a tile and split the hidden units.
+// Thread tiles: OT = (AB/kTA) x (Kp/kTB) for AB predecessor rows per block; HS threads share a
+// tile and split the hidden units.
 // Tile (ta, tb) holds predecessor rows ta*kTA + i and successor rows tb + j*tiles_b (strided, so
 // that neighbouring threads read rows in different shared-memory banks).
 struct Tile {
   int tiles_b, OT, HS, hs, ta, tb;
   bool active;
 };
-template <int NT>
+template <int NT, int AB>
 __device__ __forceinline__ Tile make_tile(int Kp) {
   Tile t;
   t.tiles_b = Kp / kTB;
-  t.OT = (kAB / kTA) * t.tiles_b;
+  t.OT = (AB / kTA) * t.tiles_b;
   t.HS = NT / t.OT;  // OT <= 64 (K <= 64), so HS >= NT / 64
   const int ot = threadIdx.x % t.OT;
   t.hs = threadIdx.x / t.OT;
@@ -221,7 +223,7 @@ __global__ void __launch_bounds__(kThreads) score_kernel(const ScoreArgs a) {
   float* Q = P + kAB * (hc + kPad);  // [Kp][ld]
   float* red = Q + Kp * (hc + kPad);  // [kThreads][kTA * kTB] partial sums
   Act* raw = reinterpret_cast<Act*>(red + kThreads * kTA * kTB);  // [rows][hc] next chunk, as stored
-  const Tile t = make_tile<kThreads>(Kp);
+  const Tile t = make_tile<kThreads, kAB>(Kp);
 
   const size_t row_p = (static_cast<size_t>(n) * B + p) * K;      // candidate rows of slot p
   const size_t row_q = (static_cast<size_t>(n) * B + p + 1) * K;  // candidate rows of slot p+1
@@ -324,7 +326,7 @@ template <bool kBf16>
 __host__ __device__ __forceinline__ int prep_chunk(int H, int K) {
   const int esz = kBf16 ? 2 : 4;
   const int Kp = (K + kTB - 1) / kTB * kTB;
-  return (kAB + Kp) * (H * esz + 16) <= kPrepBudget ? H : score_chunk(H);
+  return (kABP + Kp) * (H * esz + 16) <= kPrepBudget ? H : score_chunk(H);
 }
 
 template <bool kBf16>
@@ -335,18 +337,18 @@ __global__ void __launch_bounds__(kPrepThreads, 8) score_prepped_kernel(const Sc
   const int K = a.K, H = a.H, B = a.B;
   const int np = blockIdx.x;  // n * (B-1) + p
   const int n = np / (B - 1), p = np % (B - 1);
-  const int a0 = blockIdx.y * kAB;
-  const int na = min(kAB, K - a0);
+  const int a0 = blockIdx.y * kABP;
+  const int na = min(kABP, K - a0);
   const int Kp = (K + kTB - 1) / kTB * kTB;
   const int hc = prep_chunk<kBf16>(H, K);
   const int ld = hc + 16 / esz;  // row pitch (elements): rows start on 16-byte boundaries
-  const int rows = kAB + Kp;
+  const int rows = kABP + Kp;
   Op* wv = reinterpret_cast<Op*>(sm);  // [H] output weights
-  Op* P = wv + H;                      // [kAB][ld]
-  Op* Q = P + kAB * ld;                // [Kp][ld]
+  Op* P = wv + H;                      // [kABP][ld]
+  Op* Q = P + kABP * ld;                // [Kp][ld]
   // partial sums [kPrepThreads][kTA * kTB], over P/Q once every thread is done with them
   float* red = reinterpret_cast<float*>(P);
-  const Tile t = make_tile<kPrepThreads>(Kp);
+  const Tile t = make_tile<kPrepThreads, kABP>(Kp);
 
   const size_t row_p = (static_cast<size_t>(n) * B + p) * K + a0;  // first predecessor row
   const size_t row_q = (static_cast<size_t>(n) * B + p + 1) * K;   // first successor row
@@ -355,8 +357,8 @@ __global__ void __launch_bounds__(kPrepThreads, 8) score_prepped_kernel(const Sc
   // Rows past na (P) or K (Q) are zero-filled.
   auto fetch = [&](int h0) {
     for (int r = warp; r < rows; r += kPrepThreads / 32) {
-      const bool is_p = r < kAB;
-      const int rr = is_p ? r : r - kAB;
+      const bool is_p = r < kABP;
+      const int rr = is_p ? r : r - kABP;
       const bool live = is_p ? rr < na : rr < K;
       const Op* src = static_cast<const Op*>(is_p ? a.uz : a.vz) +
                       (live ? (is_p ? row_p : row_q) + rr : 0) * static_cast<size_t>(H) + h0;
@@ -413,7 +415,7 @@ size_t score_prepped_smem_bytes(int H, int K, bool is_bf16) {
   const int Kp = (K + kTB - 1) / kTB * kTB;
   // the partial sums reuse the P/Q buffers; the chunk of a small H may leave them shorter
   return static_cast<size_t>(H) * esz +
-         std::max(static_cast<size_t>(kAB + Kp) * (hc * esz + 16),
+         std::max(static_cast<size_t>(kABP + Kp) * (hc * esz + 16),
                   static_cast<size_t>(kPrepThreads) * kTA * kTB * sizeof(float));
 }
 
@@ -464,7 +466,7 @@ cudaError_t launch_scores(const ScoreArgs& a, bool is_bf16, cudaStream_t stream)
 cudaError_t launch_scores_prepped(const ScoreArgs& a, bool is_bf16, cudaStream_t stream) {
   const size_t smem = score_prepped_smem_bytes(a.H, a.K, is_bf16);
   if (smem > 226 * 1024) return cudaErrorInvalidValue;
-  const dim3 grid(a.N * (a.B - 1), (a.K + kAB - 1) / kAB);
+  const dim3 grid(a.N * (a.B - 1), (a.K + kABP - 1) / kABP);
   cudaError_t e = configure_once();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};

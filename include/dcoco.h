@@ -104,6 +104,15 @@ int dcoco_device_status(void* stream, uint32_t* bits);
 int dcoco_selftest_timeout(uint32_t polls, void* stream);
 
 /*
+ * Helper streams of dcoco_cycle, dcoco_cycle_table and dcoco_cycle_lm on the calling host thread:
+ * two distinct caller-owned cudaStream_t of the device the cycles run on (the caller keeps them
+ * alive while cycles use them), or NULL, NULL for the library's shared per-device streams (the
+ * default).  Applies to later calls on this host thread only.  Errors: DCOCO_ERR_INVALID_ARG when
+ * exactly one is NULL or both are the same stream.
+ */
+int dcoco_set_helper_streams(void* helper_a, void* helper_b);
+
+/*
  * Tuning knob: thread blocks per logits row in dcoco_topk (1..8; 0 = automatic).
  * Process-wide; returns the previous value.
  */
@@ -245,11 +254,14 @@ int dcoco_verify_speculative(const int32_t* draft, const float* p, const float* 
  * One whole correction cycle a1..a6: top-K, candidate representation, pair state,
  * transition scores, walk and verification, with intermediates in the workspace.  Inputs as
  * above; `t` (greedy) or `q`,`u` (stochastic) per `mode`.
- * The projections that need only h (pair states and W s; g and its fusion half) run on two
- * library-owned helper streams of the current device (created on the first call, highest
- * priority) that fork from `stream` after top-K and join back into it through events, so they
- * overlap the embedding-row projection; the call can be captured into a CUDA graph after that
- * first call.  Enqueueing is serialised per process by a mutex.
+ * Besides `stream`, the call uses two helper streams for the projections that need only h (g and
+ * its fusion half; the pair states and W s): they fork from `stream` and join back into it through
+ * events, so they overlap top-K.  By default these are two library-owned streams per device
+ * (created on the first call, highest priority), shared by every host thread of the process; a
+ * process-wide lock then serialises enqueueing, and cycles enqueued on different streams queue
+ * behind one another on the helper streams.  dcoco_set_helper_streams gives a host thread its own
+ * pair of helper streams (and its own events), with no lock.  The call can be captured into a CUDA
+ * graph once the helper streams exist (after the first call, or with caller-owned streams).
  * Outputs (any may be NULL except tokens, accept_len, committed, n_commit):
  *   vals, ids [N,B,K]; S [N,B-1,K,K]; k_sel, tokens [N,B]; accept_len, n_commit [N];
  *   committed [N,B+1]; near_tie [N].

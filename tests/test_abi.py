@@ -166,3 +166,10 @@ def test_cycle_lm_argument_errors(L):
 def test_selftest_timeout_argument_errors(L):
     assert L.dcoco_selftest_timeout(0, None) == 1 and b"polls" in L.dcoco_last_error()
     assert L.dcoco_selftest_timeout(65537, None) == 1
+
+
+def test_helper_streams_argument_errors(L):
+    assert L.dcoco_set_helper_streams(FAKE, None) == 1 and b"two" in L.dcoco_last_error()
+    assert L.dcoco_set_helper_streams(None, FAKE) == 1
+    assert L.dcoco_set_helper_streams(FAKE, FAKE) == 1 and b"differ" in L.dcoco_last_error()
+    assert L.dcoco_set_helper_streams(None, None) == 0

@@ -197,3 +197,43 @@ def test_cycle_with_table(cfg, variant):
 
 def test_cycle_with_table_headline():
     run_cycle_and_compare(wl.HEADLINE, use_table=True)
+
+
+def test_cycle_on_caller_helper_streams_from_two_host_threads():
+    """Two host threads, each with its own stream and its own pair of helper streams, enqueue
+    cycles at the same time; each result equals the cycle run alone on the library's streams."""
+    import threading
+    cfg = SMALL_BF16
+    c = case(cfg)
+    w = dc.CorrectorWeights.from_numpy(c["w"], cfg.dtype)
+    emb, lg, h = dc.to_device(c["emb"], cfg.dtype), dc.to_device(c["logits"], cfg.dtype), dc.to_device(c["h"], cfg.dtype)
+    t = dc.to_device(wl.verifier_tokens(cfg, np.zeros((cfg.N, cfg.B), dtype=np.int64)), "i32")
+    want = {k: v.cpu().numpy() for k, v in dc.Cycle(w, cfg.N, cfg.B, cfg.K, cfg.V).run(lg, emb, h, t=t).items()}
+    torch.cuda.synchronize()
+    got, errors = [None, None], []
+
+    def worker(i):
+        try:
+            torch.cuda.set_device(lg.device)
+            s, ha, hb = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+            dc.set_helper_streams(ha, hb)
+            with torch.cuda.stream(s):
+                cyc = dc.Cycle(w, cfg.N, cfg.B, cfg.K, cfg.V)
+                for _ in range(5):
+                    out = cyc.run(lg, emb, h, t=t)
+                s.synchronize()
+                got[i] = {k: v.cpu().numpy() for k, v in out.items()}
+        except Exception as exc:  # reported below
+            errors.append(exc)
+        finally:
+            dc.set_helper_streams(None, None)
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    for g in got:
+        for k, v in want.items():
+            np.testing.assert_array_equal(g[k], v, err_msg=k)
