@@ -7,9 +7,9 @@
 // Kernel shape (one 128-row x BN-column output tile per CTA, 10 warps):
 //   warp 0     TMA producer.  B tiles come from a 2-D tensor map, and so do A tiles of
 //              activations.  For the candidate embeddings the epilogue warps gather the A
-//              rows Emb[c] themselves while the main loop runs (16-byte asynchronous copies
-//              straight into the swizzled operand layout) -- the embedding table is never
-//              copied to a dense matrix.
+//              rows Emb[c] themselves while the main loop runs (32-byte register loads, stored
+//              into the swizzled operand layout) -- the embedding table is never copied to a
+//              dense matrix.
 //   warp 1     allocates tensor memory; lane 0 issues tcgen05.mma (bf16 -> kind::f16,
 //              f32 -> kind::tf32) into an fp32 accumulator of 128 lanes x BN columns and
 //              commits each stage back to the producer.
@@ -17,9 +17,10 @@
 //              (LayerNorm over the full row, SiLU with a per-slot bias, the scorer operands,
 //              or a plain store).  Two warps share each 32-lane quarter of the accumulator
 //              and split its columns; LayerNorm exchanges row partial sums in shared memory.
-// Split-K: with split_k > 1 the CTAs of one tile form a cluster along z, each reduces a
-// K range, stages its partial tile in its shared memory, and each CTA then sums a slice
-// of rows across the cluster in rank order (distributed shared memory) -- deterministic.
+// Split-K: with split_k > 1 the CTAs of one tile form a cluster along z and each reduces a
+// K range.  Each CTA owns a slice of the tile's rows: every CTA writes its partial rows into
+// the owner's shared memory (distributed shared memory stores), and the owner adds them in
+// rank order -- deterministic.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -40,6 +41,7 @@ constexpr int kSmemBudget = 200 * 1024;
 constexpr int kGatherThreads = kEpiThreads;  // epilogue warps that gather the A operand
 constexpr int kGatherDepth = 4;              // k-blocks of gathered rows in flight per thread
 constexpr int kBiasStageBytes = 20 * 1024;  // per-slot bias rows of one tile (SiLU epilogue)
+constexpr int SPLIT_RP = BM + 1;            // split-K buffer: float4 slots per column group
 
 __device__ unsigned int g_status_word;
 
@@ -139,7 +141,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   constexpr int NMMA = BN / NH;
   constexpr uint32_t TMEM_COLS = BN < 32 ? 32 : BN;
   constexpr uint32_t IDESC = mma_idesc(T::fmt, BM, NMMA);
-  constexpr int LDS = BN + 4;                  // staging row pitch (floats), split-K only
 
   extern __shared__ uint8_t dyn_smem[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
@@ -159,6 +160,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     ++gi;
   }
   const GemmGroup& grp = args.g[gi];
+  // The group's scalars in registers: gi is not a compile-time index, so every read through
+  // grp is a generic load from parameter memory, which stores through other pointers force the
+  // compiler to repeat (one memory round trip each).
+  const int g_epi = grp.epi;
+  void* const g_out = grp.out;
+  const int g_ldo = grp.ldo;
+  const void* const g_col_u = grp.col_u;
+  const void* const g_col_b = grp.col_b;
+  const float* const g_row_bias = grp.row_bias;
   const int ks = blockIdx.z;
   const int nkb_total = (args.K + T::BK - 1) / T::BK;
   const int per = (nkb_total + split_k - 1) / split_k;
@@ -273,8 +283,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       // loads kGatherDepth k-blocks ahead with 32-byte non-caching loads, and stores each k-block
       // into the 128-byte swizzled operand layout once its stage is free; a generic-to-async
       // proxy fence and one arrival per thread hand the stage to the tensor core.  (Measured on
-      // this GPU: 32-byte register loads reach about 6.4 TB/s on this gather, 16-byte
-      // asynchronous copies about 3 TB/s at any ring depth.)
+      // this GPU with clean L2 lines: this access pattern alone reads 8192 random 8 KB rows at
+      // 3.4 to 4 TB/s, whole rows per warp at about 4.2 TB/s; TMA bulk copies of 128 or 512
+      // bytes per row are issue-bound near 0.6 and 2 TB/s.)
       const int t = threadIdx.x - 64;
       const int pc = t & 3;                    // 32-byte piece of the 128-byte row
       const int rA = t >> 2, rB = 64 + (t >> 2);
@@ -344,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     // While the main loop runs, stage this tile's per-slot bias rows in shared memory.
     const float* sbias = nullptr;
     int first_slot = 0, prep_nslots = 0;
-    if (grp.epi == EPI_SILU_BIAS) {
+    if (g_epi == EPI_SILU_BIAS) {
       first_slot = (m_tile * BM) / args.bias_div;
       const int last_slot = (min(args.M, m_tile * BM + BM) - 1) / args.bias_div;
       const int nslots = last_slot - first_slot + 1;
@@ -358,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         sbias = dst;
       }
       named_barrier_sync(1, kEpiThreads);
-    } else if (grp.epi == EPI_PREP) {
+    } else if (g_epi == EPI_PREP) {
       // Rows 0..nslots-1: (col_b + the slot's pair-bias row) / 2; row nslots: col_u / 2.
       first_slot = (m_tile * BM) / args.bias_div;
       const int last_slot = (min(args.M, m_tile * BM + BM) - 1) / args.bias_div;
@@ -370,13 +381,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           const int col = nt * BN + c4 * 4;
           float4 v;
           if (sl == nslots) {
-            v = ldw4<kBf16>(grp.col_u, col);
+            v = ldw4<kBf16>(g_col_u, col);
           } else {
-            v = grp.col_b != nullptr ? ldw4<kBf16>(grp.col_b, col) : make_float4(0.f, 0.f, 0.f, 0.f);
+            v = g_col_b != nullptr ? ldw4<kBf16>(g_col_b, col) : make_float4(0.f, 0.f, 0.f, 0.f);
             const int qs = first_slot + sl, stream_i = qs / args.slots;
-            if (grp.row_bias != nullptr && qs - stream_i * args.slots < args.slots - 1) {
+            if (g_row_bias != nullptr && qs - stream_i * args.slots < args.slots - 1) {
               const float4 rb = *reinterpret_cast<const float4*>(
-                  grp.row_bias + static_cast<size_t>(qs - stream_i) * args.ld_bias + col);
+                  g_row_bias + static_cast<size_t>(qs - stream_i) * args.ld_bias + col);
               v.x += rb.x;
               v.y += rb.y;
               v.z += rb.z;
@@ -397,14 +408,38 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     tc_fence_after();
     const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16);
     if constexpr (kSplit) {
-      float* stg = reinterpret_cast<float*>(smem);
+      // Every CTA of the cluster is past its main loop, so its pipeline buffers are free, before
+      // any partial row is written into them.  Row rr of the slice owned by rank o receives this
+      // CTA's partial at slot row (rank * rpc + rr) of o's buffer: stores only, no round trips.
+      // The buffer is column-group major (four columns of every slot row, then the next four),
+      // so the 32 lanes of a warp (32 consecutive rows) store 512 contiguous bytes.
+      cluster_arrive();
+      cluster_wait();
+      const int rank = static_cast<int>(cluster_rank());  // the cluster spans grid.z
+      const int rpc = BM / split_k;
+      const int owner = row_local / rpc;
+      const uint32_t dst = map_to_rank(smem_u32(smem), static_cast<uint32_t>(owner)) +
+                           static_cast<uint32_t>(rank * rpc + row_local - owner * rpc) * 16u;
       constexpr int SH = BN >= 64 ? 2 : 1;  // warps per quarter sharing the columns
-      for (int c = half * BN / SH; half < SH && c < (half + 1) * BN / SH; c += 32) {
-        float v[32];
-        tmem_ld32(trow + c, v);
+      constexpr int CW = BN / SH;           // columns per warp
+      if (half < SH) {
+#pragma unroll 1
+        for (int c = half * CW; c < (half + 1) * CW; c += 64) {
+          uint32_t v[2][32];
+          const int n2 = c + 32 < (half + 1) * CW ? 2 : 1;  // two 32-column loads in flight
+          tmem_ld32_nowait(trow + c, v[0]);
+          if (n2 == 2) tmem_ld32_nowait(trow + c + 32, v[1]);
+          tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; i += 4)
-          *reinterpret_cast<float4*>(&stg[row_local * LDS + c + i]) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+          for (int u = 0; u < 2; ++u) {
+            if (u >= n2) break;
+#pragma unroll
+            for (int i = 0; i < 32; i += 4)
+              st_cluster_f32x4(dst + static_cast<uint32_t>((c + 32 * u + i) >> 2) * (SPLIT_RP * 16u),
+                               __uint_as_float(v[u][i]), __uint_as_float(v[u][i + 1]), __uint_as_float(v[u][i + 2]),
+                               __uint_as_float(v[u][i + 3]));
+          }
+        }
       }
     } else {
       // Row-per-thread values go through a swizzled staging buffer per warp (two 32 x 128-byte
@@ -412,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       // write whole rows coalesced and clip rows past M.  Every epilogue warp runs this block,
       // even after a timed-out wait (then nothing is stored), so the named barriers always
       // see all of them.
-      const bool out_bf16 = kBf16 && grp.epi != EPI_F32;
+      const bool out_bf16 = kBf16 && g_epi != EPI_F32;
       const int cps = out_bf16 ? 64 : 32;  // output columns per 128-byte sub-tile
       const int nsub = BN / cps;           // 128-byte sub-tiles in the tile's columns
       const int halves = nsub >= 2 ? 2 : 1;
@@ -421,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       const int y0 = m_tile * BM + q * 32;
       const bool any_rows = y0 < args.M;
       float mean = 0.f, rstd = 1.f;
-      if (grp.epi == EPI_LN) {
+      if (g_epi == EPI_LN) {
         // Two-pass row statistics over the full row: each warp sums its columns, the two
         // warps of a quarter exchange their partial sums.
         const int c0 = half < halves ? j0 * cps : 0, c1 = half < halves ? j1 * cps : 0;
@@ -454,23 +489,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         rstd = rsqrtf(ss / BN + args.ln_eps);
       }
       const float* bias = nullptr;
-      if (grp.epi == EPI_SILU_BIAS && live) {
+      if (g_epi == EPI_SILU_BIAS && live) {
         bias = sbias != nullptr ? sbias + (m / args.bias_div - first_slot) * BN
                                 : args.bias + static_cast<size_t>(m / args.bias_div) * args.ld_bias + nt * BN;
       }
       // EPI_PREP: this row's scale and pair-bias row
       float row_l = 0.f;
       const float* rbias = nullptr;
-      if (grp.epi == EPI_PREP && live) {
+      if (g_epi == EPI_PREP && live) {
         row_l = args.row_l[m];
         const int q_slot = m / args.bias_div;  // stream * slots + slot
         const int stream_i = q_slot / args.slots, slot = q_slot - stream_i * args.slots;
-        if (grp.row_bias != nullptr && slot < args.slots - 1)
-          rbias = grp.row_bias + static_cast<size_t>(q_slot - stream_i) * args.ld_bias + nt * BN;
+        if (g_row_bias != nullptr && slot < args.slots - 1)
+          rbias = g_row_bias + static_cast<size_t>(q_slot - stream_i) * args.ld_bias + nt * BN;
       }
       // The fused op on 32 consecutive columns starting at `col` (compile-time trip counts).
       auto apply32 = [&](float(&x)[32], int col) {
-        if (grp.epi == EPI_LN) {
+        if (g_epi == EPI_LN) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) x[i] = (x[i] - mean) * rstd;
         } else if (bias != nullptr) {
@@ -482,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             x[i + 2] = silu(x[i + 2] + bb.z);
             x[i + 3] = silu(x[i + 3] + bb.w);
           }
-        } else if (grp.epi == EPI_PREP && sbias != nullptr) {
+        } else if (g_epi == EPI_PREP && sbias != nullptr) {
           const float* add = sbias + (m / args.bias_div - first_slot) * BN + col;
           const float* uu = sbias + prep_nslots * BN + col;
 #pragma unroll
@@ -494,12 +529,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             x[i + 2] = fmaf(0.5f, x[i + 2], fmaf(u4.z, row_l, a4.z));
             x[i + 3] = fmaf(0.5f, x[i + 3], fmaf(u4.w, row_l, a4.w));
           }
-        } else if (grp.epi == EPI_PREP) {
+        } else if (g_epi == EPI_PREP) {
           const int c0 = nt * BN + col;
 #pragma unroll
           for (int i = 0; i < 32; i += 4) {
-            const float4 uu = ldw4<kBf16>(grp.col_u, c0 + i);
-            float4 add = grp.col_b != nullptr ? ldw4<kBf16>(grp.col_b, c0 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 uu = ldw4<kBf16>(g_col_u, c0 + i);
+            float4 add = g_col_b != nullptr ? ldw4<kBf16>(g_col_b, c0 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
             if (rbias != nullptr) {
               const float4 rb = *reinterpret_cast<const float4*>(rbias + col + i);
               add.x += rb.x;
@@ -529,7 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           if (lane == 0) bulk_wait_read<1>();  // the store that used this half has read it
           __syncwarp();
         }
-        if (grp.epi == EPI_PREP && kBf16)
+        if (g_epi == EPI_PREP && kBf16)
           stage_row<2>(buf, lane, v);
         else if (out_bf16)
           stage_row<1>(buf, lane, v);
@@ -547,88 +582,90 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   }
 
   if constexpr (kSplit) {
-    // Partial tiles are staged; reduce a slice of rows per CTA across the cluster.
+    // The producer and MMA warps take the first cluster barrier of the epilogue warps here; the
+    // second one makes every pushed partial row visible to its owner.
+    if (warp < 2) {
+      cluster_arrive();
+      cluster_wait();
+    }
     tc_fence_before();
     cluster_sync();
-    // Phase A: this CTA owns rows [rank*rpc, (rank+1)*rpc) of the tile.  Every thread sums
-    // float4 column chunks of those rows over the cluster's partial tiles (rank order, so
-    // the result is deterministic) into a local buffer behind the staging area.
-    const int rank = static_cast<int>(cluster_rank());  // the cluster spans grid.z
+    const int rank = static_cast<int>(cluster_rank());
     const int rpc = BM / split_k;
-    float* red = reinterpret_cast<float*>(smem) + BM * LDS;
-    const uint32_t stg0 = smem_u32(smem);
-    constexpr int C4 = BN / 4;
-    const int items = rpc * C4;
-    for (int it0 = threadIdx.x; it0 < items; it0 += 4 * kThreads) {
-      float4 acc[4];
-      uint32_t off[4];
+    // partial rows, column-group major: column c of slot row sr at ((c / 4) * SPLIT_RP + sr) * 4 + c % 4
+    const float* red = reinterpret_cast<const float*>(smem);
+    // One warp per owned row, two rows at a time so that their loads and reductions overlap:
+    // the partials are added in rank order (deterministic).
+    constexpr int NW = kThreads / 32;
+    constexpr int NJ = (BN + 31) / 32;
+    for (int rr0 = warp; rr0 < rpc; rr0 += 2 * NW) {
+      float v[2][NJ];
+      int mm[2];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-        const int it = it0 + q * kThreads;
-        const int rr = it / C4, c4 = it % C4;
-        off[q] = static_cast<uint32_t>(((rank * rpc + rr) * LDS + c4 * 4) * 4);
-      }
-      for (int src = 0; src < split_k; ++src) {
-        const uint32_t rb = map_to_rank(stg0, src);
+      for (int u = 0; u < 2; ++u) {
+        const int rr = rr0 + u * NW;
+        mm[u] = rr < rpc ? m_tile * BM + rank * rpc + rr : args.M;  // args.M: nothing to write
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          if (it0 + q * kThreads < items) {
-            const float4 x = ld_cluster_f32x4(rb + off[q]);
-            acc[q].x += x.x;
-            acc[q].y += x.y;
-            acc[q].z += x.z;
-            acc[q].w += x.w;
+        for (int j = 0; j < NJ; ++j) v[u][j] = 0.f;
+        if (rr >= rpc) continue;
+        for (int src = 0; src < split_k; ++src) {
+          const float* part = red + (src * rpc + rr) * 4;
+#pragma unroll
+          for (int j = 0; j < NJ; ++j) {
+            const int c = lane + 32 * j;  // lanes read 32 different banks (SPLIT_RP * 4 = 4 mod 32)
+            if (c < BN) v[u][j] += part[(c >> 2) * (SPLIT_RP * 4) + (c & 3)];
           }
         }
       }
+      if (g_epi == EPI_LN) {
+        float mean[2], rstd[2];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int it = it0 + q * kThreads;
-        if (it < items) *reinterpret_cast<float4*>(&red[(it / C4) * LDS + (it % C4) * 4]) = acc[q];
-      }
-    }
-    __syncthreads();
-    // Phase B: one warp per row from local shared memory, all six warps.
-    for (int rr = warp; rr < rpc; rr += kThreads / 32) {
-      const int m = m_tile * BM + rank * rpc + rr;
-      if (m >= args.M) continue;
-      constexpr int NJ = (BN + 31) / 32;
-      float v[NJ];
+        for (int u = 0; u < 2; ++u) {
+          float sum = 0.f;
 #pragma unroll
-      for (int j = 0; j < NJ; ++j) v[j] = (lane + 32 * j < BN) ? red[rr * LDS + lane + 32 * j] : 0.f;
-      const size_t obase = static_cast<size_t>(m) * grp.ldo + static_cast<size_t>(nt) * BN;
-      if (grp.epi == EPI_LN) {
-        float sum = 0.f;
+          for (int j = 0; j < NJ; ++j) sum += v[u][j];
+          mean[u] = warp_sum(sum) / BN;
+        }
 #pragma unroll
-        for (int j = 0; j < NJ; ++j) sum += v[j];
-        const float mean = warp_sum(sum) / BN;
-        float ss = 0.f;
+        for (int u = 0; u < 2; ++u) {
+          float ss = 0.f;
 #pragma unroll
-        for (int j = 0; j < NJ; ++j)
-          if (lane + 32 * j < BN) ss += (v[j] - mean) * (v[j] - mean);
-        const float rstd = rsqrtf(warp_sum(ss) / BN + args.ln_eps);
+          for (int j = 0; j < NJ; ++j)
+            if (lane + 32 * j < BN) ss += (v[u][j] - mean[u]) * (v[u][j] - mean[u]);
+          rstd[u] = rsqrtf(warp_sum(ss) / BN + args.ln_eps);
+        }
 #pragma unroll
-        for (int j = 0; j < NJ; ++j)
-          if (lane + 32 * j < BN) store_act1<kBf16>(grp.out, obase + lane + 32 * j, (v[j] - mean) * rstd);
-      } else if (grp.epi == EPI_F32) {
+        for (int u = 0; u < 2; ++u)
 #pragma unroll
-        for (int j = 0; j < NJ; ++j)
-          if (lane + 32 * j < BN) static_cast<float*>(grp.out)[obase + lane + 32 * j] = v[j];
+          for (int j = 0; j < NJ; ++j)
+            if (mm[u] < args.M && lane + 32 * j < BN)
+              store_act1<kBf16>(g_out, static_cast<size_t>(mm[u]) * g_ldo + static_cast<size_t>(nt) * BN + lane + 32 * j,
+                                (v[u][j] - mean[u]) * rstd[u]);
       } else {
-        const float* bias = (grp.epi == EPI_SILU_BIAS)
-                                ? args.bias + static_cast<size_t>(m / args.bias_div) * args.ld_bias + nt * BN
-                                : nullptr;
 #pragma unroll
-        for (int j = 0; j < NJ; ++j) {
-          if (lane + 32 * j >= BN) continue;
-          float x = v[j];
-          if (bias != nullptr) x = silu(x + bias[lane + 32 * j]);
-          store_act1<kBf16>(grp.out, obase + lane + 32 * j, x);
+        for (int u = 0; u < 2; ++u) {
+          const int m = mm[u];
+          if (m >= args.M) continue;
+          const size_t obase = static_cast<size_t>(m) * g_ldo + static_cast<size_t>(nt) * BN;
+          if (g_epi == EPI_F32) {
+#pragma unroll
+            for (int j = 0; j < NJ; ++j)
+              if (lane + 32 * j < BN) static_cast<float*>(g_out)[obase + lane + 32 * j] = v[u][j];
+          } else {
+            const float* bias = (g_epi == EPI_SILU_BIAS)
+                                    ? args.bias + static_cast<size_t>(m / args.bias_div) * args.ld_bias + nt * BN
+                                    : nullptr;
+#pragma unroll
+            for (int j = 0; j < NJ; ++j) {
+              if (lane + 32 * j >= BN) continue;
+              float x = v[u][j];
+              if (bias != nullptr) x = silu(x + bias[lane + 32 * j]);
+              store_act1<kBf16>(g_out, obase + lane + 32 * j, x);
+            }
+          }
         }
       }
     }
-    cluster_sync();
   }
 
   tc_fence_before();
@@ -651,8 +688,9 @@ cudaError_t launch_gemm_t(const GemmArgs& args, int split_k, cudaStream_t stream
   if (kSplit && any_group([](int epi) { return epi == EPI_PREP; })) return cudaErrorInvalidValue;
   constexpr int STAGE_BYTES = BM * 128 + BN * 128;
   int stages = std::min(kMaxStages, kSmemBudget / STAGE_BYTES);
-  // split-K reuses the pipeline buffers: partial tile (BM x LDS) plus this CTA's reduced rows
-  const int split_bytes = kSplit ? (BM + BM / 2) * (BN + 4) * 4 : 0;
+  // split-K reuses the pipeline buffers for the partial rows it receives (BN / 4 column groups
+  // of SPLIT_RP float4 slots)
+  const int split_bytes = kSplit ? (BN / 4) * SPLIT_RP * 16 : 0;
   auto staged = [](int epi) { return epi == EPI_SILU_BIAS || epi == EPI_PREP; };
   const bool has_bias = any_group(staged);
   if (has_bias) stages = std::min(stages, 4);
@@ -725,13 +763,16 @@ __global__ void pair_combine_kernel(const float* __restrict__ hp, void* __restri
 //   phase 1  acc1 = b W_f[:, 0:r]^T in TMEM (b tile loaded once by TMA, W_f k-blocks through a
 //            two-stage ring); the epilogue warps write z = SiLU(acc1 + gw[slot]) in bf16 over the
 //            b tile, in the 128-byte swizzled operand layout, and hand it to the MMA warp;
-//   phase 2  acc2 = z U^T (grid.y = 0) or z V^T (grid.y = 1), the weight k-blocks through the
-//            same ring; the epilogue adds the logit term (and for P the bias and W s_p), halves,
-//            and stores f16 rows with tensor-map stores.
+//   phase 2  acc2 = z U^T (grid.y = 0) or z V^T (grid.y = 1), one block of at most 256 output
+//            columns after the other, their weight k-blocks through the same ring; the epilogue
+//            of a column block (the logit term, for P the bias and W s_p, the halving, f16 rows
+//            by tensor-map stores) runs while the MMAs of the next block do.
+// The ring's four 32 KB stages take every W_f k-block before the kernel waits for its
+// predecessors, and the first U or V k-blocks while phase 1 runs.
 // z never leaves shared memory.  Warp roles as in gemm_kernel: 0 TMA producer, 1 MMA issuer,
 // 2-9 epilogue (two per TMEM lane quarter, each with half of the columns).
-constexpr int kZuvRing = 2;
-constexpr int kZuvStage = 512 * 128;  // one k-block of up to 512 weight rows
+constexpr int kZuvRing = 4;
+constexpr int kZuvStage = 256 * 128;  // one k-block of up to 256 weight rows
 constexpr int kZuvConst = 32 * 1024;  // per-tile constants of the epilogues
 
 // tanh of two values in packed half precision (one SFU instruction for both).
@@ -740,6 +781,25 @@ __device__ __forceinline__ float2 tanh2_f16(float a, float b) {
   uint32_t t;
   asm("tanh.approx.f16x2 %0, %1;" : "=r"(t) : "r"(*reinterpret_cast<const uint32_t*>(&x)));
   return __half22float2(*reinterpret_cast<const __half2*>(&t));
+}
+
+// Eight values in half precision, clamped to +-30000 so that a sum of two stays finite.
+__device__ __forceinline__ uint4 pack8_f16_clamped(const float* v) {
+  uint32_t w[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const __half2 t = __floats2half2_rn(fminf(fmaxf(v[2 * e], -30000.f), 30000.f),
+                                        fminf(fmaxf(v[2 * e + 1], -30000.f), 30000.f));
+    w[e] = *reinterpret_cast<const uint32_t*>(&t);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// One 32-byte store to a 32-byte aligned global address.
+__device__ __forceinline__ void st_global_32(void* p, const uint4& a, const uint4& b) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a.x), "r"(a.y), "r"(a.z),
+               "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+               : "memory");
 }
 
 __device__ __forceinline__ uint4 pack8_bf16(const float* v) {
@@ -762,7 +822,8 @@ __global__ void __launch_bounds__(kThreads, 1) zuv_kernel(const __grid_constant_
   uint8_t* ring = smem + NK * A_KB;  // kZuvRing x kZuvStage
   __shared__ __align__(8) uint64_t full_bar[kZuvRing];
   __shared__ __align__(8) uint64_t empty_bar[kZuvRing];
-  __shared__ __align__(8) uint64_t a_bar, acc1_bar, z_bar, acc2_bar;
+  __shared__ __align__(8) uint64_t a_bar, acc1_bar, z_bar;
+  __shared__ __align__(8) uint64_t acc2_bar[2];  // one per phase-2 column block
   __shared__ uint32_t tmem_base_s;
 
   const int warp = threadIdx.x >> 5;
@@ -770,10 +831,12 @@ __global__ void __launch_bounds__(kThreads, 1) zuv_kernel(const __grid_constant_
   const int m_tile = blockIdx.x;
   const bool is_q = blockIdx.y != 0;
   const int H = args.H;
-  const int NC = H <= 256 ? H : 256;  // columns per phase-2 MMA
+  const int NC = H <= 256 ? H : 256;  // columns per phase-2 MMA (and per column block)
+  const int NH2 = H / NC;              // phase-2 column blocks (1 or 2)
   const uint32_t idesc2 = mma_idesc(1u, BM, static_cast<uint32_t>(NC));
   const CUtensorMap* w2_map = is_q ? &args.v_map : &args.u_map;
-  constexpr int total = 2 * NK;  // ring loads: NK k-blocks of W_f, then NK of U or V
+  // ring loads: NK k-blocks of W_f, then NK k-blocks of U or V per column block
+  const int total = NK + NH2 * NK;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kZuvRing; ++s) {
@@ -783,12 +846,12 @@ __global__ void __launch_bounds__(kThreads, 1) zuv_kernel(const __grid_constant_
     mbar_init(smem_u32(&a_bar), 1);
     mbar_init(smem_u32(&acc1_bar), 1);
     mbar_init(smem_u32(&z_bar), 1);
-    mbar_init(smem_u32(&acc2_bar), 1);
+    mbar_init(smem_u32(&acc2_bar[0]), 1);
+    mbar_init(smem_u32(&acc2_bar[1]), 1);
     fence_mbar_init();
     prefetch_tmap(&args.b_map);
     prefetch_tmap(&args.wf_map);
     prefetch_tmap(w2_map);
-    prefetch_tmap(is_q ? &args.q_map : &args.p_map);
   }
   if (warp == 1) tmem_alloc(smem_u32(&tmem_base_s), 512);
   tc_fence_before();
@@ -808,8 +871,9 @@ __global__ void __launch_bounds__(kThreads, 1) zuv_kernel(const __grid_constant_
           mbar_expect_tx(fb, R * 128);
           tma_load_2d(dst, &args.wf_map, i * 64, 0, fb);
         } else {
-          mbar_expect_tx(fb, H * 128);
-          for (int h0 = 0; h0 < H; h0 += NC) tma_load_2d(dst + h0 * 128, w2_map, (i - NK) * 64, h0, fb);
+          const int j = i - NK, cb = j / NK, kb = j - cb * NK;
+          mbar_expect_tx(fb, NC * 128);
+          tma_load_2d(dst, w2_map, kb * 64, cb * NC, fb);
         }
       };
       // the weight tiles do not depend on the preceding kernels: request them first
@@ -851,21 +915,21 @@ __global__ void __launch_bounds__(kThreads, 1) zuv_kernel(const __grid_constant_
         }
         tc_fence_after();
         const uint32_t b_s = ring0 + s * kZuvStage;
-        const int kb = i < NK ? i : i - NK;
+        const int cb = i < NK ? 0 : (i - NK) / NK;  // phase-2 column block
+        const int kb = i < NK ? i : i - NK - cb * NK;
         const uint32_t a_s = a0 + kb * A_KB;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const uint64_t ad = sw128_desc(a_s + j * 32);
           const uint32_t acc = (kb > 0 || j > 0) ? 1u : 0u;
-          if (i < NK) {
+          if (i < NK)
             tc_mma<false>(tmem, ad, sw128_desc(b_s + j * 32), IDESC1, acc);
-          } else {
-            for (int c = 0; c < H; c += NC) tc_mma<false>(tmem + c, ad, sw128_desc(b_s + c * 128 + j * 32), idesc2, acc);
-          }
+          else
+            tc_mma<false>(tmem + cb * NC, ad, sw128_desc(b_s + j * 32), idesc2, acc);
         }
         tc_commit(smem_u32(&empty_bar[s]));
+        if (i >= NK && kb == NK - 1) tc_commit(smem_u32(&acc2_bar[cb]));  // this column block is done
       }
-      if (ok) tc_commit(smem_u32(&acc2_bar));
     }
     __syncwarp();
   } else {
@@ -923,10 +987,19 @@ __global__ void __launch_bounds__(kThreads, 1) zuv_kernel(const __grid_constant_
     if (!ok && lane == 0) atomicOr(args.status, DEV_TIMEOUT_ACC);
     tc_fence_after();
     const float* gwr = staged ? s_gw + (slot - first_slot) * R : args.gw + static_cast<size_t>(slot) * R;
-#pragma unroll 1
-    for (int c = half * (R / 2); c < (half + 1) * (R / 2); c += 32) {
+    // 32-column chunks of this warp's half of the row; the next chunk's TMEM load is in flight
+    // while the current one is converted.
+    constexpr int NCH = R / 64;  // chunks per warp
+    uint32_t rbuf[2][32];
+    tmem_ld32_nowait(trow + half * (R / 2), rbuf[0]);
+#pragma unroll
+    for (int k = 0; k < NCH; ++k) {
+      const int c = half * (R / 2) + 32 * k;
+      tmem_ld_wait();
+      if (k + 1 < NCH) tmem_ld32_nowait(trow + c + 32, rbuf[(k + 1) & 1]);
       float v[32];
-      tmem_ld32(trow + c, v);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(rbuf[k & 1][i]);
 #pragma unroll
       for (int i = 0; i < 32; i += 4) {
         const float4 g4 = *reinterpret_cast<const float4*>(gwr + c + i);
@@ -948,70 +1021,83 @@ __global__ void __launch_bounds__(kThreads, 1) zuv_kernel(const __grid_constant_
     tc_fence_before();
     named_barrier_sync(1, kEpiThreads);
     if (threadIdx.x == 64) mbar_arrive(smem_u32(&z_bar));
-    // phase 2: P or Q
-    ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&acc2_bar), 0));
-    if (!ok && lane == 0) atomicOr(args.status, DEV_TIMEOUT_ACC);
-    grid_dep_launch();  // main loops done: the next kernel may start its prologue
-    tc_fence_after();
+    // phase 2: P or Q, one column block at a time.  Each thread owns one row and stores its
+    // f16 values straight to global memory, 32 bytes per store (16 when the output is only
+    // 16-byte aligned): the ring still feeds the next block's MMAs, so nothing is staged.
     const float l = live ? args.vals[m] : 0.f;
     const int stream_i = slot / args.slots, p = slot - stream_i * args.slots;
     const float* rb = (!is_q && live && p < args.slots - 1) ? args.wsp + static_cast<size_t>(slot - stream_i) * H
                                                             : nullptr;
     const float* addr = s_add + (slot - first_slot) * H;
-    const int nsub = H / 64;  // 128-byte (64-column f16) sub-tiles of the row
+    const int nsub = NC / 64;  // 128-byte (64-column f16) sub-tiles of a column block
     const int halves = nsub >= 2 ? 2 : 1;
-    const int j0 = half * nsub / halves, j1 = (half + 1) * nsub / halves;
-    uint8_t* stg = ring + (warp - 2) * 8192;  // the ring is drained: every MMA has completed
-    const int y0 = m_tile * BM + q * 32;
-    const CUtensorMap* out_map = is_q ? &args.q_map : &args.p_map;
-    for (int j = j0; half < halves && j < j1; ++j) {
-      float v[64];
-      tmem_ld32(trow + j * 64, *reinterpret_cast<float(*)[32]>(v));
-      tmem_ld32(trow + j * 64 + 32, *reinterpret_cast<float(*)[32]>(v + 32));
-      if (staged) {
+    __half* out_row = static_cast<__half*>(is_q ? args.q : args.p) + static_cast<size_t>(live ? m : 0) * H;
+    const bool wide = ((reinterpret_cast<uintptr_t>(is_q ? args.q : args.p) | static_cast<uintptr_t>(H) * 2) & 31) == 0;
+    for (int cb = 0; cb < NH2; ++cb) {
+      const bool got = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&acc2_bar[cb]), 0));
+      if (!got && lane == 0) atomicOr(args.status, DEV_TIMEOUT_ACC);
+      ok = ok && got;
+      if (cb == 0) grid_dep_launch();  // the next kernel may start its prologue
+      tc_fence_after();
+      const int j0 = cb * nsub + half * nsub / halves, j1 = cb * nsub + (half + 1) * nsub / halves;
+      for (int j = j0; half < halves && j < j1; ++j) {
+        float v[64];
+        {
+          uint32_t r[2][32];
+          tmem_ld32_nowait(trow + j * 64, r[0]);
+          tmem_ld32_nowait(trow + j * 64 + 32, r[1]);
+          tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 64; i += 4) {
-          const int col = j * 64 + i;
-          const float4 u4 = *reinterpret_cast<const float4*>(s_u + col);
-          const float4 a4 = *reinterpret_cast<const float4*>(addr + col);
-          v[i] = fmaf(0.5f, v[i], fmaf(u4.x, l, a4.x));
-          v[i + 1] = fmaf(0.5f, v[i + 1], fmaf(u4.y, l, a4.y));
-          v[i + 2] = fmaf(0.5f, v[i + 2], fmaf(u4.z, l, a4.z));
-          v[i + 3] = fmaf(0.5f, v[i + 3], fmaf(u4.w, l, a4.w));
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 64; i += 4) {
-          const int col = j * 64 + i;
-          const float4 u4 = ldw4<true>(col_u, col);
-          float4 add = (!is_q) ? ldw4<true>(args.b1, col) : make_float4(0.f, 0.f, 0.f, 0.f);
-          if (rb != nullptr) {
-            const float4 r4 = *reinterpret_cast<const float4*>(rb + col);
-            add.x += r4.x;
-            add.y += r4.y;
-            add.z += r4.z;
-            add.w += r4.w;
+          for (int i = 0; i < 32; ++i) {
+            v[i] = __uint_as_float(r[0][i]);
+            v[32 + i] = __uint_as_float(r[1][i]);
           }
-          v[i] = 0.5f * (v[i] + add.x + u4.x * l);
-          v[i + 1] = 0.5f * (v[i + 1] + add.y + u4.y * l);
-          v[i + 2] = 0.5f * (v[i + 2] + add.z + u4.z * l);
-          v[i + 3] = 0.5f * (v[i + 3] + add.w + u4.w * l);
         }
-      }
-      uint8_t* buf = stg + ((j - j0) & 1) * 4096;
-      if (j - j0 >= 2) {
-        if (lane == 0) bulk_wait_read<1>();  // the store that used this half has read it
-        __syncwarp();
-      }
-      stage_row<2>(buf, lane, v);
-      fence_proxy_async();
-      __syncwarp();
-      if (lane == 0 && y0 < args.M && ok) {
-        tma_store_2d(out_map, j * 64, y0, smem_u32(buf));
-        bulk_commit();
+        if (staged) {
+#pragma unroll
+          for (int i = 0; i < 64; i += 4) {
+            const int col = j * 64 + i;
+            const float4 u4 = *reinterpret_cast<const float4*>(s_u + col);
+            const float4 a4 = *reinterpret_cast<const float4*>(addr + col);
+            v[i] = fmaf(0.5f, v[i], fmaf(u4.x, l, a4.x));
+            v[i + 1] = fmaf(0.5f, v[i + 1], fmaf(u4.y, l, a4.y));
+            v[i + 2] = fmaf(0.5f, v[i + 2], fmaf(u4.z, l, a4.z));
+            v[i + 3] = fmaf(0.5f, v[i + 3], fmaf(u4.w, l, a4.w));
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 64; i += 4) {
+            const int col = j * 64 + i;
+            const float4 u4 = ldw4<true>(col_u, col);
+            float4 add = (!is_q) ? ldw4<true>(args.b1, col) : make_float4(0.f, 0.f, 0.f, 0.f);
+            if (rb != nullptr) {
+              const float4 r4 = *reinterpret_cast<const float4*>(rb + col);
+              add.x += r4.x;
+              add.y += r4.y;
+              add.z += r4.z;
+              add.w += r4.w;
+            }
+            v[i] = 0.5f * (v[i] + add.x + u4.x * l);
+            v[i + 1] = 0.5f * (v[i + 1] + add.y + u4.y * l);
+            v[i + 2] = 0.5f * (v[i + 2] + add.z + u4.z * l);
+            v[i + 3] = 0.5f * (v[i + 3] + add.w + u4.w * l);
+          }
+        }
+        if (live && ok) {
+          uint4 h[8];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) h[c] = pack8_f16_clamped(v + 8 * c);
+          __half* dst = out_row + j * 64;
+          if (wide) {
+#pragma unroll
+            for (int c = 0; c < 8; c += 2) st_global_32(dst + 8 * c, h[c], h[c + 1]);
+          } else {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(dst + 8 * c) = h[c];
+          }
+        }
       }
     }
-    if (lane == 0) bulk_wait<0>();
   }
   tc_fence_before();
   __syncthreads();

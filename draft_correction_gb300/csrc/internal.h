@@ -116,8 +116,8 @@ struct ZuvArgs {
   CUtensorMap wf_map;  // W_f [r, 2r] (its first r columns act on b), box {64, r}
   CUtensorMap u_map;   // U [H, r], box {64, min(H, 256)}
   CUtensorMap v_map;   // V [H, r], same box
-  CUtensorMap p_map;   // P [M, H] f16, box {64, 32}
-  CUtensorMap q_map;   // Q [M, H] f16, box {64, 32}
+  void* p;             // P [M, H] f16 (16-byte aligned)
+  void* q;             // Q [M, H] f16 (16-byte aligned)
   const float* gw;     // [slots total, r] f32: W_f[:, r:2r] g of each slot
   const float* wsp;    // [pairs, H] f32: W s_p
   const float* vals;   // [M] f32: the candidate's logit l

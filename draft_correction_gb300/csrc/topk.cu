@@ -63,6 +63,17 @@ __device__ __forceinline__ void ld_stream32(const uint4* p, uint4& a, uint4& b) 
                : "l"(p));
 }
 
+// 32 bytes of a suspect, read again after the stream: the access hands the line back to L2's
+// normal eviction order as one to evict first (the stream marked it to keep).
+__device__ __forceinline__ void ld_release32(const uint4* p, uint4& a, uint4& b) {
+  asm volatile(
+      "{\n\t.reg .b64 pol;\n\t"
+      "createpolicy.fractional.L2::evict_first.b64 pol, 1.0;\n\t"
+      "ld.global.nc.L1::no_allocate.L2::cache_hint.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8], pol;\n\t}"
+      : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
+      : "l"(p));
+}
+
 __device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
   uint32_t d;
   asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
@@ -478,6 +489,9 @@ __global__ void __launch_bounds__(kThreads, 4) topk_kernel(const void* __restric
     if (maybe) {
       const int pos = nsus + __popc(bal & ((1u << lane) - 1));
       if (pos < kSusW) s_sus[warp * kSusW + pos] = vidx(it, 0);
+      // the suspect's 64 bytes are read again after the loop: keep them in L2 past the stream
+      // (whole 64-byte chunks only: those are the ones read back with the matching release)
+      if (vidx(it, 0) + kU <= g.vend) prefetch_l2_keep(g.vp + vidx(it, 0));
     }
     nsus += __popc(bal);
 #pragma unroll
@@ -507,8 +521,8 @@ __global__ void __launch_bounds__(kThreads, 4) topk_kernel(const void* __restric
       // round's are keyed, so the rounds' memory latencies overlap
       auto fetch = [&](int vi0, uint4(&v)[kU]) {
         if (vi0 + kU <= g.vend) {  // the lane's 64 contiguous bytes, one burst
-          ld_stream32(g.vp + vi0, v[0], v[1]);
-          ld_stream32(g.vp + vi0 + 2, v[2], v[3]);
+          ld_release32(g.vp + vi0, v[0], v[1]);
+          ld_release32(g.vp + vi0 + 2, v[2], v[3]);
         } else {
 #pragma unroll
           for (int u = 0; u < kU; ++u) v[u] = vi0 + u < g.vend ? ld_stream(g.vp + vi0 + u) : neg_inf;
@@ -527,18 +541,46 @@ __global__ void __launch_bounds__(kThreads, 4) topk_kernel(const void* __restric
           vi_next = jn < nsus ? s_sus[warp * kSusW + jn] : g.vend;
           fetch(vi_next, v_next);
         }
+        // Only values reaching the threshold value can have a key above it: mark them (a rolled
+        // loop over the lane's 16 words, so that this code stays a few instruction-cache lines),
+        // give every lane its output range with one warp scan, and key the marked values.  A value
+        // at the threshold whose key is not above it stays a zero key, which every later step
+        // ignores.
+        auto word_at = [&](int w) -> uint32_t {
+          const uint4 q = (w >> 2) == 0 ? v[0] : (w >> 2) == 1 ? v[1] : (w >> 2) == 2 ? v[2] : v[3];
+          const int c = w & 3;
+          return c == 0 ? q.x : c == 1 ? q.y : c == 2 ? q.z : q.w;
+        };
+        constexpr int EPW = kBf16 ? 2 : 1;  // elements per 32-bit word
+        uint32_t mark = 0;
+#pragma unroll 1
+        for (int w = 0; w < 4 * kU; ++w) {
+          const uint32_t x = word_at(w);
 #pragma unroll
-        for (int u = 0; u < kU; ++u) {
-          const int vi = vi0 + u;
-#pragma unroll
-          for (int e = 0; e < EPV; ++e) {
-            const uint32_t bits = elem_bits<kBf16>(v[u], e);
-            // only values reaching the threshold value can have a key above it
-            const bool reach = vi < g.vend && !(__uint_as_float(bits) < tval);
-            const uint64_t key = reach ? make_key(bits, g.head + vi * EPV + e) : 0ull;
-            append(reach && key > thr, key);
+          for (int h = 0; h < EPW; ++h) {
+            const int e = w * EPW + h;  // element of the lane's 64 bytes
+            const uint32_t bits = kBf16 ? (h ? (x & 0xFFFF0000u) : (x << 16)) : x;
+            if (vi0 + e / EPV < g.vend && !(__uint_as_float(bits) < tval)) mark |= 1u << e;
           }
         }
+        const int cnt = __popc(mark);
+        int incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int t = __shfl_up_sync(kFull, incl, o);
+          if (lane >= o) incl += t;
+        }
+        int pos = ncand + incl - cnt;
+        while (mark != 0) {
+          const int e = __ffs(mark) - 1;
+          mark &= mark - 1;
+          const uint32_t x = word_at(e / EPW);
+          const uint32_t bits = kBf16 ? ((e & 1) ? (x & 0xFFFF0000u) : (x << 16)) : x;
+          const uint64_t key = make_key(bits, g.head + vi0 * EPV + e);
+          if (pos < kCapW) wbuf[pos] = key > thr ? key : 0ull;
+          ++pos;
+        }
+        ncand += __shfl_sync(kFull, incl, 31);
       }
     }
     if (warp == 0) {

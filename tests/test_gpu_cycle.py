@@ -124,7 +124,8 @@ def test_cycle_worked_example_printed_logits():
     assert list(g["tokens"][0]) == [0, 4, 7, 9]
 
 
-@pytest.mark.parametrize("cfg", [SMALL_BF16, SMALL_R256, SMALL_R512, SMALL_BF16.replace(K=1)],
+@pytest.mark.parametrize("cfg", [SMALL_BF16, SMALL_R256, SMALL_R512, SMALL_BF16.replace(K=1),
+                                 SMALL_BF16.replace(name="small_h64", H=64)],
                          ids=lambda c: f"{c.name}_K{c.K}")
 @pytest.mark.parametrize("variant", [None, "amplified"])
 def test_cycle_small(cfg, variant):
