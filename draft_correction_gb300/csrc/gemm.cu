@@ -90,6 +90,16 @@ __device__ __forceinline__ void stage_row(uint8_t* buf, int r, const float* v) {
   }
 }
 
+// Eight values as bf16, round to nearest even.
+__device__ __forceinline__ uint4 pack8_bf16(const float* v) {
+  __nv_bfloat162 t0 = __floats2bfloat162_rn(v[0], v[1]);
+  __nv_bfloat162 t1 = __floats2bfloat162_rn(v[2], v[3]);
+  __nv_bfloat162 t2 = __floats2bfloat162_rn(v[4], v[5]);
+  __nv_bfloat162 t3 = __floats2bfloat162_rn(v[6], v[7]);
+  return make_uint4(*reinterpret_cast<uint32_t*>(&t0), *reinterpret_cast<uint32_t*>(&t1),
+                    *reinterpret_cast<uint32_t*>(&t2), *reinterpret_cast<uint32_t*>(&t3));
+}
+
 // Four consecutive entries of a weight-dtype vector as float.
 template <bool kBf16>
 __device__ __forceinline__ float4 ldw4(const void* p, int i) {
@@ -594,8 +604,61 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     const int rpc = BM / split_k;
     // partial rows, column-group major: column c of slot row sr at ((c / 4) * SPLIT_RP + sr) * 4 + c % 4
     const float* red = reinterpret_cast<const float*>(smem);
-    // One warp per owned row, two rows at a time so that their loads and reductions overlap:
-    // the partials are added in rank order (deterministic).
+    if (g_epi == EPI_LN) {
+      // LayerNorm rows: four threads per row, each with a quarter of the columns in registers
+      // (the partials added in rank order: deterministic).  Lane = quarter * 8 + row within the
+      // warp's 8 rows, so a warp's loads cover 8 consecutive slot rows of 4 column groups
+      // (conflict-free) and the row sums need two shuffles.  Each thread stores its quarter of
+      // the row with 16-byte stores.
+      constexpr int CQ = BN / 4;  // columns per thread
+      const int t = threadIdx.x;
+      const int rr = (t >> 5) * 8 + (t & 7), q = (t >> 3) & 3;
+      const bool on = t < rpc * 4;  // rpc is a multiple of 8
+      const int m = m_tile * BM + rank * rpc + rr;
+      float v[CQ];
+#pragma unroll
+      for (int i = 0; i < CQ; ++i) v[i] = 0.f;
+      if (on) {
+        for (int src = 0; src < split_k; ++src) {
+#pragma unroll
+          for (int k = 0; k < CQ / 4; ++k) {
+            const float4 x = *reinterpret_cast<const float4*>(red + ((q * (CQ / 4) + k) * SPLIT_RP + src * rpc + rr) * 4);
+            v[4 * k] += x.x;
+            v[4 * k + 1] += x.y;
+            v[4 * k + 2] += x.z;
+            v[4 * k + 3] += x.w;
+          }
+        }
+      }
+      float sum = 0.f;
+#pragma unroll
+      for (int i = 0; i < CQ; ++i) sum += v[i];
+      sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 8);
+      sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 16);
+      const float mean = sum / BN;
+      float ss = 0.f;
+#pragma unroll
+      for (int i = 0; i < CQ; ++i) ss += (v[i] - mean) * (v[i] - mean);
+      ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 8);
+      ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 16);
+      const float rstd = rsqrtf(ss / BN + args.ln_eps);
+      if (on && m < args.M) {
+        const size_t obase = static_cast<size_t>(m) * g_ldo + static_cast<size_t>(nt) * BN + q * CQ;
+#pragma unroll
+        for (int i = 0; i < CQ; ++i) v[i] = (v[i] - mean) * rstd;
+        if constexpr (kBf16) {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(g_out) + obase);
+#pragma unroll
+          for (int k = 0; k < CQ / 8; ++k) dst[k] = pack8_bf16(v + 8 * k);
+        } else {
+          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(g_out) + obase);
+#pragma unroll
+          for (int k = 0; k < CQ / 4; ++k) dst[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+        }
+      }
+    } else {
+    // Other epilogues: one warp per owned row, two rows at a time so that their loads and
+    // reductions overlap; the partials are added in rank order (deterministic).
     constexpr int NW = kThreads / 32;
     constexpr int NJ = (BN + 31) / 32;
     for (int rr0 = warp; rr0 < rpc; rr0 += 2 * NW) {
@@ -665,6 +728,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           }
         }
       }
+    }
     }
   }
 
@@ -802,14 +866,6 @@ __device__ __forceinline__ void st_global_32(void* p, const uint4& a, const uint
                : "memory");
 }
 
-__device__ __forceinline__ uint4 pack8_bf16(const float* v) {
-  __nv_bfloat162 t0 = __floats2bfloat162_rn(v[0], v[1]);
-  __nv_bfloat162 t1 = __floats2bfloat162_rn(v[2], v[3]);
-  __nv_bfloat162 t2 = __floats2bfloat162_rn(v[4], v[5]);
-  __nv_bfloat162 t3 = __floats2bfloat162_rn(v[6], v[7]);
-  return make_uint4(*reinterpret_cast<uint32_t*>(&t0), *reinterpret_cast<uint32_t*>(&t1),
-                    *reinterpret_cast<uint32_t*>(&t2), *reinterpret_cast<uint32_t*>(&t3));
-}
 
 template <int R>
 __global__ void __launch_bounds__(kThreads, 1) zuv_kernel(const __grid_constant__ ZuvArgs args) {
