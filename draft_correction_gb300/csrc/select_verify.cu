@@ -31,6 +31,7 @@ namespace {
 constexpr int kThreads = 512;
 constexpr int kMaxB = 64;
 constexpr int kStageFloats = 8 * 1024;  // score grid staged in shared memory up to 32 KB
+constexpr int kIdsStage = 2048;         // candidate ids staged with it (in the draw's 8 KB buffer)
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
 // argmax over the order codes row[0..K) (K <= 64; 0 marks no entry): the largest code, the
@@ -122,20 +123,46 @@ __global__ void __launch_bounds__(kThreads) select_verify_kernel(const SelectVer
     const float* Sn = a.S + static_cast<size_t>(n) * grid_floats;
     const bool staged = grid_floats <= static_cast<size_t>(kStageFloats);
     const bool greedy = a.rule == 0;
+    // first-slot logits and candidate ids staged with the grid (greedy walk, B K <= kIdsStage)
+    const bool pre = staged && greedy && B * K <= kIdsStage;
+    uint32_t* s_v0 = reinterpret_cast<uint32_t*>(s_draft);  // read by warp 0 before it writes s_draft
+    int32_t* s_ids = reinterpret_cast<int32_t*>(s_sb);      // the residual draw uses s_sb only later
     if (staged) {
       // greedy walk: order codes (argmax by integer max); whole-path rule: values, NaN as -inf.
-      // Every thread issues all its loads before storing any, so they are in flight together.
+      // Every thread issues all its loads before storing any, so they are in flight together;
+      // for the greedy walk the first slot's logits and the stream's candidate ids come in the
+      // same batch, so the walk and the token look-up touch only shared memory.
       constexpr int kPer = kStageFloats / kThreads;
+      constexpr int kIdPer = kIdsStage / kThreads;
       float x[kPer];
+      int32_t idv[kIdPer];
+      float v0 = 0.f;
 #pragma unroll
       for (int q = 0; q < kPer; ++q) {
         const size_t i = threadIdx.x + static_cast<size_t>(q) * kThreads;
         x[q] = i < grid_floats ? Sn[i] : 0.f;
       }
+      if (pre) {
+        const size_t base = static_cast<size_t>(n) * B * K;
+        if (static_cast<int>(threadIdx.x) < K) v0 = a.vals[base + threadIdx.x];
+#pragma unroll
+        for (int q = 0; q < kIdPer; ++q) {
+          const int i = static_cast<int>(threadIdx.x) + q * kThreads;
+          idv[q] = i < B * K ? a.ids[base + i] : 0;
+        }
+      }
 #pragma unroll
       for (int q = 0; q < kPer; ++q) {
         const size_t i = threadIdx.x + static_cast<size_t>(q) * kThreads;
         if (i < grid_floats) s_S[i] = greedy ? ord32(__float_as_uint(x[q])) : __float_as_uint(canon(x[q]));
+      }
+      if (pre) {
+        if (static_cast<int>(threadIdx.x) < K) s_v0[threadIdx.x] = ord32(__float_as_uint(v0));
+#pragma unroll
+        for (int q = 0; q < kIdPer; ++q) {
+          const int i = static_cast<int>(threadIdx.x) + q * kThreads;
+          if (i < B * K) s_ids[i] = idv[q];
+        }
       }
     }
     __syncthreads();
@@ -198,7 +225,8 @@ __global__ void __launch_bounds__(kThreads) select_verify_kernel(const SelectVer
     } else if (warp == 0) {
       // The chain of argmaxes touches only shared memory (and registers); the token ids of
       // the chosen candidates are looked up together afterwards.
-      int k = warp_argmax(a.vals + static_cast<size_t>(n) * B * K, K, lane);
+      int k = pre ? warp_argmax_ord(lane < K ? s_v0[lane] : 0u, lane + 32 < K ? s_v0[lane + 32] : 0u, lane)
+                  : warp_argmax(a.vals + static_cast<size_t>(n) * B * K, K, lane);
       if (lane == 0) s_k[0] = k;
       for (int p = 0; p + 1 < B; ++p) {
         const size_t row = (static_cast<size_t>(p) * K + k) * K;
@@ -217,7 +245,7 @@ __global__ void __launch_bounds__(kThreads) select_verify_kernel(const SelectVer
       const int32_t* idn = a.ids + static_cast<size_t>(n) * B * K;
       for (int j = lane; j < B; j += 32) {
         const int kj = s_k[j];
-        const int32_t tok = idn[static_cast<size_t>(j) * K + kj];
+        const int32_t tok = pre ? s_ids[j * K + kj] : idn[static_cast<size_t>(j) * K + kj];
         s_draft[j] = tok;
         if (rank == 0) {
           a.k_sel[static_cast<size_t>(n) * B + j] = kj;
