@@ -878,7 +878,8 @@ __global__ void __launch_bounds__(kThreads, 1) zuv_kernel(const __grid_constant_
   uint8_t* ring = smem + NK * A_KB;  // kZuvRing x kZuvStage
   __shared__ __align__(8) uint64_t full_bar[kZuvRing];
   __shared__ __align__(8) uint64_t empty_bar[kZuvRing];
-  __shared__ __align__(8) uint64_t a_bar, acc1_bar, z_bar;
+  __shared__ __align__(8) uint64_t a_bar, acc1_bar;
+  __shared__ __align__(8) uint64_t z_bar[2];  // the two column halves of z (k-blocks of phase 2)
   __shared__ __align__(8) uint64_t acc2_bar[2];  // one per phase-2 column block
   __shared__ uint32_t tmem_base_s;
 
@@ -901,7 +902,8 @@ __global__ void __launch_bounds__(kThreads, 1) zuv_kernel(const __grid_constant_
     }
     mbar_init(smem_u32(&a_bar), 1);
     mbar_init(smem_u32(&acc1_bar), 1);
-    mbar_init(smem_u32(&z_bar), 1);
+    mbar_init(smem_u32(&z_bar[0]), 1);
+    mbar_init(smem_u32(&z_bar[1]), 1);
     mbar_init(smem_u32(&acc2_bar[0]), 1);
     mbar_init(smem_u32(&acc2_bar[1]), 1);
     fence_mbar_init();
@@ -953,14 +955,18 @@ __global__ void __launch_bounds__(kThreads, 1) zuv_kernel(const __grid_constant_
       bool ok = mbar_wait(smem_u32(&a_bar), 0);
       if (!ok) atomicOr(args.status, DEV_TIMEOUT_TMA);
       for (int i = 0; ok && i < total; ++i) {
-        if (i == NK) {
-          // phase 2 reads z, which the epilogue writes over b once it has read acc1
-          tc_commit(smem_u32(&acc1_bar));
-          if (!mbar_wait(smem_u32(&z_bar), 0)) {
-            atomicOr(args.status, DEV_TIMEOUT_ACC);
-            ok = false;
-            break;
+        // phase 2 reads z, which the epilogue writes over b once it has read acc1: its first
+        // k-blocks as soon as the first column half of z is written, the rest after the second
+        if (i == NK) tc_commit(smem_u32(&acc1_bar));
+        if (i == NK || i == NK + NK / 2) {
+          const int first = i == NK ? 0 : 1, last = (i == NK && NK / 2 > 0) ? 0 : 1;
+          for (int zh = first; ok && zh <= last; ++zh) {
+            if (!mbar_wait(smem_u32(&z_bar[zh]), 0)) {
+              atomicOr(args.status, DEV_TIMEOUT_ACC);
+              ok = false;
+            }
           }
+          if (!ok) break;
           tc_fence_after();
         }
         const int s = i % kZuvRing;
@@ -1043,40 +1049,50 @@ __global__ void __launch_bounds__(kThreads, 1) zuv_kernel(const __grid_constant_
     if (!ok && lane == 0) atomicOr(args.status, DEV_TIMEOUT_ACC);
     tc_fence_after();
     const float* gwr = staged ? s_gw + (slot - first_slot) * R : args.gw + static_cast<size_t>(slot) * R;
-    // 32-column chunks of this warp's half of the row; the next chunk's TMEM load is in flight
-    // while the current one is converted.
-    constexpr int NCH = R / 64;  // chunks per warp
-    uint32_t rbuf[2][32];
-    tmem_ld32_nowait(trow + half * (R / 2), rbuf[0]);
+    // z in two passes over the column halves [0, R/2) and [R/2, R), each handed to the MMA warp
+    // as soon as it is written; within a pass the two warps of a lane quarter split the 32-column
+    // chunks, whose TMEM loads are issued together before they are converted.
+    constexpr int NCHK = R / 32;       // 32-column chunks of the row
+    constexpr int PASS = NCHK / 2;     // chunks per pass
+    constexpr int MINE = PASS >= 2 ? PASS / 2 : 1;  // chunks of one warp per pass
 #pragma unroll
-    for (int k = 0; k < NCH; ++k) {
-      const int c = half * (R / 2) + 32 * k;
-      tmem_ld_wait();
-      if (k + 1 < NCH) tmem_ld32_nowait(trow + c + 32, rbuf[(k + 1) & 1]);
-      float v[32];
+    for (int zh = 0; zh < 2; ++zh) {
+      const bool work = PASS >= 2 || half == zh;  // one chunk per pass (r = 64): one warp of two
+      const int c0 = zh * (R / 2) + (PASS >= 2 ? half * MINE * 32 : 0);
+      if (work) {
+        uint32_t rbuf[MINE][32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(rbuf[k & 1][i]);
+        for (int k = 0; k < MINE; ++k) tmem_ld32_nowait(trow + c0 + 32 * k, rbuf[k]);
+        tmem_ld_wait();
 #pragma unroll
-      for (int i = 0; i < 32; i += 4) {
-        const float4 g4 = *reinterpret_cast<const float4*>(gwr + c + i);
-        const float h0 = 0.5f * (v[i] + g4.x), h1 = 0.5f * (v[i + 1] + g4.y);
-        const float h2 = 0.5f * (v[i + 2] + g4.z), h3 = 0.5f * (v[i + 3] + g4.w);
-        const float2 t01 = tanh2_f16(h0, h1), t23 = tanh2_f16(h2, h3);
-        v[i] = live ? fmaf(h0, t01.x, h0) : 0.f;
-        v[i + 1] = live ? fmaf(h1, t01.y, h1) : 0.f;
-        v[i + 2] = live ? fmaf(h2, t23.x, h2) : 0.f;
-        v[i + 3] = live ? fmaf(h3, t23.y, h3) : 0.f;
+        for (int k = 0; k < MINE; ++k) {
+          const int c = c0 + 32 * k;
+          float v[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(rbuf[k][i]);
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            const float4 g4 = *reinterpret_cast<const float4*>(gwr + c + i);
+            const float h0 = 0.5f * (v[i] + g4.x), h1 = 0.5f * (v[i + 1] + g4.y);
+            const float h2 = 0.5f * (v[i + 2] + g4.z), h3 = 0.5f * (v[i + 3] + g4.w);
+            const float2 t01 = tanh2_f16(h0, h1), t23 = tanh2_f16(h2, h3);
+            v[i] = live ? fmaf(h0, t01.x, h0) : 0.f;
+            v[i + 1] = live ? fmaf(h1, t01.y, h1) : 0.f;
+            v[i + 2] = live ? fmaf(h2, t23.x, h2) : 0.f;
+            v[i + 3] = live ? fmaf(h3, t23.y, h3) : 0.f;
+          }
+          uint8_t* kbase = a_reg + (c / 64) * A_KB + row * 128;
+          const int ch0 = (c % 64) / 8;
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+            *reinterpret_cast<uint4*>(kbase + (((ch0 + t) ^ (row & 7)) << 4)) = pack8_bf16(v + 8 * t);
+        }
       }
-      uint8_t* kbase = a_reg + (c / 64) * A_KB + row * 128;
-      const int ch0 = (c % 64) / 8;
-#pragma unroll
-      for (int t = 0; t < 4; ++t)
-        *reinterpret_cast<uint4*>(kbase + (((ch0 + t) ^ (row & 7)) << 4)) = pack8_bf16(v + 8 * t);
+      fence_proxy_async();  // the tensor core reads this half of z next
+      tc_fence_before();
+      named_barrier_sync(1, kEpiThreads);
+      if (threadIdx.x == 64) mbar_arrive(smem_u32(&z_bar[zh]));
     }
-    fence_proxy_async();  // the tensor core reads z next
-    tc_fence_before();
-    named_barrier_sync(1, kEpiThreads);
-    if (threadIdx.x == 64) mbar_arrive(smem_u32(&z_bar));
     // phase 2: P or Q, one column block at a time.  Each thread owns one row and stores its
     // f16 values straight to global memory, 32 bytes per store (16 when the output is only
     // 16-byte aligned): the ring still feeds the next block's MMAs, so nothing is staged.
