@@ -341,7 +341,8 @@ int enqueue_repr_fuse(const Dims& D, const dcoco_weights* w, void* uz, void* vz,
     const char* err = nullptr;
     if (!make_tmap(&z.b_map, s.b, true, M, r, r, 128, &err) || !make_tmap(&z.wf_map, w->W_f, true, r, 2 * r, 2 * r, r, &err) ||
         !make_tmap(&z.u_map, w->U, true, H, r, r, std::min(H, 256), &err) ||
-        !make_tmap(&z.v_map, w->V, true, H, r, r, std::min(H, 256), &err))
+        !make_tmap(&z.v_map, w->V, true, H, r, r, std::min(H, 256), &err) ||
+        !make_tmap(&z.p_map, uz, true, M, H, H, 32, &err) || !make_tmap(&z.q_map, vz, true, M, H, H, 32, &err))
       return fail(DCOCO_ERR_CUDA, "%s", err);
     z.p = uz;
     z.q = vz;

@@ -910,6 +910,7 @@ __global__ void __launch_bounds__(kThreads, 1) zuv_kernel(const __grid_constant_
     prefetch_tmap(&args.b_map);
     prefetch_tmap(&args.wf_map);
     prefetch_tmap(w2_map);
+    prefetch_tmap(is_q ? &args.q_map : &args.p_map);
   }
   if (warp == 1) tmem_alloc(smem_u32(&tmem_base_s), 512);
   tc_fence_before();
@@ -1104,6 +1105,9 @@ __global__ void __launch_bounds__(kThreads, 1) zuv_kernel(const __grid_constant_
     const int nsub = NC / 64;  // 128-byte (64-column f16) sub-tiles of a column block
     const int halves = nsub >= 2 ? 2 : 1;
     __half* out_row = static_cast<__half*>(is_q ? args.q : args.p) + static_cast<size_t>(live ? m : 0) * H;
+    uint8_t* stg = ring + (warp - 2) * 8192;  // staging of the last block (see below)
+    const int y0 = m_tile * BM + q * 32;
+    const CUtensorMap* out_map = is_q ? &args.q_map : &args.p_map;
     const bool wide = ((reinterpret_cast<uintptr_t>(is_q ? args.q : args.p) | static_cast<uintptr_t>(H) * 2) & 31) == 0;
     for (int cb = 0; cb < NH2; ++cb) {
       const bool got = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&acc2_bar[cb]), 0));
@@ -1155,7 +1159,24 @@ __global__ void __launch_bounds__(kThreads, 1) zuv_kernel(const __grid_constant_
             v[i + 3] = 0.5f * (v[i + 3] + add.w + u4.w * l);
           }
         }
-        if (live && ok) {
+        if (cb == NH2 - 1) {
+          // The last block: every MMA has completed, so the ring is free to stage the rows (two
+          // 4 KB halves per warp) for tensor-map stores, which leave the warps at once.
+          uint8_t* buf = stg + ((j - j0) & 1) * 4096;
+          if (j - j0 >= 2) {
+            if (lane == 0) bulk_wait_read<1>();  // the store that used this half has read it
+            __syncwarp();
+          }
+          stage_row<2>(buf, lane, v);
+          fence_proxy_async();
+          __syncwarp();
+          if (lane == 0 && y0 < args.M && ok) {
+            tma_store_2d(out_map, j * 64, y0, smem_u32(buf));
+            bulk_commit();
+          }
+        } else if (live && ok) {
+          // Earlier blocks: the ring still feeds the next block's MMAs, so each thread stores its
+          // row's 64 values straight from registers.
           uint4 h[8];
 #pragma unroll
           for (int c = 0; c < 8; ++c) h[c] = pack8_f16_clamped(v + 8 * c);
@@ -1170,6 +1191,7 @@ __global__ void __launch_bounds__(kThreads, 1) zuv_kernel(const __grid_constant_
         }
       }
     }
+    if (lane == 0) bulk_wait<0>();
   }
   tc_fence_before();
   __syncthreads();

@@ -118,6 +118,8 @@ struct ZuvArgs {
   CUtensorMap v_map;   // V [H, r], same box
   void* p;             // P [M, H] f16 (16-byte aligned)
   void* q;             // Q [M, H] f16 (16-byte aligned)
+  CUtensorMap p_map;   // P, box {64, 32} (stores of the last column block)
+  CUtensorMap q_map;   // Q, same box
   const float* gw;     // [slots total, r] f32: W_f[:, r:2r] g of each slot
   const float* wsp;    // [pairs, H] f32: W s_p
   const float* vals;   // [M] f32: the candidate's logit l
