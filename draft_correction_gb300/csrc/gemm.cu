@@ -831,6 +831,9 @@ __global__ void pair_combine_kernel(const float* __restrict__ hp, void* __restri
 //            columns after the other, their weight k-blocks through the same ring; the epilogue
 //            of a column block (the logit term, for P the bias and W s_p, the halving, f16 rows
 //            by tensor-map stores) runs while the MMAs of the next block do.
+// TMEM columns: acc1 at [0, r); the first phase-2 block at [256, 256 + NC), clear of acc1 while
+// its second column half is still being read; a second block at [0, NC), issued only once all
+// of acc1 has been read.
 // The ring's four 32 KB stages take every W_f k-block before the kernel waits for its
 // predecessors, and the first U or V k-blocks while phase 1 runs.
 // z never leaves shared memory.  Warp roles as in gemm_kernel: 0 TMA producer, 1 MMA issuer,
@@ -894,6 +897,8 @@ __global__ void __launch_bounds__(kThreads, 1) zuv_kernel(const __grid_constant_
   const CUtensorMap* w2_map = is_q ? &args.v_map : &args.u_map;
   // ring loads: NK k-blocks of W_f, then NK k-blocks of U or V per column block
   const int total = NK + NH2 * NK;
+  // TMEM column of phase-2 column block cb (acc1 holds [0, R))
+  auto acc2_col = [](int cb) { return cb == 0 ? 256u : 0u; };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kZuvRing; ++s) {
@@ -988,7 +993,7 @@ __global__ void __launch_bounds__(kThreads, 1) zuv_kernel(const __grid_constant_
           if (i < NK)
             tc_mma<false>(tmem, ad, sw128_desc(b_s + j * 32), IDESC1, acc);
           else
-            tc_mma<false>(tmem + cb * NC, ad, sw128_desc(b_s + j * 32), idesc2, acc);
+            tc_mma<false>(tmem + acc2_col(cb), ad, sw128_desc(b_s + j * 32), idesc2, acc);
         }
         tc_commit(smem_u32(&empty_bar[s]));
         if (i >= NK && kb == NK - 1) tc_commit(smem_u32(&acc2_bar[cb]));  // this column block is done
@@ -1004,10 +1009,12 @@ __global__ void __launch_bounds__(kThreads, 1) zuv_kernel(const __grid_constant_
     const bool live = m < args.M;
     const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16);
     grid_dep_wait();  // gw, W s and the logits come from earlier kernels
-    const int slot = live ? m / args.cand : 0;  // stream * slots + slot
     // Per-tile constants, staged in shared memory while the MMAs run (when they fit): the gw rows
-    // of the tile's slots; per slot (b1 + W s_p) / 2 for P (zero for Q); u / 2.
+    // of the tile's slots; per slot (b1 + W s_p) / 2 for P (zero for Q); u / 2.  Rows past M (a
+    // ragged last tile) take the tile's first slot, so that their lookups stay inside what is
+    // staged.
     const int first_slot = (m_tile * BM) / args.cand;
+    const int slot = live ? m / args.cand : first_slot;  // stream * slots + slot
     const int nslots = (min(args.M, m_tile * BM + BM) - 1) / args.cand - first_slot + 1;
     const bool staged = (nslots * (R + H) + H) * 4 <= kZuvConst;
     float* s_gw = reinterpret_cast<float*>(ring + kZuvRing * kZuvStage);  // [nslots][R]
@@ -1120,8 +1127,9 @@ __global__ void __launch_bounds__(kThreads, 1) zuv_kernel(const __grid_constant_
         float v[64];
         {
           uint32_t r[2][32];
-          tmem_ld32_nowait(trow + j * 64, r[0]);
-          tmem_ld32_nowait(trow + j * 64 + 32, r[1]);
+          const uint32_t tc = trow + acc2_col(cb) + (j - cb * nsub) * 64;
+          tmem_ld32_nowait(tc, r[0]);
+          tmem_ld32_nowait(tc + 32, r[1]);
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 32; ++i) {

@@ -125,7 +125,10 @@ def test_cycle_worked_example_printed_logits():
 
 
 @pytest.mark.parametrize("cfg", [SMALL_BF16, SMALL_R256, SMALL_R512, SMALL_BF16.replace(K=1),
-                                 SMALL_BF16.replace(name="small_h64", H=64)],
+                                 SMALL_BF16.replace(name="small_h64", H=64),
+                                 # 515 candidate rows, one slot each: five 128-row tiles, the
+                                 # last one with 3 live rows whose slot lookups start at 512
+                                 SMALL_BF16.replace(name="small_ragged", N=103, K=1)],
                          ids=lambda c: f"{c.name}_K{c.K}")
 @pytest.mark.parametrize("variant", [None, "amplified"])
 def test_cycle_small(cfg, variant):
