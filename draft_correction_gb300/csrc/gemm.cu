@@ -827,10 +827,11 @@ __global__ void pair_combine_kernel(const float* __restrict__ hp, void* __restri
 //   phase 1  acc1 = b W_f[:, 0:r]^T in TMEM (b tile loaded once by TMA, W_f k-blocks through a
 //            two-stage ring); the epilogue warps write z = SiLU(acc1 + gw[slot]) in bf16 over the
 //            b tile, in the 128-byte swizzled operand layout, and hand it to the MMA warp;
-//   phase 2  acc2 = z U^T (grid.y = 0) or z V^T (grid.y = 1), one block of at most 256 output
-//            columns after the other, their weight k-blocks through the same ring; the epilogue
-//            of a column block (the logit term, for P the bias and W s_p, the halving, f16 rows
-//            by tensor-map stores) runs while the MMAs of the next block do.
+//   phase 2  acc2 = z U^T (grid.y even) or z V^T (grid.y odd), one block of at most 256 output
+//            columns after the other (or, when the grid is small, one block per CTA), their
+//            weight k-blocks through the same ring; the epilogue of a column block (the logit
+//            term, for P the bias and W s_p, the halving, f16 rows by tensor-map stores) runs
+//            while the MMAs of the next block do.
 // TMEM columns: acc1 at [0, r); the first phase-2 block at [256, 256 + NC), clear of acc1 while
 // its second column half is still being read; a second block at [0, NC), issued only once all
 // of acc1 has been read.
@@ -889,10 +890,14 @@ __global__ void __launch_bounds__(kThreads, 1) zuv_kernel(const __grid_constant_
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int m_tile = blockIdx.x;
-  const bool is_q = blockIdx.y != 0;
+  const bool is_q = (blockIdx.y & 1) != 0;
   const int H = args.H;
   const int NC = H <= 256 ? H : 256;  // columns per phase-2 MMA (and per column block)
-  const int NH2 = H / NC;              // phase-2 column blocks (1 or 2)
+  // grid.y = 2: every column block of P (y = 0) or Q (y = 1) in this CTA; grid.y = 2 H / NC
+  // (small grids): only column block y >> 1 of P or Q, so that the CTAs' chains are shorter
+  const bool one_block = gridDim.y > 2;
+  const int cb0 = one_block ? static_cast<int>(blockIdx.y >> 1) : 0;  // first column block
+  const int NH2 = one_block ? 1 : H / NC;                                // column blocks here
   const uint32_t idesc2 = mma_idesc(1u, BM, static_cast<uint32_t>(NC));
   const CUtensorMap* w2_map = is_q ? &args.v_map : &args.u_map;
   // ring loads: NK k-blocks of W_f, then NK k-blocks of U or V per column block
@@ -937,7 +942,7 @@ __global__ void __launch_bounds__(kThreads, 1) zuv_kernel(const __grid_constant_
         } else {
           const int j = i - NK, cb = j / NK, kb = j - cb * NK;
           mbar_expect_tx(fb, NC * 128);
-          tma_load_2d(dst, w2_map, kb * 64, cb * NC, fb);
+          tma_load_2d(dst, w2_map, kb * 64, (cb0 + cb) * NC, fb);
         }
       };
       // the weight tiles do not depend on the preceding kernels: request them first
@@ -1122,12 +1127,13 @@ __global__ void __launch_bounds__(kThreads, 1) zuv_kernel(const __grid_constant_
       ok = ok && got;
       if (cb == 0) grid_dep_launch();  // the next kernel may start its prologue
       tc_fence_after();
-      const int j0 = cb * nsub + half * nsub / halves, j1 = cb * nsub + (half + 1) * nsub / halves;
+      const int cbg = cb0 + cb;  // the column block in P or Q
+      const int j0 = cbg * nsub + half * nsub / halves, j1 = cbg * nsub + (half + 1) * nsub / halves;
       for (int j = j0; half < halves && j < j1; ++j) {
         float v[64];
         {
           uint32_t r[2][32];
-          const uint32_t tc = trow + acc2_col(cb) + (j - cb * nsub) * 64;
+          const uint32_t tc = trow + acc2_col(cb) + (j - cbg * nsub) * 64;
           tmem_ld32_nowait(tc, r[0]);
           tmem_ld32_nowait(tc + 32, r[1]);
           tmem_ld_wait();
@@ -1223,7 +1229,9 @@ cudaError_t launch_zuv_t(const ZuvArgs& a, cudaStream_t stream) {
     configured[dev] = 1;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((a.M + BM - 1) / BM, 2, 1);
+  // one column block per CTA when that still fits one wave
+  const int tiles = (a.M + BM - 1) / BM, nh = a.H > 256 ? a.H / 256 : 1;
+  cfg.gridDim = dim3(tiles, (nh > 1 && tiles * 2 * nh <= sm_count()) ? 2 * nh : 2, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;

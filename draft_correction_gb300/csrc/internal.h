@@ -110,7 +110,9 @@ cudaError_t launch_gemm(const GemmArgs& args, bool is_bf16, int BN, int split_k,
 //   z = SiLU(b W_f[:, 0:r]^T + gw[slot])                      kept in shared memory, never stored
 //   P = (z U^T + b1 + W s[pair] + u_a l) / 2,  Q = (z V^T + u_b l) / 2     f16, clamped to +-30000
 // with the row and slot conventions of EPI_SILU_BIAS and EPI_PREP.  Grid (m_tiles, 2): y = 0
-// writes P and y = 1 writes Q; both recompute z for their 128 rows.
+// writes P and y = 1 writes Q; both recompute z for their 128 rows.  When H spans two 256-column
+// blocks and 4 m_tiles CTAs fit on the SMs, the grid is (m_tiles, 4): y & 1 picks P or Q and
+// y >> 1 the column block.
 struct ZuvArgs {
   CUtensorMap b_map;   // b [M, r], box {64, 128}
   CUtensorMap wf_map;  // W_f [r, 2r] (its first r columns act on b), box {64, r}
