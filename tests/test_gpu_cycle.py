@@ -128,7 +128,11 @@ def test_cycle_worked_example_printed_logits():
                                  SMALL_BF16.replace(name="small_h64", H=64),
                                  # 515 candidate rows, one slot each: five 128-row tiles, the
                                  # last one with 3 live rows whose slot lookups start at 512
-                                 SMALL_BF16.replace(name="small_ragged", N=103, K=1)],
+                                 SMALL_BF16.replace(name="small_ragged", N=103, K=1),
+                                 # the degenerate block of two slots (one transition per stream)
+                                 # and the largest candidate count
+                                 SMALL_BF16.replace(name="small_b2", B=2),
+                                 SMALL_BF16.replace(name="small_k64", K=64)],
                          ids=lambda c: f"{c.name}_K{c.K}")
 @pytest.mark.parametrize("variant", [None, "amplified"])
 def test_cycle_small(cfg, variant):
