@@ -285,14 +285,6 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t caddr) {
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(caddr) : "memory");
   return v;
 }
-__device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t caddr) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(caddr)
-               : "memory");
-  return v;
-}
 __device__ __forceinline__ uint64_t ld_cluster_u64(uint32_t caddr) {
   uint64_t v;
   asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(caddr) : "memory");
