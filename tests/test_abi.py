@@ -91,6 +91,15 @@ def test_workspace_errors(L):
     assert L.dcoco_cycle(*args, FAKE, need - 1, None) == 3
 
 
+def test_cycle_shape_errors(L):
+    """The cycle's block shape is checked before anything is enqueued: 2 <= B <= 64,
+    1 <= K <= 64, N >= 1 (DCOCO_ERR_INVALID_ARG)."""
+    w = _weights()
+    for N, B, K in [(0, 4, 3), (1, 1, 3), (1, 65, 3), (1, 4, 0), (1, 4, 65)]:
+        args = [FAKE, 100, FAKE, FAKE, ctypes.byref(w), N, B, K, 0, FAKE, None, None] + [None] * 4 + [FAKE] * 4 + [None]
+        assert L.dcoco_cycle(*args, FAKE, 1 << 30, None) == 1, (N, B, K)
+
+
 def test_verify_errors(L):
     assert L.dcoco_verify(3, FAKE, FAKE, None, None, 1, 4, 0, FAKE, FAKE, FAKE, None, None) == 1
     assert L.dcoco_verify(0, FAKE, None, None, None, 1, 4, 0, FAKE, FAKE, FAKE, None, None) == 1   # greedy, no t
