@@ -824,9 +824,10 @@ __global__ void pair_combine_kernel(const float* __restrict__ hp, void* __restri
 // ---------------------------------------------------------------- fused z -> P / Q
 // The candidate fusion z = SiLU(W_f [b; g]) and the candidate blocks of the first MLP layer
 // (U z, V z, folded into the scorer's operands P and Q) for one 128-row tile, in one kernel:
-//   phase 1  acc1 = b W_f[:, 0:r]^T in TMEM (b tile loaded once by TMA, W_f k-blocks through a
-//            two-stage ring); the epilogue warps write z = SiLU(acc1 + gw[slot]) in bf16 over the
-//            b tile, in the 128-byte swizzled operand layout, and hand it to the MMA warp;
+//   phase 1  acc1 = b W_f[:, 0:r]^T in TMEM (b tile loaded once by TMA, W_f k-blocks through the
+//            ring); the epilogue warps write z = SiLU(acc1 + gw[slot]) in bf16 over the b tile,
+//            in the 128-byte swizzled operand layout, and hand it to the MMA warp in two column
+//            halves, so that the first phase-2 k-blocks start while the second half is written;
 //   phase 2  acc2 = z U^T (grid.y even) or z V^T (grid.y odd), one block of at most 256 output
 //            columns after the other (or, when the grid is small, one block per CTA), their
 //            weight k-blocks through the same ring; the epilogue of a column block (the logit
