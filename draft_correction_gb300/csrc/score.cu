@@ -8,15 +8,18 @@
 // once upstream; this kernel forms the K x K broadcast sum on chip and never writes the
 // [K, K, H] hidden layer to memory.
 //
-// One thread block handles one transition (n, p) and AB = 8 predecessor rows a.  Per chunk of
-// HC hidden units it stages, in shared memory,
+// One thread block handles one transition (n, p) and AB predecessor rows a (8 in score_kernel,
+// 4 in the cycle's score_prepped_kernel).  Per chunk of HC hidden units it stages, in shared
+// memory,
 //   P[a][h] = (uz[n,p,a,h] + ws[n,p,h] + u_a[h] l_p(a) + b1[h]) / 2
 //   Q[b][h] = (vz[n,p+1,b,h] + u_b[h] l_{p+1}(b)) / 2
 // so that with x = 2(P + Q):  SiLU(x) = x sigmoid(x) = y + y tanh(y), y = P + Q.
 // Each thread owns a 2 x 4 tile of (a, b) outputs over a strided subset of the hidden units
 // (7 shared-memory vector loads per 32 SiLUs); the partial sums are then added in a fixed
-// order.  For bf16 inputs the tanh runs as packed half-precision SFU instructions (two values
-// each; pre-activations and sums stay fp32); for f32 inputs as tanh.approx.f32.
+// order.  For bf16 inputs P and Q are kept in half precision, and their sum, the tanh (packed
+// half-precision SFU instructions, two values each) and the 8-term partial sums are half
+// precision too, each partial sum then added to the output's fp32 total; for f32 inputs
+// everything is fp32, with tanh.approx.f32.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
